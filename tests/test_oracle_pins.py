@@ -1,0 +1,339 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself:
+library conversions, closed forms, invariants, brute force in exact rational
+arithmetic, and the figures the pages print.  No GPU needed."""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from weight_streaming_gemv_bf16_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- formats
+
+def test_bf16_decode_all_patterns_match_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_bf16_encode_matches_torch_on_fp32_inputs():
+    rng = np.random.default_rng(1)
+    # normals over a wide exponent range, subnormals, exact ties
+    v = np.concatenate([
+        rng.standard_normal(20000) * np.exp2(rng.integers(-140, 120, 20000)),
+        rng.standard_normal(2000) * 1e-39,
+        (np.arange(-300, 300) * 2.0 + 1.0) * 2.0 ** -8,  # halfway between bf16 steps near 1
+    ]).astype(np.float32)
+    ours = oracle.f64_to_bf16(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+@pytest.mark.parametrize("value,bits", [
+    (1.0, 0x3F80),
+    (1.0 + 2.0 ** -8, 0x3F80),          # tie -> even (down)
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),      # tie -> even (up)
+    (-2.0, 0xC000),
+    (2.0 ** -133, 0x0001),              # smallest subnormal
+    (2.0 ** -134, 0x0000),              # tie with zero -> even (zero)
+    ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),   # largest finite
+    ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),   # tie above largest -> infinity
+])
+def test_bf16_encode_ieee_cases(value, bits):
+    assert int(oracle.f64_to_bf16(np.array([value]))[0]) == bits
+
+
+def test_fp16_decode_and_encode_match_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.fp16_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    rng = np.random.default_rng(2)
+    v = np.concatenate([
+        rng.standard_normal(20000) * np.exp2(rng.integers(-30, 18, 20000)),
+        (np.arange(-500, 500) * 2.0 + 1.0) * 2.0 ** -11,   # ties near 1
+        np.array([65504.0, 65519.99, 65520.0, 2.0 ** -25, 3 * 2.0 ** -26]),
+    ])
+    assert np.array_equal(oracle.f64_to_fp16(v), v.astype(np.float16).view(np.uint16))
+
+
+# ---------------------------------------------------------------- GEMV
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_gemv_identity_and_permutation_are_exact():
+    K = 64
+    x = oracle.round_bf16(np.random.default_rng(3).standard_normal((3, K)))
+    assert np.array_equal(oracle.gemv(_bf16(np.eye(K)), x), x)
+    perm = np.random.default_rng(4).permutation(K)
+    P = np.zeros((K, K), np.float32)
+    P[np.arange(K), perm] = 1.0                      # row m picks x[perm[m]]
+    assert np.array_equal(oracle.gemv(_bf16(P), x), x[:, perm])
+
+
+def test_gemv_one_hot_picks_the_column():
+    M, K = 5, 40
+    W = np.zeros((M, K), np.float32)
+    cols = [0, 7, 39, 12, 7]
+    for m, c in enumerate(cols):
+        W[m, c] = 2.0 ** m
+    x = oracle.round_bf16(np.random.default_rng(5).standard_normal((2, K)))
+    y = oracle.gemv(_bf16(W), x)
+    for m, c in enumerate(cols):
+        assert np.array_equal(y[:, m], x[:, c] * 2.0 ** m)
+
+
+def test_gemv_all_ones():
+    for K in (8, 1536, 8960):
+        y = oracle.gemv(_bf16(np.ones((3, K))), np.ones((2, K)))
+        assert np.all(y == K)
+
+
+def test_gemv_brute_force_exact_rational():
+    """16x16 and a non-square 12x20 case, summed exactly with Fractions."""
+    for (M, K, B, seed) in [(16, 16, 1, 6), (16, 16, 4, 7), (12, 20, 3, 8)]:
+        W = synth.normal_bf16((M, K), 1.0, seed, "bf")
+        xb = synth.normal_bf16((B, K), 1.0, seed, "bx")
+        Wd, xd = oracle.bf16_to_f64(W), oracle.bf16_to_f64(xb)
+        y = oracle.gemv(W, xd)
+        for b in range(B):
+            for m in range(M):
+                exact = sum(Fraction(float(Wd[m, k])) * Fraction(float(xd[b, k])) for k in range(K))
+                scale = sum(abs(Fraction(float(Wd[m, k])) * Fraction(float(xd[b, k]))) for k in range(K))
+                assert abs(Fraction(float(y[b, m])) - exact) <= scale * Fraction(1, 2 ** 50)
+                # both round to the same binary32 value
+                assert np.float32(float(exact)) == np.float32(y[b, m]) or \
+                    abs(float(exact) - y[b, m]) <= 2 ** -40 * float(scale)
+
+
+def test_gemv_linearity():
+    M, K = 64, 1536
+    W = synth.normal_bf16((M, K), 0.02, 0, "lin/W")
+    x = oracle.bf16_to_f64(synth.normal_bf16((1, K), 1.0, 0, "lin/x"))
+    z = oracle.bf16_to_f64(synth.normal_bf16((1, K), 1.0, 0, "lin/z"))
+    lhs = oracle.gemv(W, 2 * x + z / 4)
+    rhs = 2 * oracle.gemv(W, x) + oracle.gemv(W, z) / 4
+    assert np.allclose(lhs, rhs, rtol=0, atol=1e-13)
+
+
+def test_gemv_thread_count_does_not_change_result():
+    W = synth.normal_bf16((257, 96), 0.02, 0, "thr/W")
+    x = oracle.bf16_to_f64(synth.normal_bf16((3, 96), 1.0, 0, "thr/x"))
+    assert np.array_equal(oracle.gemv(W, x, threads=1), oracle.gemv(W, x, threads=4))
+
+
+# ---------------------------------------------------------------- norms
+
+def test_rmsnorm_unit_rms_invariant():
+    x = np.random.default_rng(9).standard_normal((4, 1536)) * 3.0
+    eps = 1e-6
+    out = oracle.rmsnorm(x, np.ones(1536), eps)
+    ms = np.mean(x * x, axis=1)
+    assert np.allclose(np.sqrt(np.mean(out * out, axis=1)), np.sqrt(ms / (ms + eps)), rtol=1e-12)
+
+
+def test_rmsnorm_eps_inside_the_square_root_and_gamma_per_column():
+    # constant rows: out = c / sqrt(c^2 + eps) * gamma  (eps inside the root)
+    c, eps = 0.01, 1e-4
+    g = np.linspace(0.5, 1.5, 8)
+    out = oracle.rmsnorm(np.full((1, 8), c), g, eps)
+    assert np.allclose(out[0], c / math.sqrt(c * c + eps) * g, rtol=1e-14)
+    # gamma multiplies column-wise
+    x = np.random.default_rng(10).standard_normal((2, 8))
+    assert np.allclose(oracle.rmsnorm(x, g, eps), oracle.rmsnorm(x, np.ones(8), eps) * g, rtol=1e-14)
+
+
+def test_rmsnorm_scale_invariance_without_eps():
+    x = np.random.default_rng(11).standard_normal((3, 896))
+    g = np.random.default_rng(12).uniform(0.5, 1.5, 896)
+    assert np.allclose(oracle.rmsnorm(x * 1024.0, g, 0.0), oracle.rmsnorm(x, g, 0.0), rtol=1e-13)
+
+
+def test_layernorm_moments_and_shift_invariance():
+    x = np.random.default_rng(13).standard_normal((4, 768)) * 2 + 5
+    out = oracle.layernorm(x, np.full(768, 3.0), np.full(768, -0.25), 0.0)
+    assert np.allclose(out.mean(axis=1), -0.25, atol=1e-12)
+    assert np.allclose(out.var(axis=1), 9.0, rtol=1e-12)
+    g = np.random.default_rng(14).uniform(0.5, 1.5, 768)
+    bt = np.random.default_rng(15).standard_normal(768) * 0.02
+    assert np.allclose(oracle.layernorm(x + 7.0, g, bt, 1e-5), oracle.layernorm(x, g, bt, 1e-5), atol=1e-12)
+    # two elements: (x - mean) / sqrt(var + eps) = +-d / sqrt(d^2 + eps)
+    d, eps = 0.5, 1e-5
+    out2 = oracle.layernorm(np.array([[1.0 - d, 1.0 + d]]), np.ones(2), np.zeros(2), eps)
+    assert np.allclose(out2[0], [-d / math.sqrt(d * d + eps), d / math.sqrt(d * d + eps)], rtol=1e-14)
+
+
+# ---------------------------------------------------------------- activations
+
+def test_gelu_against_the_normal_table():
+    for z, phi in _golden("normal_cdf.txt"):
+        z, phi = float(z), float(phi)
+        assert abs(oracle.gelu(np.array([z]))[0] - z * phi) <= z * 6e-10
+        assert abs(oracle.gelu(np.array([-z]))[0] - (-z) * (1 - phi)) <= z * 6e-10
+    assert oracle.gelu(np.array([0.0]))[0] == 0.0
+
+
+def test_gelu_odd_part_identity():
+    z = np.random.default_rng(16).standard_normal(1000) * 4
+    assert np.allclose(oracle.gelu(z) - oracle.gelu(-z), z, atol=1e-14)
+
+
+def test_swiglu_closed_forms():
+    # silu(ln 3) = ln 3 * 3/4 ; silu(0) = 0 ; silu(g) - silu(-g) = g ; u scales linearly
+    ln3 = math.log(3.0)
+    assert abs(oracle.swiglu(np.array([ln3]), np.array([1.0]))[0] - 0.75 * ln3) < 1e-15
+    assert oracle.swiglu(np.array([0.0]), np.array([5.0]))[0] == 0.0
+    g = np.random.default_rng(17).standard_normal(1000) * 6
+    one = np.ones_like(g)
+    assert np.allclose(oracle.swiglu(g, one) - oracle.swiglu(-g, one), g, atol=1e-13)
+    assert np.allclose(oracle.swiglu(g, 3 * one), 3 * oracle.swiglu(g, one), rtol=1e-15)
+    assert abs(oracle.swiglu(np.array([40.0]), np.array([1.0]))[0] - 40.0) < 1e-15
+
+
+# ---------------------------------------------------------------- argmax
+
+def test_argmax_planted_and_ties():
+    v = np.random.default_rng(18).standard_normal((3, 151936))
+    v[0, 123456] = 10.0
+    v[1, 5] = v[1, 99] = v[1, 151935] = 10.0     # ties -> lowest index
+    v[2, :] = -1.0                               # all equal -> 0
+    assert list(oracle.argmax_rows(v)) == [123456, 5, 0]
+
+
+# ---------------------------------------------------------------- block structure
+
+def _tiny_block(H, KV, I, seed):
+    t = f"tiny{seed}/"
+    return {
+        "gamma1": synth.uniform_bf16((H,), 0.5, 1.5, seed, t + "g1"),
+        "Wq": synth.normal_bf16((H, H), 0.02, seed, t + "Wq"),
+        "Wk": synth.normal_bf16((KV, H), 0.02, seed, t + "Wk"),
+        "Wv": synth.normal_bf16((KV, H), 0.02, seed, t + "Wv"),
+        "Wo": synth.normal_bf16((H, H), 0.02, seed, t + "Wo"),
+        "gamma2": synth.uniform_bf16((H,), 0.5, 1.5, seed, t + "g2"),
+        "Wg": synth.normal_bf16((I, H), 0.02, seed, t + "Wg"),
+        "Wu": synth.normal_bf16((I, H), 0.02, seed, t + "Wu"),
+        "Wd": synth.normal_bf16((H, I), 0.02, seed, t + "Wd"),
+    }
+
+
+def test_block_special_cases_expose_each_step():
+    H, KV, I, B = 32, 8, 32, 2
+    eps = 1e-6
+    blk = _tiny_block(H, KV, I, 0)
+    h = oracle.bf16_to_f64(synth.normal_bf16((B, H), 1.0, 0, "tiny/h"))
+    attn = oracle.bf16_to_f64(synth.normal_bf16((B, H), 1.0, 0, "tiny/attn"))
+    g1 = oracle.bf16_to_f64(blk["gamma1"])
+    g2 = oracle.bf16_to_f64(blk["gamma2"])
+    zero = lambda a: np.zeros_like(a)
+    eye = _bf16(np.eye(H))
+
+    # zero Wo and Wd: the residual passes through unchanged
+    z = dict(blk, Wo=zero(blk["Wo"]), Wd=zero(blk["Wd"]))
+    out = oracle.qwen_block(h, z, attn, eps)
+    assert np.array_equal(out["h"], h)
+
+    # Wq = I: q is the bf16-rounded RMSNorm of h with gamma1 (not gamma2)
+    out = oracle.qwen_block(h, dict(blk, Wq=eye), attn, eps)
+    ms = np.mean(h * h, axis=1, keepdims=True)
+    a_ref = torch.from_numpy(h / np.sqrt(ms + eps) * g1).to(torch.bfloat16).double().numpy()
+    assert np.allclose(out["q"], a_ref, rtol=0, atol=0) or np.max(np.abs(out["q"] - a_ref)) <= 2 ** -8 * np.max(np.abs(a_ref))
+
+    # Wo = I, Wd = 0: h_mid = h + attn (the attention stand-in, not a)
+    out = oracle.qwen_block(h, dict(blk, Wo=eye, Wd=zero(blk["Wd"])), attn, eps)
+    assert np.allclose(out["h"], h + attn, rtol=1e-7)
+
+    # Wg = Wu = I, Wd = I (I == H): h = h_mid + bf16(silu(m) * m), m from gamma2
+    out = oracle.qwen_block(h, dict(blk, Wg=eye, Wu=eye, Wd=eye), attn, eps)
+    hm = out["h_mid"]
+    ms = np.mean(hm * hm, axis=1, keepdims=True)
+    m = torch.from_numpy(hm / np.sqrt(ms + eps) * g2).to(torch.bfloat16).double().numpy()
+    s = torch.from_numpy(m * m / (1 + np.exp(-m))).to(torch.bfloat16).double().numpy()
+    assert np.max(np.abs(out["h"] - (hm + s))) <= 2 ** -7 * np.max(np.abs(s)) + 1e-6
+
+
+def test_chain_identity_head_picks_the_largest_normalised_element():
+    H, KV, I, B, L = 32, 8, 32, 3, 2
+    blocks = [_tiny_block(H, KV, I, s) for s in range(L)]
+    attns = [oracle.bf16_to_f64(synth.normal_bf16((B, H), 1.0, s, "tiny/attn")) for s in range(L)]
+    h0 = oracle.bf16_to_f64(synth.normal_bf16((B, H), 1.0, 0, "tiny/h"))
+    gf = _bf16(np.ones(H))
+    out = oracle.qwen_chain(h0, blocks, attns, gf, _bf16(np.eye(H)), 1e-6, keep_blocks=True)
+    a = oracle.round_bf16(oracle.rmsnorm(out["h"], np.ones(H), 1e-6))
+    assert np.array_equal(out["logits"], a)
+    assert list(out["idx"]) == [int(np.argmax(r)) for r in a]
+    assert np.array_equal(out["blocks"][-1]["h"], out["h"])
+    # block l's output is block l+1's input
+    again = oracle.qwen_block(out["blocks"][0]["h"], blocks[1], attns[1], 1e-6)
+    assert np.array_equal(again["h"], out["h"])
+
+
+def test_mlp_block_zero_weight_reduces_to_gelu_of_bias():
+    w, B = 16, 2
+    blk = {"gamma": _bf16(np.ones(w)), "beta": _bf16(np.zeros(w)),
+           "W": _bf16(np.zeros((w, w))), "b": synth.normal_bf16((w,), 1.0, 0, "mlpz/b")}
+    x = synth.normal_bf16((B, w), 1.0, 0, "mlpz/x")
+    z = oracle.mlp_block(x, blk)
+    bvals = oracle.bf16_to_f64(blk["b"])
+    ref = torch.from_numpy(bvals).to(torch.bfloat16).float()
+    ref = torch.nn.functional.gelu(ref.double()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(z, np.broadcast_to(ref, (B, w)))
+
+
+def test_mlp_block_identity_weight_reduces_to_gelu_of_layernorm():
+    w, B = 16, 2
+    g = synth.uniform_bf16((w,), 0.5, 1.5, 0, "mlpi/g")
+    bt = synth.normal_bf16((w,), 0.02, 0, "mlpi/bt")
+    blk = {"gamma": g, "beta": bt, "W": _bf16(np.eye(w)), "b": _bf16(np.zeros(w))}
+    x = synth.normal_bf16((B, w), 1.0, 0, "mlpi/x")
+    z = oracle.bf16_to_f64(oracle.mlp_block(x, blk))
+    xt = torch.from_numpy(oracle.bf16_to_f64(x))
+    ln = torch.nn.functional.layer_norm(xt, (w,), torch.from_numpy(oracle.bf16_to_f64(g)),
+                                        torch.from_numpy(oracle.bf16_to_f64(bt)), 1e-5)
+    ref = torch.nn.functional.gelu(ln.to(torch.bfloat16).double()).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(z, ref)
+
+
+# ---------------------------------------------------------------- the pages' figures
+
+def test_workload_shapes_reproduce_the_pages_byte_counts():
+    s = synth.QWEN2_5_1_5B
+    vals = {}
+    for key, value, _unit, digits, *_where in _golden("qwen2_5_1_5b_bytes.txt"):
+        vals[key] = (float(value), int(digits))
+
+    def close(x, key):
+        v, d = vals[key]
+        if d == 0:
+            return x == v
+        return abs(x - v) <= 0.5 * 10 ** (math.floor(math.log10(v)) - d + 1)
+
+    assert close(s.chain_weight_bytes(), "chain_weight_bytes")
+    assert close(s.lm_head_bytes(), "lm_head_bytes")
+    assert close(2 * s.kv_dim * s.hidden, "kv_proj_bytes")
+    assert close(7 * s.layers + 1, "gemv_count")
+    assert close(s.vocab, "lm_head_rows") and close(s.hidden, "lm_head_cols")
