@@ -1,0 +1,343 @@
+/*
+ * wsgemv.h -- C ABI of libwsgemv.so: the BF16 weight-streaming decode chain
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  At decode batch 1..16 every linear layer of a Llama-style
+ * model is a matrix-vector product: y[b][m] = sum_k W[m][k] * x[b][k], BF16
+ * weights and activations, FP32 accumulation ("One Token, Kernel by Kernel: A
+ * Decode Step on a Laptop GPU", Step 1, "What one block launches").  The
+ * library streams each weight matrix from HBM exactly once per call, fuses
+ * the RMSNorm in front ("GPU Kernel Optimization", Architecture) and the
+ * SwiGLU, residual, bias+GELU or argmax after, and replays whole decode
+ * chains in one CUDA graph while a side stream prefetches the next op's
+ * weights into L2 ("Making small PyTorch ops faster on a laptop GPU",
+ * "Prefetching the next layer while this one runs" and "Measuring instead of
+ * predicting").
+ *
+ * Conventions for every call:
+ *  - Pointers named W*, x, h, y, gamma, beta, bias, s, z, idx, logits and
+ *    workspace are DEVICE pointers owned by the caller; the library never
+ *    frees them.  Host pointers appear only where a name ends in _host.
+ *  - bf16/fp16 tensors are passed as void* to their 16-bit patterns.
+ *  - Layouts are row-major: W is [M][K] (a linear layer's weight[out][in],
+ *    K contiguous); x is [B][K]; outputs are [B][M].
+ *  - Device pointers must be 16-byte aligned, K a multiple of 8 and
+ *    1 <= B <= 16; otherwise WS_ERR_ALIGN / WS_ERR_SHAPE is returned and
+ *    nothing is launched.  There is no fallback path of any kind.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  A launch error is returned as WS_ERR_CUDA.
+ *  - Every GEMV-family call takes an optional workspace (device memory, may be
+ *    NULL).  It enables split-K, which the schedule uses for skinny shapes
+ *    and needs when B * K is too large for the activations to sit in shared
+ *    memory (then a NULL workspace gives WS_ERR_ARG).  Size it with
+ *    ws_workspace_bytes().
+ *  - A workspace must be zero-filled before its first use; the library
+ *    leaves it zeroed again after every successful call, so one workspace
+ *    serves any number of calls ordered on one stream.  Calls that share a
+ *    workspace must not overlap in time.
+ *  - Device-side waits are bounded; a wait that runs out sets a device error
+ *    flag read by ws_device_error() and the kernel returns.
+ *  - No exception crosses the ABI.  ws_last_error() gives a thread-local
+ *    message for the last failing call.
+ */
+#ifndef WSGEMV_H
+#define WSGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WS_OK = 0,
+  WS_ERR_ARG = -1,      /* null pointer, bad enum, workspace too small       */
+  WS_ERR_ALIGN = -2,    /* a device pointer not 16-byte aligned              */
+  WS_ERR_SHAPE = -3,    /* K % 8 != 0, B outside 1..16, sizes <= 0           */
+  WS_ERR_CUDA = -4,     /* a CUDA runtime call failed                        */
+  WS_ERR_TIMEOUT = -5,  /* a bounded device wait ran out                     */
+  WS_ERR_NOMEM = -6,    /* the chain could not allocate its own buffers      */
+  WS_ERR_STATE = -7     /* chain call out of order (e.g. run before capture) */
+} ws_status;
+
+typedef void *ws_stream_t; /* a cudaStream_t */
+
+enum { WS_DTYPE_F32 = 0, WS_DTYPE_BF16 = 1, WS_DTYPE_F16 = 2 };
+
+/* ------------------------------------------------------------------------
+ * GEMV family.  All accumulate in fp32; the activations the dot products read
+ * are bf16 (a normalisation prologue rounds its output to bf16 once).
+ * ---------------------------------------------------------------------- */
+
+/* y[b][m] = sum_k W[m][k] x[b][k].  W bf16 [M][K], x bf16 [B][K], y fp32
+ * [B][M].  A workspace enables split-K for skinny shapes such as the
+ * 256 x 1536 K/V projections, which lose bandwidth as one short kernel ("One
+ * Token, Kernel by Kernel", Step 2, "The GEMVs, through Nsight Compute");
+ * size it with ws_workspace_bytes(WS_OP_GEMV, M, K, B).  Split partials are
+ * summed in a fixed order, so results do not depend on timing. */
+ws_status ws_gemv_bf16(const void *W, const void *x, float *y, int M, int K, int B,
+                       void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* h_out[b][m] = h_in[b][m] + sum_k W[m][k] x[b][k]: the residual add of a
+ * decoder block folded into the GEMV's epilogue ("One Token, Kernel by
+ * Kernel", Step 1, "What one block launches").  x bf16 [B][K]; h_in, h_out
+ * fp32 [B][M]; h_in may equal h_out (in place) or be NULL (= h_out). */
+ws_status ws_gemv_residual(const void *W, const void *x, const float *h_in, float *h_out,
+                           int M, int K, int B, void *workspace, size_t workspace_bytes,
+                           ws_stream_t stream);
+
+/* y = bf16(RMSNorm(x, gamma)) . W^T with RMSNorm(x) = x / sqrt(mean_k x^2 + eps)
+ * * gamma per row ("GPU Kernel Optimization", Architecture: mean square,
+ * rsqrt and weight multiply in one kernel).  x fp32 or bf16 [B][K]
+ * (x_dtype), gamma bf16 [K], y fp32 [B][M]. */
+ws_status ws_rmsnorm_gemv(const void *x, int x_dtype, const void *gamma, const void *W,
+                          float *y, int M, int K, int B, float eps,
+                          void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* Merged Q/K/V projection in one launch: a = bf16(RMSNorm(x, gamma));
+ * q = a.Wq^T [B][Mq], k = a.Wk^T [B][Mkv], v = a.Wv^T [B][Mkv], all fp32.
+ * One launch instead of three removes the small-GEMV loss ("One Token, Kernel
+ * by Kernel", "In the real world": merged QKV projections). */
+ws_status ws_qkv_gemv(const void *x, int x_dtype, const void *gamma,
+                      const void *Wq, const void *Wk, const void *Wv,
+                      float *q, float *k, float *v, int Mq, int Mkv, int K, int B,
+                      float eps, void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* SwiGLU MLP front half in one pass over Wg and Wu:
+ * m = bf16(RMSNorm(x, gamma)) (or m = x when gamma is NULL; x must then be
+ * bf16); s = bf16(silu(m.Wg^T) * (m.Wu^T)) with silu(g) = g / (1 + exp(-g)).
+ * Wg, Wu bf16 [M][K]; s bf16 [B][M] ("One Token, Kernel by Kernel", Step 1,
+ * "The setup": SwiGLU MLP). */
+ws_status ws_swiglu_gemv(const void *x, int x_dtype, const void *gamma,
+                         const void *Wg, const void *Wu, void *s,
+                         int M, int K, int B, float eps,
+                         void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* z = bf16(gelu(bf16(bf16(LayerNorm(x)) . W^T + bias))), exact-erf GELU,
+ * biased variance: one LayerNorm -> Linear -> GELU block in bf16 ("Making
+ * small PyTorch ops faster on a laptop GPU", "Beyond language models").
+ * x bf16 [B][K]; gamma, beta bf16 [K]; W bf16 [M][K]; bias bf16 [M];
+ * z bf16 [B][M]. */
+ws_status ws_ln_gemv_gelu(const void *x, const void *gamma, const void *beta,
+                          const void *W, const void *bias, void *z,
+                          int M, int K, int B, float eps,
+                          void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* LM head with a fused argmax: logits = bf16(RMSNorm(h, gamma)) . W^T and
+ * idx[b] = the lowest j with logits[b][j] == max_j logits[b][j] ("One Token,
+ * Kernel by Kernel", "The whole step": LM head 151,936 x 1,536, then an
+ * argmax over the logits).  h fp32 or bf16 [B][K] (h_dtype); idx int32 [B];
+ * logits fp32 [B][V] or NULL.  Workspace required:
+ * ws_workspace_bytes(WS_OP_LMHEAD_ARGMAX, V, K, B). */
+ws_status ws_lmhead_argmax(const void *h, int h_dtype, const void *gamma, const void *W,
+                           int32_t *idx, float *logits, int V, int K, int B, float eps,
+                           void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* idx[r] = the lowest j with v[r][j] == max_j v[r][j] for fp32 rows
+ * [rows][cols] ("One Token, Kernel by Kernel", "The whole step").  Workspace
+ * required: ws_workspace_bytes(WS_OP_ARGMAX_ROWS, rows, cols, 1). */
+ws_status ws_argmax_rows(const float *logits, int32_t *idx, int rows, int cols,
+                         void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
+/* Standalone RMSNorm of [R][N] rows, fp16 or bf16 in and out (dtype), gamma of
+ * the same dtype: y = x / sqrt(mean x^2 + eps) * gamma computed in fp32 and
+ * rounded once ("GPU Kernel Optimization", Architecture: one program per
+ * row).  N must be a multiple of 8. */
+ws_status ws_rmsnorm(const void *x, const void *gamma, void *y, int R, int N, int dtype,
+                     float eps, ws_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * L2 prefetch ("Making small PyTorch ops faster on a laptop GPU",
+ * "Prefetching the next layer while this one runs"): a small kernel asks L2
+ * to fetch `bytes` starting at `ptr` and never writes memory, so every result
+ * of the ops around it stays bit-identical.
+ * ---------------------------------------------------------------------- */
+enum {
+  WS_PREFETCH_NONE = 0,
+  WS_PREFETCH_L2 = 1,            /* prefetch.global.L2 every stride_bytes         */
+  WS_PREFETCH_L2_EVICT_LAST = 2, /* prefetch.global.L2::evict_last every stride   */
+  WS_PREFETCH_BULK = 3           /* cp.async.bulk.prefetch.L2, stride_bytes chunks */
+};
+
+typedef struct {
+  int blocks;       /* CTAs of the prefetch kernel                         */
+  int threads;      /* threads per CTA                                     */
+  int stride_bytes; /* bytes between prefetches / bytes per bulk prefetch  */
+  int mode;         /* WS_PREFETCH_*                                       */
+} ws_prefetch_plan;
+
+/* Enqueue one prefetch kernel over [ptr, ptr + bytes).  mode NONE (or
+ * bytes == 0) enqueues nothing.  BULK needs ptr 16-byte aligned and
+ * stride_bytes a multiple of 16. */
+ws_status ws_l2_prefetch(const void *ptr, size_t bytes, ws_prefetch_plan plan,
+                         ws_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Chain executor: a block list replayed as one CUDA graph.
+ * ---------------------------------------------------------------------- */
+enum { WS_BLOCK_QWEN = 1, WS_BLOCK_MLP = 2, WS_BLOCK_HEAD = 3 };
+
+/* One decoder block of a Llama-style model at decode ("One Token, Kernel by
+ * Kernel", Step 1): a = bf16(RMSNorm(h, gamma1)); q,k,v = a.W{q,k,v}^T;
+ * h += attn.Wo^T; m = bf16(RMSNorm(h, gamma2)); s = bf16(silu(m.Wg^T) *
+ * m.Wu^T); h += s.Wd^T.  The attention itself is outside this library: its
+ * output is supplied in `attn` (bf16 [B][H]). */
+typedef struct {
+  const void *gamma1, *Wq, *Wk, *Wv, *Wo, *gamma2, *Wg, *Wu, *Wd; /* bf16 */
+  const void *attn;      /* bf16 [B][H]                                  */
+  float *q, *k, *v;      /* fp32 [B][H], [B][KV], [B][KV]; NULL: internal */
+} ws_qwen_block;
+
+/* z = bf16(gelu(bf16(bf16(LayerNorm(x)) . W^T + bias))) ("Making small
+ * PyTorch ops faster on a laptop GPU", "Beyond language models"). */
+typedef struct {
+  const void *gamma, *beta, *W, *bias; /* bf16 [w], [w], [w][w], [w] */
+} ws_mlp_block;
+
+/* Final RMSNorm, LM head and argmax ("One Token, Kernel by Kernel", "The
+ * whole step"). */
+typedef struct {
+  const void *gamma;  /* bf16 [H]            */
+  const void *W;      /* bf16 [V][H]         */
+  int32_t *idx;       /* int32 [B]           */
+  float *logits;      /* fp32 [B][V] or NULL */
+} ws_head_block;
+
+typedef struct {
+  int kind; /* WS_BLOCK_* */
+  union {
+    ws_qwen_block qwen;
+    ws_mlp_block mlp;
+    ws_head_block head;
+  } u;
+} ws_block_desc;
+
+typedef struct {
+  int batch;        /* B, 1..16                                             */
+  int hidden;       /* H (Qwen) or width (MLP)                              */
+  int kv_dim;       /* K/V projection rows (Qwen)                           */
+  int inter;        /* MLP rows I (Qwen)                                    */
+  int vocab;        /* LM head rows V (head block)                          */
+  float eps;        /* RMSNorm / LayerNorm epsilon                          */
+  /* Qwen chains: the residual stream.  The first block reads h_in (fp32
+   * [B][H], read-only) and every block updates h_out (fp32 [B][H]), so each
+   * replay starts again from h_in. */
+  const float *h_in;
+  float *h_out;
+  /* MLP chains: x_in bf16 [B][w] (read-only) and the chain output y_out bf16
+   * [B][w]. */
+  const void *x_in;
+  void *y_out;
+  /* Optional: fp32 [L][B][H] copy of h after every Qwen block (per-block
+   * checks; adds one copy per block to the graph). */
+  float *h_trace;
+  int use_pdl;          /* 1: programmatic dependent launch between ops      */
+  int prefetch;         /* 0 off, 1 tuned plans, 2 fixed_plan for every op   */
+  ws_prefetch_plan fixed_plan;
+  int distance;         /* prefetch op i + distance while op i runs (>= 1)   */
+  int decoy;            /* 1: aim each prefetch at the wrong op (control)    */
+  int tune_pairs;       /* paired replays per candidate (>= 8)               */
+  float tune_min_gain;  /* keep a plan only if the 95% CI lower bound of its
+                           relative gain exceeds this (e.g. 0.01)            */
+} ws_chain_opts;
+
+typedef struct ws_chain ws_chain;
+
+ws_status ws_chain_create(const ws_block_desc *blocks, int n, const ws_chain_opts *opts,
+                          ws_chain **out);
+/* Measure prefetch plans per distinct op shape on throwaway weights and keep
+ * the best only if its 95% confidence interval clears the minimum gain
+ * ("Making small PyTorch ops faster on a laptop GPU", "Measuring instead of
+ * predicting").  Blocks the calling thread; uses `stream`. */
+ws_status ws_chain_tune(ws_chain *c, ws_stream_t stream);
+/* Capture the chain: all ops on the main branch, each prefetch on a side
+ * branch forked before op i and joined at the end, as one graph. */
+ws_status ws_chain_capture(ws_chain *c, ws_stream_t stream);
+/* One decode step: one cudaGraphLaunch. */
+ws_status ws_chain_run(ws_chain *c, ws_stream_t stream);
+/* The same ops launched one by one without a graph (no prefetch). */
+ws_status ws_chain_run_eager(ws_chain *c, ws_stream_t stream);
+/* One decode step from HOST buffers: copies in_host (Qwen: fp32 [B][H] to
+ * h_in; MLP: bf16 [B][w] to x_in) and, if not NULL, attn_host (bf16
+ * [L][B][H], block order) to the chain's device inputs, replays the graph,
+ * copies the result (head: int32 idx [B]; MLP: bf16 [B][w]) to out_host and
+ * waits for the stream. */
+ws_status ws_chain_step_host(ws_chain *c, const void *in_host, const void *attn_host,
+                             void *out_host, ws_stream_t stream);
+int ws_chain_num_ops(const ws_chain *c);
+/* Plan and measured gain (95% CI lower bound, mean) of each op; n entries. */
+ws_status ws_chain_plans(const ws_chain *c, ws_prefetch_plan *plans, float *gain_lo,
+                         float *gain_mean, int n);
+/* Weight bytes each op streams (its algorithmic bytes); n entries. */
+ws_status ws_chain_op_bytes(const ws_chain *c, size_t *bytes, int n);
+void ws_chain_destroy(ws_chain *c);
+
+/* ------------------------------------------------------------------------
+ * Sizing, errors, tuning knobs and measurement kernels.
+ * ---------------------------------------------------------------------- */
+enum {
+  WS_OP_GEMV = 1,           /* ws_gemv_bf16, ws_gemv_residual, ws_rmsnorm_gemv,
+                               ws_ln_gemv_gelu: M rows                          */
+  WS_OP_SWIGLU_GEMV = 2,    /* ws_swiglu_gemv: M rows of each of Wg, Wu         */
+  WS_OP_QKV_GEMV = 3,       /* ws_qkv_gemv: M = Mq + 2 * Mkv                    */
+  WS_OP_LMHEAD_ARGMAX = 4,  /* ws_lmhead_argmax: M = V                          */
+  WS_OP_ARGMAX_ROWS = 5     /* ws_argmax_rows: M = rows, K = cols               */
+};
+
+/* Workspace bytes an op's schedule uses on the current device (0: none). */
+size_t ws_workspace_bytes(int op, int M, int K, int B);
+
+const char *ws_last_error(void);
+
+/* Device error flag of the current device (nonzero after a bounded wait ran
+ * out); reset != 0 clears it.  Synchronises the device.  Returns -1 if the
+ * flag cannot be read. */
+int ws_device_error(int reset);
+
+typedef struct {
+  int ring_bytes;      /* shared-memory weight ring per CTA (default 96 KiB)  */
+  int grid_cap;        /* max CTAs per GEMV launch (0: one per SM)            */
+  int force_ksplit;    /* K splits (0: heuristic)                             */
+  int force_kg;        /* warps per row, 1/2/4/8 (0: heuristic)               */
+  int evict_first;     /* stream weights with an L2 evict-first hint          */
+  unsigned long long timeout_ns; /* bound of every device wait                */
+} ws_tuning;
+
+void ws_get_tuning(ws_tuning *t);
+ws_status ws_set_tuning(const ws_tuning *t);
+
+/* Schedule a GEMV launch would use (for tests and reports). */
+typedef struct {
+  int KG, RS, S, KS, NS, stage_bytes, RG, units, grid, smem_bytes;
+} ws_gemv_schedule;
+ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind,
+                       int epilogue_kind, int allow_split, ws_gemv_schedule *out);
+
+/* Every bulk copy the producer of CTA `cta` would issue for a one-segment
+ * GEMV of the given shape, as (source byte offset from the first matrix --
+ * the second matrix of a pair counts from M*K*2 --, destination byte offset
+ * into the CTA's ring, bytes) triples.  Returns the count (host only). */
+long ws_debug_gemv_copies(int M, int K, int B, int nmat, int allow_split, int cta,
+                          long long *triples, long max_triples);
+
+/* Read-only streaming kernel over [ptr, ptr + bytes): a read-roofline probe.
+ * Writes one checksum per CTA into sink (uint32 [blocks]). */
+ws_status ws_read_probe(const void *ptr, size_t bytes, int blocks, uint32_t *sink,
+                        ws_stream_t stream);
+/* An empty kernel (touch = 0), or one that makes one global-memory round trip
+ * (touch = 1), for the launch-latency floor. */
+ws_status ws_empty_probe(int touch, const uint32_t *ptr, uint32_t *sink, ws_stream_t stream);
+
+/* Test hook for the bounded waits: one CTA waits on an mbarrier that nothing
+ * arrives on, for timeout_ns, then records the time-out in the device error
+ * flag and returns. */
+ws_status ws_test_bounded_wait(unsigned long long timeout_ns, ws_stream_t stream);
+
+const char *ws_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WSGEMV_H */

@@ -1,0 +1,133 @@
+// ws_common.cuh -- definitions shared by the library's translation units.
+//
+// The streaming GEMV computes y[b][m] = sum_k W[m][k] * x[b][k] with bf16 W and
+// x and fp32 accumulation ("One Token, Kernel by Kernel: A Decode Step on a
+// Laptop GPU", Step 1, "What one block launches"), with an optional
+// normalisation prologue and a per-output epilogue.
+//
+// Work decomposition.  The rows of up to three weight matrices ("segments",
+// e.g. Q, K and V) are cut into row groups of RS rows; each row group may be
+// cut along K into S splits of KS columns.  A unit is one (split, row group)
+// pair; units are numbered split-major and handed out to the CTAs in
+// contiguous, balanced ranges.  Inside a CTA a producer warp streams each
+// unit's weight rows into a ring of shared-memory stages with bulk async
+// copies; 8 consumer warps reduce them against the activations, which sit in
+// shared memory as bf16.  The KG warps that share one row each take a
+// contiguous slice of its 16-byte chunks.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ws {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kMaxSeg = 3;
+constexpr int kMaxStages = 16;
+constexpr int kMaxBatch = 16;
+
+enum Prologue { PRO_NONE = 0, PRO_RMSNORM = 1, PRO_LAYERNORM = 2 };
+enum Epilogue {
+  EPI_F32 = 0,        // out fp32 = acc
+  EPI_BF16 = 1,       // out bf16 = acc
+  EPI_RESID = 2,      // out fp32 = res_in + acc (res_in may be out itself)
+  EPI_BIAS_GELU = 3,  // out bf16 = gelu(bf16(acc + bias))
+  EPI_SWIGLU = 4,     // out bf16 = silu(acc_gate) * acc_up
+  EPI_ARGMAX = 5      // optional fp32 logits; per-row argmax over all outputs
+};
+enum DType { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
+enum DeviceError { DERR_TIMEOUT = 1 };
+
+struct Seg {
+  const uint16_t* W0;  // bf16 [M][K]
+  const uint16_t* W1;  // second matrix read in lockstep (SwiGLU up), or null
+  void* out;           // [B][M]
+  int M;
+  int rg_begin;        // first row group of this segment (all segments)
+  int row_base;        // first row of this segment in the concatenated rows
+};
+
+struct Sched {
+  int KG;           // consumer warps sharing one row
+  int RS;           // rows per stage = kConsumerWarps / KG
+  int S;            // K splits across units
+  int KS;           // columns per split
+  int NS;           // ring stages
+  int stage_bytes;  // bytes of one ring stage
+  int RG;           // row groups, all segments
+  int units;        // RG * S
+  int grid;         // CTAs
+  int BT;           // batch the kernel is instantiated for (>= B)
+  int smem_bytes;
+  int off_bar, off_flags, off_stats, off_arg, off_red, off_xs, off_ring;
+};
+
+struct GemvParams {
+  Seg seg[kMaxSeg];
+  int nseg;
+  int nmat;  // 1, or 2 for a gate/up pair
+  int K, B, M_total;
+  const void* x;
+  int x_dtype;
+  int prologue;
+  const uint16_t* gamma;
+  const uint16_t* beta;
+  float eps;
+  int epilogue;
+  const uint16_t* bias;
+  const float* res_in;
+  int* argmax_idx;
+  float* logits;
+  // workspace (split-K partials and tickets, argmax partials)
+  float* part;
+  unsigned* tickets;
+  float* arg_val;
+  int* arg_idx;
+  unsigned* arg_ticket;
+  int* err;
+  unsigned long long timeout_ns;
+  int evict_first;
+  Sched sc;
+};
+
+__host__ __device__ inline void cta_units(int cta, int grid, int units, int& u0, int& u1) {
+  u0 = (int)((long long)cta * units / grid);
+  u1 = (int)((long long)(cta + 1) * units / grid);
+}
+
+__host__ __device__ inline void decode_unit(const GemvParams& p, int u, int& seg, int& rg,
+                                            int& ks) {
+  ks = u / p.sc.RG;
+  const int g = u - ks * p.sc.RG;
+  seg = 0;
+  while (seg + 1 < p.nseg && g >= p.seg[seg + 1].rg_begin) ++seg;
+  rg = g - p.seg[seg].rg_begin;
+}
+
+struct Tuning {
+  int ring_bytes;    // shared-memory ring budget per CTA
+  int grid_cap;      // max CTAs (0: one per SM)
+  int force_ksplit;  // 0: heuristic
+  int force_kg;      // 0: heuristic
+  int evict_first;   // weights streamed with an L2 evict-first policy
+  unsigned long long timeout_ns;
+};
+
+// Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.
+Tuning& tuning();
+int device_sm_count();
+int* device_error_ptr();
+void set_error(const char* fmt, ...);
+bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len);
+size_t workspace_layout(const GemvParams& p, size_t* off_tickets, size_t* off_part,
+                        size_t* off_argv, size_t* off_argi, size_t* off_argt);
+bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes);
+bool prepare_gemv(const GemvParams& p);
+cudaError_t launch_gemv(const GemvParams& p, cudaStream_t stream, bool pdl);
+void init_gemv_params(GemvParams& p, int K, int B);
+size_t argmax_rows_workspace(int rows, int cols);
+
+}  // namespace ws
