@@ -1,0 +1,57 @@
+"""Shared helpers for the tests: device transfer of bit patterns and the
+comparison metrics (fp32: |g - r| / max(|r|, rms(r)) <= 2e-3 per row; bf16 and
+fp16: at most 1 unit in the last place)."""
+import numpy as np
+import torch
+
+FP32_TOL = 2e-3
+ULP_TOL = 1
+
+
+def dev_bf16(bits, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def dev_fp16(bits, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.float16).to(device)
+
+
+def dev_f32(a, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def host_bits(t) -> np.ndarray:
+    """uint16 bit patterns of a bf16/fp16 tensor."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def rel_err_rows(got, ref) -> float:
+    """max_i |g_i - r_i| / max(|r_i|, rms(r_row)) over every row."""
+    got = np.asarray(got, np.float64).reshape(-1, np.asarray(ref).shape[-1])
+    ref = np.asarray(ref, np.float64).reshape(got.shape)
+    rms = np.sqrt(np.mean(ref * ref, axis=1, keepdims=True))
+    scale = np.maximum(np.abs(ref), np.maximum(rms, 1e-30))
+    return float(np.max(np.abs(got - ref) / scale))
+
+
+def _ordered(bits):
+    b = np.asarray(bits, np.uint16).astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def ulp_dist(a_bits, b_bits) -> np.ndarray:
+    """Distance in units in the last place between two 16-bit float patterns."""
+    return np.abs(_ordered(a_bits) - _ordered(b_bits))
+
+
+def assert_fp32(got, ref, tol=FP32_TOL, what=""):
+    e = rel_err_rows(got, ref)
+    assert e <= tol, f"{what}: max relative error {e:.3g} > {tol}"
+    return e
+
+
+def assert_ulp(got_bits, ref_bits, tol=ULP_TOL, what=""):
+    d = ulp_dist(got_bits, ref_bits)
+    assert int(d.max()) <= tol, f"{what}: {int((d > tol).sum())} elements beyond {tol} ulp (max {int(d.max())})"
+    return int(d.max())

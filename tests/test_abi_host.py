@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and exports
+every function include/wsgemv.h declares; argument validation rejects bad
+calls before anything is launched; every bulk copy the GEMV schedule issues
+stays inside its source matrix and its ring stage, is 16-byte aligned, and the
+copies of all CTAs cover every weight byte exactly once."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from weight_streaming_gemv_bf16_gb300 import binding as wb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from weight_streaming_gemv_bf16_gb300 import _build
+    _build.build()
+    return wb.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "wsgemv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(ws_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 30
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_is_built_for_sm_103a(lib):
+    assert "sm_103a" in wb.version()
+
+
+# fake device addresses: the validation fails before any of them is touched
+A = 0x7F0000000000
+MIS = A + 8
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A, A, A, 64, 12, 1), -3),     # K % 8 != 0
+    ((A, A, A, 64, 16, 0), -3),     # B = 0
+    ((A, A, A, 64, 16, 17), -3),    # B > 16
+    ((A, A, A, 0, 16, 1), -3),      # M = 0
+    ((None, A, A, 64, 16, 1), -1),  # null W
+    ((MIS, A, A, 64, 16, 1), -2),   # misaligned W
+    ((A, MIS, A, 64, 16, 1), -2),   # misaligned x
+])
+def test_gemv_argument_validation(lib, args, status):
+    W, x, y, M, K, B = args
+    assert lib.ws_gemv_bf16(W, x, y, M, K, B, None, 0, None) == status
+    assert lib.ws_last_error()
+
+
+def test_other_entry_points_validate(lib):
+    assert lib.ws_rmsnorm_gemv(A, 7, A, A, A, 64, 16, 1, 1e-6, None, 0, None) == -1  # dtype
+    assert lib.ws_swiglu_gemv(A, 0, None, A, A, A, 64, 16, 1, 1e-6, None, 0, None) == -1  # fp32 w/o norm
+    assert lib.ws_lmhead_argmax(A, 0, A, A, A, None, 64, 16, 1, 1e-6, None, 0, None) == -1  # no workspace
+    assert lib.ws_argmax_rows(A, A, 0, 10, A, 4096, None) == -3
+    assert lib.ws_argmax_rows(A, A, 2, 10, A, 1, None) == -1  # workspace too small
+    assert lib.ws_rmsnorm(A, A, A, 4, 12, 2, 1e-6, None) == -3
+    assert lib.ws_rmsnorm(A, A, A, 4, 16, 5, 1e-6, None) == -1
+    bad = wb.PrefetchPlan(0, 256, 128, 1)
+    assert lib.ws_l2_prefetch(A, 4096, bad, None) == -1
+    bulk = wb.PrefetchPlan(4, 256, 100, 3)
+    assert lib.ws_l2_prefetch(A, 4096, bulk, None) == -2
+    none = wb.PrefetchPlan(0, 0, 0, 0)
+    assert lib.ws_l2_prefetch(A, 4096, none, None) == 0  # enqueues nothing
+    assert lib.ws_test_bounded_wait(0, None) == -1
+    t = wb.Tuning(96 * 1024, 0, 0, 0, 1, 0)
+    assert lib.ws_set_tuning(wb.ctypes.byref(t)) == -1
+
+
+def test_chain_create_rejects_bad_block_lists(lib):
+    opts = wb.ChainOpts(batch=1, hidden=64, kv_dim=16, inter=128, vocab=100, eps=1e-6,
+                        h_in=A, h_out=A + 4096)
+    head = wb.BlockDesc(kind=wb.BLOCK_HEAD)
+    head.u.head = wb.HeadBlock(A, A, A, None)
+    mlp = wb.BlockDesc(kind=wb.BLOCK_MLP)
+    mlp.u.mlp = wb.MlpBlock(A, A, A, A)
+    h = wb.P()
+    two = (wb.BlockDesc * 2)(head, mlp)  # head must be last and alone with MLP
+    assert lib.ws_chain_create(two, 2, wb.ctypes.byref(opts), wb.ctypes.byref(h)) == -1
+    one = (wb.BlockDesc * 1)(wb.BlockDesc(kind=9))
+    assert lib.ws_chain_create(one, 1, wb.ctypes.byref(opts), wb.ctypes.byref(h)) == -1
+    opts.batch = 0
+    one = (wb.BlockDesc * 1)(head)
+    assert lib.ws_chain_create(one, 1, wb.ctypes.byref(opts), wb.ctypes.byref(h)) == -3
+
+
+SHAPES = [
+    # (M, K, B, nmat, allow_split)
+    (256, 256, 1, 1, False),      # fused RMSNorm + GEMV config
+    (2048, 1536, 1, 1, False),    # merged QKV rows
+    (1536, 1536, 1, 1, True),     # Wo
+    (8960, 1536, 1, 2, False),    # gate/up pair
+    (1536, 8960, 1, 1, True),     # Wd
+    (256, 1536, 1, 1, True),      # K/V projection: split-K
+    (256, 1536, 16, 1, True),
+    (1536, 8960, 16, 1, True),    # activations too big: split needed
+    (8960, 1536, 8, 2, True),
+    (151936, 1536, 1, 1, False),  # LM head
+    (768, 768, 16, 1, True),      # MLP chain block
+    (37, 40, 3, 1, True),         # ragged tiny
+    (1, 8, 1, 1, True),           # minimal
+    (1000, 264, 5, 2, True),
+]
+
+
+@pytest.mark.parametrize("M,K,B,nmat,split", SHAPES)
+def test_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, split):
+    sc = wb.gemv_plan(M, K, B, nmat=nmat, allow_split=split)
+    assert sc["smem_bytes"] <= 227 * 1024
+    assert 2 <= sc["NS"] <= 16
+    assert sc["stage_bytes"] % 128 == 0
+    assert sc["grid"] <= sc["units"]
+    assert sc["KS"] * sc["S"] == K and sc["KS"] % 8 == 0
+    covered = np.zeros(nmat * M * K * 2 // 16, np.int32)
+    for cta in range(sc["grid"]):
+        per_slot = {}
+        for src, dst, n in wb.debug_gemv_copies(M, K, B, nmat, split, cta):
+            assert n > 0 and n % 16 == 0 and src % 16 == 0 and dst % 16 == 0
+            assert 0 <= src and src + n <= nmat * M * K * 2
+            # a copy never crosses from one matrix of a pair into the other
+            assert src // (M * K * 2) == (src + n - 1) // (M * K * 2)
+            slot, off = divmod(dst, sc["stage_bytes"])
+            assert slot < sc["NS"] and off + n <= sc["stage_bytes"]
+            covered[src // 16:(src + n) // 16] += 1
+            per_slot.setdefault(slot, 0)
+            per_slot[slot] += 1
+    assert covered.min() == 1 and covered.max() == 1
+
+
+def test_workspace_sizes(lib):
+    assert wb.workspace_bytes(wb.OP_GEMV, 1536, 1536, 1) == 0  # no split needed
+    assert wb.workspace_bytes(wb.OP_GEMV, 256, 1536, 1) > 0    # skinny: split
+    assert wb.workspace_bytes(wb.OP_LMHEAD_ARGMAX, 151936, 1536, 1) > 0
+    assert wb.workspace_bytes(wb.OP_ARGMAX_ROWS, 16, 151936, 1) > 0
+    assert wb.workspace_bytes(wb.OP_GEMV, 1536, 8960, 16) > 0  # activations need a split
