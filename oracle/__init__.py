@@ -220,14 +220,17 @@ def rmsnorm_gemv(x, gamma, W_bits, eps: float, threads: int = 1) -> np.ndarray:
     return gemv(W_bits, a, threads)
 
 
-def swiglu_gemv(x, gamma, Wg_bits, Wu_bits, eps: float, threads: int = 1) -> np.ndarray:
+def swiglu_gemv(x, gamma, Wg_bits, Wu_bits, eps: float, threads: int = 1,
+                exact: bool = False) -> np.ndarray:
     """s = bf16(silu(m.Wg^T) * (m.Wu^T)), m = bf16(RMSNorm(x)) or x when gamma is None.
 
-    Returns the bf16 bit patterns of s."""
+    Returns the bf16 bit patterns of s, or with exact=True the value of s
+    before its final rounding (double)."""
     m = x if gamma is None else round_bf16(rmsnorm(x, gamma, eps))
     g = gemv(Wg_bits, m, threads)
     u = gemv(Wu_bits, m, threads)
-    return f64_to_bf16(swiglu(g, u))
+    s = swiglu(g, u)
+    return s if exact else f64_to_bf16(s)
 
 
 def lmhead_logits(h, gamma, Wlm_bits, eps: float, threads: int = 1) -> np.ndarray:
@@ -281,14 +284,17 @@ def qwen_chain(h0, blocks, attns, gamma_f, Wlm_bits, eps: float,
     return {"h": h, "logits": logits, "idx": idx, "blocks": per_block}
 
 
-def mlp_block(x_bits, blk: dict, eps: float = 1e-5, threads: int = 1) -> np.ndarray:
+def mlp_block(x_bits, blk: dict, eps: float = 1e-5, threads: int = 1,
+              exact: bool = False) -> np.ndarray:
     """bf16 LayerNorm -> Linear(+bias) -> GELU, each module's output rounded to bf16.
 
-    Returns the bf16 bits of z = bf16(gelu(bf16(bf16(LN(x)).W^T + b)))."""
+    Returns the bf16 bits of z = bf16(gelu(bf16(bf16(LN(x)).W^T + b))), or with
+    exact=True the value of gelu(...) before its final rounding (double)."""
     x = bf16_to_f64(x_bits)
     a = round_bf16(layernorm(x, bf16_to_f64(blk["gamma"]), bf16_to_f64(blk["beta"]), eps))
     y = round_bf16(gemv(blk["W"], a, threads) + bf16_to_f64(blk["b"])[None, :])
-    return f64_to_bf16(gelu(y))
+    z = gelu(y)
+    return z if exact else f64_to_bf16(z)
 
 
 def mlp_chain(x_bits, blocks, eps: float = 1e-5, threads: int = 1) -> np.ndarray:

@@ -1,0 +1,226 @@
+"""GPU parity of the chain executor (one CUDA graph per step) against the
+oracle: per-block teacher-forced checks through the h trace, end-to-end argmax
+where the oracle's top-2 margin exceeds the tolerance, bit-identity between
+graph/eager/PDL on/off and prefetch on/off/decoy, and the host-buffer step."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from weight_streaming_gemv_bf16_gb300 import binding as wb
+from weight_streaming_gemv_bf16_gb300 import chain as wc
+from weight_streaming_gemv_bf16_gb300 import synth
+from _util import (assert_bf16_close, assert_fp32, bf16_bits_to_f64, dev_bf16, dev_f32,
+                   host_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    assert wb.device_error(reset=True) == 0
+    yield
+    torch.cuda.synchronize()
+    assert wb.device_error() == 0
+
+
+SMALL = synth.QwenShape(hidden=256, kv_dim=64, inter=512, vocab=1000, layers=3)
+
+
+def _host_weights(shape, seed):
+    blocks = [synth.qwen_block_weights(shape, seed, l) for l in range(shape.layers)]
+    head = synth.qwen_head_weights(shape, seed)
+    return blocks, head
+
+
+def _dev(ws):
+    return {k: dev_bf16(v) for k, v in ws.items()}
+
+
+def _make(shape, B, seed, **kw):
+    blocks, head = _host_weights(shape, seed)
+    attn = np.stack([synth.qwen_attn(shape, B, seed, l) for l in range(shape.layers)])
+    h0 = synth.qwen_hidden(shape, B, seed)
+    ch = wc.qwen_chain([_dev(b) for b in blocks], _dev(head), dev_bf16(attn), dev_f32(h0), **kw)
+    return ch, blocks, head, attn, h0
+
+
+def _margin_ok(logits):
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    rms = np.sqrt(np.mean(logits * logits, axis=1))
+    return (top2[:, 1] - top2[:, 0]) > 2 * 2e-3 * np.maximum(np.abs(top2[:, 1]), rms)
+
+
+def _check_chain(ch, blocks, head, attn, h0, eps=1e-6):
+    """Teacher-forced per-block parity on the h trace, q/k/v of every block,
+    then the head on the GPU's final h, and the end-to-end oracle argmax."""
+    L = len(blocks)
+    trace = ch.h_trace.cpu().numpy().astype(np.float64)
+    h_prev = h0.astype(np.float64)
+    for l in range(L):
+        ref = oracle.qwen_block(h_prev, blocks[l], bf16_bits_to_f64(attn[l]), eps, threads=8)
+        assert_fp32(trace[l], ref["h"], what=f"block {l} h")
+        if ch.qkv:
+            for name, t in zip("qkv", ch.qkv[l]):
+                assert_fp32(t.cpu().numpy(), ref[name], what=f"block {l} {name}")
+        h_prev = trace[l]
+    assert np.array_equal(ch.h_out.cpu().numpy(), trace[-1].astype(np.float32))
+    logits = oracle.lmhead_logits(trace[-1], oracle.bf16_to_f64(head["gamma_f"]), head["Wlm"],
+                                  eps, threads=8)
+    got = ch.idx.cpu().numpy()
+    ok = _margin_ok(logits)
+    assert np.array_equal(got[ok], oracle.argmax_rows(logits)[ok])
+    if ch.logits is not None:
+        assert_fp32(ch.logits.cpu().numpy(), logits, what="logits")
+    # end to end from h0 (no teacher forcing): the argmax where the margin allows
+    full = oracle.qwen_chain(h0, blocks, [bf16_bits_to_f64(a) for a in attn], head["gamma_f"],
+                             head["Wlm"], eps, threads=8)
+    ok2 = _margin_ok(full["logits"])
+    assert np.array_equal(got[ok2], full["idx"][ok2])
+    assert_fp32(trace[-1], full["h"], what="final h end to end")
+    return int(ok2.sum())
+
+
+@pytest.mark.parametrize("B", [1, 3, 16])
+def test_small_chain_matches_oracle(B):
+    ch, blocks, head, attn, h0 = _make(SMALL, B, 21, trace=True, keep_qkv=True, logits=True)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    _check_chain(ch, blocks, head, attn, h0)
+
+
+def test_graph_eager_and_pdl_are_bit_identical():
+    B = 2
+    outs = []
+    for use_pdl, graph in ((True, True), (False, True), (True, False)):
+        ch, *_ = _make(SMALL, B, 22, use_pdl=use_pdl, trace=True, logits=True)
+        if graph:
+            ch.chain.capture()
+            for _ in range(3):
+                ch.run()  # replays start again from h_in
+        else:
+            ch.chain.run_eager()
+        torch.cuda.synchronize()
+        outs.append((ch.h_out.cpu(), ch.logits.cpu(), ch.idx.cpu(), ch.h_trace.cpu()))
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("mode,stride", [(1, 128), (2, 128), (3, 16384)])
+def test_prefetch_and_decoy_leave_outputs_bit_identical(mode, stride):
+    B = 1
+    base, *_ = _make(SMALL, B, 23, logits=True)
+    base.chain.capture()
+    base.run()
+    plan = wb.PrefetchPlan(8, 256, stride, mode)
+    for decoy in (False, True):
+        ch, *_ = _make(SMALL, B, 23, logits=True, prefetch=2, fixed_plan=plan, decoy=decoy)
+        ch.chain.capture()
+        ch.run()
+        ch.run()
+        torch.cuda.synchronize()
+        assert torch.equal(ch.h_out.cpu(), base.h_out.cpu())
+        assert torch.equal(ch.logits.cpu(), base.logits.cpu())
+        assert torch.equal(ch.idx.cpu(), base.idx.cpu())
+
+
+def test_tuner_measures_plans_and_keeps_bits():
+    B = 1
+    base, *_ = _make(SMALL, B, 24, logits=True)
+    base.chain.capture()
+    base.run()
+    ch, *_ = _make(SMALL, B, 24, logits=True, prefetch=1, tune_pairs=8)
+    ch.chain.tune()
+    plans = ch.chain.plans()
+    assert len(plans) == 4 * SMALL.layers + 1
+    for (mode, blocks, threads, stride), lo, mean in plans:
+        assert mode in (0, 1, 2, 3)
+        assert np.isfinite(lo) and np.isfinite(mean)
+        if mode:
+            assert lo > 0.01  # kept only when the CI lower bound clears +1%
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    assert torch.equal(ch.logits.cpu(), base.logits.cpu())
+
+
+def test_step_host_matches_device_run():
+    B = 4
+    ch, blocks, head, attn, h0 = _make(SMALL, B, 25)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    ref_idx = ch.idx.cpu().numpy().copy()
+    h_host = torch.from_numpy(h0).pin_memory()
+    attn_host = torch.from_numpy(attn.view(np.int16)).pin_memory()
+    out = torch.full((B,), -1, dtype=torch.int32).pin_memory()
+    ch.chain.step_host(h_host, attn_host, out)
+    assert np.array_equal(out.numpy(), ref_idx)
+    # new inputs through the host path change the answer the same way a device run does
+    h2 = (h0[::-1].copy())
+    ch.chain.step_host(torch.from_numpy(h2).pin_memory(), attn_host, out)
+    ch.h_in.copy_(torch.from_numpy(h2))
+    ch.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.numpy(), ch.idx.cpu().numpy())
+
+
+def test_one_full_size_block_matches_oracle():
+    """One Qwen2.5-1.5B-shaped block at batch 1 (hidden 1536, KV 256, MLP 8960)."""
+    shape = synth.QwenShape(layers=1)
+    ch, blocks, head, attn, h0 = _make(shape, 1, 0, trace=True, keep_qkv=True)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    ref = oracle.qwen_block(h0.astype(np.float64), blocks[0], bf16_bits_to_f64(attn[0]), 1e-6,
+                            threads=8)
+    for name, t in zip("qkv", ch.qkv[0]):
+        assert_fp32(t.cpu().numpy(), ref[name], what=name)
+    assert_fp32(ch.h_out.cpu().numpy(), ref["h"], what="h")
+
+
+def test_full_chain_28_blocks_matches_oracle():
+    """The full 28-block chain + final RMSNorm + LM head 151936 x 1536 + argmax,
+    batch 1, one CUDA graph: per-block teacher forcing and the end-to-end argmax."""
+    ch, blocks, head, attn, h0 = _make(synth.QWEN2_5_1_5B, 1, 0, trace=True, logits=True)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    eligible = _check_chain(ch, blocks, head, attn, h0)
+    assert eligible == 1
+
+
+@pytest.mark.parametrize("B", [4, 16])
+def test_mlp_chain_72_blocks(B):
+    sh = synth.MlpShape()
+    blocks = [synth.mlp_block_weights(sh, 0, i) for i in range(sh.blocks)]
+    x = synth.mlp_input(sh, B, 0)
+    dblocks = [_dev(b) for b in blocks]
+    ch = wc.mlp_chain(dblocks, dev_bf16(x))
+    ch.chain.capture()
+    ch.run()
+    # teacher-forced: the same kernel launched op by op, each op against the oracle
+    cur = dev_bf16(x)
+    ws = wb.new_workspace(wb.OP_GEMV, sh.width, sh.width, B)
+    for i, (hb, db) in enumerate(zip(blocks, dblocks)):
+        z = torch.empty_like(cur)
+        wb.ln_gemv_gelu(cur, db["gamma"], db["beta"], db["W"], db["b"], z, sh.eps, workspace=ws)
+        if i % 12 == 0 or i == sh.blocks - 1:
+            assert_bf16_close(host_bits(z), oracle.mlp_block(host_bits(cur), hb, sh.eps, 8,
+                                                             exact=True), what=f"mlp block {i}")
+        cur = z
+    torch.cuda.synchronize()
+    assert torch.equal(ch.y_out.cpu(), cur.cpu())
+    # prefetch with a fixed plan and with a decoy: same bits
+    for decoy in (False, True):
+        pch = wc.mlp_chain(dblocks, dev_bf16(x), prefetch=2,
+                           fixed_plan=wb.PrefetchPlan(8, 256, 128, 1), decoy=decoy)
+        pch.chain.capture()
+        pch.run()
+        torch.cuda.synchronize()
+        assert torch.equal(pch.y_out.cpu(), ch.y_out.cpu())

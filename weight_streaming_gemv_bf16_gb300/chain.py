@@ -1,0 +1,128 @@
+"""Assemble decode chains from device tensors and hand them to the C ABI.
+
+Two chain kinds, both replayed as one CUDA graph by the library:
+* a Llama-style decode weight chain ("One Token, Kernel by Kernel: A Decode
+  Step on a Laptop GPU", Step 1 and "The whole step"): L decoder blocks
+  (merged QKV with the first RMSNorm, Wo + residual, gate/up with the second
+  RMSNorm and SwiGLU, Wd + residual), then the final RMSNorm, the LM head and
+  the argmax;
+* an MLP chain of LayerNorm -> Linear -> GELU blocks ("Making small PyTorch
+  ops faster on a laptop GPU", "Beyond language models").
+
+Only pointers, sizes and options are marshalled here; the tensors stay owned
+by the returned objects.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import binding as wb
+
+
+@dataclass
+class QwenChain:
+    chain: wb.Chain
+    h_in: torch.Tensor
+    h_out: torch.Tensor
+    attn: torch.Tensor
+    idx: torch.Tensor | None
+    logits: torch.Tensor | None
+    h_trace: torch.Tensor | None
+    qkv: list = field(default_factory=list)
+
+    def run(self, stream=None):
+        self.chain.run(stream)
+
+
+@dataclass
+class MlpChain:
+    chain: wb.Chain
+    x_in: torch.Tensor
+    y_out: torch.Tensor
+
+    def run(self, stream=None):
+        self.chain.run(stream)
+
+
+def _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, tune_pairs,
+          min_gain):
+    o = wb.ChainOpts()
+    o.batch, o.hidden, o.kv_dim, o.inter, o.vocab, o.eps = B, H, KV, I, V, eps
+    o.use_pdl = 1 if use_pdl else 0
+    o.prefetch = prefetch
+    if fixed_plan is not None:
+        o.fixed_plan = fixed_plan
+    o.distance = distance
+    o.decoy = 1 if decoy else 0
+    o.tune_pairs = tune_pairs
+    o.tune_min_gain = min_gain
+    return o
+
+
+def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
+               fixed_plan=None, distance=1, decoy=False, trace=False, keep_qkv=False,
+               logits=False, tune_pairs=30, min_gain=0.01) -> QwenChain:
+    """blocks: list of dicts of bf16 device tensors gamma1, Wq, Wk, Wv, Wo, gamma2,
+    Wg, Wu, Wd; head: dict gamma_f, Wlm (or None); attn: bf16 [L, B, H];
+    h_in: fp32 [B, H]."""
+    B, H = h_in.shape
+    L = len(blocks)
+    KV = blocks[0]["Wk"].shape[0] if L else 0
+    I = blocks[0]["Wg"].shape[0] if L else 0
+    V = head["Wlm"].shape[0] if head else 0
+    dev = h_in.device
+    h_out = torch.empty_like(h_in)
+    h_trace = torch.empty((L, B, H), dtype=torch.float32, device=dev) if trace else None
+    descs, keep, qkv = [], [blocks, head, attn, h_in], []
+    for l, w in enumerate(blocks):
+        d = wb.BlockDesc(kind=wb.BLOCK_QWEN)
+        q = k = v = None
+        if keep_qkv:
+            q = torch.empty((B, H), device=dev)
+            k = torch.empty((B, KV), device=dev)
+            v = torch.empty((B, KV), device=dev)
+            qkv.append((q, k, v))
+        d.u.qwen = wb.QwenBlock(*(w[n].data_ptr() for n in ("gamma1", "Wq", "Wk", "Wv", "Wo",
+                                                             "gamma2", "Wg", "Wu", "Wd")),
+                                attn[l].data_ptr(),
+                                q.data_ptr() if q is not None else None,
+                                k.data_ptr() if k is not None else None,
+                                v.data_ptr() if v is not None else None)
+        descs.append(d)
+    idx = lg = None
+    if head is not None:
+        idx = torch.full((B,), -1, dtype=torch.int32, device=dev)
+        lg = torch.empty((B, V), device=dev) if logits else None
+        d = wb.BlockDesc(kind=wb.BLOCK_HEAD)
+        d.u.head = wb.HeadBlock(head["gamma_f"].data_ptr(), head["Wlm"].data_ptr(),
+                                idx.data_ptr(), lg.data_ptr() if lg is not None else None)
+        descs.append(d)
+    o = _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, tune_pairs,
+              min_gain)
+    o.h_in = h_in.data_ptr()
+    o.h_out = h_out.data_ptr()
+    o.h_trace = h_trace.data_ptr() if h_trace is not None else None
+    keep += [h_out, h_trace, idx, lg, qkv]
+    ch = wb.Chain(descs, o, keepalive=keep)
+    return QwenChain(ch, h_in, h_out, attn, idx, lg, h_trace, qkv)
+
+
+def mlp_chain(blocks, x_in, *, eps=1e-5, use_pdl=True, prefetch=0, fixed_plan=None,
+              distance=1, decoy=False, tune_pairs=30, min_gain=0.01) -> MlpChain:
+    """blocks: list of dicts of bf16 device tensors gamma, beta, W, b; x_in bf16 [B, w]."""
+    B, w = x_in.shape
+    y_out = torch.empty_like(x_in)
+    descs = []
+    for blk in blocks:
+        d = wb.BlockDesc(kind=wb.BLOCK_MLP)
+        d.u.mlp = wb.MlpBlock(blk["gamma"].data_ptr(), blk["beta"].data_ptr(),
+                              blk["W"].data_ptr(), blk["b"].data_ptr())
+        descs.append(d)
+    o = _opts(B, w, 0, 0, 0, eps, use_pdl, prefetch, fixed_plan, distance, decoy, tune_pairs,
+              min_gain)
+    o.x_in = x_in.data_ptr()
+    o.y_out = y_out.data_ptr()
+    ch = wb.Chain(descs, o, keepalive=[blocks, x_in, y_out])
+    return MlpChain(ch, x_in, y_out)
