@@ -1,0 +1,431 @@
+"""Benchmark: the Qwen2.5-1.5B-shaped BF16 decode weight chain on GB300.
+
+One step = one replay of the whole chain as one CUDA graph: 28 decoder blocks
+(merged QKV + RMSNorm, Wo + residual, gate/up + RMSNorm + SwiGLU, Wd +
+residual), the final RMSNorm, the LM head 151936 x 1536 and the argmax, batch
+1, with the tuned L2-prefetch plans.  Weights are seeded synthetic bf16
+(N(0, 0.02)); 3.09 GB per step is far larger than L2, so no flush is needed
+between steps.
+
+Prints one JSON line.  `value` is achieved HBM GB/s = algorithmic bytes per
+step / device time per step (higher is better); `us_per_step` is the time.
+
+  python bench.py [--steps K] [--warmup W] [--batch B] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the chain has
+no exchange step); `value` sums all ranks' bytes over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-chain µs/step and achieved HBM GB/s (fraction of GB300 roofline), 1 GPU"
+WORKLOAD = ("Qwen2.5-1.5B-shaped decode weight chain: 28 blocks (H 1536, KV 256, MLP 8960, "
+            "SwiGLU) + final RMSNorm + LM head 151936x1536 + argmax, one CUDA graph")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["ws_gemv.cu", "ws_common.cuh", "ws_device.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefetch", choices=["tuned", "off"], default="tuned")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "weight_streaming_gemv_bf16_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)
+        e = d.get(kernel_key)
+        if e and e.get("kernel_source_hash") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------- inputs
+
+def make_host_inputs(B, seed):
+    from weight_streaming_gemv_bf16_gb300 import synth
+    sh = synth.QWEN2_5_1_5B
+    blocks = [synth.qwen_block_weights(sh, seed, l) for l in range(sh.layers)]
+    head = synth.qwen_head_weights(sh, seed)
+    attn = np.stack([synth.qwen_attn(sh, B, seed, l) for l in range(sh.layers)])
+    h0 = synth.qwen_hidden(sh, B, seed)
+    return sh, blocks, head, attn, h0
+
+
+def to_dev(bits, torch):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+# --------------------------------------------------------------------------- oracle arm
+
+def oracle_sample(sh, blocks, head, attn, h0, budget_s):
+    """Time the oracle (all host cores) on the chain: whole steps while they fit
+    in the time budget (at least one block).  Returns (GB/s, seconds, sample)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    att = [oracle.bf16_to_f64(a) for a in attn]
+    bytes_block = sh.block_weight_bytes()
+    done_bytes = 0
+    t0 = time.perf_counter()
+    h = h0.astype(np.float64)
+    nblk = 0
+    while True:
+        for l in range(sh.layers):
+            h = oracle.qwen_block(h, blocks[l], att[l], sh.eps, threads)["h"]
+            done_bytes += bytes_block
+            nblk += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        if time.perf_counter() - t0 > budget_s:
+            break
+        oracle.argmax_rows(oracle.lmhead_logits(h, oracle.bf16_to_f64(head["gamma_f"]),
+                                                head["Wlm"], sh.eps, threads))
+        done_bytes += sh.lm_head_bytes()
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    sample = f"{nblk} decoder blocks (+ LM heads of completed steps), batch {h0.shape[0]}, {threads} threads"
+    return done_bytes / dt / 1e9, dt, sample, threads
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    sh, blocks, head, attn, h0 = make_host_inputs(args.batch, args.seed)
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0))
+    att = [oracle.bf16_to_f64(a) for a in attn]
+    # one reference "step" = one decoder block of the chain (a bounded sample)
+    h = h0.astype(np.float64)
+    for w in range(args.warmup):
+        h = oracle.qwen_block(h, blocks[w % sh.layers], att[w % sh.layers], sh.eps, threads)["h"]
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        h = oracle.qwen_block(h, blocks[k % sh.layers], att[k % sh.layers], sh.eps, threads)["h"]
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    gbs = sh.block_weight_bytes() / dt / 1e9
+    us_chain = sh.chain_weight_bytes() / (gbs * 1e9) * 1e6
+    sample = f"one decoder block per step (93.6 MB of bf16 weights), batch {args.batch}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(us_chain / 1e3, 3), "us_per_step": round(us_chain, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "batch": args.batch,
+                                       "reference": "CPU oracle (plain C, double accumulation)"},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+
+def read_roofline(torch, wb, nbytes=4 << 30, reps=5):
+    buf = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda")
+    buf.fill_(1)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.zeros(nsm * 4, dtype=torch.int32, device="cuda")
+    best = 0.0
+    for blocks in (nsm * 2, nsm * 4):
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            wb.read_probe(buf, nbytes, blocks, sink)
+            e1.record()
+            e1.synchronize()
+            best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del buf
+    return best
+
+
+def time_dominant_kernel(torch, wb, dblocks, sh, B, reps=3):
+    """The gate/up GEMV (RMSNorm prologue + SwiGLU epilogue, 2 x 8960 x 1536),
+    launched alone over all blocks' weights in turn (cold in L2), timed with
+    CUDA events on the launching stream."""
+    x = torch.randn((B, sh.hidden), device="cuda")
+    s = torch.empty((B, sh.inter), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream()
+    ts = []
+    for r in range(reps + 1):
+        for w in dblocks:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            wb.swiglu_gemv(x, w["gamma2"], w["Wg"], w["Wu"], s, sh.eps, stream=st)
+            e1.record(st)
+            if r > 0:
+                ts.append((e0, e1))
+    torch.cuda.synchronize()
+    dur = float(np.mean([a.elapsed_time(b) for a, b in ts])) * 1e-3
+    nbytes = 2 * sh.inter * sh.hidden * 2 + sh.hidden * 2  # Wg + Wu + gamma2
+    return nbytes, dur, len(ts)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+
+    B = args.batch
+    sh, blocks, head, attn, h0 = make_host_inputs(B, args.seed + rank)
+    dblocks = [{k: to_dev(v, torch) for k, v in b.items()} for b in blocks]
+    dhead = {k: to_dev(v, torch) for k, v in head.items()}
+    dattn = to_dev(attn, torch)
+    dh0 = torch.from_numpy(h0).cuda()
+    step_bytes = sh.chain_weight_bytes() + sh.chain_gamma_bytes()
+
+    read_gbs = read_roofline(torch, wb)
+
+    def make_chain(prefetch, decoy=False):
+        return wc.qwen_chain(dblocks, dhead, dattn, dh0, eps=sh.eps, use_pdl=True,
+                             prefetch=prefetch, decoy=decoy, tune_pairs=30, min_gain=0.01)
+
+    t_tune = time.perf_counter()
+    main = make_chain(1 if args.prefetch == "tuned" else 0)
+    main.chain.tune()
+    t_tune = time.perf_counter() - t_tune
+    main.chain.capture()
+    plans = main.chain.plans()
+    n_prefetch_launches = 0
+    op_reads = [3, 1, 2, 1] * sh.layers + [1]
+    for i, (pl, lo, mean) in enumerate(plans):
+        if pl[0] != 0 and i >= 1:
+            n_prefetch_launches += op_reads[i]
+
+    def timed(ch, steps, warmup):
+        st = torch.cuda.current_stream()
+        for _ in range(warmup):
+            ch.run(st)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("timed")
+        e0.record(st)
+        for _ in range(steps):
+            ch.run(st)
+        e1.record(st)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return e0.elapsed_time(e1) * 1e-3
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    dt = timed(main, args.steps, args.warmup)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([dt], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    per_step = dt / max(args.steps, 1)
+    value = world * step_bytes / per_step / 1e9
+
+    # controls: no prefetch, and a decoy of the same traffic (when a plan was kept)
+    variants = {}
+    ksteps = max(10, min(args.steps, 500))
+    if rank == 0:
+        off = make_chain(0)
+        off.chain.capture()
+        variants["no_prefetch_us"] = round(timed(off, ksteps, 5) / ksteps * 1e6, 2)
+        if any(p[0][0] != 0 for p in plans):
+            dec = make_chain(1, decoy=True)
+            dec.chain.tune()
+            dec.chain.capture()
+            variants["decoy_us"] = round(timed(dec, ksteps, 5) / ksteps * 1e6, 2)
+        variants["tuned_us"] = round(per_step * 1e6, 2)
+
+    hbm, hbm_kind = peaks()
+    nbytes, kdur, nlaunch = time_dominant_kernel(torch, wb, dblocks, sh, B)
+    achieved = nbytes / kdur / 1e9
+    dom_key = "k_stream_gemv<1,2> gate/up+SwiGLU 8960x1536 B=1"
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": ncu_traffic(dom_key),
+                "kernel": dom_key, "algorithmic_bytes_per_launch": nbytes,
+                "avg_launch_us": round(kdur * 1e6, 3), "launches_timed": nlaunch,
+                "peak_kind": f"{hbm_kind} (copy, MEASURED_PEAKS hbm_gbs)" if hbm_kind == "measured"
+                else "fallback"}
+
+    e2e = None
+    if not args.no_e2e:
+        import torch as _t
+        h_host = _t.from_numpy(h0).pin_memory()
+        a_host = _t.from_numpy(np.ascontiguousarray(attn).view(np.int16)).pin_memory()
+        out = _t.empty((B,), dtype=_t.int32).pin_memory()
+        n_e2e = max(5, min(args.steps, 300))
+        for _ in range(3):
+            main.chain.step_host(h_host, a_host, out)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            main.chain.step_host(h_host, a_host, out)
+        e_dt = (time.perf_counter() - t0) / n_e2e
+        e2e = {"value": round(world * step_bytes / e_dt / 1e9, 1), "unit": "GB/s",
+               "us_per_step": round(e_dt * 1e6, 2),
+               "h2d_bytes_per_step": int(h0.nbytes + attn.nbytes), "d2h_bytes_per_step": 4 * B,
+               "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        gbs, secs, sample, threads = oracle_sample(sh, blocks, head, attn, h0, budget_s=12.0)
+        cpu = {"value": round(gbs, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": sample, "seconds": round(secs, 1)}
+
+    if rank != 0:
+        return 0
+    n_ops = main.chain.n_ops
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 4),
+        "us_per_step": round(per_step * 1e6, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) bf16 weights)",
+        "config": {"workload": WORKLOAD, "batch": B, "layers": sh.layers,
+                   "bytes_per_step": step_bytes, "prefetch": args.prefetch, "pdl": True,
+                   "l2": "inputs larger than L2 (3.09 GB of weights per step, no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "frac_of_copy_peak": round(value / world / hbm, 4),
+        "read_roofline_gbs": round(read_gbs, 1),
+        "frac_of_read_roofline": round(value / world / read_gbs, 4),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(args.steps * (n_ops + n_prefetch_launches)),
+        "clocks": clk,
+        "prefetch_plans": {"kept": sum(1 for p in plans if p[0][0] != 0), "ops": len(plans),
+                           "tune_seconds": round(t_tune, 2),
+                           "best_lower_ci": round(max([p[1] for p in plans] or [0.0]), 4)},
+        "variants": variants,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -4,9 +4,9 @@ benchmark and the oracle's callers.
 This module draws random numbers and stores them in the formats the chain
 reads (bf16 / fp16 bit patterns as uint16, fp32); it holds none of the
 method's arithmetic.  Every tensor gets its own independent stream, keyed by
-(seed, tag), from numpy's PCG64, so a tensor does not change when another one
-is added or resized.  Rounding from float32 to bf16/fp16 uses torch's and
-numpy's own conversions (round to nearest even).
+(seed, tag): torch's CPU generator seeded with seed * 2^32 + crc32(tag), so a
+tensor does not change when another one is added or resized.  Rounding from
+float32 to bf16/fp16 uses torch's own conversions (round to nearest even).
 
 Shapes follow the pages' models:
 * Qwen2.5-1.5B decode block ("One Token, Kernel by Kernel: A Decode Step on a
@@ -24,48 +24,64 @@ the attention stand-in ~ N(0, 1).
 from __future__ import annotations
 
 import zlib
-from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
+import torch
 
 WEIGHT_STD = 0.02
 
 
-def _rng(seed: int, tag: str) -> np.random.Generator:
-    return np.random.Generator(np.random.PCG64([int(seed), zlib.crc32(tag.encode())]))
+def _gen(seed: int, tag: str) -> torch.Generator:
+    return torch.Generator().manual_seed((int(seed) << 32) + zlib.crc32(tag.encode()))
 
 
-def _f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    import torch
-    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
-    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+_CHUNK = 1 << 23
+
+
+def _normal(shape, std, seed, tag) -> torch.Tensor:
+    # large tensors are drawn in chunks of 2^23 values, chunk i from the stream
+    # of (seed, tag#i): torch's CPU generator is much slower on huge single draws
+    n = int(np.prod(shape)) if len(shape) else 1
+    if n <= _CHUNK:
+        t = torch.randn(tuple(shape), generator=_gen(seed, tag), dtype=torch.float32)
+    else:
+        t = torch.empty(n, dtype=torch.float32)
+        for i, lo in enumerate(range(0, n, _CHUNK)):
+            hi = min(n, lo + _CHUNK)
+            t[lo:hi] = torch.randn(hi - lo, generator=_gen(seed, f"{tag}#{i}"))
+        t = t.view(tuple(shape))
+    return t.mul_(std) if std != 1.0 else t
+
+
+def _uniform(shape, lo, hi, seed, tag) -> torch.Tensor:
+    t = torch.rand(tuple(shape), generator=_gen(seed, tag), dtype=torch.float32)
+    return t.mul_(hi - lo).add_(lo)
 
 
 def normal_f32(shape, std: float, seed: int, tag: str) -> np.ndarray:
-    out = _rng(seed, tag).standard_normal(size=shape, dtype=np.float32)
-    if std != 1.0:
-        out *= np.float32(std)
-    return out
+    return _normal(shape, std, seed, tag).numpy()
 
 
 def normal_bf16(shape, std: float, seed: int, tag: str) -> np.ndarray:
     """bf16 bit patterns of N(0, std^2) draws (drawn in fp32, rounded once)."""
-    return _f32_to_bf16_bits(normal_f32(shape, std, seed, tag))
+    return _bits(_normal(shape, std, seed, tag).to(torch.bfloat16))
 
 
 def uniform_bf16(shape, lo: float, hi: float, seed: int, tag: str) -> np.ndarray:
-    u = _rng(seed, tag).uniform(lo, hi, size=shape).astype(np.float32)
-    return _f32_to_bf16_bits(u)
+    return _bits(_uniform(shape, lo, hi, seed, tag).to(torch.bfloat16))
 
 
 def normal_fp16(shape, std: float, seed: int, tag: str) -> np.ndarray:
-    return normal_f32(shape, std, seed, tag).astype(np.float16).view(np.uint16)
+    return _bits(_normal(shape, std, seed, tag).to(torch.float16))
 
 
 def uniform_fp16(shape, lo: float, hi: float, seed: int, tag: str) -> np.ndarray:
-    u = _rng(seed, tag).uniform(lo, hi, size=shape)
-    return u.astype(np.float16).view(np.uint16)
+    return _bits(_uniform(shape, lo, hi, seed, tag).to(torch.float16))
 
 
 def bf16_bits_as_f32(bits: np.ndarray) -> np.ndarray:
@@ -122,8 +138,7 @@ def qwen_block_weights(shape: QwenShape, seed: int, layer: int) -> dict:
             return name, uniform_bf16(shp, 0.5, 1.5, seed, t + name)
         return name, normal_bf16(shp, WEIGHT_STD, seed, t + name)
 
-    with ThreadPoolExecutor(max_workers=4) as ex:
-        return dict(ex.map(make, specs.items()))
+    return dict(make(item) for item in specs.items())
 
 
 def qwen_head_weights(shape: QwenShape, seed: int) -> dict:
