@@ -252,7 +252,9 @@ ws_status ws_chain_create(const ws_block_desc *blocks, int n, const ws_chain_opt
  * predicting").  Blocks the calling thread; uses `stream`. */
 ws_status ws_chain_tune(ws_chain *c, ws_stream_t stream);
 /* Capture the chain: all ops on the main branch, each prefetch on a side
- * branch forked before op i and joined at the end, as one graph. */
+ * branch forked before op i and joined at the end, as one graph.  Capture
+ * happens on a stream the chain owns (any caller stream, including the
+ * legacy default stream, can then replay it); `stream` is not used. */
 ws_status ws_chain_capture(ws_chain *c, ws_stream_t stream);
 /* One decode step: one cudaGraphLaunch. */
 ws_status ws_chain_run(ws_chain *c, ws_stream_t stream);

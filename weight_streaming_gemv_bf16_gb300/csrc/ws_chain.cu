@@ -96,6 +96,7 @@ struct ws_chain {
   float* qkv_scratch = nullptr;
   void* pp[2] = {nullptr, nullptr};
   cudaStream_t side = nullptr;
+  cudaStream_t cap = nullptr;  // graphs are captured here, launched on the caller's stream
   std::vector<cudaEvent_t> fork_ev;
   cudaEvent_t join_ev = nullptr;
   cudaGraph_t graph = nullptr;
@@ -111,6 +112,7 @@ static void free_chain_buffers(ws_chain* c) {
     if (e) cudaEventDestroy(e);
   if (c->join_ev) cudaEventDestroy(c->join_ev);
   if (c->side) cudaStreamDestroy(c->side);
+  if (c->cap) cudaStreamDestroy(c->cap);
   if (c->ws) cudaFree(c->ws);
   if (c->s_buf) cudaFree(c->s_buf);
   if (c->qkv_scratch) cudaFree(c->qkv_scratch);
@@ -121,6 +123,7 @@ static void free_chain_buffers(ws_chain* c) {
   c->fork_ev.clear();
   c->join_ev = nullptr;
   c->side = nullptr;
+  c->cap = nullptr;
   c->ws = c->s_buf = nullptr;
   c->qkv_scratch = nullptr;
   c->pp[0] = c->pp[1] = nullptr;
@@ -381,11 +384,11 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
 static ws_status capture_graph(ws_chain* c, const std::vector<GemvParams>& ps,
                                const std::vector<std::vector<std::pair<const void*, size_t>>>& reads,
                                const std::vector<ws_prefetch_plan>& plans, bool decoy,
-                               const std::vector<int>& trace, cudaStream_t stream,
-                               cudaGraphExec_t* out) {
+                               const std::vector<int>& trace, cudaGraphExec_t* out) {
   cudaGraph_t g = nullptr;
+  cudaStream_t stream = c->cap;
   if (cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-    set_error("cudaStreamBeginCapture failed (a NULL stream cannot be captured)");
+    set_error("cudaStreamBeginCapture failed");
     return WS_ERR_CUDA;
   }
   const ws_status s = enqueue_ops(c, ps, reads, plans, c->o.distance, decoy, stream, trace,
@@ -515,6 +518,8 @@ ws_status ws_chain_create(const ws_block_desc* blocks, int n, const ws_chain_opt
   ws_status s = build_ops(c);
   if (s == WS_OK) {
     if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess) s = WS_ERR_CUDA;
+    if (s == WS_OK && cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking) != cudaSuccess)
+      s = WS_ERR_CUDA;
     c->fork_ev.assign(c->ops.size(), nullptr);
     for (auto& e : c->fork_ev)
       if (s == WS_OK && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
@@ -630,14 +635,14 @@ ws_status ws_chain_tune(ws_chain* c, ws_stream_t stream) {
 
     std::vector<ws_prefetch_plan> none(np, kNoPlan);
     cudaGraphExec_t gA = nullptr;
-    status = capture_graph(c, ps, reads, none, false, {}, st, &gA);
+    status = capture_graph(c, ps, reads, none, false, {}, &gA);
     double best_lo = -1e30, best_mean = 0;
     int best_c = -1;
     for (size_t ci = 0; ci < cands.size() && status == WS_OK; ++ci) {
       std::vector<ws_prefetch_plan> pl(np, kNoPlan);
       for (int k = 1; k < np; k += 2) pl[k] = cands[ci];  // prefetch every op j (odd slots)
       cudaGraphExec_t gB = nullptr;
-      status = capture_graph(c, ps, reads, pl, false, {}, st, &gB);
+      status = capture_graph(c, ps, reads, pl, false, {}, &gB);
       if (status != WS_OK) break;
       // warm up both
       for (int w = 0; w < 3; ++w) {
@@ -712,8 +717,9 @@ ws_status ws_chain_capture(ws_chain* c, ws_stream_t stream) {
   if (c->o.h_trace) {
     for (const ChainOp& op : c->ops) trace.push_back(op.trace_block);
   }
+  (void)stream;
   return capture_graph(c, chain_params(c), chain_reads(c), plans, c->o.decoy != 0, trace,
-                       (cudaStream_t)stream, &c->exec);
+                       &c->exec);
 }
 
 ws_status ws_chain_run(ws_chain* c, ws_stream_t stream) {
