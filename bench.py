@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--mode", choices=["chain", "kernel"], default="chain")
     return ap.parse_args()
 
 
@@ -420,10 +421,50 @@ def run_ours(args):
     return 0
 
 
+def run_kernel_only(args):
+    """The dominant kernel alone (gate/up GEMV + RMSNorm + SwiGLU, 2 x 8960 x
+    1536, batch B) over 4 rotating weight copies (220 MB, larger than L2): the
+    small case for profiler captures."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import synth
+    sh = synth.QWEN2_5_1_5B
+    B = args.batch
+    copies = [{k: to_dev(synth.normal_bf16((sh.inter, sh.hidden), 0.02, args.seed, f"k{i}/{k}"), torch)
+               for k in ("Wg", "Wu")} for i in range(4)]
+    g = to_dev(synth.uniform_bf16((sh.hidden,), 0.5, 1.5, args.seed, "k/g"), torch)
+    x = torch.from_numpy(synth.normal_f32((B, sh.hidden), 1.0, args.seed, "k/x")).cuda()
+    s = torch.empty((B, sh.inter), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        c = copies[i % 4]
+        wb.swiglu_gemv(x, g, c["Wg"], c["Wu"], s, sh.eps, stream=st)
+    torch.cuda.synchronize()
+    ev = []
+    for i in range(args.steps):
+        c = copies[i % 4]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        wb.swiglu_gemv(x, g, c["Wg"], c["Wu"], s, sh.eps, stream=st)
+        e1.record(st)
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    dur = float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e-3
+    nbytes = 2 * sh.inter * sh.hidden * 2 + sh.hidden * 2
+    print(json.dumps({"mode": "kernel", "kernel": "gate/up GEMV + RMSNorm + SwiGLU 8960x1536",
+                      "batch": B, "launches": args.steps, "avg_us": round(dur * 1e6, 3),
+                      "gbs": round(nbytes / dur / 1e9, 1)}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "kernel":
+        return run_kernel_only(args)
     return run_ours(args)
 
 
