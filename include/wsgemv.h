@@ -298,20 +298,23 @@ const char *ws_last_error(void);
 int ws_device_error(int reset);
 
 typedef struct {
-  int ring_bytes;      /* shared-memory weight ring per CTA (default 96 KiB)  */
-  int grid_cap;        /* max CTAs per GEMV launch (0: one per SM)            */
-  int force_ksplit;    /* K splits (0: heuristic)                             */
-  int force_kg;        /* warps per row, 1/2/4/8 (0: heuristic)               */
-  int evict_first;     /* stream weights with an L2 evict-first hint          */
-  unsigned long long timeout_ns; /* bound of every device wait                */
+  int ring_bytes;      /* shared-memory weight rings per CTA, all warps        */
+  int grid_cap;        /* CTAs per GEMV launch (0: one per SM)                 */
+  int force_ksplit;    /* K splits (0: heuristic)                              */
+  int force_rt;        /* rows per warp task, 1 or 2 (0: heuristic)            */
+  int evict_first;     /* stream weights with an L2 evict-first hint           */
+  int piece_bytes;     /* target bytes of one ring stage                       */
+  unsigned long long timeout_ns; /* bound of every device wait                 */
 } ws_tuning;
 
 void ws_get_tuning(ws_tuning *t);
 ws_status ws_set_tuning(const ws_tuning *t);
 
-/* Schedule a GEMV launch would use (for tests and reports). */
+/* Schedule a GEMV launch would use (for tests and reports): rows per warp
+ * task RT, K splits S of KS columns, pieces of PC columns (NP per task),
+ * NSW ring stages per warp of piece_bytes, RG row groups, grid CTAs. */
 typedef struct {
-  int KG, RS, S, KS, NS, stage_bytes, RG, units, grid, smem_bytes;
+  int RT, S, KS, PC, NP, NSW, piece_bytes, RG, grid, smem_bytes;
 } ws_gemv_schedule;
 ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind,
                        int epilogue_kind, int allow_split, ws_gemv_schedule *out);

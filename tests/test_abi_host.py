@@ -118,23 +118,23 @@ SHAPES = [
 def test_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, split):
     sc = wb.gemv_plan(M, K, B, nmat=nmat, allow_split=split)
     assert sc["smem_bytes"] <= 227 * 1024
-    assert 2 <= sc["NS"] <= 16
-    assert sc["stage_bytes"] % 128 == 0
-    assert sc["grid"] <= sc["units"]
-    assert sc["KS"] * sc["S"] == K and sc["KS"] % 8 == 0
+    assert 2 <= sc["NSW"] <= 8
+    assert sc["piece_bytes"] % 128 == 0
+    assert sc["grid"] % sc["S"] == 0 and sc["grid"] // sc["S"] <= sc["RG"]
+    assert sc["KS"] * sc["S"] == K and sc["KS"] % 8 == 0 and sc["PC"] % 8 == 0
+    assert sc["NP"] == -(-sc["KS"] // sc["PC"])
+    warp_ring = sc["NSW"] * sc["piece_bytes"]
     covered = np.zeros(nmat * M * K * 2 // 16, np.int32)
     for cta in range(sc["grid"]):
-        per_slot = {}
         for src, dst, n in wb.debug_gemv_copies(M, K, B, nmat, split, cta):
             assert n > 0 and n % 16 == 0 and src % 16 == 0 and dst % 16 == 0
             assert 0 <= src and src + n <= nmat * M * K * 2
             # a copy never crosses from one matrix of a pair into the other
             assert src // (M * K * 2) == (src + n - 1) // (M * K * 2)
-            slot, off = divmod(dst, sc["stage_bytes"])
-            assert slot < sc["NS"] and off + n <= sc["stage_bytes"]
+            warp, rest = divmod(dst, warp_ring)
+            slot, off = divmod(rest, sc["piece_bytes"])
+            assert warp < 8 and slot < sc["NSW"] and off + n <= sc["piece_bytes"]
             covered[src // 16:(src + n) // 16] += 1
-            per_slot.setdefault(slot, 0)
-            per_slot[slot] += 1
     assert covered.min() == 1 and covered.max() == 1
 
 

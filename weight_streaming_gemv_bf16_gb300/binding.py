@@ -76,11 +76,12 @@ class ChainOpts(C.Structure):
 
 class Tuning(C.Structure):
     _fields_ = [("ring_bytes", I32), ("grid_cap", I32), ("force_ksplit", I32),
-                ("force_kg", I32), ("evict_first", I32), ("timeout_ns", C.c_ulonglong)]
+                ("force_rt", I32), ("evict_first", I32), ("piece_bytes", I32),
+                ("timeout_ns", C.c_ulonglong)]
 
 
 class GemvSchedule(C.Structure):
-    _fields_ = [(n, I32) for n in ("KG", "RS", "S", "KS", "NS", "stage_bytes", "RG", "units",
+    _fields_ = [(n, I32) for n in ("RT", "S", "KS", "PC", "NP", "NSW", "piece_bytes", "RG",
                                    "grid", "smem_bytes")]
 
 

@@ -6,14 +6,16 @@
 // normalisation prologue and a per-output epilogue.
 //
 // Work decomposition.  The rows of up to three weight matrices ("segments",
-// e.g. Q, K and V) are cut into row groups of RS rows; each row group may be
-// cut along K into S splits of KS columns.  A unit is one (split, row group)
-// pair; units are numbered split-major and handed out to the CTAs in
-// contiguous, balanced ranges.  Inside a CTA a producer warp streams each
-// unit's weight rows into a ring of shared-memory stages with bulk async
-// copies; 8 consumer warps reduce them against the activations, which sit in
-// shared memory as bf16.  The KG warps that share one row each take a
-// contiguous slice of its 16-byte chunks.
+// e.g. Q, K and V) are cut into row groups of RT rows; K may be cut into S
+// splits of KS columns.  One warp computes one (row group, split) task from
+// start to end: it streams the task's weight rows through its own ring of
+// shared-memory stages with bulk async copies, in pieces of PC columns,
+// accumulates in registers and runs the epilogue itself.  Warps never wait on
+// each other, so eight independent copy/compute pipelines overlap per CTA.
+// CTAs are grouped by split (grid = S * Gs); CTA g of a split takes a
+// contiguous, balanced range of row groups and deals them to its warps
+// round-robin.  The activations (normalised by the prologue) sit in shared
+// memory as bf16, the KS columns of the CTA's split.
 #pragma once
 
 #include <cstddef>
@@ -22,11 +24,10 @@
 
 namespace ws {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSeg = 3;
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 8;  // ring stages per warp
 constexpr int kMaxBatch = 16;
 
 enum Prologue { PRO_NONE = 0, PRO_RMSNORM = 1, PRO_LAYERNORM = 2 };
@@ -51,18 +52,19 @@ struct Seg {
 };
 
 struct Sched {
-  int KG;           // consumer warps sharing one row
-  int RS;           // rows per stage = kConsumerWarps / KG
-  int S;            // K splits across units
+  int RT;           // rows per task
+  int S;            // K splits
   int KS;           // columns per split
-  int NS;           // ring stages
-  int stage_bytes;  // bytes of one ring stage
-  int RG;           // row groups, all segments
-  int units;        // RG * S
-  int grid;         // CTAs
+  int PC;           // columns per piece (one ring stage)
+  int NP;           // pieces per task, ceil(KS / PC)
+  int NSW;          // ring stages per warp
+  int piece_bytes;  // bytes of one ring stage
+  int RG;           // row groups (tasks per split), all segments
+  int Gs;           // CTAs per split
+  int grid;         // S * Gs
   int BT;           // batch the kernel is instantiated for (>= B)
   int smem_bytes;
-  int off_bar, off_flags, off_stats, off_arg, off_red, off_xs, off_ring;
+  int off_bar, off_flags, off_stats, off_arg, off_xs, off_ring;
 };
 
 struct GemvParams {
@@ -93,26 +95,33 @@ struct GemvParams {
   Sched sc;
 };
 
-__host__ __device__ inline void cta_units(int cta, int grid, int units, int& u0, int& u1) {
-  u0 = (int)((long long)cta * units / grid);
-  u1 = (int)((long long)(cta + 1) * units / grid);
+// The split and the row-group range of CTA `cta`.
+__host__ __device__ inline void cta_range(const Sched& sc, int cta, int& ks, int& rg0, int& rg1) {
+  ks = cta / sc.Gs;
+  const int g = cta - ks * sc.Gs;
+  rg0 = (int)((long long)g * sc.RG / sc.Gs);
+  rg1 = (int)((long long)(g + 1) * sc.RG / sc.Gs);
 }
 
-__host__ __device__ inline void decode_unit(const GemvParams& p, int u, int& seg, int& rg,
-                                            int& ks) {
-  ks = u / p.sc.RG;
-  const int g = u - ks * p.sc.RG;
+// Tasks of warp `w` in a CTA whose row groups are [rg0, rg1): rg0 + w + t * kWarps.
+__host__ __device__ inline int warp_tasks(int rg0, int rg1, int w) {
+  return rg1 - rg0 > w ? (rg1 - rg0 - w + kWarps - 1) / kWarps : 0;
+}
+
+// Segment and local row group of a global row group.
+__host__ __device__ inline void decode_rg(const GemvParams& p, int rg, int& seg, int& rgl) {
   seg = 0;
-  while (seg + 1 < p.nseg && g >= p.seg[seg + 1].rg_begin) ++seg;
-  rg = g - p.seg[seg].rg_begin;
+  while (seg + 1 < p.nseg && rg >= p.seg[seg + 1].rg_begin) ++seg;
+  rgl = rg - p.seg[seg].rg_begin;
 }
 
 struct Tuning {
-  int ring_bytes;    // shared-memory ring budget per CTA
+  int ring_bytes;    // shared-memory ring budget per CTA (all warps)
   int grid_cap;      // max CTAs (0: one per SM)
   int force_ksplit;  // 0: heuristic
-  int force_kg;      // 0: heuristic
+  int force_rt;      // rows per task, 1 or 2 (0: heuristic)
   int evict_first;   // weights streamed with an L2 evict-first policy
+  int piece_bytes;   // target bytes per ring stage
   unsigned long long timeout_ns;
 };
 

@@ -4,18 +4,19 @@
 // y[b][m] = sum_k W[m][k] * x[b][k], bf16 W and x, fp32 accumulation ("One
 // Token, Kernel by Kernel: A Decode Step on a Laptop GPU", Step 1, "What one
 // block launches").  The design for GB300:
-//  * one CTA per SM; a producer warp streams the CTA's contiguous share of
-//    weight rows from HBM into a ring of shared-memory stages with 1-D bulk
-//    async copies (cp.async.bulk, mbarrier completion), so ~100 KB per SM is
-//    in flight without tying up registers, and tags them L2 evict-first since
-//    each weight byte is read once;
-//  * the ring is filled before griddepcontrol.wait: weights do not depend on
-//    the previous op, so inside a chain the next op's weights stream in while
-//    the previous op finishes (programmatic dependent launch);
-//  * eight consumer warps take 16-byte chunks of each row, unpack bf16 pairs
-//    to fp32 and accumulate with FMA; lanes are summed with a butterfly of
-//    warp shuffles and, when several warps share a row, through shared memory
-//    in warp order;
+//  * every warp is an independent pipeline: it owns whole rows (a task of
+//    RT rows, one K split), streams them from HBM through its own ring of
+//    shared-memory stages with 1-D bulk async copies (cp.async.bulk, mbarrier
+//    completion, L2 evict-first since each weight byte is read once), and
+//    refills a stage as soon as its lanes have read it; no warp ever waits for
+//    another, so one slow step does not stall the CTA;
+//  * the first stages are issued before griddepcontrol.wait: weights do not
+//    depend on the previous op, so inside a chain the next op's weights stream
+//    in while the previous op finishes (programmatic dependent launch);
+//  * lanes take 16-byte chunks of each row, unpack bf16 pairs to fp32 and
+//    accumulate with FMA; at the end of a task a butterfly of warp shuffles
+//    gives every lane every sum, and lane r*B+b runs the epilogue of output
+//    (row r, batch b);
 //  * split-K for skinny shapes: partial sums go to a workspace and the last
 //    of a row group's splits (atomic ticket) adds them in split order, so the
 //    result is the same whatever order the CTAs finish in; the ticket is
@@ -103,7 +104,7 @@ __device__ __forceinline__ float load_x(const GemvParams& p, int b, int k) {
 // x^2 + eps); LayerNorm mean and rstd = rsqrt(var + eps).  One warp per row.
 __device__ void prologue_stats(const GemvParams& p, float* stats, int warp, int lane) {
   if (p.prologue == PRO_NONE) return;
-  for (int b = warp; b < p.B; b += kConsumerWarps) {
+  for (int b = warp; b < p.B; b += kWarps) {
     if (p.prologue == PRO_RMSNORM) {
       float ss = 0.f;
       for (int k = lane; k < p.K; k += 32) {
@@ -137,7 +138,7 @@ __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, i
   const int KS = p.sc.KS;
   const int nch = KS >> 3;
   const int k0 = ks * KS;
-  for (int o = tid; o < BT * nch; o += kConsumerThreads) {
+  for (int o = tid; o < BT * nch; o += kThreads) {
     const int b = o / nch;
     const int c = o - b * nch;
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
@@ -186,273 +187,247 @@ __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, i
   }
 }
 
-template <int BT, int NMAT>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_stream_gemv(const __grid_constant__ GemvParams p) {
+// Issue the bulk copies of piece q of this warp's task list into its ring.
+template <int NMAT, int RT>
+__device__ __forceinline__ void issue_piece(const GemvParams& p, int q, int warp, int rg0, int k0,
+                                            uint8_t* ring, uint64_t* full, uint64_t pol) {
+  const Sched& sc = p.sc;
+  const int ti = q / sc.NP;
+  const int j = q - ti * sc.NP;
+  int seg, rgl;
+  decode_rg(p, rg0 + warp + ti * kWarps, seg, rgl);
+  const Seg& S = p.seg[seg];
+  const int row0 = rgl * RT;
+  const int rows = min(RT, S.M - row0);
+  const int c0 = k0 + j * sc.PC;
+  const int len = min(sc.PC, sc.KS - j * sc.PC);
+  const int slot = q % sc.NSW;
+  uint8_t* dst = ring + (size_t)slot * sc.piece_bytes;
+  const int K = p.K;
+  mbar_arrive_expect_tx(&full[slot], (uint32_t)(NMAT * rows * len * 2));
+#pragma unroll
+  for (int mat = 0; mat < NMAT; ++mat) {
+    const uint16_t* W = mat == 0 ? S.W0 : S.W1;
+    if (len == K) {  // whole rows: one contiguous copy
+      bulk_copy_g2s(dst + (size_t)mat * RT * sc.PC * 2, W + (size_t)row0 * K,
+                    (uint32_t)(rows * K * 2), &full[slot], pol);
+    } else {
+      for (int r = 0; r < rows; ++r)
+        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * sc.PC * 2, W + (size_t)(row0 + r) * K + c0,
+                      (uint32_t)(len * 2), &full[slot], pol);
+    }
+  }
+}
+
+template <int BT, int NMAT, int RT>
+__global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Sched& sc = p.sc;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sc.off_bar);
-  uint64_t* empty = full + sc.NS;
-  // flags[0] abort, flags[1] "this CTA is last", flags[2] producer done,
-  // flags[16 + s] last stage index issued into slot s
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + sc.off_flags);
-  float* stats = reinterpret_cast<float*>(smem + sc.off_stats);
-  float* red = reinterpret_cast<float*>(smem + sc.off_red);
-  float* argv = reinterpret_cast<float*>(smem + sc.off_arg);
-  int* argi = reinterpret_cast<int*>(argv + kConsumerWarps * BT);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sc.off_xs);
-  uint8_t* ring = smem + sc.off_ring;
-
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  int u0, u1;
-  cta_units(blockIdx.x, gridDim.x, sc.units, u0, u1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sc.off_bar) + warp * kMaxStages;
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + sc.off_flags);
+  float* stats = reinterpret_cast<float*>(smem + sc.off_stats);
+  float* argv = reinterpret_cast<float*>(smem + sc.off_arg);
+  int* argi = reinterpret_cast<int*>(argv + kWarps * 32);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sc.off_xs);
+  uint8_t* ring = smem + sc.off_ring + (size_t)warp * sc.NSW * sc.piece_bytes;
 
-  if (tid == 0) {
-    for (int s = 0; s < sc.NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-      flags[16 + s] = -1;
-    }
-    flags[0] = 0;
-    flags[1] = 0;
-    flags[2] = 0;
+  int ks, rg0, rg1;
+  cta_range(sc, blockIdx.x, ks, rg0, rg1);
+  const int k0 = ks * sc.KS;
+  const int npw = warp_tasks(rg0, rg1, warp) * sc.NP;  // pieces of this warp
+  uint64_t pol = 0;
+
+  if (lane == 0) {
+    for (int s = 0; s < sc.NSW; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
+    pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+    // Weights do not depend on the previous kernel: start streaming them
+    // before waiting for it.
+    for (int q = 0; q < sc.NSW && q < npw; ++q)
+      issue_piece<NMAT, RT>(p, q, warp, rg0, k0, ring, full, pol);
   }
-  __syncthreads();
   pdl_launch_dependents();
-
-  if (warp == kConsumerWarps) {
-    // ---------------- producer: stream weight rows into the ring ----------
-    if (lane == 0) {
-      const uint64_t pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-      const int RS = sc.RS, KS = sc.KS, K = p.K;
-      for (int u = u0, i = 0; u < u1; ++u, ++i) {
-        const int slot = i % sc.NS;
-        if (i >= sc.NS && !flags[0]) {
-          if (!mbar_wait_bounded(&empty[slot], ((i / sc.NS) - 1) & 1, p.timeout_ns)) {
-            raise_device_error(p.err, DERR_TIMEOUT);
-            flags[0] = 1;
-          }
-        }
-        if (flags[0]) break;
-        int seg, rg, ks;
-        decode_unit(p, u, seg, rg, ks);
-        const Seg& S = p.seg[seg];
-        const int row0 = rg * RS;
-        const int rows = min(RS, S.M - row0);
-        const int k0 = ks * KS;
-        const uint32_t bytes = (uint32_t)(NMAT * rows * KS * 2);
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        uint8_t* dst = ring + (size_t)slot * sc.stage_bytes;
-#pragma unroll
-        for (int mat = 0; mat < NMAT; ++mat) {
-          const uint16_t* W = mat == 0 ? S.W0 : S.W1;
-          if (KS == K) {
-            bulk_copy_g2s(dst + (size_t)mat * RS * KS * 2, W + (size_t)row0 * K,
-                          (uint32_t)(rows * K * 2), &full[slot], pol);
-          } else {
-            for (int r = 0; r < rows; ++r)
-              bulk_copy_g2s(dst + ((size_t)mat * RS + r) * KS * 2,
-                            W + (size_t)(row0 + r) * K + k0, (uint32_t)(KS * 2), &full[slot],
-                            pol);
-          }
-        }
-        flags[16 + slot] = i;
-      }
-      __threadfence_block();
-      flags[2] = 1;
-    }
-    return;
-  }
-
-  // ---------------- consumers ----------------------------------------------
   pdl_wait();
-  prologue_stats(p, stats, warp, lane);
-  consumer_sync(kConsumerThreads);
 
-  const int KG = sc.KG, RS = sc.RS, KS = sc.KS, S = sc.S;
-  const int wk = warp % KG;  // which slice of the row's chunks
-  const int r = warp / KG;   // which row of the stage
-  const int nch = KS >> 3;
-  const int c_lo = (wk * nch) / KG;
-  const int c_hi = ((wk + 1) * nch) / KG;
+  prologue_stats(p, stats, warp, lane);
+  __syncthreads();
+  stage_x<BT>(p, stats, xs, ks, tid);
+  __syncthreads();
+
+  const int nchx = sc.KS >> 3;  // chunks of x in shared memory
+  const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
+  const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
   float best_v = -INFINITY;
   int best_i = 0x7fffffff;
-  int cur_ks = -1;
+  bool abort = false;
+  int issued = npw < sc.NSW ? npw : sc.NSW;
 
-  for (int u = u0, i = 0; u < u1; ++u, ++i) {
-    const int slot = i % sc.NS;
-    int seg, rg, ks;
-    decode_unit(p, u, seg, rg, ks);
+  float acc[NMAT][RT][BT];
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
+
+  for (int q = 0; q < npw; ++q) {
+    const int slot = q % sc.NSW;
+    const int ti = q / sc.NP;
+    const int j = q - ti * sc.NP;
+    const int rg = rg0 + warp + ti * kWarps;
+    int seg, rgl;
+    decode_rg(p, rg, seg, rgl);
     const int Mseg = p.seg[seg].M;
-    const int row0 = rg * RS;
-    const int rows = min(RS, Mseg - row0);
-    if (ks != cur_ks) {
-      consumer_sync(kConsumerThreads);
-      stage_x<BT>(p, stats, xs, ks, tid);
-      consumer_sync(kConsumerThreads);
-      cur_ks = ks;
-    }
-    if (!flags[0]) {
-      if (!mbar_wait_bounded(&full[slot], (i / sc.NS) & 1, p.timeout_ns)) {
-        raise_device_error(p.err, DERR_TIMEOUT);
-        flags[0] = 1;
-      }
+    const int row0 = rgl * RT;
+    const int rows = min(RT, Mseg - row0);
+    const int len = min(sc.PC, sc.KS - j * sc.PC);
+    bool ok = abort || mbar_wait_bounded(&full[slot], (q / sc.NSW) & 1, p.timeout_ns);
+    if (__any_sync(0xffffffffu, !ok) && !abort) {
+      abort = true;
+      if (lane == 0) raise_device_error(p.err, DERR_TIMEOUT);
     }
 
-    float acc[NMAT][BT];
-#pragma unroll
-    for (int mat = 0; mat < NMAT; ++mat)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[mat][b] = 0.f;
-
-    if (r < rows) {
-      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.stage_bytes);
-      const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
+    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.piece_bytes);
+    const int xoff = (j * sc.PC) >> 3;
 #pragma unroll 2
-      for (int c = c_lo + lane; c < c_hi; c += 32) {
-        float wf[NMAT][8];
+    for (int c = lane; c < (len >> 3); c += 32) {
+      float wf[NMAT][RT][8];
 #pragma unroll
-        for (int mat = 0; mat < NMAT; ++mat) {
-          const uint4 w = st[(size_t)(mat * RS + r) * nch + c];
-          wf[mat][0] = bf16lo(w.x); wf[mat][1] = bf16hi(w.x);
-          wf[mat][2] = bf16lo(w.y); wf[mat][3] = bf16hi(w.y);
-          wf[mat][4] = bf16lo(w.z); wf[mat][5] = bf16hi(w.z);
-          wf[mat][6] = bf16lo(w.w); wf[mat][7] = bf16hi(w.w);
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const uint4 w = r < rows ? st[(size_t)(m * RT + r) * ncp + c] : make_uint4(0, 0, 0, 0);
+          wf[m][r][0] = bf16lo(w.x); wf[m][r][1] = bf16hi(w.x);
+          wf[m][r][2] = bf16lo(w.y); wf[m][r][3] = bf16hi(w.y);
+          wf[m][r][4] = bf16lo(w.z); wf[m][r][5] = bf16hi(w.z);
+          wf[m][r][6] = bf16lo(w.w); wf[m][r][7] = bf16hi(w.w);
         }
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          const uint4 xv = xs4[(size_t)b * nch + c];
-          float xf[8];
-          xf[0] = bf16lo(xv.x); xf[1] = bf16hi(xv.x); xf[2] = bf16lo(xv.y); xf[3] = bf16hi(xv.y);
-          xf[4] = bf16lo(xv.z); xf[5] = bf16hi(xv.z); xf[6] = bf16lo(xv.w); xf[7] = bf16hi(xv.w);
+      for (int b = 0; b < BT; ++b) {
+        const uint4 xv = xs4[(size_t)b * nchx + xoff + c];
+        const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
+                             bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
 #pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat)
+        for (int r = 0; r < RT; ++r)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[mat][b] = fmaf(wf[mat][j], xf[j], acc[mat][b]);
-        }
+          for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[m][r][b] = fmaf(wf[m][r][e], xf[e], acc[m][r][b]);
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-
-#pragma unroll
-    for (int mat = 0; mat < NMAT; ++mat)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[mat][b] = warp_sum(acc[mat][b]);
-
-    const int rowg = p.seg[seg].row_base + row0;  // first concatenated row of the group
-    if (KG == 1) {
-      if (r < rows) {
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-          if (lane == b && b < p.B) {
-            const float v1 = NMAT > 1 ? acc[NMAT - 1][b] : 0.f;
-            if (S == 1) {
-              apply_epilogue(p, seg, row0 + r, b, acc[0][b], v1, best_v, best_i);
-            } else {
-#pragma unroll
-              for (int mat = 0; mat < NMAT; ++mat)
-                p.part[((size_t)(ks * NMAT + mat) * p.B + b) * p.M_total + rowg + r] =
-                    acc[mat][b];
-            }
-          }
-        }
-      }
-    } else {
-      float* rb = red + (size_t)((i & 1) * kConsumerWarps + warp) * (NMAT * BT);
-      if (lane == 0) {
-#pragma unroll
-        for (int mat = 0; mat < NMAT; ++mat)
-#pragma unroll
-          for (int b = 0; b < BT; ++b) rb[mat * BT + b] = acc[mat][b];
-      }
-      consumer_sync(kConsumerThreads);
-      if (wk == 0 && r < rows && lane < p.B) {
-        const int b = lane;
-        float v[NMAT];
-#pragma unroll
-        for (int mat = 0; mat < NMAT; ++mat) {
-          float t = 0.f;
-          for (int g = 0; g < KG; ++g)
-            t += red[(size_t)((i & 1) * kConsumerWarps + r * KG + g) * (NMAT * BT) + mat * BT +
-                     b];
-          v[mat] = t;
-        }
-        if (S == 1) {
-          apply_epilogue(p, seg, row0 + r, b, v[0], NMAT > 1 ? v[NMAT - 1] : 0.f, best_v, best_i);
-        } else {
-#pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat)
-            p.part[((size_t)(ks * NMAT + mat) * p.B + b) * p.M_total + rowg + r] = v[mat];
-        }
-      }
+    if (lane == 0 && !abort && issued < npw) {
+      // every lane has finished reading this slot: refill it
+      fence_proxy_async_smem();
+      issue_piece<NMAT, RT>(p, issued, warp, rg0, k0, ring, full, pol);
+      ++issued;
     }
 
-    if (S > 1) {
-      // The last of the S splits of this row group adds the partials in split
-      // order and runs the epilogue.
-      consumer_sync(kConsumerThreads);
-      if (tid == 0) {
-        __threadfence();
-        const int gidx = p.seg[seg].rg_begin + rg;
-        const unsigned old = atomicAdd(&p.tickets[gidx], 1u);
-        const int last = old == (unsigned)(S - 1);
-        if (last) atomicExch(&p.tickets[gidx], 0u);
-        flags[1] = last;
-      }
-      consumer_sync(kConsumerThreads);
-      if (flags[1]) {
-        __threadfence();
-        for (int o = tid; o < rows * p.B; o += kConsumerThreads) {
-          const int rr = o / p.B;
-          const int b = o - rr * p.B;
-          float v[NMAT];
+    if (j == sc.NP - 1) {
+      // task complete: sum over lanes (every lane ends with every sum)
 #pragma unroll
-          for (int mat = 0; mat < NMAT; ++mat) {
-            float t = 0.f;
-            for (int s = 0; s < S; ++s)
-              t += __ldcg(&p.part[((size_t)(s * NMAT + mat) * p.B + b) * p.M_total + rowg + rr]);
-            v[mat] = t;
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) acc[m][r][b] = warp_sum(acc[m][r][b]);
+      const int rowg = p.seg[seg].row_base + row0;
+      if (sc.S == 1) {
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b)
+            if (lane == r * BT + b && r < rows && b < p.B)
+              apply_epilogue(p, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v,
+                             best_i);
+      } else {
+        // split-K: write this split's partials; the last split of the row
+        // group adds all splits in split order and runs the epilogue
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b)
+            if (lane == r * BT + b && r < rows && b < p.B) {
+#pragma unroll
+              for (int m = 0; m < NMAT; ++m)
+                p.part[((size_t)(ks * NMAT + m) * p.B + b) * p.M_total + rowg + r] = acc[m][r][b];
+            }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const unsigned old = atomicAdd(&p.tickets[rg], 1u);
+          last = old == (unsigned)(sc.S - 1);
+          if (last) atomicExch(&p.tickets[rg], 0u);
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          for (int o = lane; o < rows * p.B; o += 32) {
+            const int rr = o / p.B;
+            const int b = o - rr * p.B;
+            float v[NMAT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              float t = 0.f;
+              for (int s = 0; s < sc.S; ++s)
+                t += __ldcg(&p.part[((size_t)(s * NMAT + m) * p.B + b) * p.M_total + rowg + rr]);
+              v[m] = t;
+            }
+            float dv = -INFINITY;
+            int di = 0x7fffffff;
+            apply_epilogue(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di);
           }
-          float dv = -INFINITY;
-          int di = 0x7fffffff;
-          apply_epilogue(p, seg, row0 + rr, b, v[0], NMAT > 1 ? v[NMAT - 1] : 0.f, dv, di);
         }
       }
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
     }
   }
 
+  if (abort && lane == 0) {
+    // a wait ran out: no copy may still be landing when the CTA exits
+    for (int q = issued - sc.NSW; q < issued; ++q)
+      if (q >= 0) mbar_wait_bounded(&full[q % sc.NSW], (q / sc.NSW) & 1, p.timeout_ns);
+  }
+
   if (p.epilogue == EPI_ARGMAX) {
-    // CTA-level argmax per batch row, then the last CTA combines all CTAs.
-    if (lane < BT) {
-      argv[warp * BT + lane] = best_v;
-      argi[warp * BT + lane] = best_i;
-    }
-    consumer_sync(kConsumerThreads);
+    // per batch row: lanes r*BT + b hold a running best; combine the warps,
+    // then the last CTA (ticket) combines all CTAs
+    argv[warp * 32 + lane] = best_v;
+    argi[warp * 32 + lane] = best_i;
+    __syncthreads();
     if (tid < p.B) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
-      for (int w = 0; w < kConsumerWarps; ++w)
-        if (arg_better(argv[w * BT + tid], argi[w * BT + tid], bv, bi)) {
-          bv = argv[w * BT + tid];
-          bi = argi[w * BT + tid];
+      for (int w = 0; w < kWarps; ++w)
+        for (int r = 0; r < RT; ++r) {
+          const int l = r * BT + tid;
+          if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
+            bv = argv[w * 32 + l];
+            bi = argi[w * 32 + l];
+          }
         }
       p.arg_val[(size_t)blockIdx.x * p.B + tid] = bv;
       p.arg_idx[(size_t)blockIdx.x * p.B + tid] = bi;
-    }
-    consumer_sync(kConsumerThreads);
-    if (tid == 0) {
       __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) {
       const unsigned old = atomicAdd(p.arg_ticket, 1u);
       const int last = old == gridDim.x - 1;
       if (last) atomicExch(p.arg_ticket, 0u);
-      flags[1] = last;
+      flags[0] = last;
     }
-    consumer_sync(kConsumerThreads);
-    if (flags[1] && tid < p.B) {
+    __syncthreads();
+    if (flags[0] && tid < p.B) {
       __threadfence();
       float bv = -INFINITY;
       int bi = 0x7fffffff;
@@ -465,18 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       p.argmax_idx[tid] = bi;
-    }
-  }
-
-  if (flags[0] && tid == 0) {
-    // A wait ran out: let the producer finish, then wait (bounded) for every
-    // copy still in flight before the CTA's shared memory goes away.
-    const uint64_t t0 = global_ns();
-    while (!flags[2] && global_ns() - t0 < p.timeout_ns) {
-    }
-    for (int s = 0; s < sc.NS; ++s) {
-      const int last = flags[16 + s];
-      if (last >= 0) mbar_wait_bounded(&full[s], (last / sc.NS) & 1, p.timeout_ns);
     }
   }
 }
@@ -495,7 +458,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 2000000000ull};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 6144, 2000000000ull};
   return t;
 }
 
@@ -537,34 +500,37 @@ static int batch_template(int B) {
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 static constexpr int kXsMax = 64 * 1024;
-static constexpr int kStageTarget = 24 * 1024;
 static constexpr int kSmemMax = 227 * 1024;
+
+static int row_groups(GemvParams& p, int RT) {
+  int RG = 0;
+  for (int s = 0; s < p.nseg; ++s) {
+    p.seg[s].rg_begin = RG;
+    RG += (p.seg[s].M + RT - 1) / RT;
+  }
+  return RG;
+}
 
 // Choose the schedule.  force_S > 0 fixes the K split; force_S == 0 lets the
 // heuristic split skinny shapes; force_S < 0 forbids splitting.
 bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   const Tuning& tu = tuning();
   const int nsm = device_sm_count();
+  const int grid_target = tu.grid_cap > 0 ? tu.grid_cap : nsm;
+  const int warps_total = grid_target * kWarps;
   Sched sc;
   memset(&sc, 0, sizeof sc);
   sc.BT = batch_template(p.B);
   const int K = p.K, nmat = p.nmat;
 
-  int KG = 1;
-  if (tu.force_kg == 1 || tu.force_kg == 2 || tu.force_kg == 4 || tu.force_kg == 8) {
-    KG = tu.force_kg;
-  } else {
-    while (KG < kConsumerWarps && (long)(kConsumerWarps / KG) * K * 2 * nmat > kStageTarget)
-      KG *= 2;
-  }
-  sc.KG = KG;
-  sc.RS = kConsumerWarps / KG;
-
-  int RG = 0;
-  for (int s = 0; s < p.nseg; ++s) {
-    p.seg[s].rg_begin = RG;
-    RG += (p.seg[s].M + sc.RS - 1) / sc.RS;
-  }
+  // rows per task: 2 when the batch is small enough for the accumulators and
+  // there are enough tasks to keep every warp busy, else 1
+  int RT = sc.BT <= 8 ? 2 : 1;
+  if (tu.force_rt == 1 || tu.force_rt == 2) RT = tu.force_rt;
+  if (sc.BT > 8) RT = 1;
+  if (RT == 2 && tu.force_rt == 0 && row_groups(p, 2) < 2 * warps_total) RT = 1;
+  sc.RT = RT;
+  const int RG = row_groups(p, RT);
   sc.RG = RG;
 
   auto valid_split = [&](int S) { return S >= 1 && K % (8 * S) == 0; };
@@ -575,14 +541,14 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   } else if (force_S == 0) {
     if (tu.force_ksplit > 0) {
       S = tu.force_ksplit;
-    } else if (RG < nsm / 2) {
-      // skinny: split K until the units cover about half the SMs, keeping at
-      // least 32 chunks per warp slice
+    } else if (RG < warps_total / 2) {
+      // skinny: split K until the tasks cover about half of the warps,
+      // keeping at least 256 columns (one chunk per lane) per split
       for (int s = 2; s <= 16; ++s) {
         if (!valid_split(s)) continue;
-        if ((K / s) / 8 < 32 * KG) break;
+        if (K / s < 256) break;
         S = s;
-        if (RG * s >= nsm / 2) break;
+        if (RG * s >= warps_total / 2) break;
       }
     }
   }
@@ -610,41 +576,52 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   }
   sc.S = S;
   sc.KS = K / S;
-  sc.units = RG * S;
-  sc.stage_bytes = align_up(nmat * sc.RS * sc.KS * 2, 128);
+
+  // pieces: about piece_bytes each, evenly sized, multiples of 8 columns
+  const int target = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
+  int pc = target / (nmat * RT * 2);
+  pc = pc < 256 ? 256 : pc;
+  if (pc >= sc.KS) {
+    sc.PC = sc.KS;
+    sc.NP = 1;
+  } else {
+    sc.NP = (sc.KS + pc - 1) / pc;
+    sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 8);
+    sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
+  }
+  sc.piece_bytes = align_up(nmat * RT * sc.PC * 2, 128);
 
   int off = 0;
   sc.off_bar = off;
-  off += 2 * kMaxStages * 8;
+  off += kWarps * kMaxStages * 8;
   sc.off_flags = off;
-  off += 256;
+  off += 128;
   sc.off_stats = off;
   off += align_up(sc.BT * 2 * 4, 16);
   sc.off_arg = off;
-  off += align_up(kConsumerWarps * sc.BT * 8, 16);
-  sc.off_red = off;
-  off += align_up(2 * kConsumerWarps * nmat * sc.BT * 4, 16);
+  off += kWarps * 32 * 8;
   sc.off_xs = align_up(off, 128);
   off = sc.off_xs + align_up(sc.BT * sc.KS * 2, 128);
   sc.off_ring = align_up(off, 128);
   int ring_budget = tu.ring_bytes > 0 ? tu.ring_bytes : 96 * 1024;
   if (sc.off_ring + ring_budget > kSmemMax) ring_budget = kSmemMax - sc.off_ring;
-  int NS = ring_budget / sc.stage_bytes;
-  if (NS > kMaxStages) NS = kMaxStages;
-  if (NS < 2) {
-    if (sc.off_ring + 2 * sc.stage_bytes <= kSmemMax) {
-      NS = 2;
+  int NSW = ring_budget / (kWarps * sc.piece_bytes);
+  if (NSW > kMaxStages) NSW = kMaxStages;
+  if (NSW < 2) {
+    if (sc.off_ring + 2 * kWarps * sc.piece_bytes <= kSmemMax) {
+      NSW = 2;
     } else {
-      snprintf(why, why_len, "stage of %d bytes does not fit twice in shared memory",
-               sc.stage_bytes);
+      snprintf(why, why_len, "pieces of %d bytes do not fit twice per warp", sc.piece_bytes);
       return false;
     }
   }
-  sc.NS = NS;
-  sc.smem_bytes = sc.off_ring + NS * sc.stage_bytes;
-  const int cap = tu.grid_cap > 0 ? tu.grid_cap : nsm;
-  sc.grid = sc.units < cap ? sc.units : cap;
-  if (sc.grid < 1) sc.grid = 1;
+  sc.NSW = NSW;
+  sc.smem_bytes = sc.off_ring + kWarps * NSW * sc.piece_bytes;
+  int Gs = grid_target / S;
+  if (Gs < 1) Gs = 1;
+  if (Gs > RG) Gs = RG;
+  sc.Gs = Gs;
+  sc.grid = S * Gs;
   p.sc = sc;
   p.M_total = 0;
   for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
@@ -699,29 +676,34 @@ bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes) {
 
 typedef void (*GemvKernel)(const GemvParams);
 
-static GemvKernel pick_kernel(int BT, int nmat) {
-#define WS_PICK(bt)                                                                    \
-  case bt:                                                                             \
-    return nmat == 2 ? (GemvKernel)k_stream_gemv<bt, 2> : (GemvKernel)k_stream_gemv<bt, 1>;
+static GemvKernel pick_kernel(int BT, int nmat, int RT) {
+#define WS_PICK2(bt)                                                                  \
+  case bt:                                                                            \
+    if (RT == 2)                                                                      \
+      return nmat == 2 ? (GemvKernel)k_stream_gemv<bt, 2, 2>                          \
+                       : (GemvKernel)k_stream_gemv<bt, 1, 2>;                         \
+    return nmat == 2 ? (GemvKernel)k_stream_gemv<bt, 2, 1> : (GemvKernel)k_stream_gemv<bt, 1, 1>;
   switch (BT) {
-    WS_PICK(1)
-    WS_PICK(2)
-    WS_PICK(4)
-    WS_PICK(8)
-    WS_PICK(16)
+    WS_PICK2(1)
+    WS_PICK2(2)
+    WS_PICK2(4)
+    WS_PICK2(8)
+    case 16:
+      if (RT != 1) return nullptr;
+      return nmat == 2 ? (GemvKernel)k_stream_gemv<16, 2, 1> : (GemvKernel)k_stream_gemv<16, 1, 1>;
     default:
       return nullptr;
   }
-#undef WS_PICK
+#undef WS_PICK2
 }
 
 static bool ensure_smem_attr(GemvKernel k) {
   static std::mutex mu;
-  static unsigned long long done[64][10] = {{0}};
+  static unsigned long long done[64][32] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lk(mu);
-  for (int i = 0; i < 10; ++i) {
+  for (int i = 0; i < 32; ++i) {
     if (done[dev][i] == (unsigned long long)(uintptr_t)k) return true;
     if (done[dev][i] == 0) {
       if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -735,12 +717,12 @@ static bool ensure_smem_attr(GemvKernel k) {
 }
 
 bool prepare_gemv(const GemvParams& p) {
-  GemvKernel k = pick_kernel(p.sc.BT, p.nmat);
+  GemvKernel k = pick_kernel(p.sc.BT, p.nmat, p.sc.RT);
   return k && ensure_smem_attr(k);
 }
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t stream, bool pdl) {
-  GemvKernel k = pick_kernel(p.sc.BT, p.nmat);
+  GemvKernel k = pick_kernel(p.sc.BT, p.nmat, p.sc.RT);
   if (!k) return cudaErrorInvalidValue;
   if (!ensure_smem_attr(k)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
@@ -1062,14 +1044,16 @@ void ws_get_tuning(ws_tuning* t) {
   t->ring_bytes = tu.ring_bytes;
   t->grid_cap = tu.grid_cap;
   t->force_ksplit = tu.force_ksplit;
-  t->force_kg = tu.force_kg;
+  t->force_rt = tu.force_rt;
   t->evict_first = tu.evict_first;
+  t->piece_bytes = tu.piece_bytes;
   t->timeout_ns = tu.timeout_ns;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
   if (!t || t->ring_bytes < 0 || t->ring_bytes > kSmemMax || t->grid_cap < 0 ||
-      t->force_ksplit < 0 || t->force_kg < 0 || t->timeout_ns == 0) {
+      t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt > 2 || t->piece_bytes < 0 ||
+      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -1077,8 +1061,9 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.ring_bytes = t->ring_bytes;
   tu.grid_cap = t->grid_cap;
   tu.force_ksplit = t->force_ksplit;
-  tu.force_kg = t->force_kg;
+  tu.force_rt = t->force_rt;
   tu.evict_first = t->evict_first;
+  tu.piece_bytes = t->piece_bytes;
   tu.timeout_ns = t->timeout_ns;
   return WS_OK;
 }
@@ -1104,14 +1089,14 @@ ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind, i
     return WS_ERR_SHAPE;
   }
   const Sched& sc = p.sc;
-  out->KG = sc.KG;
-  out->RS = sc.RS;
+  out->RT = sc.RT;
   out->S = sc.S;
   out->KS = sc.KS;
-  out->NS = sc.NS;
-  out->stage_bytes = sc.stage_bytes;
+  out->PC = sc.PC;
+  out->NP = sc.NP;
+  out->NSW = sc.NSW;
+  out->piece_bytes = sc.piece_bytes;
   out->RG = sc.RG;
-  out->units = sc.units;
   out->grid = sc.grid;
   out->smem_bytes = sc.smem_bytes;
   return WS_OK;
@@ -1130,35 +1115,42 @@ long ws_debug_gemv_copies(int M, int K, int B, int nmat, int allow_split, int ct
   if (!plan_gemv(p, allow_split ? 0 : -1, why, sizeof why)) return -1;
   const Sched& sc = p.sc;
   if (cta < 0 || cta >= sc.grid) return -1;
-  int u0, u1;
-  cta_units(cta, sc.grid, sc.units, u0, u1);
+  int ks, rg0, rg1;
+  cta_range(sc, cta, ks, rg0, rg1);
+  const int k0 = ks * sc.KS;
+  const long long warp_ring = (long long)sc.NSW * sc.piece_bytes;
   long n = 0;
-  for (int u = u0, i = 0; u < u1; ++u, ++i) {
-    const int slot = i % sc.NS;
-    int seg, rg, ks;
-    decode_unit(p, u, seg, rg, ks);
-    const int row0 = rg * sc.RS;
-    const int rows = (sc.RS < M - row0) ? sc.RS : M - row0;
-    const int k0 = ks * sc.KS;
-    for (int mat = 0; mat < nmat; ++mat) {
-      const long long mat_off = (long long)mat * M * K * 2;
-      if (sc.KS == K) {
-        if (triples && n < max_triples) {
-          triples[3 * n] = mat_off + (long long)row0 * K * 2;
-          triples[3 * n + 1] =
-              (long long)slot * sc.stage_bytes + (long long)mat * sc.RS * sc.KS * 2;
-          triples[3 * n + 2] = (long long)rows * K * 2;
-        }
-        ++n;
-      } else {
-        for (int r = 0; r < rows; ++r) {
+  // the same order as issue_piece: warp by warp, piece by piece
+  for (int w = 0; w < kWarps; ++w) {
+    const int npw = warp_tasks(rg0, rg1, w) * sc.NP;
+    for (int q = 0; q < npw; ++q) {
+      const int ti = q / sc.NP;
+      const int j = q - ti * sc.NP;
+      int seg, rgl;
+      decode_rg(p, rg0 + w + ti * kWarps, seg, rgl);
+      const int row0 = rgl * sc.RT;
+      const int rows = (sc.RT < M - row0) ? sc.RT : M - row0;
+      const int c0 = k0 + j * sc.PC;
+      const int len = (sc.PC < sc.KS - j * sc.PC) ? sc.PC : sc.KS - j * sc.PC;
+      const long long dst0 = w * warp_ring + (long long)(q % sc.NSW) * sc.piece_bytes;
+      for (int mat = 0; mat < nmat; ++mat) {
+        const long long mat_off = (long long)mat * M * K * 2;
+        if (len == K) {
           if (triples && n < max_triples) {
-            triples[3 * n] = mat_off + ((long long)(row0 + r) * K + k0) * 2;
-            triples[3 * n + 1] =
-                (long long)slot * sc.stage_bytes + ((long long)mat * sc.RS + r) * sc.KS * 2;
-            triples[3 * n + 2] = (long long)sc.KS * 2;
+            triples[3 * n] = mat_off + (long long)row0 * K * 2;
+            triples[3 * n + 1] = dst0 + (long long)mat * sc.RT * sc.PC * 2;
+            triples[3 * n + 2] = (long long)rows * K * 2;
           }
           ++n;
+        } else {
+          for (int r = 0; r < rows; ++r) {
+            if (triples && n < max_triples) {
+              triples[3 * n] = mat_off + ((long long)(row0 + r) * K + c0) * 2;
+              triples[3 * n + 1] = dst0 + ((long long)mat * sc.RT + r) * sc.PC * 2;
+              triples[3 * n + 2] = (long long)len * 2;
+            }
+            ++n;
+          }
         }
       }
     }
