@@ -301,7 +301,7 @@ typedef struct {
   int ring_bytes;      /* shared-memory weight rings per CTA, all warps        */
   int grid_cap;        /* CTAs per GEMV launch (0: one per SM)                 */
   int force_ksplit;    /* K splits (0: heuristic)                              */
-  int force_rt;        /* rows per warp task, 1 or 2 (0: heuristic)            */
+  int force_rt;        /* rows per warp task, 1, 2 or 4 (0: heuristic)         */
   int evict_first;     /* stream weights with an L2 evict-first hint           */
   int piece_bytes;     /* target bytes of one ring stage                       */
   unsigned long long timeout_ns; /* bound of every device wait                 */

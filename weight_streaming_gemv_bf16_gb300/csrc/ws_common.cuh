@@ -64,7 +64,7 @@ struct Sched {
   int grid;         // S * Gs
   int BT;           // batch the kernel is instantiated for (>= B)
   int smem_bytes;
-  int off_bar, off_flags, off_stats, off_arg, off_xs, off_ring;
+  int off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
 };
 
 struct GemvParams {

@@ -1,32 +1,7 @@
-// ws_gemv.cu -- the streaming GEMV kernel, its schedule, and the GEMV-family
-// entry points of the C ABI.
-//
-// y[b][m] = sum_k W[m][k] * x[b][k], bf16 W and x, fp32 accumulation ("One
-// Token, Kernel by Kernel: A Decode Step on a Laptop GPU", Step 1, "What one
-// block launches").  The design for GB300:
-//  * every warp is an independent pipeline: it owns whole rows (a task of
-//    RT rows, one K split), streams them from HBM through its own ring of
-//    shared-memory stages with 1-D bulk async copies (cp.async.bulk, mbarrier
-//    completion, L2 evict-first since each weight byte is read once), and
-//    refills a stage as soon as its lanes have read it; no warp ever waits for
-//    another, so one slow step does not stall the CTA;
-//  * the first stages are issued before griddepcontrol.wait: weights do not
-//    depend on the previous op, so inside a chain the next op's weights stream
-//    in while the previous op finishes (programmatic dependent launch);
-//  * lanes take 16-byte chunks of each row, unpack bf16 pairs to fp32 and
-//    accumulate with FMA; at the end of a task a butterfly of warp shuffles
-//    gives every lane every sum, and lane r*B+b runs the epilogue of output
-//    (row r, batch b);
-//  * split-K for skinny shapes: partial sums go to a workspace and the last
-//    of a row group's splits (atomic ticket) adds them in split order, so the
-//    result is the same whatever order the CTAs finish in; the ticket is
-//    reset for the next call or graph replay ("Making small PyTorch ops
-//    faster on a laptop GPU", "A full decode step is a different story": the
-//    last block to finish merges and resets the ticket);
-//  * the activations are normalised once per CTA (RMSNorm or LayerNorm
-//    prologue, fp32, rounded once to bf16) into shared memory.
-// There are no tensor cores here: at batch <= 16 this is a vector product.
-#include <cuda_bf16.h>
+// ws_gemv_host.cu -- host side of the streaming GEMV: the schedule (rows per
+// warp task, K splits, pieces, ring depth, grid), workspace layout, kernel
+// selection and launch, and the GEMV-family entry points of the C ABI.  The
+// kernel itself is in ws_gemv_kernel.cuh.
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -37,414 +12,14 @@
 
 #include "wsgemv.h"
 #include "ws_common.cuh"
-#include "ws_device.cuh"
+#include "ws_gemv_kernel.cuh"
 
 namespace ws {
 
+// Device error flag: set by a bounded wait that ran out (read by
+// ws_device_error).
 __device__ int g_device_error;
 
-__device__ __forceinline__ float bf16_round(float v) {
-  return __bfloat162float(__float2bfloat16_rn(v));
-}
-
-__device__ __forceinline__ void raise_device_error(int* err, int code) {
-  if (err) atomicExch(err, code);
-}
-
-// Epilogue for one output element (segment seg, row m, batch row b).  v0 is
-// the dot product with the first matrix, v1 with the second (SwiGLU up).
-__device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int m, int b,
-                                               float v0, float v1, float& best_v, int& best_i) {
-  const Seg& S = p.seg[seg];
-  const size_t o = (size_t)b * S.M + m;
-  switch (p.epilogue) {
-    case EPI_F32:
-      static_cast<float*>(S.out)[o] = v0;
-      break;
-    case EPI_BF16:
-      static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(v0);
-      break;
-    case EPI_RESID: {
-      const float* src = p.res_in ? p.res_in : static_cast<const float*>(S.out);
-      static_cast<float*>(S.out)[o] = src[o] + v0;
-      break;
-    }
-    case EPI_BIAS_GELU: {
-      const float t = bf16_round(v0 + __uint_as_float((uint32_t)p.bias[m] << 16));
-      const float z = 0.5f * t * (1.0f + erff(t * 0.70710678118654752f));
-      static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(z);
-      break;
-    }
-    case EPI_SWIGLU: {
-      const float sv = v0 / (1.0f + expf(-v0)) * v1;
-      static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(sv);
-      break;
-    }
-    case EPI_ARGMAX: {
-      if (p.logits) p.logits[o] = v0;
-      const int row = S.row_base + m;
-      if (arg_better(v0, row, best_v, best_i)) {
-        best_v = v0;
-        best_i = row;
-      }
-      break;
-    }
-    default:
-      break;
-  }
-}
-
-__device__ __forceinline__ float load_x(const GemvParams& p, int b, int k) {
-  if (p.x_dtype == DT_F32) return static_cast<const float*>(p.x)[(size_t)b * p.K + k];
-  const uint16_t h = static_cast<const uint16_t*>(p.x)[(size_t)b * p.K + k];
-  return __uint_as_float((uint32_t)h << 16);
-}
-
-// Per-row statistics of the prologue over the full K: RMSNorm r = rsqrt(mean
-// x^2 + eps); LayerNorm mean and rstd = rsqrt(var + eps).  One warp per row.
-__device__ void prologue_stats(const GemvParams& p, float* stats, int warp, int lane) {
-  if (p.prologue == PRO_NONE) return;
-  for (int b = warp; b < p.B; b += kWarps) {
-    if (p.prologue == PRO_RMSNORM) {
-      float ss = 0.f;
-      for (int k = lane; k < p.K; k += 32) {
-        const float v = load_x(p, b, k);
-        ss = fmaf(v, v, ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) stats[2 * b] = rsqrtf(ss / (float)p.K + p.eps);
-    } else {
-      float s = 0.f;
-      for (int k = lane; k < p.K; k += 32) s += load_x(p, b, k);
-      const float mean = warp_sum(s) / (float)p.K;
-      float v = 0.f;
-      for (int k = lane; k < p.K; k += 32) {
-        const float d = load_x(p, b, k) - mean;
-        v = fmaf(d, d, v);
-      }
-      v = warp_sum(v) / (float)p.K;
-      if (lane == 0) {
-        stats[2 * b] = mean;
-        stats[2 * b + 1] = rsqrtf(v + p.eps);
-      }
-    }
-  }
-}
-
-// Stage columns [k0, k0 + KS) of the (normalised) activations as bf16 into
-// shared memory, [BT][KS]; rows b >= B are zero.
-template <int BT>
-__device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, int ks, int tid) {
-  const int KS = p.sc.KS;
-  const int nch = KS >> 3;
-  const int k0 = ks * KS;
-  for (int o = tid; o < BT * nch; o += kThreads) {
-    const int b = o / nch;
-    const int c = o - b * nch;
-    uint4 out = make_uint4(0u, 0u, 0u, 0u);
-    if (b < p.B) {
-      const int k = k0 + c * 8;
-      if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16) {
-        out = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
-                                              (size_t)b * p.K + k);
-      } else {
-        float v[8];
-        if (p.x_dtype == DT_F32) {
-          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) +
-                                                              (size_t)b * p.K + k);
-          const float4 a = src[0], c2 = src[1];
-          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-          v[4] = c2.x; v[5] = c2.y; v[6] = c2.z; v[7] = c2.w;
-        } else {
-          const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
-                                                          (size_t)b * p.K + k);
-          v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
-          v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
-        }
-        if (p.prologue == PRO_RMSNORM) {
-          const float r = stats[2 * b];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            v[j] = v[j] * r * __uint_as_float((uint32_t)p.gamma[k + j] << 16);
-        } else if (p.prologue == PRO_LAYERNORM) {
-          const float mean = stats[2 * b], rstd = stats[2 * b + 1];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            v[j] = (v[j] - mean) * rstd * __uint_as_float((uint32_t)p.gamma[k + j] << 16) +
-                   __uint_as_float((uint32_t)p.beta[k + j] << 16);
-        }
-        uint32_t w[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * j]));
-          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * j + 1]));
-          w[j] = lo | (hi << 16);
-        }
-        out = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    reinterpret_cast<uint4*>(xs)[(size_t)b * nch + c] = out;
-  }
-}
-
-// Issue the bulk copies of piece q of this warp's task list into its ring.
-template <int NMAT, int RT>
-__device__ __forceinline__ void issue_piece(const GemvParams& p, int q, int warp, int rg0, int k0,
-                                            uint8_t* ring, uint64_t* full, uint64_t pol) {
-  const Sched& sc = p.sc;
-  const int ti = q / sc.NP;
-  const int j = q - ti * sc.NP;
-  int seg, rgl;
-  decode_rg(p, rg0 + warp + ti * kWarps, seg, rgl);
-  const Seg& S = p.seg[seg];
-  const int row0 = rgl * RT;
-  const int rows = min(RT, S.M - row0);
-  const int c0 = k0 + j * sc.PC;
-  const int len = min(sc.PC, sc.KS - j * sc.PC);
-  const int slot = q % sc.NSW;
-  uint8_t* dst = ring + (size_t)slot * sc.piece_bytes;
-  const int K = p.K;
-  mbar_arrive_expect_tx(&full[slot], (uint32_t)(NMAT * rows * len * 2));
-#pragma unroll
-  for (int mat = 0; mat < NMAT; ++mat) {
-    const uint16_t* W = mat == 0 ? S.W0 : S.W1;
-    if (len == K) {  // whole rows: one contiguous copy
-      bulk_copy_g2s(dst + (size_t)mat * RT * sc.PC * 2, W + (size_t)row0 * K,
-                    (uint32_t)(rows * K * 2), &full[slot], pol);
-    } else {
-      for (int r = 0; r < rows; ++r)
-        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * sc.PC * 2, W + (size_t)(row0 + r) * K + c0,
-                      (uint32_t)(len * 2), &full[slot], pol);
-    }
-  }
-}
-
-template <int BT, int NMAT, int RT>
-__global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant__ GemvParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const Sched& sc = p.sc;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sc.off_bar) + warp * kMaxStages;
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + sc.off_flags);
-  float* stats = reinterpret_cast<float*>(smem + sc.off_stats);
-  float* argv = reinterpret_cast<float*>(smem + sc.off_arg);
-  int* argi = reinterpret_cast<int*>(argv + kWarps * 32);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sc.off_xs);
-  uint8_t* ring = smem + sc.off_ring + (size_t)warp * sc.NSW * sc.piece_bytes;
-
-  int ks, rg0, rg1;
-  cta_range(sc, blockIdx.x, ks, rg0, rg1);
-  const int k0 = ks * sc.KS;
-  const int npw = warp_tasks(rg0, rg1, warp) * sc.NP;  // pieces of this warp
-  uint64_t pol = 0;
-
-  if (lane == 0) {
-    for (int s = 0; s < sc.NSW; ++s) mbar_init(&full[s], 1);
-    fence_mbar_init();
-    pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-    // Weights do not depend on the previous kernel: start streaming them
-    // before waiting for it.
-    for (int q = 0; q < sc.NSW && q < npw; ++q)
-      issue_piece<NMAT, RT>(p, q, warp, rg0, k0, ring, full, pol);
-  }
-  pdl_launch_dependents();
-  pdl_wait();
-
-  prologue_stats(p, stats, warp, lane);
-  __syncthreads();
-  stage_x<BT>(p, stats, xs, ks, tid);
-  __syncthreads();
-
-  const int nchx = sc.KS >> 3;  // chunks of x in shared memory
-  const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
-  const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
-  float best_v = -INFINITY;
-  int best_i = 0x7fffffff;
-  bool abort = false;
-  int issued = npw < sc.NSW ? npw : sc.NSW;
-
-  float acc[NMAT][RT][BT];
-#pragma unroll
-  for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-    for (int r = 0; r < RT; ++r)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
-
-  for (int q = 0; q < npw; ++q) {
-    const int slot = q % sc.NSW;
-    const int ti = q / sc.NP;
-    const int j = q - ti * sc.NP;
-    const int rg = rg0 + warp + ti * kWarps;
-    int seg, rgl;
-    decode_rg(p, rg, seg, rgl);
-    const int Mseg = p.seg[seg].M;
-    const int row0 = rgl * RT;
-    const int rows = min(RT, Mseg - row0);
-    const int len = min(sc.PC, sc.KS - j * sc.PC);
-    bool ok = abort || mbar_wait_bounded(&full[slot], (q / sc.NSW) & 1, p.timeout_ns);
-    if (__any_sync(0xffffffffu, !ok) && !abort) {
-      abort = true;
-      if (lane == 0) raise_device_error(p.err, DERR_TIMEOUT);
-    }
-
-    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.piece_bytes);
-    const int xoff = (j * sc.PC) >> 3;
-#pragma unroll 2
-    for (int c = lane; c < (len >> 3); c += 32) {
-      float wf[NMAT][RT][8];
-#pragma unroll
-      for (int r = 0; r < RT; ++r)
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint4 w = r < rows ? st[(size_t)(m * RT + r) * ncp + c] : make_uint4(0, 0, 0, 0);
-          wf[m][r][0] = bf16lo(w.x); wf[m][r][1] = bf16hi(w.x);
-          wf[m][r][2] = bf16lo(w.y); wf[m][r][3] = bf16hi(w.y);
-          wf[m][r][4] = bf16lo(w.z); wf[m][r][5] = bf16hi(w.z);
-          wf[m][r][6] = bf16lo(w.w); wf[m][r][7] = bf16hi(w.w);
-        }
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        const uint4 xv = xs4[(size_t)b * nchx + xoff + c];
-        const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
-                             bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[m][r][b] = fmaf(wf[m][r][e], xf[e], acc[m][r][b]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0 && !abort && issued < npw) {
-      // every lane has finished reading this slot: refill it
-      fence_proxy_async_smem();
-      issue_piece<NMAT, RT>(p, issued, warp, rg0, k0, ring, full, pol);
-      ++issued;
-    }
-
-    if (j == sc.NP - 1) {
-      // task complete: sum over lanes (every lane ends with every sum)
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int b = 0; b < BT; ++b) acc[m][r][b] = warp_sum(acc[m][r][b]);
-      const int rowg = p.seg[seg].row_base + row0;
-      if (sc.S == 1) {
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int b = 0; b < BT; ++b)
-            if (lane == r * BT + b && r < rows && b < p.B)
-              apply_epilogue(p, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v,
-                             best_i);
-      } else {
-        // split-K: write this split's partials; the last split of the row
-        // group adds all splits in split order and runs the epilogue
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int b = 0; b < BT; ++b)
-            if (lane == r * BT + b && r < rows && b < p.B) {
-#pragma unroll
-              for (int m = 0; m < NMAT; ++m)
-                p.part[((size_t)(ks * NMAT + m) * p.B + b) * p.M_total + rowg + r] = acc[m][r][b];
-            }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-          const unsigned old = atomicAdd(&p.tickets[rg], 1u);
-          last = old == (unsigned)(sc.S - 1);
-          if (last) atomicExch(&p.tickets[rg], 0u);
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          for (int o = lane; o < rows * p.B; o += 32) {
-            const int rr = o / p.B;
-            const int b = o - rr * p.B;
-            float v[NMAT];
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-              float t = 0.f;
-              for (int s = 0; s < sc.S; ++s)
-                t += __ldcg(&p.part[((size_t)(s * NMAT + m) * p.B + b) * p.M_total + rowg + rr]);
-              v[m] = t;
-            }
-            float dv = -INFINITY;
-            int di = 0x7fffffff;
-            apply_epilogue(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di);
-          }
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
-    }
-  }
-
-  if (abort && lane == 0) {
-    // a wait ran out: no copy may still be landing when the CTA exits
-    for (int q = issued - sc.NSW; q < issued; ++q)
-      if (q >= 0) mbar_wait_bounded(&full[q % sc.NSW], (q / sc.NSW) & 1, p.timeout_ns);
-  }
-
-  if (p.epilogue == EPI_ARGMAX) {
-    // per batch row: lanes r*BT + b hold a running best; combine the warps,
-    // then the last CTA (ticket) combines all CTAs
-    argv[warp * 32 + lane] = best_v;
-    argi[warp * 32 + lane] = best_i;
-    __syncthreads();
-    if (tid < p.B) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int w = 0; w < kWarps; ++w)
-        for (int r = 0; r < RT; ++r) {
-          const int l = r * BT + tid;
-          if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
-            bv = argv[w * 32 + l];
-            bi = argi[w * 32 + l];
-          }
-        }
-      p.arg_val[(size_t)blockIdx.x * p.B + tid] = bv;
-      p.arg_idx[(size_t)blockIdx.x * p.B + tid] = bi;
-      __threadfence();
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const unsigned old = atomicAdd(p.arg_ticket, 1u);
-      const int last = old == gridDim.x - 1;
-      if (last) atomicExch(p.arg_ticket, 0u);
-      flags[0] = last;
-    }
-    __syncthreads();
-    if (flags[0] && tid < p.B) {
-      __threadfence();
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int c = 0; c < (int)gridDim.x; ++c) {
-        const float v = __ldcg(&p.arg_val[(size_t)c * p.B + tid]);
-        const int ix = __ldcg(&p.arg_idx[(size_t)c * p.B + tid]);
-        if (arg_better(v, ix, bv, bi)) {
-          bv = v;
-          bi = ix;
-        }
-      }
-      p.argmax_idx[tid] = bi;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -523,12 +98,15 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   sc.BT = batch_template(p.B);
   const int K = p.K, nmat = p.nmat;
 
-  // rows per task: 2 when the batch is small enough for the accumulators and
-  // there are enough tasks to keep every warp busy, else 1
-  int RT = sc.BT <= 8 ? 2 : 1;
-  if (tu.force_rt == 1 || tu.force_rt == 2) RT = tu.force_rt;
-  if (sc.BT > 8) RT = 1;
-  if (RT == 2 && tu.force_rt == 0 && row_groups(p, 2) < 2 * warps_total) RT = 1;
+  // rows per task: as many as the accumulators allow (4 up to batch 4, 2 up
+  // to batch 8, else 1) while there are still two tasks per warp
+  const int rt_max = sc.BT <= 4 ? 4 : (sc.BT <= 8 ? 2 : 1);
+  int RT = rt_max;
+  if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
+    RT = tu.force_rt < rt_max ? tu.force_rt : rt_max;
+  } else {
+    while (RT > 1 && row_groups(p, RT) < 2 * warps_total) RT /= 2;
+  }
   sc.RT = RT;
   const int RG = row_groups(p, RT);
   sc.RG = RG;
@@ -598,6 +176,8 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   off += 128;
   sc.off_stats = off;
   off += align_up(sc.BT * 2 * 4, 16);
+  sc.off_red = off;
+  off += align_up((kWarps + 1) * sc.BT * 4, 16);
   sc.off_arg = off;
   off += kWarps * 32 * 8;
   sc.off_xs = align_up(off, 128);
@@ -674,27 +254,10 @@ bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes) {
   return true;
 }
 
-typedef void (*GemvKernel)(const GemvParams);
-
 static GemvKernel pick_kernel(int BT, int nmat, int RT) {
-#define WS_PICK2(bt)                                                                  \
-  case bt:                                                                            \
-    if (RT == 2)                                                                      \
-      return nmat == 2 ? (GemvKernel)k_stream_gemv<bt, 2, 2>                          \
-                       : (GemvKernel)k_stream_gemv<bt, 1, 2>;                         \
-    return nmat == 2 ? (GemvKernel)k_stream_gemv<bt, 2, 1> : (GemvKernel)k_stream_gemv<bt, 1, 1>;
-  switch (BT) {
-    WS_PICK2(1)
-    WS_PICK2(2)
-    WS_PICK2(4)
-    WS_PICK2(8)
-    case 16:
-      if (RT != 1) return nullptr;
-      return nmat == 2 ? (GemvKernel)k_stream_gemv<16, 2, 1> : (GemvKernel)k_stream_gemv<16, 1, 1>;
-    default:
-      return nullptr;
-  }
-#undef WS_PICK2
+  if (BT <= 2) return pick_kernel_b12(BT, nmat, RT);
+  if (BT == 4) return pick_kernel_b4(BT, nmat, RT);
+  return pick_kernel_b816(BT, nmat, RT);
 }
 
 static bool ensure_smem_attr(GemvKernel k) {
@@ -1052,7 +615,8 @@ void ws_get_tuning(ws_tuning* t) {
 
 ws_status ws_set_tuning(const ws_tuning* t) {
   if (!t || t->ring_bytes < 0 || t->ring_bytes > kSmemMax || t->grid_cap < 0 ||
-      t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt > 2 || t->piece_bytes < 0 ||
+      t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt == 3 || t->force_rt > 4 ||
+      t->piece_bytes < 0 ||
       t->piece_bytes > 64 * 1024 || t->timeout_ns == 0) {
     set_error("bad tuning values");
     return WS_ERR_ARG;

@@ -1,0 +1,15 @@
+// Streaming GEMV instantiations for batch 3-4 (rows per task 1, 2, 4).
+#include "ws_gemv_kernel.cuh"
+
+namespace ws {
+
+#define WS_INST(bt, nm, rt) \
+  if (BT == bt && nmat == nm && RT == rt) return (GemvKernel)k_stream_gemv<bt, nm, rt>;
+
+GemvKernel pick_kernel_b4(int BT, int nmat, int RT) {
+  WS_INST(4, 1, 1) WS_INST(4, 1, 2) WS_INST(4, 1, 4)
+  WS_INST(4, 2, 1) WS_INST(4, 2, 2) WS_INST(4, 2, 4)
+  return nullptr;
+}
+
+}  // namespace ws

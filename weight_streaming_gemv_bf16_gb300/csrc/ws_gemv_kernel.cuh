@@ -1,0 +1,495 @@
+// ws_gemv_kernel.cuh -- the streaming GEMV kernel (device code), included by
+// the translation units that instantiate it for each batch size.
+//
+// y[b][m] = sum_k W[m][k] * x[b][k], bf16 W and x, fp32 accumulation ("One
+// Token, Kernel by Kernel: A Decode Step on a Laptop GPU", Step 1, "What one
+// block launches").  Design for GB300:
+//  * every warp is an independent pipeline: it owns whole rows (a task of RT
+//    rows, one K split), streams them from HBM through its own ring of
+//    shared-memory stages with 1-D bulk async copies (cp.async.bulk, mbarrier
+//    completion, L2 evict-first since each weight byte is read once), and
+//    refills a stage as soon as its lanes have read it; no warp ever waits for
+//    another in the main loop;
+//  * the first stages are issued before griddepcontrol.wait: weights do not
+//    depend on the previous op, so inside a chain the next op's weights stream
+//    in while the previous op finishes (programmatic dependent launch);
+//  * lanes take 16-byte chunks of each row, unpack bf16 pairs to fp32 and
+//    accumulate with FMA, RT rows at a time (independent FMA chains); at the
+//    end of a task a butterfly of warp shuffles gives every lane every sum and
+//    lane r*BT+b runs the epilogue of output (row r, batch b);
+//  * split-K for skinny shapes: partial sums go to a workspace and the last
+//    split of a row group (atomic ticket) adds them in split order, so the
+//    result does not depend on the order CTAs finish in; the ticket is reset
+//    for the next call or graph replay ("Making small PyTorch ops faster on a
+//    laptop GPU", "A full decode step is a different story": the last block
+//    to finish merges and resets the ticket);
+//  * the activations are normalised once per CTA (RMSNorm or LayerNorm
+//    prologue in fp32, all threads, vector loads) and rounded once to bf16
+//    into shared memory.
+// There are no tensor cores here: at batch <= 16 this is a vector product.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ws_common.cuh"
+#include "ws_device.cuh"
+
+namespace ws {
+
+typedef void (*GemvKernel)(const GemvParams);
+
+__device__ __forceinline__ float bf16_round(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+__device__ __forceinline__ void raise_device_error(int* err, int code) {
+  if (err) atomicExch(err, code);
+}
+
+// Epilogue for one output element (segment seg, row m, batch row b).  v0 is
+// the dot product with the first matrix, v1 with the second (SwiGLU up).
+__device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int m, int b,
+                                               float v0, float v1, float& best_v, int& best_i) {
+  const Seg& S = p.seg[seg];
+  const size_t o = (size_t)b * S.M + m;
+  switch (p.epilogue) {
+    case EPI_F32:
+      static_cast<float*>(S.out)[o] = v0;
+      break;
+    case EPI_BF16:
+      static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(v0);
+      break;
+    case EPI_RESID: {
+      const float* src = p.res_in ? p.res_in : static_cast<const float*>(S.out);
+      static_cast<float*>(S.out)[o] = src[o] + v0;
+      break;
+    }
+    case EPI_BIAS_GELU: {
+      const float t = bf16_round(v0 + __uint_as_float((uint32_t)p.bias[m] << 16));
+      const float z = 0.5f * t * (1.0f + erff(t * 0.70710678118654752f));
+      static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(z);
+      break;
+    }
+    case EPI_SWIGLU: {
+      const float sv = v0 / (1.0f + expf(-v0)) * v1;
+      static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(sv);
+      break;
+    }
+    case EPI_ARGMAX: {
+      if (p.logits) p.logits[o] = v0;
+      const int row = S.row_base + m;
+      if (arg_better(v0, row, best_v, best_i)) {
+        best_v = v0;
+        best_i = row;
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// Eight consecutive activations x[b][8c .. 8c+7] as fp32.
+__device__ __forceinline__ void load_x8(const GemvParams& p, int b, int c, float (&v)[8]) {
+  if (p.x_dtype == DT_F32) {
+    const float4* src =
+        reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + (size_t)b * p.K) + 2 * c;
+    const float4 a = src[0], d = src[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = d.x; v[5] = d.y; v[6] = d.z; v[7] = d.w;
+  } else {
+    const uint4 u =
+        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + (size_t)b * p.K)[c];
+    v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+    v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+  }
+}
+
+// Sum of s[b] over the CTA for every batch row; the totals land in tot[b].
+template <int BT>
+__device__ __forceinline__ void block_sum(float (&s)[BT], float* red, float* tot, int B, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    const float w = warp_sum(s[b]);
+    if (lane == 0) red[warp * BT + b] = w;
+  }
+  __syncthreads();
+  if (tid < B) {
+    float t = 0.f;
+    for (int w = 0; w < kWarps; ++w) t += red[w * BT + tid];
+    tot[tid] = t;
+  }
+  __syncthreads();
+}
+
+// Per-row statistics of the prologue over the full K, by all threads with
+// vector loads: RMSNorm r = rsqrt(mean x^2 + eps); LayerNorm mean and
+// rstd = rsqrt(mean (x - mean)^2 + eps) (two passes).
+template <int BT>
+__device__ void prologue_stats(const GemvParams& p, float* stats, float* red, int tid) {
+  if (p.prologue == PRO_NONE) return;
+  const int nch = p.K >> 3;
+  float* tot = red + kWarps * BT;
+  float s[BT];
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    s[b] = 0.f;
+    if (b < p.B)
+      for (int c = tid; c < nch; c += kThreads) {
+        float v[8];
+        load_x8(p, b, c, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[b] = p.prologue == PRO_RMSNORM ? fmaf(v[e], v[e], s[b]) : s[b] + v[e];
+      }
+  }
+  block_sum<BT>(s, red, tot, p.B, tid);
+  if (p.prologue == PRO_RMSNORM) {
+    if (tid < p.B) stats[2 * tid] = rsqrtf(tot[tid] / (float)p.K + p.eps);
+    __syncthreads();
+    return;
+  }
+  if (tid < p.B) stats[2 * tid] = tot[tid] / (float)p.K;
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < BT; ++b) {
+    s[b] = 0.f;
+    if (b < p.B) {
+      const float mean = stats[2 * b];
+      for (int c = tid; c < nch; c += kThreads) {
+        float v[8];
+        load_x8(p, b, c, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s[b] = fmaf(v[e] - mean, v[e] - mean, s[b]);
+      }
+    }
+  }
+  block_sum<BT>(s, red, tot, p.B, tid);
+  if (tid < p.B) stats[2 * tid + 1] = rsqrtf(tot[tid] / (float)p.K + p.eps);
+  __syncthreads();
+}
+
+// Stage columns [k0, k0 + KS) of the (normalised) activations as bf16 into
+// shared memory, [BT][KS]; rows b >= B are zero.
+template <int BT>
+__device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, int ks, int tid) {
+  const int KS = p.sc.KS;
+  const int nch = KS >> 3;
+  const int c0 = (ks * KS) >> 3;
+  for (int o = tid; o < BT * nch; o += kThreads) {
+    const int b = o / nch;
+    const int c = o - b * nch;
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (b < p.B) {
+      if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16) {
+        out = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
+                                             (size_t)b * p.K)[c0 + c];
+      } else {
+        float v[8];
+        load_x8(p, b, c0 + c, v);
+        const int k = (c0 + c) * 8;
+        if (p.prologue == PRO_RMSNORM) {
+          const float r = stats[2 * b];
+          const uint4 g = *reinterpret_cast<const uint4*>(p.gamma + k);
+          const float gf[8] = {bf16lo(g.x), bf16hi(g.x), bf16lo(g.y), bf16hi(g.y),
+                               bf16lo(g.z), bf16hi(g.z), bf16lo(g.w), bf16hi(g.w)};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = v[e] * r * gf[e];
+        } else if (p.prologue == PRO_LAYERNORM) {
+          const float mean = stats[2 * b], rstd = stats[2 * b + 1];
+          const uint4 g = *reinterpret_cast<const uint4*>(p.gamma + k);
+          const uint4 bt = *reinterpret_cast<const uint4*>(p.beta + k);
+          const float gf[8] = {bf16lo(g.x), bf16hi(g.x), bf16lo(g.y), bf16hi(g.y),
+                               bf16lo(g.z), bf16hi(g.z), bf16lo(g.w), bf16hi(g.w)};
+          const float bf[8] = {bf16lo(bt.x), bf16hi(bt.x), bf16lo(bt.y), bf16hi(bt.y),
+                               bf16lo(bt.z), bf16hi(bt.z), bf16lo(bt.w), bf16hi(bt.w)};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = (v[e] - mean) * rstd * gf[e] + bf[e];
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e]));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e + 1]));
+          w[e] = lo | (hi << 16);
+        }
+        out = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    reinterpret_cast<uint4*>(xs)[(size_t)b * nch + c] = out;
+  }
+}
+
+// Issue the bulk copies of piece j (columns [k0 + j*PC, ...)) of row group rg
+// into ring slot `slot`.
+template <int NMAT, int RT>
+__device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, int slot, int k0,
+                                            uint8_t* ring, uint64_t* full, uint64_t pol) {
+  const Sched& sc = p.sc;
+  int seg, rgl;
+  decode_rg(p, rg, seg, rgl);
+  const Seg& S = p.seg[seg];
+  const int row0 = rgl * RT;
+  const int rows = min(RT, S.M - row0);
+  const int c0 = k0 + j * sc.PC;
+  const int len = min(sc.PC, sc.KS - j * sc.PC);
+  uint8_t* dst = ring + (size_t)slot * sc.piece_bytes;
+  const int K = p.K;
+  mbar_arrive_expect_tx(&full[slot], (uint32_t)(NMAT * rows * len * 2));
+#pragma unroll
+  for (int mat = 0; mat < NMAT; ++mat) {
+    const uint16_t* W = mat == 0 ? S.W0 : S.W1;
+    if (len == K) {  // whole rows: one contiguous copy
+      bulk_copy_g2s(dst + (size_t)mat * RT * sc.PC * 2, W + (size_t)row0 * K,
+                    (uint32_t)(rows * K * 2), &full[slot], pol);
+    } else {
+      for (int r = 0; r < rows; ++r)
+        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * sc.PC * 2, W + (size_t)(row0 + r) * K + c0,
+                      (uint32_t)(len * 2), &full[slot], pol);
+    }
+  }
+}
+
+template <int BT, int NMAT, int RT>
+__global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant__ GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Sched& sc = p.sc;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + sc.off_bar) + warp * kMaxStages;
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + sc.off_flags);
+  float* stats = reinterpret_cast<float*>(smem + sc.off_stats);
+  float* red = reinterpret_cast<float*>(smem + sc.off_red);
+  float* argv = reinterpret_cast<float*>(smem + sc.off_arg);
+  int* argi = reinterpret_cast<int*>(argv + kWarps * 32);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sc.off_xs);
+  uint8_t* ring = smem + sc.off_ring + (size_t)warp * sc.NSW * sc.piece_bytes;
+
+  int ks, rg0, rg1;
+  cta_range(sc, blockIdx.x, ks, rg0, rg1);
+  const int k0 = ks * sc.KS;
+  const int NP = sc.NP, NSW = sc.NSW;
+  const int npw = warp_tasks(rg0, rg1, warp) * NP;  // pieces of this warp
+  const int rgw = rg0 + warp;                         // this warp's first row group
+
+  // issue cursor (lane 0): next piece, its task, piece index and slot
+  int iq = 0, iti = 0, ij = 0, islot = 0;
+  uint64_t pol = 0;
+  if (lane == 0) {
+    for (int s = 0; s < NSW; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+    pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+    // Weights do not depend on the previous kernel: start streaming them
+    // before waiting for it.
+    while (iq < NSW && iq < npw) {
+      issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      ++iq;
+      if (++ij == NP) { ij = 0; ++iti; }
+      if (++islot == NSW) islot = 0;
+    }
+  }
+  pdl_launch_dependents();
+  pdl_wait();
+
+  prologue_stats<BT>(p, stats, red, tid);
+  stage_x<BT>(p, stats, xs, ks, tid);
+  __syncthreads();
+
+  const int nchx = sc.KS >> 3;  // chunks of x in shared memory
+  const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
+  const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
+  float best_v = -INFINITY;
+  int best_i = 0x7fffffff;
+  bool abort = false;
+
+  float acc[NMAT][RT][BT];
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
+
+  // consume cursor: piece q of task ti, piece index j, ring slot and phase
+  int ti = 0, j = 0, slot = 0;
+  uint32_t phase = 0;
+  for (int q = 0; q < npw; ++q) {
+    const int rg = rgw + ti * kWarps;
+    int seg, rgl;
+    decode_rg(p, rg, seg, rgl);
+    const int row0 = rgl * RT;
+    const int rows = min(RT, p.seg[seg].M - row0);
+    const int len = min(sc.PC, sc.KS - j * sc.PC);
+    const bool ok = abort || mbar_wait_bounded(&full[slot], phase, p.timeout_ns);
+    if (__any_sync(0xffffffffu, !ok) && !abort) {
+      abort = true;
+      if (lane == 0) raise_device_error(p.err, DERR_TIMEOUT);
+    }
+
+    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.piece_bytes);
+    const int xoff = j * ncp;
+#pragma unroll 2
+    for (int c = lane; c < (len >> 3); c += 32) {
+      float wf[NMAT][RT][8];
+#pragma unroll
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const uint4 w = r < rows ? st[(size_t)(m * RT + r) * ncp + c] : make_uint4(0, 0, 0, 0);
+          wf[m][r][0] = bf16lo(w.x); wf[m][r][1] = bf16hi(w.x);
+          wf[m][r][2] = bf16lo(w.y); wf[m][r][3] = bf16hi(w.y);
+          wf[m][r][4] = bf16lo(w.z); wf[m][r][5] = bf16hi(w.z);
+          wf[m][r][6] = bf16lo(w.w); wf[m][r][7] = bf16hi(w.w);
+        }
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        const uint4 xv = xs4[(size_t)b * nchx + xoff + c];
+        const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
+                             bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[m][r][b] = fmaf(wf[m][r][e], xf[e], acc[m][r][b]);
+      }
+    }
+    // Every lane's shared-memory reads of this slot have returned (their
+    // values fed the FMAs above, and issue is in order): refill the slot.
+    __syncwarp();
+    if (lane == 0 && !abort && iq < npw) {
+      issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      ++iq;
+      if (++ij == NP) { ij = 0; ++iti; }
+      if (++islot == NSW) islot = 0;
+    }
+
+    if (j == NP - 1) {
+      // task complete: sum over lanes (every lane ends with every sum)
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) acc[m][r][b] = warp_sum(acc[m][r][b]);
+      const int rowg = p.seg[seg].row_base + row0;
+      if (sc.S == 1) {
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b)
+            if (lane == r * BT + b && r < rows && b < p.B)
+              apply_epilogue(p, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v,
+                             best_i);
+      } else {
+        // split-K: write this split's partials; the last split of the row
+        // group adds all splits in split order and runs the epilogue
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b)
+            if (lane == r * BT + b && r < rows && b < p.B) {
+#pragma unroll
+              for (int m = 0; m < NMAT; ++m)
+                p.part[((size_t)(ks * NMAT + m) * p.B + b) * p.M_total + rowg + r] = acc[m][r][b];
+            }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const unsigned old = atomicAdd(&p.tickets[rg], 1u);
+          last = old == (unsigned)(sc.S - 1);
+          if (last) atomicExch(&p.tickets[rg], 0u);
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          for (int o = lane; o < rows * p.B; o += 32) {
+            const int rr = o / p.B;
+            const int b = o - rr * p.B;
+            float v[NMAT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+              float t = 0.f;
+              for (int s = 0; s < sc.S; ++s)
+                t += __ldcg(&p.part[((size_t)(s * NMAT + m) * p.B + b) * p.M_total + rowg + rr]);
+              v[m] = t;
+            }
+            float dv = -INFINITY;
+            int di = 0x7fffffff;
+            apply_epilogue(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di);
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
+    }
+    if (++j == NP) { j = 0; ++ti; }
+    if (++slot == NSW) { slot = 0; phase ^= 1u; }
+  }
+
+  if (abort && lane == 0) {
+    // a wait ran out: no copy may still be landing when the CTA exits; the
+    // last NSW pieces issued are the only ones that can be in flight
+    for (int q = iq - NSW; q < iq; ++q)
+      if (q >= 0) mbar_wait_bounded(&full[q % NSW], (q / NSW) & 1, p.timeout_ns);
+  }
+
+  if (p.epilogue == EPI_ARGMAX) {
+    // per batch row: lanes r*BT + b hold a running best; combine the warps,
+    // then the last CTA (ticket) combines all CTAs
+    argv[warp * 32 + lane] = best_v;
+    argi[warp * 32 + lane] = best_i;
+    __syncthreads();
+    if (tid < p.B) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int w = 0; w < kWarps; ++w)
+        for (int r = 0; r < RT; ++r) {
+          const int l = r * BT + tid;
+          if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
+            bv = argv[w * 32 + l];
+            bi = argi[w * 32 + l];
+          }
+        }
+      p.arg_val[(size_t)blockIdx.x * p.B + tid] = bv;
+      p.arg_idx[(size_t)blockIdx.x * p.B + tid] = bi;
+      __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned old = atomicAdd(p.arg_ticket, 1u);
+      const int last = old == gridDim.x - 1;
+      if (last) atomicExch(p.arg_ticket, 0u);
+      flags[0] = last;
+    }
+    __syncthreads();
+    if (flags[0] && tid < p.B) {
+      __threadfence();
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int c = 0; c < (int)gridDim.x; ++c) {
+        const float v = __ldcg(&p.arg_val[(size_t)c * p.B + tid]);
+        const int ix = __ldcg(&p.arg_idx[(size_t)c * p.B + tid]);
+        if (arg_better(v, ix, bv, bi)) {
+          bv = v;
+          bi = ix;
+        }
+      }
+      p.argmax_idx[tid] = bi;
+    }
+  }
+}
+
+// Instantiation tables, one per translation unit (compiled in parallel).
+GemvKernel pick_kernel_b12(int BT, int nmat, int RT);
+GemvKernel pick_kernel_b4(int BT, int nmat, int RT);
+GemvKernel pick_kernel_b816(int BT, int nmat, int RT);
+
+}  // namespace ws
