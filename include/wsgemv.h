@@ -79,6 +79,26 @@ enum { WS_DTYPE_F32 = 0, WS_DTYPE_BF16 = 1, WS_DTYPE_F16 = 2 };
 ws_status ws_gemv_bf16(const void *W, const void *x, float *y, int M, int K, int B,
                        void *workspace, size_t workspace_bytes, ws_stream_t stream);
 
+/* The same product as ws_gemv_bf16 for callers that cannot allocate device
+ * memory when they need it: code running while a stream is captured into a
+ * CUDA graph, serving loops that must not grow their memory after start-up,
+ * hosts that only pass in memory they allocated themselves.  The pages have
+ * no counterpart to this call; it is a convenience of this library.
+ *  - It allocates nothing.  When the schedule splits K, the partial sums and
+ *    tickets live in a fixed 1 MiB array of device memory owned by the
+ *    library (every GPU that loads the library holds it until exit).
+ *  - Shapes whose split-K scratch would exceed 1 MiB are rejected with
+ *    WS_ERR_SHAPE and a message; use ws_gemv_bf16 with a workspace for those.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Each call clears the tickets on `stream` before its kernel.  All calls
+ *    share the one array, which keeps the last call's contents: calls that
+ *    overlap on the GPU (different streams, no ordering) race on it.
+ * W bf16 [M][K], x bf16 [B][K], y fp32 [B][M]; same alignment and shape rules
+ * as ws_gemv_bf16. */
+ws_status ws_gemv_bf16_noalloc(const void *W, const void *x, float *y, int M, int K, int B,
+                               ws_stream_t stream);
+
 /* h_out[b][m] = h_in[b][m] + sum_k W[m][k] x[b][k]: the residual add of a
  * decoder block folded into the GEMV's epilogue ("One Token, Kernel by
  * Kernel", Step 1, "What one block launches").  x bf16 [B][K]; h_in, h_out

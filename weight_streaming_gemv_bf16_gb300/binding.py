@@ -87,6 +87,7 @@ class GemvSchedule(C.Structure):
 
 _SIGS = {
     "ws_gemv_bf16": [P, P, P, I32, I32, I32, P, SZ, P],
+    "ws_gemv_bf16_noalloc": [P, P, P, I32, I32, I32, P],
     "ws_gemv_residual": [P, P, P, P, I32, I32, I32, P, SZ, P],
     "ws_rmsnorm_gemv": [P, I32, P, P, P, I32, I32, I32, F32, P, SZ, P],
     "ws_qkv_gemv": [P, I32, P, P, P, P, P, P, P, I32, I32, I32, I32, F32, P, SZ, P],
@@ -203,6 +204,14 @@ def gemv_bf16(W, x, y, workspace=None, stream=None):
     B = x.shape[0]
     wp, wb = _ws(workspace)
     _check(load().ws_gemv_bf16(_ptr(W), _ptr(x), _ptr(y), M, K, B, wp, wb, _stream(stream)))
+
+
+def gemv_bf16_noalloc(W, x, y, stream=None):
+    """ws_gemv_bf16 without a workspace argument and without any allocation:
+    split-K scratch comes from the library's fixed device array."""
+    M, K = W.shape
+    B = x.shape[0]
+    _check(load().ws_gemv_bf16_noalloc(_ptr(W), _ptr(x), _ptr(y), M, K, B, _stream(stream)))
 
 
 def gemv_residual(W, x, h_out, h_in=None, workspace=None, stream=None):
