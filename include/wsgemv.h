@@ -249,8 +249,9 @@ typedef struct {
    * [B][w]. */
   const void *x_in;
   void *y_out;
-  /* Optional: fp32 [L][B][H] copy of h after every Qwen block (per-block
-   * checks; adds one copy per block to the graph). */
+  /* Optional per-block trace (for per-block checks; one copy per block):
+   * Qwen chains get h after every block, fp32 [L][B][H]; MLP chains get
+   * every block's output, bf16 [L][B][w]. */
   float *h_trace;
   int use_pdl;          /* 1: programmatic dependent launch between ops      */
   int prefetch;         /* 0 off, 1 tuned plans, 2 fixed_plan for every op   */
@@ -260,6 +261,13 @@ typedef struct {
   int tune_pairs;       /* paired replays per candidate (>= 8)               */
   float tune_min_gain;  /* keep a plan only if the 95% CI lower bound of its
                            relative gain exceeds this (e.g. 0.01)            */
+  int persistent;       /* 1: run the whole step as one persistent kernel
+                           (batch <= 4): each op is a phase of a cooperative
+                           launch with one CTA per SM, phases separated by
+                           grid barriers, and every warp's weight stream runs
+                           ahead across phase boundaries.  Prefetch plans do
+                           not apply in this mode.  0: one launch per op with
+                           programmatic dependent launch edges.              */
 } ws_chain_opts;
 
 typedef struct ws_chain ws_chain;
@@ -288,6 +296,8 @@ ws_status ws_chain_run_eager(ws_chain *c, ws_stream_t stream);
 ws_status ws_chain_step_host(ws_chain *c, const void *in_host, const void *attn_host,
                              void *out_host, ws_stream_t stream);
 int ws_chain_num_ops(const ws_chain *c);
+/* 1 if the chain runs as one persistent kernel per step, else 0. */
+int ws_chain_is_persistent(const ws_chain *c);
 /* Plan and measured gain (95% CI lower bound, mean) of each op; n entries. */
 ws_status ws_chain_plans(const ws_chain *c, ws_prefetch_plan *plans, float *gain_lo,
                          float *gain_mean, int n);

@@ -89,13 +89,35 @@ def _check_chain(ch, blocks, head, attn, h0, eps=1e-6):
     return int(ok2.sum())
 
 
+@pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("B", [1, 3, 16])
-def test_small_chain_matches_oracle(B):
-    ch, blocks, head, attn, h0 = _make(SMALL, B, 21, trace=True, keep_qkv=True, logits=True)
+def test_small_chain_matches_oracle(B, persistent):
+    ch, blocks, head, attn, h0 = _make(SMALL, B, 21, trace=True, keep_qkv=True, logits=True,
+                                       persistent=persistent)
+    # the persistent kernel takes batch <= 4; larger batches run op by op
+    assert ch.chain.persistent == (persistent and B <= 4)
     ch.chain.capture()
     ch.run()
+    ch.run()  # a second replay: barrier counters and tickets were reset
     torch.cuda.synchronize()
     _check_chain(ch, blocks, head, attn, h0)
+
+
+def test_persistent_graph_and_launch_are_bit_identical():
+    outs = []
+    for graph in (True, False):
+        ch, *_ = _make(SMALL, 2, 26, trace=True, logits=True, persistent=True)
+        assert ch.chain.persistent
+        if graph:
+            ch.chain.capture()
+            for _ in range(3):
+                ch.run()
+        else:
+            ch.chain.run_eager()
+        torch.cuda.synchronize()
+        outs.append((ch.h_out.cpu(), ch.logits.cpu(), ch.idx.cpu(), ch.h_trace.cpu()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def test_graph_eager_and_pdl_are_bit_identical():
@@ -175,10 +197,13 @@ def test_step_host_matches_device_run():
     assert np.array_equal(out.numpy(), ch.idx.cpu().numpy())
 
 
-def test_one_full_size_block_matches_oracle():
+@pytest.mark.parametrize("persistent", [False, True])
+def test_one_full_size_block_matches_oracle(persistent):
     """One Qwen2.5-1.5B-shaped block at batch 1 (hidden 1536, KV 256, MLP 8960)."""
     shape = synth.QwenShape(layers=1)
-    ch, blocks, head, attn, h0 = _make(shape, 1, 0, trace=True, keep_qkv=True)
+    ch, blocks, head, attn, h0 = _make(shape, 1, 0, trace=True, keep_qkv=True,
+                                       persistent=persistent)
+    assert ch.chain.persistent == persistent
     ch.chain.capture()
     ch.run()
     torch.cuda.synchronize()
@@ -189,10 +214,13 @@ def test_one_full_size_block_matches_oracle():
     assert_fp32(ch.h_out.cpu().numpy(), ref["h"], what="h")
 
 
-def test_full_chain_28_blocks_matches_oracle():
+@pytest.mark.parametrize("persistent", [False, True])
+def test_full_chain_28_blocks_matches_oracle(persistent):
     """The full 28-block chain + final RMSNorm + LM head 151936 x 1536 + argmax,
     batch 1, one CUDA graph: per-block teacher forcing and the end-to-end argmax."""
-    ch, blocks, head, attn, h0 = _make(synth.QWEN2_5_1_5B, 1, 0, trace=True, logits=True)
+    ch, blocks, head, attn, h0 = _make(synth.QWEN2_5_1_5B, 1, 0, trace=True, logits=True,
+                                       persistent=persistent)
+    assert ch.chain.persistent == persistent
     ch.chain.capture()
     ch.run()
     torch.cuda.synchronize()
@@ -229,3 +257,25 @@ def test_mlp_chain_72_blocks(B):
         pch.run()
         torch.cuda.synchronize()
         assert torch.equal(pch.y_out.cpu(), ch.y_out.cpu())
+
+
+@pytest.mark.parametrize("persistent,B", [(False, 4), (True, 4), (True, 1), (False, 16)])
+def test_mlp_chain_72_blocks_trace(persistent, B):
+    """Every block of the 72-block chain, teacher-forced on the chain's own
+    trace: block i's oracle is fed the GPU's output of block i-1."""
+    sh = synth.MlpShape()
+    blocks = [synth.mlp_block_weights(sh, 1, i) for i in range(sh.blocks)]
+    x = synth.mlp_input(sh, B, 1)
+    ch = wc.mlp_chain([_dev(b) for b in blocks], dev_bf16(x), persistent=persistent, trace=True)
+    assert ch.chain.persistent == persistent
+    ch.chain.capture()
+    ch.run()
+    ch.run()
+    torch.cuda.synchronize()
+    tr = host_bits(ch.trace)
+    prev = x
+    for i, hb in enumerate(blocks):
+        assert_bf16_close(tr[i], oracle.mlp_block(prev, hb, sh.eps, 8, exact=True),
+                          what=f"mlp block {i}")
+        prev = tr[i]
+    assert np.array_equal(host_bits(ch.y_out), tr[-1])

@@ -71,7 +71,7 @@ class ChainOpts(C.Structure):
                 ("vocab", I32), ("eps", F32), ("h_in", P), ("h_out", P), ("x_in", P),
                 ("y_out", P), ("h_trace", P), ("use_pdl", I32), ("prefetch", I32),
                 ("fixed_plan", PrefetchPlan), ("distance", I32), ("decoy", I32),
-                ("tune_pairs", I32), ("tune_min_gain", F32)]
+                ("tune_pairs", I32), ("tune_min_gain", F32), ("persistent", I32)]
 
 
 class Tuning(C.Structure):
@@ -116,6 +116,7 @@ _OTHER = {
     "ws_last_error": ([], C.c_char_p),
     "ws_device_error": ([I32], I32),
     "ws_chain_num_ops": ([P], I32),
+    "ws_chain_is_persistent": ([P], I32),
     "ws_chain_destroy": ([P], None),
     "ws_get_tuning": ([P], None),
     "ws_debug_gemv_copies": ([I32, I32, I32, I32, I32, I32, P, C.c_long], C.c_long),
@@ -342,6 +343,7 @@ class Chain:
         self.opts = opts
         self._keep = list(keepalive)
         self.n_ops = int(load().ws_chain_num_ops(h))
+        self.persistent = bool(load().ws_chain_is_persistent(h))
 
     def tune(self, stream=None):
         _check(load().ws_chain_tune(self.handle, _stream(stream)))

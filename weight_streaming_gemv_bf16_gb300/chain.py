@@ -41,14 +41,16 @@ class MlpChain:
     chain: wb.Chain
     x_in: torch.Tensor
     y_out: torch.Tensor
+    trace: torch.Tensor | None = None
 
     def run(self, stream=None):
         self.chain.run(stream)
 
 
 def _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, tune_pairs,
-          min_gain):
+          min_gain, persistent=False):
     o = wb.ChainOpts()
+    o.persistent = 1 if persistent else 0
     o.batch, o.hidden, o.kv_dim, o.inter, o.vocab, o.eps = B, H, KV, I, V, eps
     o.use_pdl = 1 if use_pdl else 0
     o.prefetch = prefetch
@@ -63,7 +65,7 @@ def _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, t
 
 def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
                fixed_plan=None, distance=1, decoy=False, trace=False, keep_qkv=False,
-               logits=False, tune_pairs=30, min_gain=0.01) -> QwenChain:
+               logits=False, tune_pairs=30, min_gain=0.01, persistent=False) -> QwenChain:
     """blocks: list of dicts of bf16 device tensors gamma1, Wq, Wk, Wv, Wo, gamma2,
     Wg, Wu, Wd; head: dict gamma_f, Wlm (or None); attn: bf16 [L, B, H];
     h_in: fp32 [B, H]."""
@@ -100,7 +102,7 @@ def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
                                 idx.data_ptr(), lg.data_ptr() if lg is not None else None)
         descs.append(d)
     o = _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, tune_pairs,
-              min_gain)
+              min_gain, persistent)
     o.h_in = h_in.data_ptr()
     o.h_out = h_out.data_ptr()
     o.h_trace = h_trace.data_ptr() if h_trace is not None else None
@@ -110,10 +112,13 @@ def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
 
 
 def mlp_chain(blocks, x_in, *, eps=1e-5, use_pdl=True, prefetch=0, fixed_plan=None,
-              distance=1, decoy=False, tune_pairs=30, min_gain=0.01) -> MlpChain:
-    """blocks: list of dicts of bf16 device tensors gamma, beta, W, b; x_in bf16 [B, w]."""
+              distance=1, decoy=False, tune_pairs=30, min_gain=0.01,
+              persistent=False, trace=False) -> MlpChain:
+    """blocks: list of dicts of bf16 device tensors gamma, beta, W, b; x_in bf16 [B, w].
+    trace=True keeps every block's output in `trace` (bf16 [L, B, w])."""
     B, w = x_in.shape
     y_out = torch.empty_like(x_in)
+    tr = torch.empty((len(blocks), B, w), dtype=torch.bfloat16, device=x_in.device) if trace else None
     descs = []
     for blk in blocks:
         d = wb.BlockDesc(kind=wb.BLOCK_MLP)
@@ -121,8 +126,9 @@ def mlp_chain(blocks, x_in, *, eps=1e-5, use_pdl=True, prefetch=0, fixed_plan=No
                               blk["W"].data_ptr(), blk["b"].data_ptr())
         descs.append(d)
     o = _opts(B, w, 0, 0, 0, eps, use_pdl, prefetch, fixed_plan, distance, decoy, tune_pairs,
-              min_gain)
+              min_gain, persistent)
     o.x_in = x_in.data_ptr()
     o.y_out = y_out.data_ptr()
-    ch = wb.Chain(descs, o, keepalive=[blocks, x_in, y_out])
-    return MlpChain(ch, x_in, y_out)
+    o.h_trace = tr.data_ptr() if tr is not None else None
+    ch = wb.Chain(descs, o, keepalive=[blocks, x_in, y_out, tr])
+    return MlpChain(ch, x_in, y_out, tr)

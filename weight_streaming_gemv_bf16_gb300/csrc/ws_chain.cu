@@ -103,6 +103,11 @@ struct ws_chain {
   cudaGraphExec_t exec = nullptr;
   std::vector<const void*> attn_dev;
   int32_t* idx = nullptr;
+  // persistent mode: all ops in one cooperative kernel per step
+  bool persistent = false;
+  PersistParams persist;
+  GemvParams* d_ops = nullptr;
+  unsigned* d_bar = nullptr;
 };
 
 static void free_chain_buffers(ws_chain* c) {
@@ -127,6 +132,16 @@ static void free_chain_buffers(ws_chain* c) {
   c->ws = c->s_buf = nullptr;
   c->qkv_scratch = nullptr;
   c->pp[0] = c->pp[1] = nullptr;
+  if (c->d_ops) cudaFree(c->d_ops);
+  if (c->d_bar) cudaFree(c->d_bar);
+  c->d_ops = nullptr;
+  c->d_bar = nullptr;
+}
+
+// Bytes of one trace slot: a Qwen block's fp32 residual [B][H], or an MLP
+// block's bf16 output [B][w].
+static size_t trace_bytes(const ws_chain* c) {
+  return (size_t)c->o.batch * c->o.hidden * (c->n_mlp ? 2 : 4);
 }
 
 static ws_status build_ops(ws_chain* c) {
@@ -260,7 +275,7 @@ static ws_status build_ops(ws_chain* c) {
       op.reads.push_back({m.W, (size_t)w * w * 2});
       op.kind = OP_MLP;
       op.block = bi;
-      op.trace_block = -1;
+      op.trace_block = mlp_seen;
       c->ops.push_back(op);
       ++mlp_seen;
     } else {
@@ -288,10 +303,19 @@ static ws_status build_ops(ws_chain* c) {
     }
   }
 
+  // persistent mode when asked for and every op fits its stage layout
+  c->persistent = false;
+  if (o.persistent && B <= 4) {
+    const int slot = tuning().piece_bytes > 0 ? tuning().piece_bytes : 6144;
+    bool ok = true;
+    for (ChainOp& op : c->ops)
+      if (!plan_gemv_persistent(op.p, slot, why, sizeof why)) ok = false;
+    c->persistent = ok;
+  }
   // schedules and one zeroed workspace with a slice per op
   size_t total = 0;
   for (ChainOp& op : c->ops) {
-    if (!plan_gemv(op.p, op.kind == OP_HEAD ? -1 : 0, why, sizeof why)) {
+    if (!c->persistent && !plan_gemv(op.p, op.kind == OP_HEAD ? -1 : 0, why, sizeof why)) {
       set_error("op %d: %s", (int)(&op - &c->ops[0]), why);
       return WS_ERR_SHAPE;
     }
@@ -314,10 +338,42 @@ static ws_status build_ops(ws_chain* c) {
       set_error("internal: workspace binding failed");
       return WS_ERR_ARG;
     }
-    if (!prepare_gemv(op.p)) {
+    if (!c->persistent && !prepare_gemv(op.p)) {
       set_error("could not configure the GEMV kernel");
       return WS_ERR_CUDA;
     }
+  }
+  if (c->persistent) {
+    // every op becomes one phase of the persistent kernel; the h trace is
+    // written by the kernel itself after each block's last op
+    std::vector<GemvParams> host_ops;
+    for (ChainOp& op : c->ops) {
+      op.p.trace_out =
+          (o.h_trace && op.trace_block >= 0)
+              ? reinterpret_cast<float*>(reinterpret_cast<char*>(o.h_trace) +
+                                         (size_t)op.trace_block * trace_bytes(c))
+              : nullptr;
+      host_ops.push_back(op.p);
+    }
+    const int n = (int)host_ops.size();
+    if (!plan_persistent(c->persist, host_ops.data(), n, B, why, sizeof why)) {
+      set_error("%s", why);
+      return WS_ERR_SHAPE;
+    }
+    if (cudaMalloc((void**)&c->d_ops, sizeof(GemvParams) * n) != cudaSuccess ||
+        cudaMalloc((void**)&c->d_bar, sizeof(unsigned) * (n + 1)) != cudaSuccess)
+      return WS_ERR_NOMEM;
+    if (cudaMemcpy(c->d_ops, host_ops.data(), sizeof(GemvParams) * n, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemset(c->d_bar, 0, sizeof(unsigned) * (n + 1)) != cudaSuccess)
+      return WS_ERR_CUDA;
+    c->persist.ops = c->d_ops;
+    c->persist.bar = c->d_bar;
+    if (!prepare_persistent(c->persist.BT)) {
+      set_error("could not configure the persistent chain kernel");
+      return WS_ERR_CUDA;
+    }
+    return WS_OK;
   }
   if (o.prefetch == 2)
     for (ChainOp& op : c->ops) op.plan = o.fixed_plan;
@@ -367,9 +423,9 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
     }
     prev_kernel = true;
     if (!trace.empty() && trace[i] >= 0) {
-      const size_t bytes = (size_t)c->o.batch * c->o.hidden * 4;
-      if (cudaMemcpyAsync(c->o.h_trace + (size_t)trace[i] * c->o.batch * c->o.hidden,
-                          c->o.h_out, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      const size_t bytes = trace_bytes(c);
+      if (cudaMemcpyAsync(reinterpret_cast<char*>(c->o.h_trace) + (size_t)trace[i] * bytes,
+                          ps[i].seg[0].out, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
         return WS_ERR_CUDA;
       prev_kernel = false;
     }
@@ -496,7 +552,8 @@ ws_status ws_chain_create(const ws_block_desc* blocks, int n, const ws_chain_opt
     set_error("Qwen chain needs kv_dim, inter (multiples of 8) and aligned h_in, h_out");
     return WS_ERR_ARG;
   }
-  if (nm && (!o.x_in || !o.y_out || !al16(o.x_in) || !al16(o.y_out))) {
+  if (nm && (!o.x_in || !o.y_out || !al16(o.x_in) || !al16(o.y_out) ||
+             (o.h_trace && !al16(o.h_trace)))) {
     set_error("MLP chain needs aligned x_in and y_out");
     return WS_ERR_ARG;
   }
@@ -542,7 +599,7 @@ ws_status ws_chain_tune(ws_chain* c, ws_stream_t stream) {
     set_error("null chain");
     return WS_ERR_ARG;
   }
-  if (c->o.prefetch != 1) return WS_OK;
+  if (c->o.prefetch != 1 || c->persistent) return WS_OK;
   cudaStream_t st = (cudaStream_t)stream;
   int l2 = 0;
   cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, c->device);
@@ -718,6 +775,29 @@ ws_status ws_chain_capture(ws_chain* c, ws_stream_t stream) {
     for (const ChainOp& op : c->ops) trace.push_back(op.trace_block);
   }
   (void)stream;
+  if (c->persistent) {
+    cudaGraph_t g = nullptr;
+    if (cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+      set_error("cudaStreamBeginCapture failed");
+      return WS_ERR_CUDA;
+    }
+    const cudaError_t le = launch_persistent(c->persist, c->cap);
+    const cudaError_t ce = cudaStreamEndCapture(c->cap, &g);
+    if (le != cudaSuccess || ce != cudaSuccess) {
+      if (g) cudaGraphDestroy(g);
+      set_error("capture of the persistent chain failed: %s",
+                cudaGetErrorString(le != cudaSuccess ? le : ce));
+      cudaGetLastError();
+      return WS_ERR_CUDA;
+    }
+    const cudaError_t ie = cudaGraphInstantiate(&c->exec, g, 0);
+    cudaGraphDestroy(g);
+    if (ie != cudaSuccess) {
+      set_error("graph instantiation failed: %s", cudaGetErrorString(ie));
+      return WS_ERR_CUDA;
+    }
+    return WS_OK;
+  }
   return capture_graph(c, chain_params(c), chain_reads(c), plans, c->o.decoy != 0, trace,
                        &c->exec);
 }
@@ -744,6 +824,14 @@ ws_status ws_chain_run_eager(ws_chain* c, ws_stream_t stream) {
     set_error("null chain");
     return WS_ERR_ARG;
   }
+  if (c->persistent) {
+    const cudaError_t e = launch_persistent(c->persist, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+      set_error("launch of the persistent chain failed: %s", cudaGetErrorString(e));
+      return WS_ERR_CUDA;
+    }
+    return WS_OK;
+  }
   for (size_t i = 0; i < c->ops.size(); ++i) {
     const cudaError_t e = launch_gemv(c->ops[i].p, (cudaStream_t)stream, false);
     if (e != cudaSuccess) {
@@ -751,9 +839,10 @@ ws_status ws_chain_run_eager(ws_chain* c, ws_stream_t stream) {
       return WS_ERR_CUDA;
     }
     if (c->o.h_trace && c->ops[i].trace_block >= 0) {
-      const size_t bytes = (size_t)c->o.batch * c->o.hidden * 4;
-      if (cudaMemcpyAsync(c->o.h_trace + (size_t)c->ops[i].trace_block * c->o.batch * c->o.hidden,
-                          c->o.h_out, bytes, cudaMemcpyDeviceToDevice,
+      const size_t bytes = trace_bytes(c);
+      if (cudaMemcpyAsync(reinterpret_cast<char*>(c->o.h_trace) +
+                              (size_t)c->ops[i].trace_block * bytes,
+                          c->ops[i].p.seg[0].out, bytes, cudaMemcpyDeviceToDevice,
                           (cudaStream_t)stream) != cudaSuccess)
         return WS_ERR_CUDA;
     }
@@ -825,6 +914,8 @@ ws_status ws_chain_step_host(ws_chain* c, const void* in_host, const void* attn_
 }
 
 int ws_chain_num_ops(const ws_chain* c) { return c ? (int)c->ops.size() : 0; }
+
+int ws_chain_is_persistent(const ws_chain* c) { return c && c->persistent ? 1 : 0; }
 
 ws_status ws_chain_plans(const ws_chain* c, ws_prefetch_plan* plans, float* gain_lo,
                          float* gain_mean, int n) {

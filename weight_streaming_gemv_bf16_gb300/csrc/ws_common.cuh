@@ -92,7 +92,25 @@ struct GemvParams {
   int* err;
   unsigned long long timeout_ns;
   int evict_first;
+  float* trace_out;  // persistent chain: copy seg[0].out ([B][M] fp32) here after the op
   Sched sc;
+};
+
+// The persistent chain kernel: every op of a chain as one phase of a single
+// cooperative launch (one CTA per SM), phases separated by grid barriers.
+struct PersistParams {
+  const GemvParams* ops;  // device array of nops planned ops
+  int nops;
+  unsigned* bar;          // nops + 1 counters, zero between launches
+  int* err;
+  unsigned long long timeout_ns;
+  int evict_first;
+  int BT;
+  int NSW;                // ring stages per warp
+  int slot_bytes;         // bytes per ring stage (the largest piece of any op)
+  int grid;
+  int smem_bytes;
+  int off_op, off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
 };
 
 // The split and the row-group range of CTA `cta`.
@@ -138,5 +156,11 @@ bool prepare_gemv(const GemvParams& p);
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t stream, bool pdl);
 void init_gemv_params(GemvParams& p, int K, int B);
 size_t argmax_rows_workspace(int rows, int cols);
+// persistent chain (ws_persist.cu)
+bool plan_gemv_persistent(GemvParams& p, int slot_bytes, char* why, size_t why_len);
+bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, char* why,
+                     size_t why_len);
+bool prepare_persistent(int BT);
+cudaError_t launch_persistent(const PersistParams& pp, cudaStream_t stream);
 
 }  // namespace ws

@@ -62,7 +62,7 @@ __device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int
       break;
     case EPI_RESID: {
       const float* src = p.res_in ? p.res_in : static_cast<const float*>(S.out);
-      static_cast<float*>(S.out)[o] = src[o] + v0;
+      static_cast<float*>(S.out)[o] = __ldcg(src + o) + v0;
       break;
     }
     case EPI_BIAS_GELU: {
@@ -90,17 +90,19 @@ __device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int
   }
 }
 
-// Eight consecutive activations x[b][8c .. 8c+7] as fp32.
+// Eight consecutive activations x[b][8c .. 8c+7] as fp32.  Activations are
+// read at the L2 (ld.global.cg): inside the persistent chain kernel another
+// SM wrote them after this SM may have cached an older copy in L1.
 __device__ __forceinline__ void load_x8(const GemvParams& p, int b, int c, float (&v)[8]) {
   if (p.x_dtype == DT_F32) {
     const float4* src =
         reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + (size_t)b * p.K) + 2 * c;
-    const float4 a = src[0], d = src[1];
+    const float4 a = __ldcg(src), d = __ldcg(src + 1);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
     v[4] = d.x; v[5] = d.y; v[6] = d.z; v[7] = d.w;
   } else {
-    const uint4 u =
-        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + (size_t)b * p.K)[c];
+    const uint4 u = __ldcg(
+        reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + (size_t)b * p.K) + c);
     v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
     v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
   }
@@ -183,8 +185,8 @@ __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, i
     uint4 out = make_uint4(0u, 0u, 0u, 0u);
     if (b < p.B) {
       if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16) {
-        out = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
-                                             (size_t)b * p.K)[c0 + c];
+        out = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) +
+                                                    (size_t)b * p.K) + c0 + c);
       } else {
         float v[8];
         load_x8(p, b, c0 + c, v);
