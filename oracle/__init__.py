@@ -285,15 +285,18 @@ def qwen_chain(h0, blocks, attns, gamma_f, Wlm_bits, eps: float,
 
 
 def mlp_block(x_bits, blk: dict, eps: float = 1e-5, threads: int = 1,
-              exact: bool = False) -> np.ndarray:
+              exact: bool = False, linear: bool = False) -> np.ndarray:
     """bf16 LayerNorm -> Linear(+bias) -> GELU, each module's output rounded to bf16.
 
-    Returns the bf16 bits of z = bf16(gelu(bf16(bf16(LN(x)).W^T + b))), or with
-    exact=True the value of gelu(...) before its final rounding (double)."""
+    Returns the bf16 bits of z = bf16(gelu(bf16(bf16(LN(x)).W^T + b))); with
+    exact=True the value of gelu(...) before its final rounding (double); with
+    linear=True the Linear output bf16(LN(x)).W^T + b before its rounding."""
     x = bf16_to_f64(x_bits)
     a = round_bf16(layernorm(x, bf16_to_f64(blk["gamma"]), bf16_to_f64(blk["beta"]), eps))
-    y = round_bf16(gemv(blk["W"], a, threads) + bf16_to_f64(blk["b"])[None, :])
-    z = gelu(y)
+    lin = gemv(blk["W"], a, threads) + bf16_to_f64(blk["b"])[None, :]
+    if linear:
+        return lin
+    z = gelu(round_bf16(lin))
     return z if exact else f64_to_bf16(z)
 
 

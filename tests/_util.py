@@ -65,6 +65,49 @@ def fp16_bits_to_f64(bits):
     return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
 
 
+def _bf16_neighbours(v):
+    """The bf16 values just below and just above each double v."""
+    import oracle
+    bits = oracle.f64_to_bf16(v)
+    r = bf16_bits_to_f64(bits)
+    o = _ordered(bits)
+    up = np.where(r >= v, o, o + 1)
+    lo = np.where(r <= v, o, o - 1)
+
+    def unorder(q):
+        q = np.asarray(q, np.int32)
+        return np.where(q < 0, (-q) | 0x8000, q).astype(np.uint16)
+    return bf16_bits_to_f64(unorder(lo)), bf16_bits_to_f64(unorder(up))
+
+
+def assert_mlp_block_close(got_bits, x_bits, blk, eps, what="", rel=FP32_TOL):
+    """A LayerNorm -> Linear -> GELU block output.  The block rounds the Linear
+    output t = x.W^T + b to bf16 before the GELU; that rounding is a decision
+    on an fp32 value the oracle only knows to the fp32 tolerance.  Where t
+    lies within that tolerance of a rounding boundary, either neighbour is a
+    correct intermediate, and the GPU output must be within 1 ulp of the GELU
+    of one of them (or, near a cancellation, within the fp32 bound)."""
+    import oracle
+    lin = oracle.mlp_block(x_bits, blk, eps, 8, linear=True)
+    lo, hi = _bf16_neighbours(lin)
+    rms = np.sqrt(np.mean(lin * lin, axis=1, keepdims=True))
+    near = np.abs(lin - 0.5 * (lo + hi)) <= rel * np.maximum(np.abs(lin), rms)
+    t_main = oracle.round_bf16(lin)
+    t_alt = np.where(t_main == lo, hi, lo)
+    got = np.asarray(got_bits, np.uint16).reshape(lin.shape)
+    g = bf16_bits_to_f64(got)
+    ok = np.zeros(lin.shape, bool)
+    for t, allowed in ((t_main, np.ones_like(near)), (t_alt, near)):
+        z = oracle.gelu(t)
+        d = ulp_dist(got, oracle.f64_to_bf16(z)).reshape(lin.shape)
+        zr = np.sqrt(np.mean(z * z, axis=1, keepdims=True))
+        close = (d <= 1) | (np.abs(g - z) <= rel * np.maximum(np.abs(z), zr))
+        ok |= allowed & close
+    assert ok.all(), f"{what}: {int((~ok).sum())} elements off"
+    d_main = ulp_dist(got, oracle.f64_to_bf16(oracle.gelu(t_main))).reshape(lin.shape)
+    return float(np.mean(d_main <= 1))
+
+
 def assert_bf16_close(got_bits, exact, what="", rel=FP32_TOL, min_frac_1ulp=0.995):
     """bf16 outputs that are functions of fp32 dot products: each element is
     within 1 ulp of the correctly rounded oracle value, or -- where the value
