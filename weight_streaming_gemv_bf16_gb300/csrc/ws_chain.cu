@@ -310,6 +310,13 @@ static ws_status build_ops(ws_chain* c) {
     bool ok = true;
     for (ChainOp& op : c->ops)
       if (!plan_gemv_persistent(op.p, slot, why, sizeof why)) ok = false;
+    if (ok) {
+      // the shared-memory layout must fit too; otherwise run op by op
+      std::vector<GemvParams> probe_ops;
+      for (ChainOp& op : c->ops) probe_ops.push_back(op.p);
+      PersistParams probe;
+      ok = plan_persistent(probe, probe_ops.data(), (int)probe_ops.size(), B, why, sizeof why);
+    }
     c->persistent = ok;
   }
   // schedules and one zeroed workspace with a slice per op

@@ -67,7 +67,7 @@ struct Sched {
   int off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
 };
 
-struct GemvParams {
+struct alignas(16) GemvParams {
   Seg seg[kMaxSeg];
   int nseg;
   int nmat;  // 1, or 2 for a gate/up pair

@@ -172,8 +172,119 @@ __device__ void prologue_stats(const GemvParams& p, float* stats, float* red, in
   __syncthreads();
 }
 
+// Normalise eight activations of batch row b at column 8*cg and pack them as
+// bf16 (one rounding).
+__device__ __forceinline__ uint4 normalise8(const GemvParams& p, const float* stats, int b, int cg,
+                                           float (&v)[8]) {
+  const int k = cg * 8;
+  if (p.prologue == PRO_RMSNORM) {
+    const float r = stats[2 * b];
+    const uint4 g = *reinterpret_cast<const uint4*>(p.gamma + k);
+    const float gf[8] = {bf16lo(g.x), bf16hi(g.x), bf16lo(g.y), bf16hi(g.y),
+                         bf16lo(g.z), bf16hi(g.z), bf16lo(g.w), bf16hi(g.w)};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = v[e] * r * gf[e];
+  } else if (p.prologue == PRO_LAYERNORM) {
+    const float mean = stats[2 * b], rstd = stats[2 * b + 1];
+    const uint4 g = *reinterpret_cast<const uint4*>(p.gamma + k);
+    const uint4 bt = *reinterpret_cast<const uint4*>(p.beta + k);
+    const float gf[8] = {bf16lo(g.x), bf16hi(g.x), bf16lo(g.y), bf16hi(g.y),
+                         bf16lo(g.z), bf16hi(g.z), bf16lo(g.w), bf16hi(g.w)};
+    const float bf[8] = {bf16lo(bt.x), bf16hi(bt.x), bf16lo(bt.y), bf16hi(bt.y),
+                         bf16lo(bt.z), bf16hi(bt.z), bf16lo(bt.w), bf16hi(bt.w)};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = (v[e] - mean) * rstd * gf[e] + bf[e];
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e]));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e + 1]));
+    w[e] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Prologue and staging in one pass: every thread loads all of its chunks of
+// the activations first (one round of memory latency), the CTA reduces the
+// statistics from registers, and the normalised bf16 rows go to shared
+// memory [BT][K].  Takes unsplit K and at most kMaxChunks chunks per thread;
+// returns false (having done nothing) otherwise.
+constexpr int kMaxChunks = 6;
+
+template <int BT>
+__device__ bool prologue_stage_fused(const GemvParams& p, float* stats, float* red, uint16_t* xs,
+                                     int tid) {
+  const int nch = p.K >> 3;
+  const int total = BT * nch;
+  if (p.sc.KS != p.K || total > kMaxChunks * kThreads) return false;
+  float v[kMaxChunks][8];
+#pragma unroll
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int o = tid + i * kThreads;
+    const int b = o / nch;
+    if (o < total && b < p.B) {
+      load_x8(p, b, o - b * nch, v[i]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[i][e] = 0.f;
+    }
+  }
+  if (p.prologue != PRO_NONE) {
+    float* tot = red + kWarps * BT;
+    float s[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) s[b] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxChunks; ++i) {
+      const int o = tid + i * kThreads;
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+        if (o / nch == b)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            s[b] = p.prologue == PRO_RMSNORM ? fmaf(v[i][e], v[i][e], s[b]) : s[b] + v[i][e];
+    }
+    block_sum<BT>(s, red, tot, p.B, tid);
+    if (p.prologue == PRO_RMSNORM) {
+      if (tid < p.B) stats[2 * tid] = rsqrtf(tot[tid] / (float)p.K + p.eps);
+    } else {
+      if (tid < p.B) stats[2 * tid] = tot[tid] / (float)p.K;
+      __syncthreads();
+#pragma unroll
+      for (int b = 0; b < BT; ++b) s[b] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxChunks; ++i) {
+        const int o = tid + i * kThreads;
+#pragma unroll
+        for (int b = 0; b < BT; ++b)
+          if (o / nch == b && b < p.B) {
+            const float mean = stats[2 * b];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[b] = fmaf(v[i][e] - mean, v[i][e] - mean, s[b]);
+          }
+      }
+      block_sum<BT>(s, red, tot, p.B, tid);
+      if (tid < p.B) stats[2 * tid + 1] = rsqrtf(tot[tid] / (float)p.K + p.eps);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxChunks; ++i) {
+    const int o = tid + i * kThreads;
+    if (o < total) {
+      const int b = o / nch;
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (b < p.B) out = normalise8(p, stats, b, o - b * nch, v[i]);
+      reinterpret_cast<uint4*>(xs)[o] = out;
+    }
+  }
+  return true;
+}
+
 // Stage columns [k0, k0 + KS) of the (normalised) activations as bf16 into
-// shared memory, [BT][KS]; rows b >= B are zero.
+// shared memory, [BT][KS]; rows b >= B are zero.  (General path: any K split
+// and any number of chunks per thread.)
 template <int BT>
 __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, int ks, int tid) {
   const int KS = p.sc.KS;
@@ -295,8 +406,10 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
   pdl_launch_dependents();
   pdl_wait();
 
-  prologue_stats<BT>(p, stats, red, tid);
-  stage_x<BT>(p, stats, xs, ks, tid);
+  if (!prologue_stage_fused<BT>(p, stats, red, xs, tid)) {
+    prologue_stats<BT>(p, stats, red, tid);
+    stage_x<BT>(p, stats, xs, ks, tid);
+  }
   __syncthreads();
 
   const int nchx = sc.KS >> 3;  // chunks of x in shared memory

@@ -38,43 +38,24 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Issue piece j of row group rg of op P into one ring stage (shapes at run
-// time; S = 1, so the columns are [j*PC, j*PC + len)).
-__device__ __forceinline__ void issue_piece_rt(const GemvParams& P, int rg, int j, uint8_t* dst,
-                                               uint64_t* bar, uint64_t pol) {
-  int seg, rgl;
-  decode_rg(P, rg, seg, rgl);
-  const Seg& S = P.seg[seg];
-  const int RT = P.sc.RT, PC = P.sc.PC, K = P.K;
-  const int row0 = rgl * RT;
-  const int rows = min(RT, S.M - row0);
-  const int c0 = j * PC;
-  const int len = min(PC, K - c0);
-  mbar_arrive_expect_tx(bar, (uint32_t)(P.nmat * rows * len * 2));
-  for (int mat = 0; mat < P.nmat; ++mat) {
-    const uint16_t* W = mat == 0 ? S.W0 : S.W1;
-    if (len == K) {
-      bulk_copy_g2s(dst + (size_t)mat * RT * PC * 2, W + (size_t)row0 * K, (uint32_t)(rows * K * 2),
-                    bar, pol);
-    } else {
-      for (int r = 0; r < rows; ++r)
-        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * PC * 2, W + (size_t)(row0 + r) * K + c0,
-                      (uint32_t)(len * 2), bar, pol);
-    }
-  }
-}
-
 // The copy cursor of one warp (advanced by lane 0 only): the next piece to
-// stream, walking this warp's pieces of every op in order.
+// stream, walking this warp's pieces of every op in order.  The current op's
+// shape and weight pointers are kept in registers, so a copy costs no
+// descriptor reads.
 struct IssueCursor {
-  int f;    // op
-  int q;    // piece within the op
-  int npw;  // pieces of this warp in op f
-  int ti;   // task within the op
-  int j;    // piece within the task
-  int rgw;  // this warp's first row group in op f
-  int slot; // ring stage of the next piece
-  int n;    // pieces issued so far
+  int f;     // op
+  int q;     // piece within the op
+  int npw;   // pieces of this warp in op f
+  int ti;    // task within the op
+  int j;     // piece within the task
+  int rgw;   // this warp's first row group in op f
+  int slot;  // ring stage of the next piece
+  int n;     // pieces issued so far
+  // op f, cached
+  int nseg, nmat, RT, PC, NP, K;
+  int M[kMaxSeg], rgb[kMaxSeg];
+  const uint16_t* W0[kMaxSeg];
+  const uint16_t* W1[kMaxSeg];
 };
 
 __device__ __forceinline__ void cursor_seek(const PersistParams& pp, IssueCursor& c, int warp) {
@@ -85,28 +66,78 @@ __device__ __forceinline__ void cursor_seek(const PersistParams& pp, IssueCursor
     c.j = 0;
     c.npw = 0;
     if (c.f < pp.nops) {
-      const Sched& sc = pp.ops[c.f].sc;
+      const GemvParams& P = pp.ops[c.f];
       int ks, rg0, rg1;
-      cta_range(sc, blockIdx.x, ks, rg0, rg1);
-      c.npw = warp_tasks(rg0, rg1, warp) * sc.NP;
+      cta_range(P.sc, blockIdx.x, ks, rg0, rg1);
+      c.NP = P.sc.NP;
+      c.npw = warp_tasks(rg0, rg1, warp) * c.NP;
       c.rgw = rg0 + warp;
+      c.nseg = P.nseg;
+      c.nmat = P.nmat;
+      c.RT = P.sc.RT;
+      c.PC = P.sc.PC;
+      c.K = P.K;
+#pragma unroll
+      for (int s = 0; s < kMaxSeg; ++s) {
+        c.M[s] = P.seg[s].M;
+        c.rgb[s] = P.seg[s].rg_begin;
+        c.W0[s] = P.seg[s].W0;
+        c.W1[s] = P.seg[s].W1;
+      }
     }
   }
 }
 
 __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor& c, int warp,
                                            uint8_t* ring, uint64_t* full, uint64_t pol) {
-  const GemvParams& P = pp.ops[c.f];
-  issue_piece_rt(P, c.rgw + c.ti * kWarps, c.j, ring + (size_t)c.slot * pp.slot_bytes,
-                 &full[c.slot], pol);
+  const int rg = c.rgw + c.ti * kWarps;
+  int seg = 0;
+  if (c.nseg > 1 && rg >= c.rgb[1]) seg = 1;
+  if (c.nseg > 2 && rg >= c.rgb[2]) seg = 2;
+  const int RT = c.RT, PC = c.PC, K = c.K;
+  const int row0 = (rg - c.rgb[seg]) * RT;
+  const int rows = min(RT, c.M[seg] - row0);
+  const int c0 = c.j * PC;
+  const int len = min(PC, K - c0);
+  uint8_t* dst = ring + (size_t)c.slot * pp.slot_bytes;
+  uint64_t* bar = &full[c.slot];
+  mbar_arrive_expect_tx(bar, (uint32_t)(c.nmat * rows * len * 2));
+  for (int mat = 0; mat < c.nmat; ++mat) {
+    const uint16_t* W = mat == 0 ? c.W0[seg] : c.W1[seg];
+    if (len == K) {
+      bulk_copy_g2s(dst + (size_t)mat * RT * PC * 2, W + (size_t)row0 * K,
+                    (uint32_t)(rows * K * 2), bar, pol);
+    } else {
+      for (int r = 0; r < rows; ++r)
+        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * PC * 2, W + (size_t)(row0 + r) * K + c0,
+                      (uint32_t)(len * 2), bar, pol);
+    }
+  }
   ++c.n;
   ++c.q;
-  if (++c.j == P.sc.NP) {
+  if (++c.j == c.NP) {
     c.j = 0;
     ++c.ti;
   }
   if (++c.slot == pp.NSW) c.slot = 0;
   cursor_seek(pp, c, warp);
+}
+
+// Asynchronous 16-byte copies of an op descriptor into shared memory (the
+// next op's, fetched while the current op computes).
+__device__ __forceinline__ void prefetch_descriptor(const GemvParams* src, GemvParams* dst,
+                                                    int tid) {
+  constexpr int n16 = (int)(sizeof(GemvParams) / 16);
+  if (tid < n16) {
+    const char* s = reinterpret_cast<const char*>(src) + 16 * tid;
+    const uint32_t d = smem_addr(reinterpret_cast<char*>(dst) + 16 * tid);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(s) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_descriptor() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 struct ConsumeState {
@@ -232,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  GemvParams* Ps = reinterpret_cast<GemvParams*>(smem + pp.off_op);
+  GemvParams* Ps = reinterpret_cast<GemvParams*>(smem + pp.off_op);  // two buffers
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + pp.off_bar) + warp * kMaxStages;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + pp.off_flags);
   float* stats = reinterpret_cast<float*>(smem + pp.off_stats);
@@ -265,21 +296,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   cs.slot = 0;
   cs.phase = 0;
   cs.abort = false;
+  prefetch_descriptor(pp.ops, Ps, tid);
 
   for (int f = 0; f < pp.nops; ++f) {
     if (f > 0) {
       grid_wait(pp, f - 1, flags, tid);
       copy_trace(pp.ops + (f - 1), tid);
     }
-    {
-      const int* src = reinterpret_cast<const int*>(pp.ops + f);
-      int* dst = reinterpret_cast<int*>(Ps);
-      for (int i = tid; i < (int)(sizeof(GemvParams) / sizeof(int)); i += kThreads) dst[i] = src[i];
-    }
+    wait_descriptor();
     __syncthreads();
-    const GemvParams& P = *Ps;
-    prologue_stats<BT>(P, stats, red, tid);
-    stage_x<BT>(P, stats, xs, 0, tid);
+    const GemvParams& P = Ps[f & 1];
+    // the next op's descriptor streams in while this op runs
+    if (f + 1 < pp.nops) prefetch_descriptor(pp.ops + f + 1, &Ps[(f + 1) & 1], tid);
+    if (!prologue_stage_fused<BT>(P, stats, red, xs, tid)) {
+      prologue_stats<BT>(P, stats, red, tid);
+      stage_x<BT>(P, stats, xs, 0, tid);
+    }
     __syncthreads();
 
     int ks, rg0, rg1;
@@ -448,7 +480,7 @@ bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, 
   pp.slot_bytes = align_up_p(slot, 128);
   int off = 0;
   pp.off_op = off;
-  off += align_up_p((int)sizeof(GemvParams), 128);
+  off += 2 * align_up_p((int)sizeof(GemvParams), 128);
   pp.off_bar = off;
   off += kWarps * kMaxStages * 8;
   pp.off_flags = off;
