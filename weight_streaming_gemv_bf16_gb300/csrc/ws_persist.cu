@@ -91,19 +91,23 @@ __device__ __forceinline__ void cursor_seek(const PersistParams& pp, IssueCursor
 __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor& c, int warp,
                                            uint8_t* ring, uint64_t* full, uint64_t pol) {
   const int rg = c.rgw + c.ti * kWarps;
-  int seg = 0;
-  if (c.nseg > 1 && rg >= c.rgb[1]) seg = 1;
-  if (c.nseg > 2 && rg >= c.rgb[2]) seg = 2;
+  // segment by selects (the cached arrays stay in registers)
+  const bool s1 = c.nseg > 1 && rg >= c.rgb[1];
+  const bool s2 = c.nseg > 2 && rg >= c.rgb[2];
+  const int rgb = s2 ? c.rgb[2] : (s1 ? c.rgb[1] : c.rgb[0]);
+  const int Mseg = s2 ? c.M[2] : (s1 ? c.M[1] : c.M[0]);
+  const uint16_t* W0 = s2 ? c.W0[2] : (s1 ? c.W0[1] : c.W0[0]);
+  const uint16_t* W1 = s2 ? c.W1[2] : (s1 ? c.W1[1] : c.W1[0]);
   const int RT = c.RT, PC = c.PC, K = c.K;
-  const int row0 = (rg - c.rgb[seg]) * RT;
-  const int rows = min(RT, c.M[seg] - row0);
+  const int row0 = (rg - rgb) * RT;
+  const int rows = min(RT, Mseg - row0);
   const int c0 = c.j * PC;
   const int len = min(PC, K - c0);
   uint8_t* dst = ring + (size_t)c.slot * pp.slot_bytes;
   uint64_t* bar = &full[c.slot];
   mbar_arrive_expect_tx(bar, (uint32_t)(c.nmat * rows * len * 2));
   for (int mat = 0; mat < c.nmat; ++mat) {
-    const uint16_t* W = mat == 0 ? c.W0[seg] : c.W1[seg];
+    const uint16_t* W = mat == 0 ? W0 : W1;
     if (len == K) {
       bulk_copy_g2s(dst + (size_t)mat * RT * PC * 2, W + (size_t)row0 * K,
                     (uint32_t)(rows * K * 2), bar, pol);
