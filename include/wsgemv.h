@@ -298,6 +298,14 @@ ws_status ws_chain_step_host(ws_chain *c, const void *in_host, const void *attn_
 int ws_chain_num_ops(const ws_chain *c);
 /* 1 if the chain runs as one persistent kernel per step, else 0. */
 int ws_chain_is_persistent(const ws_chain *c);
+/* Diagnostics of a persistent chain: CTAs per launch (0 if not persistent),
+ * and a device buffer (uint64 [grid][ops][4], or NULL to stop) where every
+ * later-captured step records, per CTA and op, globaltimer ns at the op's
+ * start (after its grid barrier), after its activations are staged, when its
+ * tasks are done, and when warp 0's first weight piece of the op landed.
+ * Call ws_chain_capture again after setting it. */
+int ws_chain_grid(const ws_chain *c);
+ws_status ws_chain_debug_stamps(ws_chain *c, unsigned long long *stamps, size_t n);
 /* Plan and measured gain (95% CI lower bound, mean) of each op; n entries. */
 ws_status ws_chain_plans(const ws_chain *c, ws_prefetch_plan *plans, float *gain_lo,
                          float *gain_mean, int n);

@@ -117,6 +117,8 @@ _OTHER = {
     "ws_device_error": ([I32], I32),
     "ws_chain_num_ops": ([P], I32),
     "ws_chain_is_persistent": ([P], I32),
+    "ws_chain_grid": ([P], I32),
+    "ws_chain_debug_stamps": ([P, P, SZ], I32),
     "ws_chain_destroy": ([P], None),
     "ws_get_tuning": ([P], None),
     "ws_debug_gemv_copies": ([I32, I32, I32, I32, I32, I32, P, C.c_long], C.c_long),
@@ -369,6 +371,15 @@ class Chain:
         _check(load().ws_chain_plans(self.handle, pl, lo, mean, n))
         return [((p.mode, p.blocks, p.threads, p.stride_bytes), lo[i], mean[i])
                 for i, p in enumerate(pl)]
+
+    def debug_stamps(self, buf):
+        """Record per-CTA, per-op timestamps into `buf` (int64 [grid, ops, 4]) on
+        every later-captured step; None stops.  Re-capture afterwards."""
+        n = 0 if buf is None else buf.numel()
+        _check(load().ws_chain_debug_stamps(self.handle, _ptr(buf), n))
+
+    def grid(self) -> int:
+        return int(load().ws_chain_grid(self.handle))
 
     def op_bytes(self):
         n = self.n_ops

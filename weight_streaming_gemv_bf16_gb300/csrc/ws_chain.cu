@@ -924,6 +924,25 @@ int ws_chain_num_ops(const ws_chain* c) { return c ? (int)c->ops.size() : 0; }
 
 int ws_chain_is_persistent(const ws_chain* c) { return c && c->persistent ? 1 : 0; }
 
+ws_status ws_chain_debug_stamps(ws_chain* c, unsigned long long* stamps, size_t n) {
+  if (!c || !c->persistent) {
+    set_error("stamps are recorded by persistent chains only");
+    return WS_ERR_STATE;
+  }
+  const size_t need = (size_t)c->persist.grid * c->ops.size() * 4;
+  if (stamps && n < need) {
+    set_error("stamp buffer too small: need %zu entries", need);
+    return WS_ERR_ARG;
+  }
+  c->persist.stamps = stamps;
+  return WS_OK;
+}
+
+int ws_chain_grid(const ws_chain* c) {
+  if (!c) return 0;
+  return c->persistent ? c->persist.grid : 0;
+}
+
 ws_status ws_chain_plans(const ws_chain* c, ws_prefetch_plan* plans, float* gain_lo,
                          float* gain_mean, int n) {
   if (!c || n < 0) {

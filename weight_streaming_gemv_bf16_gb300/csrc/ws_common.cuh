@@ -111,6 +111,10 @@ struct PersistParams {
   int grid;
   int smem_bytes;
   int off_op, off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
+  // optional: per CTA and op, globaltimer ns at [0] the start of the op (after
+  // its grid barrier), [1] after the activations are staged, [2] when its
+  // tasks are done, [3] the first weight piece of the op landing (warp 0)
+  unsigned long long* stamps;
 };
 
 // The split and the row-group range of CTA `cta`.

@@ -156,7 +156,8 @@ template <int BT, int NMAT, int RT>
 __device__ __forceinline__ void run_task(const PersistParams& pp, const GemvParams& P, int rg,
                                          uint8_t* ring, uint64_t* full, const uint4* xs4,
                                          ConsumeState& cs, IssueCursor& ic, uint64_t pol,
-                                         float& best_v, int& best_i, int warp, int lane) {
+                                         float& best_v, int& best_i, int warp, int lane,
+                                         unsigned long long* land_stamp) {
   int seg, rgl;
   decode_rg(P, rg, seg, rgl);
   const int row0 = rgl * RT;
@@ -173,6 +174,7 @@ __device__ __forceinline__ void run_task(const PersistParams& pp, const GemvPara
   for (int j = 0; j < NP; ++j) {
     const int len = min(PC, P.K - j * PC);
     const bool ok = cs.abort || mbar_wait_bounded(&full[cs.slot], cs.phase, pp.timeout_ns);
+    if (land_stamp && j == 0 && lane == 0) *land_stamp = global_ns();
     if (__any_sync(0xffffffffu, !ok) && !cs.abort) {
       cs.abort = true;
       if (lane == 0) raise_device_error(pp.err, DERR_TIMEOUT);
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     wait_descriptor();
     __syncthreads();
+    unsigned long long* stamp = pp.stamps ? pp.stamps + ((size_t)blockIdx.x * pp.nops + f) * 4 : nullptr;
+    if (stamp && tid == 0) stamp[0] = global_ns();
     const GemvParams& P = Ps[f & 1];
     // the next op's descriptor streams in while this op runs
     if (f + 1 < pp.nops) prefetch_descriptor(pp.ops + f + 1, &Ps[(f + 1) & 1], tid);
@@ -317,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       stage_x<BT>(P, stats, xs, 0, tid);
     }
     __syncthreads();
+    if (stamp && tid == 0) stamp[1] = global_ns();
 
     int ks, rg0, rg1;
     cta_range(P.sc, blockIdx.x, ks, rg0, rg1);
@@ -326,13 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kind = (P.nmat - 1) * 3 + (P.sc.RT == 1 ? 0 : (P.sc.RT == 2 ? 1 : 2));
     for (int t = 0; t < ntask; ++t) {
       const int rg = rg0 + warp + t * kWarps;
+      unsigned long long* land = (stamp && warp == 0 && t == 0) ? stamp + 3 : nullptr;
       switch (kind) {
-        case 0: run_task<BT, 1, 1>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane); break;
-        case 1: run_task<BT, 1, 2>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane); break;
-        case 2: run_task<BT, 1, 4>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane); break;
-        case 3: run_task<BT, 2, 1>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane); break;
-        case 4: run_task<BT, 2, 2>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane); break;
-        default: run_task<BT, 2, 4>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane); break;
+        case 0: run_task<BT, 1, 1>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
+        case 1: run_task<BT, 1, 2>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
+        case 2: run_task<BT, 1, 4>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
+        case 3: run_task<BT, 2, 1>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
+        case 4: run_task<BT, 2, 2>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
+        default: run_task<BT, 2, 4>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
       }
     }
 
@@ -382,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this CTA is done with op f: its outputs are written
     __threadfence();
     __syncthreads();
+    if (stamp && tid == 0) stamp[2] = global_ns();
     if (tid == 0) atomicAdd(pp.bar + f, 1u);
   }
   if (pp.nops > 0 && pp.ops[pp.nops - 1].trace_out) {
