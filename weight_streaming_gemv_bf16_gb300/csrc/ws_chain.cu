@@ -306,10 +306,12 @@ static ws_status build_ops(ws_chain* c) {
   // persistent mode when asked for and every op fits its stage layout
   c->persistent = false;
   if (o.persistent && B <= 4) {
-    const int slot = tuning().piece_bytes > 0 ? tuning().piece_bytes : 6144;
-    bool ok = true;
+    int kmax = 8;
+    for (ChainOp& op : c->ops) kmax = op.p.K > kmax ? op.p.K : kmax;
+    const int ring = persistent_ring_bytes(B, kmax);
+    bool ok = ring > 0;
     for (ChainOp& op : c->ops)
-      if (!plan_gemv_persistent(op.p, slot, why, sizeof why)) ok = false;
+      if (ok && !plan_gemv_persistent(op.p, ring, why, sizeof why)) ok = false;
     if (ok) {
       // the shared-memory layout must fit too; otherwise run op by op
       std::vector<GemvParams> probe_ops;

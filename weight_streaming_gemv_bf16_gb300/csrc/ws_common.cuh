@@ -161,7 +161,8 @@ cudaError_t launch_gemv(const GemvParams& p, cudaStream_t stream, bool pdl);
 void init_gemv_params(GemvParams& p, int K, int B);
 size_t argmax_rows_workspace(int rows, int cols);
 // persistent chain (ws_persist.cu)
-bool plan_gemv_persistent(GemvParams& p, int slot_bytes, char* why, size_t why_len);
+bool plan_gemv_persistent(GemvParams& p, int ring_bytes, char* why, size_t why_len);
+int persistent_ring_bytes(int B, int kmax);
 bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, char* why,
                      size_t why_len);
 bool prepare_persistent(int BT);

@@ -4,20 +4,27 @@
 // The ops of a chain depend on each other only through their small
 // activation vectors; their weights -- all but ~0.01% of the bytes -- do not
 // depend on anything.  So each warp streams its weight pieces of every op, in
-// order, through its own ring of shared-memory stages, and its copy cursor
-// runs ahead across op boundaries.  Between ops the CTAs meet at a grid
-// barrier (the previous op's outputs are complete), normalise the next
-// activation vector into shared memory and compute on pieces that have
-// usually already landed.  HBM keeps streaming through every barrier and
-// prologue as long as the rings (about 190 KB per SM) have room, which is
-// what a chain of separate launches cannot do: there each op boundary drains
-// the memory pipeline ("One Token, Kernel by Kernel: A Decode Step on a
-// Laptop GPU", Step 3, where kernel gaps are counted against the bandwidth
-// floor).
+// order, through its own byte ring in shared memory, and its copy cursor runs
+// ahead across op boundaries.  Between ops the CTAs meet at a grid barrier
+// (the previous op's outputs are complete), normalise the next activation
+// vector into shared memory and compute on pieces that have usually already
+// landed.  HBM keeps streaming through every barrier and prologue as long as
+// the rings have room, which a chain of separate launches cannot do: there
+// each op boundary drains the memory pipeline ("One Token, Kernel by Kernel:
+// A Decode Step on a Laptop GPU", Step 3, where kernel gaps are counted
+// against the bandwidth floor).
 //
-// Work split, epilogues and numerics are those of k_stream_gemv (one warp
-// per task of RT rows, full K, pieces of PC columns), so every op computes
-// exactly what the standalone entry point computes with S = 1.  All waits are
+// Work: an op's units (row group of RT rows x one of S K-splits) are dealt
+// round-robin over all warps of the grid, so every warp gets the same number
+// of units to within one; long rows are split in K so the per-warp load
+// evens out, the splits' partial sums being added by the last split to finish
+// (atomic ticket), in split order.  Pieces (RT rows x up to PC columns) are
+// packed back to back in the warp's byte ring; a piece's place follows from
+// the sizes of the pieces before it, so the copy cursor and the consumer
+// compute it the same way without sharing any state.  Eight mbarriers per
+// warp track up to eight pieces in flight.
+//
+// Epilogues and numerics are those of the standalone kernel.  All waits are
 // bounded: a grid barrier or a copy that does not arrive within timeout_ns
 // sets the device error flag and the kernel runs to its end without waiting.
 #include <cuda_runtime.h>
@@ -32,51 +39,72 @@
 
 namespace ws {
 
+constexpr int kBars = 8;  // mbarriers (pieces in flight) per warp
+
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
+// Units of op sc for global warp gw: u = gw, gw + GW, ...
+__device__ __forceinline__ int warp_units(const Sched& sc, int gw, int GW) {
+  const int U = sc.RG * sc.S;
+  return U > gw ? (U - gw + GW - 1) / GW : 0;
+}
+
+// Bytes a piece takes in the ring: RT rows reserved, `len` columns each.
+__device__ __forceinline__ int piece_size(int nmat, int RT, int len) { return nmat * RT * len * 2; }
+
+// Place a piece of `sz` bytes at linear ring position `lin`: returns the
+// offset in the ring and advances `lin` past the piece (a piece never wraps;
+// the tail is skipped instead).
+__device__ __forceinline__ int ring_place(long long& lin, int sz, int R) {
+  int off = (int)(lin % R);
+  if (off + sz > R) {
+    lin += R - off;
+    off = 0;
+  }
+  lin += sz;
+  return off;
+}
+
 // The copy cursor of one warp (advanced by lane 0 only): the next piece to
-// stream, walking this warp's pieces of every op in order.  The current op's
-// shape and weight pointers are kept in registers, so a copy costs no
-// descriptor reads.
+// stream, walking this warp's pieces of every op in order, with the current
+// op's shape and weight pointers cached in registers.
 struct IssueCursor {
-  int f;     // op
-  int q;     // piece within the op
-  int npw;   // pieces of this warp in op f
-  int ti;    // task within the op
-  int j;     // piece within the task
-  int rgw;   // this warp's first row group in op f
-  int slot;  // ring stage of the next piece
-  int n;     // pieces issued so far
-  // op f, cached
-  int nseg, nmat, RT, PC, NP, K;
+  int f;          // op
+  int q;          // piece within the op for this warp
+  int npw;        // pieces of this warp in op f
+  int ui;         // unit index within this warp's units of op f
+  int j;          // piece within the unit
+  int n;          // pieces issued so far
+  long long lin;  // linear ring position of the next piece
+  int nseg, nmat, RT, PC, NP, K, KS, S;
   int M[kMaxSeg], rgb[kMaxSeg];
   const uint16_t* W0[kMaxSeg];
   const uint16_t* W1[kMaxSeg];
 };
 
-__device__ __forceinline__ void cursor_seek(const PersistParams& pp, IssueCursor& c, int warp) {
+__device__ __forceinline__ void cursor_seek(const PersistParams& pp, IssueCursor& c, int gw,
+                                            int GW) {
   while (c.f < pp.nops && c.q >= c.npw) {
     ++c.f;
     c.q = 0;
-    c.ti = 0;
+    c.ui = 0;
     c.j = 0;
     c.npw = 0;
     if (c.f < pp.nops) {
       const GemvParams& P = pp.ops[c.f];
-      int ks, rg0, rg1;
-      cta_range(P.sc, blockIdx.x, ks, rg0, rg1);
       c.NP = P.sc.NP;
-      c.npw = warp_tasks(rg0, rg1, warp) * c.NP;
-      c.rgw = rg0 + warp;
+      c.npw = warp_units(P.sc, gw, GW) * c.NP;
       c.nseg = P.nseg;
       c.nmat = P.nmat;
       c.RT = P.sc.RT;
       c.PC = P.sc.PC;
       c.K = P.K;
+      c.KS = P.sc.KS;
+      c.S = P.sc.S;
 #pragma unroll
       for (int s = 0; s < kMaxSeg; ++s) {
         c.M[s] = P.seg[s].M;
@@ -88,32 +116,40 @@ __device__ __forceinline__ void cursor_seek(const PersistParams& pp, IssueCursor
   }
 }
 
-__device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor& c, int warp,
-                                           uint8_t* ring, uint64_t* full, uint64_t pol) {
-  const int rg = c.rgw + c.ti * kWarps;
-  // segment by selects (the cached arrays stay in registers)
+// Bytes of the cursor's next piece.
+__device__ __forceinline__ int cursor_piece_bytes(const IssueCursor& c) {
+  const int len = min(c.PC, c.KS - c.j * c.PC);
+  return piece_size(c.nmat, c.RT, len);
+}
+
+__device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor& c, int gw, int GW,
+                                           uint8_t* ring, uint64_t* bars, uint64_t pol) {
+  const int u = gw + c.ui * GW;
+  const int rg = u / c.S;
+  const int ks = u - rg * c.S;
   const bool s1 = c.nseg > 1 && rg >= c.rgb[1];
   const bool s2 = c.nseg > 2 && rg >= c.rgb[2];
   const int rgb = s2 ? c.rgb[2] : (s1 ? c.rgb[1] : c.rgb[0]);
   const int Mseg = s2 ? c.M[2] : (s1 ? c.M[1] : c.M[0]);
   const uint16_t* W0 = s2 ? c.W0[2] : (s1 ? c.W0[1] : c.W0[0]);
   const uint16_t* W1 = s2 ? c.W1[2] : (s1 ? c.W1[1] : c.W1[0]);
-  const int RT = c.RT, PC = c.PC, K = c.K;
+  const int RT = c.RT, K = c.K;
   const int row0 = (rg - rgb) * RT;
   const int rows = min(RT, Mseg - row0);
-  const int c0 = c.j * PC;
-  const int len = min(PC, K - c0);
-  uint8_t* dst = ring + (size_t)c.slot * pp.slot_bytes;
-  uint64_t* bar = &full[c.slot];
+  const int c0 = ks * c.KS + c.j * c.PC;
+  const int len = min(c.PC, c.KS - c.j * c.PC);
+  const int sz = piece_size(c.nmat, RT, len);
+  uint8_t* dst = ring + ring_place(c.lin, sz, pp.slot_bytes);
+  uint64_t* bar = &bars[c.n & (kBars - 1)];
   mbar_arrive_expect_tx(bar, (uint32_t)(c.nmat * rows * len * 2));
   for (int mat = 0; mat < c.nmat; ++mat) {
     const uint16_t* W = mat == 0 ? W0 : W1;
     if (len == K) {
-      bulk_copy_g2s(dst + (size_t)mat * RT * PC * 2, W + (size_t)row0 * K,
+      bulk_copy_g2s(dst + (size_t)mat * RT * len * 2, W + (size_t)row0 * K,
                     (uint32_t)(rows * K * 2), bar, pol);
     } else {
       for (int r = 0; r < rows; ++r)
-        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * PC * 2, W + (size_t)(row0 + r) * K + c0,
+        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * len * 2, W + (size_t)(row0 + r) * K + c0,
                       (uint32_t)(len * 2), bar, pol);
     }
   }
@@ -121,10 +157,31 @@ __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor&
   ++c.q;
   if (++c.j == c.NP) {
     c.j = 0;
-    ++c.ti;
+    ++c.ui;
   }
-  if (++c.slot == pp.NSW) c.slot = 0;
-  cursor_seek(pp, c, warp);
+  cursor_seek(pp, c, gw, GW);
+}
+
+// The consumer's view of the ring, the same in every lane.
+struct ConsumeState {
+  int n;          // pieces consumed
+  long long lin;  // linear ring position of the next piece
+  bool abort;
+};
+
+// Issue pieces while a barrier is free and the next piece fits behind the
+// consumer (lane 0 only).
+__device__ __forceinline__ void refill(const PersistParams& pp, IssueCursor& ic,
+                                       const ConsumeState& cs, int gw, int GW, uint8_t* ring,
+                                       uint64_t* bars, uint64_t pol) {
+  const int R = pp.slot_bytes;
+  while (ic.f < pp.nops && ic.n - cs.n < kBars) {
+    const int sz = cursor_piece_bytes(ic);
+    long long lin = ic.lin;
+    ring_place(lin, sz, R);
+    if (lin - cs.lin > R) break;
+    issue_next(pp, ic, gw, GW, ring, bars, pol);
+  }
 }
 
 // Asynchronous 16-byte copies of an op descriptor into shared memory (the
@@ -144,25 +201,24 @@ __device__ __forceinline__ void wait_descriptor() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-struct ConsumeState {
-  int slot;
-  uint32_t phase;
-  bool abort;
-};
-
-// One task (RT rows, full K) of op P: consume its NP pieces, refilling each
-// stage with the cursor's next piece, then reduce and run the epilogue.
+// One unit (RT rows x one K split) of op P: consume its NP pieces (refilling
+// the ring as they free up), reduce over lanes, then run the epilogue -- or,
+// for a split, publish the partial sums and let the last split finish.
 template <int BT, int NMAT, int RT>
-__device__ __forceinline__ void run_task(const PersistParams& pp, const GemvParams& P, int rg,
-                                         uint8_t* ring, uint64_t* full, const uint4* xs4,
+__device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvParams& P, int u,
+                                         uint8_t* ring, uint64_t* bars, const uint4* xs4,
                                          ConsumeState& cs, IssueCursor& ic, uint64_t pol,
-                                         float& best_v, int& best_i, int warp, int lane,
+                                         float& best_v, int& best_i, int gw, int GW, int lane,
                                          unsigned long long* land_stamp) {
+  const int S = P.sc.S;
+  const int rg = u / S;
+  const int ks = u - rg * S;
   int seg, rgl;
   decode_rg(P, rg, seg, rgl);
   const int row0 = rgl * RT;
   const int rows = min(RT, P.seg[seg].M - row0);
-  const int NP = P.sc.NP, PC = P.sc.PC, ncp = PC >> 3, nchx = P.K >> 3;
+  const int NP = P.sc.NP, PC = P.sc.PC, KS = P.sc.KS, nchx = P.K >> 3;
+  const int R = pp.slot_bytes;
   float acc[NMAT][RT][BT];
 #pragma unroll
   for (int m = 0; m < NMAT; ++m)
@@ -172,17 +228,20 @@ __device__ __forceinline__ void run_task(const PersistParams& pp, const GemvPara
       for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
 
   for (int j = 0; j < NP; ++j) {
-    const int len = min(PC, P.K - j * PC);
-    const bool ok = cs.abort || mbar_wait_bounded(&full[cs.slot], cs.phase, pp.timeout_ns);
+    const int len = min(PC, KS - j * PC);
+    const int ncp = len >> 3;
+    const int off = ring_place(cs.lin, piece_size(NMAT, RT, len), R);
+    const bool ok = cs.abort || mbar_wait_bounded(&bars[cs.n & (kBars - 1)],
+                                                  (uint32_t)((cs.n / kBars) & 1), pp.timeout_ns);
     if (land_stamp && j == 0 && lane == 0) *land_stamp = global_ns();
     if (__any_sync(0xffffffffu, !ok) && !cs.abort) {
       cs.abort = true;
       if (lane == 0) raise_device_error(pp.err, DERR_TIMEOUT);
     }
-    const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)cs.slot * pp.slot_bytes);
-    const int xoff = j * ncp;
+    const uint4* st = reinterpret_cast<const uint4*>(ring + off);
+    const int xoff = (ks * KS + j * PC) >> 3;
 #pragma unroll 2
-    for (int c = lane; c < (len >> 3); c += 32) {
+    for (int c = lane; c < ncp; c += 32) {
       float wf[NMAT][RT][8];
 #pragma unroll
       for (int r = 0; r < RT; ++r)
@@ -207,14 +266,10 @@ __device__ __forceinline__ void run_task(const PersistParams& pp, const GemvPara
             for (int e = 0; e < 8; ++e) acc[m][r][b] = fmaf(wf[m][r][e], xf[e], acc[m][r][b]);
       }
     }
-    // every lane's reads of this stage have returned: refill it with the
-    // cursor's next piece (possibly of a later op)
+    // every lane's reads of this piece have returned: its bytes are free
     __syncwarp();
-    if (lane == 0 && !cs.abort && ic.f < pp.nops) issue_next(pp, ic, warp, ring, full, pol);
-    if (++cs.slot == pp.NSW) {
-      cs.slot = 0;
-      cs.phase ^= 1u;
-    }
+    ++cs.n;
+    if (lane == 0 && !cs.abort) refill(pp, ic, cs, gw, GW, ring, bars, pol);
   }
 #pragma unroll
   for (int m = 0; m < NMAT; ++m)
@@ -222,12 +277,52 @@ __device__ __forceinline__ void run_task(const PersistParams& pp, const GemvPara
     for (int r = 0; r < RT; ++r)
 #pragma unroll
       for (int b = 0; b < BT; ++b) acc[m][r][b] = warp_sum(acc[m][r][b]);
+  if (S == 1) {
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+        if (lane == r * BT + b && r < rows && b < P.B)
+          apply_epilogue(P, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v, best_i);
+    return;
+  }
+  const int rowg = P.seg[seg].row_base + row0;
 #pragma unroll
   for (int r = 0; r < RT; ++r)
 #pragma unroll
     for (int b = 0; b < BT; ++b)
-      if (lane == r * BT + b && r < rows && b < P.B)
-        apply_epilogue(P, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v, best_i);
+      if (lane == r * BT + b && r < rows && b < P.B) {
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+          P.part[((size_t)(ks * NMAT + m) * P.B + b) * P.M_total + rowg + r] = acc[m][r][b];
+      }
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    const unsigned old = atomicAdd(&P.tickets[rg], 1u);
+    last = old == (unsigned)(S - 1);
+    if (last) atomicExch(&P.tickets[rg], 0u);
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) {
+    __threadfence();
+    for (int o = lane; o < rows * P.B; o += 32) {
+      const int rr = o / P.B;
+      const int b = o - rr * P.B;
+      float v[NMAT];
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        float t = 0.f;
+        for (int s = 0; s < S; ++s)
+          t += __ldcg(&P.part[((size_t)(s * NMAT + m) * P.B + b) * P.M_total + rowg + rr]);
+        v[m] = t;
+      }
+      float dv = -INFINITY;
+      int di = 0x7fffffff;
+      apply_epilogue(P, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di);
+    }
+  }
 }
 
 // Wait until every CTA has finished op f (bounded).  Thread 0 spins; all
@@ -269,8 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int GW = gridDim.x * kWarps;
+  const int gw = blockIdx.x * kWarps + warp;
   GemvParams* Ps = reinterpret_cast<GemvParams*>(smem + pp.off_op);  // two buffers
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pp.off_bar) + warp * kMaxStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pp.off_bar) + warp * kBars;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + pp.off_flags);
   float* stats = reinterpret_cast<float*>(smem + pp.off_stats);
   float* red = reinterpret_cast<float*>(smem + pp.off_red);
@@ -278,30 +375,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* argi = reinterpret_cast<int*>(argv + kWarps * 32);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + pp.off_xs);
   const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
-  uint8_t* ring = smem + pp.off_ring + (size_t)warp * pp.NSW * pp.slot_bytes;
+  uint8_t* ring = smem + pp.off_ring + (size_t)warp * pp.slot_bytes;
 
   IssueCursor ic;
   ic.f = -1;
   ic.q = 0;
   ic.npw = 0;
-  ic.ti = 0;
+  ic.ui = 0;
   ic.j = 0;
-  ic.rgw = 0;
-  ic.slot = 0;
   ic.n = 0;
+  ic.lin = 0;
+  ConsumeState cs;
+  cs.n = 0;
+  cs.lin = 0;
+  cs.abort = false;
   uint64_t pol = 0;
   if (tid == 0) flags[1] = 0;
   if (lane == 0) {
-    for (int s = 0; s < pp.NSW; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kBars; ++s) mbar_init(&bars[s], 1);
     fence_mbar_init();
     pol = pp.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-    cursor_seek(pp, ic, warp);
-    for (int k = 0; k < pp.NSW && ic.f < pp.nops; ++k) issue_next(pp, ic, warp, ring, full, pol);
+    cursor_seek(pp, ic, gw, GW);
+    refill(pp, ic, cs, gw, GW, ring, bars, pol);
   }
-  ConsumeState cs;
-  cs.slot = 0;
-  cs.phase = 0;
-  cs.abort = false;
   prefetch_descriptor(pp.ops, Ps, tid);
 
   for (int f = 0; f < pp.nops; ++f) {
@@ -311,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     wait_descriptor();
     __syncthreads();
-    unsigned long long* stamp = pp.stamps ? pp.stamps + ((size_t)blockIdx.x * pp.nops + f) * 4 : nullptr;
+    unsigned long long* stamp =
+        pp.stamps ? pp.stamps + ((size_t)blockIdx.x * pp.nops + f) * 4 : nullptr;
     if (stamp && tid == 0) stamp[0] = global_ns();
     const GemvParams& P = Ps[f & 1];
     // the next op's descriptor streams in while this op runs
@@ -323,22 +420,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (stamp && tid == 0) stamp[1] = global_ns();
 
-    int ks, rg0, rg1;
-    cta_range(P.sc, blockIdx.x, ks, rg0, rg1);
-    const int ntask = warp_tasks(rg0, rg1, warp);
+    const int nunits = warp_units(P.sc, gw, GW);
     float best_v = -INFINITY;
     int best_i = 0x7fffffff;
     const int kind = (P.nmat - 1) * 3 + (P.sc.RT == 1 ? 0 : (P.sc.RT == 2 ? 1 : 2));
-    for (int t = 0; t < ntask; ++t) {
-      const int rg = rg0 + warp + t * kWarps;
+    for (int t = 0; t < nunits; ++t) {
+      const int u = gw + t * GW;
       unsigned long long* land = (stamp && warp == 0 && t == 0) ? stamp + 3 : nullptr;
       switch (kind) {
-        case 0: run_task<BT, 1, 1>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
-        case 1: run_task<BT, 1, 2>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
-        case 2: run_task<BT, 1, 4>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
-        case 3: run_task<BT, 2, 1>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
-        case 4: run_task<BT, 2, 2>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
-        default: run_task<BT, 2, 4>(pp, P, rg, ring, full, xs4, cs, ic, pol, best_v, best_i, warp, lane, land); break;
+        case 0: run_unit<BT, 1, 1>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
+        case 1: run_unit<BT, 1, 2>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
+        case 2: run_unit<BT, 1, 4>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
+        case 3: run_unit<BT, 2, 1>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
+        case 4: run_unit<BT, 2, 2>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
+        default: run_unit<BT, 2, 4>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
       }
     }
 
@@ -398,8 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (cs.abort && lane == 0) {
     // a wait ran out: let the copies still in flight land before exit
-    for (int q = ic.n - pp.NSW; q < ic.n; ++q)
-      if (q >= 0) mbar_wait_bounded(&full[q % pp.NSW], (q / pp.NSW) & 1, pp.timeout_ns);
+    for (int q = cs.n; q < ic.n; ++q)
+      mbar_wait_bounded(&bars[q & (kBars - 1)], (uint32_t)((q / kBars) & 1), pp.timeout_ns);
   }
   // the last CTA out resets the barrier counters for the next launch
   __syncthreads();
@@ -418,82 +513,19 @@ static int batch_template_p(int B) { return B <= 1 ? 1 : (B <= 2 ? 2 : (B <= 4 ?
 static int align_up_p(int v, int a) { return (v + a - 1) / a * a; }
 static constexpr int kSmemMaxP = 227 * 1024;
 
-bool plan_gemv_persistent(GemvParams& p, int slot_bytes, char* why, size_t why_len) {
-  const int nsm = device_sm_count();
-  const int warps_total = nsm * kWarps;
-  Sched sc;
-  memset(&sc, 0, sizeof sc);
-  sc.BT = batch_template_p(p.B);
-  if (!sc.BT) {
-    snprintf(why, why_len, "the persistent chain supports batch <= 4");
-    return false;
-  }
-  const int K = p.K, nmat = p.nmat;
-  const int rt_max = 4;  // BT <= 4
-  int RT = rt_max;
-  const Tuning& tu = tuning();
-  auto rgs = [&](int rt) {
-    int RG = 0;
-    for (int s = 0; s < p.nseg; ++s) {
-      p.seg[s].rg_begin = RG;
-      RG += (p.seg[s].M + rt - 1) / rt;
-    }
-    return RG;
-  };
-  if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
-    RT = tu.force_rt;
-  } else {
-    while (RT > 1 && rgs(RT) < 2 * warps_total) RT /= 2;
-  }
-  // a piece of RT rows must fit a stage with at least 8 columns
-  while (RT > 1 && nmat * RT * 8 * 2 > slot_bytes) RT /= 2;
-  sc.RT = RT;
-  sc.RG = rgs(RT);
-  sc.S = 1;
-  sc.KS = K;
-  int maxpc = (slot_bytes / (nmat * RT * 2)) & ~7;
-  if (maxpc < 8) {
-    snprintf(why, why_len, "stage of %d bytes too small", slot_bytes);
-    return false;
-  }
-  if (maxpc >= K) {
-    sc.PC = K;
-    sc.NP = 1;
-  } else {
-    sc.NP = (K + maxpc - 1) / maxpc;
-    sc.PC = align_up_p((K + sc.NP - 1) / sc.NP, 8);
-    sc.NP = (K + sc.PC - 1) / sc.PC;
-  }
-  sc.piece_bytes = nmat * RT * sc.PC * 2;
-  sc.NSW = 0;
-  sc.Gs = nsm;
-  sc.grid = nsm;
-  p.sc = sc;
-  p.M_total = 0;
-  for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
-  return true;
-}
-
-bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, char* why,
-                     size_t why_len) {
-  memset(&pp, 0, sizeof pp);
+// Shared-memory layout of the persistent kernel for batch B and the largest
+// K of the chain; the rest of shared memory becomes the warps' byte rings.
+static bool layout_persistent(PersistParams& pp, int B, int kmax, char* why, size_t why_len) {
   pp.BT = batch_template_p(B);
-  if (!pp.BT || nops <= 0) {
+  if (!pp.BT) {
     snprintf(why, why_len, "the persistent chain supports batch <= 4");
     return false;
   }
-  const Tuning& tu = tuning();
-  int kmax = 8, slot = 0;
-  for (int i = 0; i < nops; ++i) {
-    if (ops[i].K > kmax) kmax = ops[i].K;
-    if (ops[i].sc.piece_bytes > slot) slot = ops[i].sc.piece_bytes;
-  }
-  pp.slot_bytes = align_up_p(slot, 128);
   int off = 0;
   pp.off_op = off;
   off += 2 * align_up_p((int)sizeof(GemvParams), 128);
   pp.off_bar = off;
-  off += kWarps * kMaxStages * 8;
+  off += kWarps * kBars * 8;
   pp.off_flags = off;
   off += 128;
   pp.off_stats = off;
@@ -505,16 +537,124 @@ bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, 
   pp.off_xs = align_up_p(off, 128);
   off = pp.off_xs + align_up_p(pp.BT * kmax * 2, 128);
   pp.off_ring = align_up_p(off, 128);
+  const Tuning& tu = tuning();
   int budget = kSmemMaxP - pp.off_ring;
   if (tu.ring_bytes > 96 * 1024 && tu.ring_bytes < budget) budget = tu.ring_bytes;
-  int NSW = budget / (kWarps * pp.slot_bytes);
-  if (NSW > kMaxStages) NSW = kMaxStages;
-  if (NSW < 2) {
+  pp.slot_bytes = (budget / kWarps) & ~127;  // per-warp ring bytes
+  if (pp.slot_bytes < 4096) {
     snprintf(why, why_len, "activations of K=%d at batch %d leave no room for the rings", kmax, B);
     return false;
   }
-  pp.NSW = NSW;
-  pp.smem_bytes = pp.off_ring + kWarps * NSW * pp.slot_bytes;
+  pp.NSW = kBars;
+  pp.smem_bytes = pp.off_ring + kWarps * pp.slot_bytes;
+  return true;
+}
+
+// Per-op schedule inside the persistent kernel: rows per unit, K split and
+// pieces, for a per-warp ring of ring_bytes.
+bool plan_gemv_persistent(GemvParams& p, int ring_bytes, char* why, size_t why_len) {
+  const int nsm = device_sm_count();
+  const int GW = nsm * kWarps;
+  Sched sc;
+  memset(&sc, 0, sizeof sc);
+  sc.BT = batch_template_p(p.B);
+  if (!sc.BT) {
+    snprintf(why, why_len, "the persistent chain supports batch <= 4");
+    return false;
+  }
+  const int K = p.K, nmat = p.nmat;
+  const Tuning& tu = tuning();
+  auto rgs = [&](int rt) {
+    int RG = 0;
+    for (int s = 0; s < p.nseg; ++s) {
+      p.seg[s].rg_begin = RG;
+      RG += (p.seg[s].M + rt - 1) / rt;
+    }
+    return RG;
+  };
+  int RT = 4;
+  if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
+    RT = tu.force_rt;
+  } else {
+    while (RT > 1 && rgs(RT) < 2 * GW) RT /= 2;
+  }
+  const int RG = rgs(RT);
+  // K split: when the units are few compared with the warps, pick the split
+  // that minimises the most loaded warp's share of rows (S = 1 preferred).
+  int S = 1;
+  if (tu.force_ksplit > 0 && K % (8 * tu.force_ksplit) == 0) {
+    S = tu.force_ksplit;
+  } else if (RG < 4 * GW) {
+    double best = (double)((RG + GW - 1) / GW);
+    for (int s = 2; s <= 16; ++s) {
+      if (K % (8 * s) != 0 || K / s < 512) continue;
+      const double load = (double)(((long long)RG * s + GW - 1) / GW) / s;
+      if (load < best - 1e-9) {
+        best = load;
+        S = s;
+      }
+    }
+  }
+  sc.RT = RT;
+  sc.RG = RG;
+  sc.S = S;
+  sc.KS = K / S;
+  // pieces of at most a quarter of the ring, multiples of 8 columns, even
+  const int target = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
+  const int cap = ring_bytes / 4 < target ? ring_bytes / 4 : target;
+  int maxpc = (cap / (nmat * RT * 2)) & ~7;
+  if (maxpc < 8) {
+    snprintf(why, why_len, "ring of %d bytes too small", ring_bytes);
+    return false;
+  }
+  if (maxpc >= sc.KS) {
+    sc.PC = sc.KS;
+    sc.NP = 1;
+  } else {
+    sc.NP = (sc.KS + maxpc - 1) / maxpc;
+    sc.PC = align_up_p((sc.KS + sc.NP - 1) / sc.NP, 8);
+    sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
+  }
+  sc.piece_bytes = nmat * RT * sc.PC * 2;
+  sc.NSW = kBars;
+  // one "CTA per split" grouping is not used here: units go round-robin over
+  // all warps of the grid; Gs and grid describe the launch for the workspace
+  sc.Gs = nsm;
+  sc.grid = nsm;
+  p.sc = sc;
+  p.M_total = 0;
+  for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
+  return true;
+}
+
+// The ring bytes per warp the chain's layout leaves (0 if it does not fit).
+int persistent_ring_bytes(int B, int kmax) {
+  PersistParams pp;
+  memset(&pp, 0, sizeof pp);
+  char why[128];
+  if (!layout_persistent(pp, B, kmax, why, sizeof why)) return 0;
+  return pp.slot_bytes;
+}
+
+bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, char* why,
+                     size_t why_len) {
+  memset(&pp, 0, sizeof pp);
+  if (nops <= 0) {
+    snprintf(why, why_len, "empty chain");
+    return false;
+  }
+  int kmax = 8;
+  for (int i = 0; i < nops; ++i)
+    if (ops[i].K > kmax) kmax = ops[i].K;
+  if (!layout_persistent(pp, B, kmax, why, why_len)) return false;
+  for (int i = 0; i < nops; ++i) {
+    if (ops[i].sc.piece_bytes > pp.slot_bytes / 2) {
+      snprintf(why, why_len, "op %d: pieces of %d bytes exceed half a ring", i,
+               ops[i].sc.piece_bytes);
+      return false;
+    }
+  }
+  const Tuning& tu = tuning();
   pp.grid = device_sm_count();
   pp.nops = nops;
   pp.timeout_ns = tu.timeout_ns;
