@@ -89,10 +89,15 @@ def _check_chain(ch, blocks, head, attn, h0, eps=1e-6):
     return int(ok2.sum())
 
 
+SMALL_SPLIT = synth.QwenShape(hidden=256, kv_dim=64, inter=2048, vocab=1000, layers=2)
+
+
 @pytest.mark.parametrize("persistent", [False, True])
-@pytest.mark.parametrize("B", [1, 3, 16])
-def test_small_chain_matches_oracle(B, persistent):
-    ch, blocks, head, attn, h0 = _make(SMALL, B, 21, trace=True, keep_qkv=True, logits=True,
+@pytest.mark.parametrize("B,shape", [(1, SMALL), (3, SMALL), (16, SMALL), (1, SMALL_SPLIT),
+                                     (4, SMALL_SPLIT)])
+def test_small_chain_matches_oracle(B, shape, persistent):
+    """SMALL_SPLIT's down projection (K = 2048 over 256 rows) is split in K."""
+    ch, blocks, head, attn, h0 = _make(shape, B, 21, trace=True, keep_qkv=True, logits=True,
                                        persistent=persistent)
     # the persistent kernel takes batch <= 4; larger batches run op by op
     assert ch.chain.persistent == (persistent and B <= 4)

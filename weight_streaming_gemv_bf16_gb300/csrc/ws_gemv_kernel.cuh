@@ -207,8 +207,8 @@ __device__ __forceinline__ uint4 normalise8(const GemvParams& p, const float* st
 
 // Prologue and staging in one pass: every thread loads all of its chunks of
 // the activations first (one round of memory latency), the CTA reduces the
-// statistics from registers, and the normalised bf16 rows go to shared
-// memory [BT][K].  Takes unsplit K and at most kMaxChunks chunks per thread;
+// statistics from registers, and the normalised bf16 rows -- all K columns --
+// go to shared memory [BT][K].  Takes at most kMaxChunks chunks per thread;
 // returns false (having done nothing) otherwise.
 constexpr int kMaxChunks = 6;
 
@@ -217,7 +217,7 @@ __device__ bool prologue_stage_fused(const GemvParams& p, float* stats, float* r
                                      int tid) {
   const int nch = p.K >> 3;
   const int total = BT * nch;
-  if (p.sc.KS != p.K || total > kMaxChunks * kThreads) return false;
+  if (total > kMaxChunks * kThreads) return false;
   float v[kMaxChunks][8];
 #pragma unroll
   for (int i = 0; i < kMaxChunks; ++i) {
@@ -282,14 +282,12 @@ __device__ bool prologue_stage_fused(const GemvParams& p, float* stats, float* r
   return true;
 }
 
-// Stage columns [k0, k0 + KS) of the (normalised) activations as bf16 into
-// shared memory, [BT][KS]; rows b >= B are zero.  (General path: any K split
-// and any number of chunks per thread.)
+// Stage `nch` chunks of 8 columns, from chunk c0 on, of the (normalised)
+// activations as bf16 into shared memory, [BT][nch]; rows b >= B are zero.
+// (General path: any column range and any number of chunks per thread.)
 template <int BT>
-__device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, int ks, int tid) {
-  const int KS = p.sc.KS;
-  const int nch = KS >> 3;
-  const int c0 = (ks * KS) >> 3;
+__device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, int c0, int nch,
+                        int tid) {
   for (int o = tid; o < BT * nch; o += kThreads) {
     const int b = o / nch;
     const int c = o - b * nch;
@@ -406,9 +404,10 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
   pdl_launch_dependents();
   pdl_wait();
 
-  if (!prologue_stage_fused<BT>(p, stats, red, xs, tid)) {
+  // the activations of this CTA's split, [BT][KS]
+  if (sc.KS != p.K || !prologue_stage_fused<BT>(p, stats, red, xs, tid)) {
     prologue_stats<BT>(p, stats, red, tid);
-    stage_x<BT>(p, stats, xs, ks, tid);
+    stage_x<BT>(p, stats, xs, k0 >> 3, sc.KS >> 3, tid);
   }
   __syncthreads();
 

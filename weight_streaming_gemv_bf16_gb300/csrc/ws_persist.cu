@@ -413,9 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const GemvParams& P = Ps[f & 1];
     // the next op's descriptor streams in while this op runs
     if (f + 1 < pp.nops) prefetch_descriptor(pp.ops + f + 1, &Ps[(f + 1) & 1], tid);
+    // all K columns: units of every split index into them
     if (!prologue_stage_fused<BT>(P, stats, red, xs, tid)) {
       prologue_stats<BT>(P, stats, red, tid);
-      stage_x<BT>(P, stats, xs, 0, tid);
+      stage_x<BT>(P, stats, xs, 0, P.K >> 3, tid);
     }
     __syncthreads();
     if (stamp && tid == 0) stamp[1] = global_ns();
