@@ -56,17 +56,24 @@ __device__ __forceinline__ int warp_units(const Sched& sc, int gw, int GW) {
 // Bytes a piece takes in the ring: RT rows reserved, `len` columns each.
 __device__ __forceinline__ int piece_size(int nmat, int RT, int len) { return nmat * RT * len * 2; }
 
-// Place a piece of `sz` bytes at linear ring position `lin`: returns the
-// offset in the ring and advances `lin` past the piece (a piece never wraps;
-// the tail is skipped instead).
-__device__ __forceinline__ int ring_place(long long& lin, int sz, int R) {
-  int off = (int)(lin % R);
-  if (off + sz > R) {
-    lin += R - off;
-    off = 0;
+// A position in a warp's ring: the linear byte count since the start and its
+// offset within the ring (kept side by side, so placing costs no division).
+struct RingPos {
+  long long lin;
+  int off;
+};
+
+// Place a piece of `sz` bytes at `pos`: returns its offset in the ring and
+// advances `pos` past it (a piece never wraps; the tail is skipped instead).
+__device__ __forceinline__ int ring_place(RingPos& pos, int sz, int R) {
+  if (pos.off + sz > R) {
+    pos.lin += R - pos.off;
+    pos.off = 0;
   }
-  lin += sz;
-  return off;
+  const int at = pos.off;
+  pos.off += sz;
+  pos.lin += sz;
+  return at;
 }
 
 // The copy cursor of one warp (advanced by lane 0 only): the next piece to
@@ -79,7 +86,7 @@ struct IssueCursor {
   int ui;         // unit index within this warp's units of op f
   int j;          // piece within the unit
   int n;          // pieces issued so far
-  long long lin;  // linear ring position of the next piece
+  RingPos pos;    // ring position of the next piece
   int nseg, nmat, RT, PC, NP, K, KS, S;
   int M[kMaxSeg], rgb[kMaxSeg];
   const uint16_t* W0[kMaxSeg];
@@ -139,7 +146,7 @@ __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor&
   const int c0 = ks * c.KS + c.j * c.PC;
   const int len = min(c.PC, c.KS - c.j * c.PC);
   const int sz = piece_size(c.nmat, RT, len);
-  uint8_t* dst = ring + ring_place(c.lin, sz, pp.slot_bytes);
+  uint8_t* dst = ring + ring_place(c.pos, sz, pp.slot_bytes);
   uint64_t* bar = &bars[c.n & (kBars - 1)];
   mbar_arrive_expect_tx(bar, (uint32_t)(c.nmat * rows * len * 2));
   for (int mat = 0; mat < c.nmat; ++mat) {
@@ -165,7 +172,7 @@ __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor&
 // The consumer's view of the ring, the same in every lane.
 struct ConsumeState {
   int n;          // pieces consumed
-  long long lin;  // linear ring position of the next piece
+  RingPos pos;    // ring position of the next piece
   bool abort;
 };
 
@@ -177,9 +184,9 @@ __device__ __forceinline__ void refill(const PersistParams& pp, IssueCursor& ic,
   const int R = pp.slot_bytes;
   while (ic.f < pp.nops && ic.n - cs.n < kBars) {
     const int sz = cursor_piece_bytes(ic);
-    long long lin = ic.lin;
-    ring_place(lin, sz, R);
-    if (lin - cs.lin > R) break;
+    RingPos end = ic.pos;
+    ring_place(end, sz, R);
+    if (end.lin - cs.pos.lin > R) break;
     issue_next(pp, ic, gw, GW, ring, bars, pol);
   }
 }
@@ -230,7 +237,7 @@ __device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvPara
   for (int j = 0; j < NP; ++j) {
     const int len = min(PC, KS - j * PC);
     const int ncp = len >> 3;
-    const int off = ring_place(cs.lin, piece_size(NMAT, RT, len), R);
+    const int off = ring_place(cs.pos, piece_size(NMAT, RT, len), R);
     const bool ok = cs.abort || mbar_wait_bounded(&bars[cs.n & (kBars - 1)],
                                                   (uint32_t)((cs.n / kBars) & 1), pp.timeout_ns);
     if (land_stamp && j == 0 && lane == 0) *land_stamp = global_ns();
@@ -384,10 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ic.ui = 0;
   ic.j = 0;
   ic.n = 0;
-  ic.lin = 0;
+  ic.pos.lin = 0;
+  ic.pos.off = 0;
   ConsumeState cs;
   cs.n = 0;
-  cs.lin = 0;
+  cs.pos.lin = 0;
+  cs.pos.off = 0;
   cs.abort = false;
   uint64_t pol = 0;
   if (tid == 0) flags[1] = 0;
@@ -580,29 +589,19 @@ bool plan_gemv_persistent(GemvParams& p, int ring_bytes, char* why, size_t why_l
     while (RT > 1 && rgs(RT) < 2 * GW) RT /= 2;
   }
   const int RG = rgs(RT);
-  // K split: when the units are few compared with the warps, pick the split
-  // that minimises the most loaded warp's share of rows (S = 1 preferred).
+  // No K split unless asked for: inside one launch every split unit would pay
+  // a fence and an atomic ticket round trip through an L2 loaded by the
+  // weight stream, which costs more than the imbalance it removes.
   int S = 1;
-  if (tu.force_ksplit > 0 && K % (8 * tu.force_ksplit) == 0) {
+  if (tu.force_ksplit > 0 && K % (8 * tu.force_ksplit) == 0 && p.epilogue != EPI_ARGMAX)
     S = tu.force_ksplit;
-  } else if (RG < 4 * GW) {
-    double best = (double)((RG + GW - 1) / GW);
-    for (int s = 2; s <= 16; ++s) {
-      if (K % (8 * s) != 0 || K / s < 512) continue;
-      const double load = (double)(((long long)RG * s + GW - 1) / GW) / s;
-      if (load < best - 1e-9) {
-        best = load;
-        S = s;
-      }
-    }
-  }
   sc.RT = RT;
   sc.RG = RG;
   sc.S = S;
   sc.KS = K / S;
-  // pieces of at most a quarter of the ring, multiples of 8 columns, even
-  const int target = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
-  const int cap = ring_bytes / 4 < target ? ring_bytes / 4 : target;
+  // pieces of at most half the ring, multiples of 8 columns, even
+  const int target = tu.piece_bytes > 0 ? tu.piece_bytes : 12288;
+  const int cap = ring_bytes / 2 < target ? ring_bytes / 2 : target;
   int maxpc = (cap / (nmat * RT * 2)) & ~7;
   if (maxpc < 8) {
     snprintf(why, why_len, "ring of %d bytes too small", ring_bytes);
