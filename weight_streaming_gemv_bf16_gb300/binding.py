@@ -77,7 +77,7 @@ class ChainOpts(C.Structure):
 class Tuning(C.Structure):
     _fields_ = [("ring_bytes", I32), ("grid_cap", I32), ("force_ksplit", I32),
                 ("force_rt", I32), ("evict_first", I32), ("piece_bytes", I32),
-                ("timeout_ns", C.c_ulonglong)]
+                ("timeout_ns", C.c_ulonglong), ("l2_ahead", I32)]
 
 
 class GemvSchedule(C.Structure):
@@ -373,8 +373,9 @@ class Chain:
                 for i, p in enumerate(pl)]
 
     def debug_stamps(self, buf):
-        """Record per-CTA, per-op timestamps into `buf` (int64 [grid, ops, 4]) on
-        every later-captured step; None stops.  Re-capture afterwards."""
+        """Record per-CTA, per-op timestamps and per-warp wait times into `buf`
+        (int64 [grid, ops, 44]) on every later-captured step; None stops.
+        Re-capture afterwards."""
         n = 0 if buf is None else buf.numel()
         _check(load().ws_chain_debug_stamps(self.handle, _ptr(buf), n))
 

@@ -931,7 +931,7 @@ ws_status ws_chain_debug_stamps(ws_chain* c, unsigned long long* stamps, size_t 
     set_error("stamps are recorded by persistent chains only");
     return WS_ERR_STATE;
   }
-  const size_t need = (size_t)c->persist.grid * c->ops.size() * 4;
+  const size_t need = (size_t)c->persist.grid * c->ops.size() * kStampsPerOp;
   if (stamps && n < need) {
     set_error("stamp buffer too small: need %zu entries", need);
     return WS_ERR_ARG;

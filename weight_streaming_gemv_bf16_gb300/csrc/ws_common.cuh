@@ -105,17 +105,23 @@ struct PersistParams {
   int* err;
   unsigned long long timeout_ns;
   int evict_first;
+  int l2_ahead;           // pieces per warp prefetched into L2 ahead of its copies
   int BT;
   int NSW;                // ring stages per warp
   int slot_bytes;         // bytes per ring stage (the largest piece of any op)
   int grid;
   int smem_bytes;
-  int off_op, off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
-  // optional: per CTA and op, globaltimer ns at [0] the start of the op (after
-  // its grid barrier), [1] after the activations are staged, [2] when its
-  // tasks are done, [3] the first weight piece of the op landing (warp 0)
+  int off_op, off_bar, off_empty, off_ends, off_flags, off_stats, off_red, off_arg, off_xs,
+      off_ring;
+  // optional: per CTA and op (kStampsPerOp entries), globaltimer ns at [0]
+  // the start of the op (after its grid barrier), [1] after the activations
+  // are staged, [2] when its tasks are done, [3] the first weight piece of
+  // the op landing (warp 0); then per compute warp w, at [4 + 5w], the ns it
+  // spent waiting for weight pieces, 0 (unused), in dot products and in the
+  // reduction and epilogue, and the units it ran
   unsigned long long* stamps;
 };
+constexpr int kStampsPerOp = 4 + 5 * kWarps;
 
 // The split and the row-group range of CTA `cta`.
 __host__ __device__ inline void cta_range(const Sched& sc, int cta, int& ks, int& rg0, int& rg1) {
@@ -145,6 +151,7 @@ struct Tuning {
   int evict_first;   // weights streamed with an L2 evict-first policy
   int piece_bytes;   // target bytes per ring stage
   unsigned long long timeout_ns;
+  int l2_ahead;      // persistent chain: pieces per warp prefetched into L2 ahead of the copies
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

@@ -44,6 +44,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (mbarrier.test_wait): true once the phase with
+// the given parity has completed.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -113,7 +127,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Named barrier 1 over the consumer warps only (the producer warp is not in it).
+// Named barrier 1 over the compute warps only: the whole CTA of a
+// standalone GEMV, every warp but the copy producer in the persistent kernel.
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -121,10 +136,62 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 __device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// acc += w.lo * x.lo, then acc += w.hi * x.hi, for two bf16 pairs packed in
+// 32-bit words: the mixed-precision fma takes bf16 operands and an fp32
+// addend and rounds once, so each step equals fmaf(float(w), float(x), acc)
+// (a product of two bf16 values is exact in fp32) without unpacking.
+__device__ __forceinline__ float fma_bf16x2(uint32_t w, uint32_t x, float acc) {
+  asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, wl, xl, %0;\n\t"
+      "fma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w), "r"(x));
+  return acc;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// One step of warp_reduce_scatter: N values left per lane, shuffle distance
+// OFF.  While N > 1 the lane keeps the half of its values selected by bit OFF
+// of its lane index and adds the partner's copy of that half; once one value
+// is left the remaining distances are a plain butterfly.
+template <int NMAT, int V, int N, int OFF>
+struct ReduceScatterStep {
+  static __device__ __forceinline__ void run(float (&v)[NMAT][V], int lane) {
+    if constexpr (N > 1) {
+      constexpr int H = N / 2;
+      const bool up = (lane & OFF) != 0;
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float send = up ? v[m][i] : v[m][i + H];
+          const float keep = up ? v[m][i + H] : v[m][i];
+          v[m][i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+        }
+      ReduceScatterStep<NMAT, V, H, OFF / 2>::run(v, lane);
+    } else if constexpr (OFF >= 1) {
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) v[m][0] += __shfl_xor_sync(0xffffffffu, v[m][0], OFF);
+      ReduceScatterStep<NMAT, V, 1, OFF / 2>::run(v, lane);
+    }
+  }
+};
+
+// Sums V per-lane partials (V a power of two, at most 32; NMAT matrices) over
+// the warp and scatters the totals: afterwards v[m][0] of every lane in group
+// g = lane / (32 / V) holds the total of value g.  Takes V - 1 + log2(32 / V)
+// shuffles per matrix, against 5 V for V separate butterflies.
+template <int NMAT, int V>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[NMAT][V], int lane) {
+  static_assert(V >= 1 && V <= 32 && (V & (V - 1)) == 0, "V must be a power of two <= 32");
+  ReduceScatterStep<NMAT, V, V, 16>::run(v, lane);
 }
 
 // (value, index) order for argmax: larger value wins, equal values go to the

@@ -33,7 +33,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 6144, 2000000000ull};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0};
   return t;
 }
 
@@ -611,13 +611,15 @@ void ws_get_tuning(ws_tuning* t) {
   t->evict_first = tu.evict_first;
   t->piece_bytes = tu.piece_bytes;
   t->timeout_ns = tu.timeout_ns;
+  t->l2_ahead = tu.l2_ahead;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
   if (!t || t->ring_bytes < 0 || t->ring_bytes > kSmemMax || t->grid_cap < 0 ||
       t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt == 3 || t->force_rt > 4 ||
       t->piece_bytes < 0 ||
-      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0) {
+      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
+      t->l2_ahead > 64) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -629,6 +631,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.evict_first = t->evict_first;
   tu.piece_bytes = t->piece_bytes;
   tu.timeout_ns = t->timeout_ns;
+  tu.l2_ahead = t->l2_ahead;
   return WS_OK;
 }
 

@@ -13,10 +13,12 @@
 //  * the first stages are issued before griddepcontrol.wait: weights do not
 //    depend on the previous op, so inside a chain the next op's weights stream
 //    in while the previous op finishes (programmatic dependent launch);
-//  * lanes take 16-byte chunks of each row, unpack bf16 pairs to fp32 and
-//    accumulate with FMA, RT rows at a time (independent FMA chains); at the
-//    end of a task a butterfly of warp shuffles gives every lane every sum and
-//    lane r*BT+b runs the epilogue of output (row r, batch b);
+//  * lanes take 16-byte chunks of each row and accumulate with the
+//    mixed-precision fma (bf16 operands, fp32 addend, one rounding: the same
+//    result as unpacking to fp32 and fmaf, in one instruction per product),
+//    RT rows at a time (independent chains); at the end of a task a warp
+//    reduce-scatter (halving shuffles) leaves the total of output (row r,
+//    batch b) in lane group r*BT+b, whose first lane runs its epilogue;
 //  * split-K for skinny shapes: partial sums go to a workspace and the last
 //    split of a row group (atomic ticket) adds them in split order, so the
 //    result does not depend on the order CTAs finish in; the ticket is reset
@@ -108,7 +110,9 @@ __device__ __forceinline__ void load_x8(const GemvParams& p, int b, int c, float
   }
 }
 
-// Sum of s[b] over the CTA for every batch row; the totals land in tot[b].
+// Sum of s[b] over the kThreads compute threads for every batch row; the
+// totals land in tot[b].  (The staging code below synchronises the compute
+// threads only, with named barrier 1.)
 template <int BT>
 __device__ __forceinline__ void block_sum(float (&s)[BT], float* red, float* tot, int B, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
@@ -117,13 +121,13 @@ __device__ __forceinline__ void block_sum(float (&s)[BT], float* red, float* tot
     const float w = warp_sum(s[b]);
     if (lane == 0) red[warp * BT + b] = w;
   }
-  __syncthreads();
+  consumer_sync(kThreads);
   if (tid < B) {
     float t = 0.f;
     for (int w = 0; w < kWarps; ++w) t += red[w * BT + tid];
     tot[tid] = t;
   }
-  __syncthreads();
+  consumer_sync(kThreads);
 }
 
 // Per-row statistics of the prologue over the full K, by all threads with
@@ -149,11 +153,11 @@ __device__ void prologue_stats(const GemvParams& p, float* stats, float* red, in
   block_sum<BT>(s, red, tot, p.B, tid);
   if (p.prologue == PRO_RMSNORM) {
     if (tid < p.B) stats[2 * tid] = rsqrtf(tot[tid] / (float)p.K + p.eps);
-    __syncthreads();
+    consumer_sync(kThreads);
     return;
   }
   if (tid < p.B) stats[2 * tid] = tot[tid] / (float)p.K;
-  __syncthreads();
+  consumer_sync(kThreads);
 #pragma unroll
   for (int b = 0; b < BT; ++b) {
     s[b] = 0.f;
@@ -169,7 +173,7 @@ __device__ void prologue_stats(const GemvParams& p, float* stats, float* red, in
   }
   block_sum<BT>(s, red, tot, p.B, tid);
   if (tid < p.B) stats[2 * tid + 1] = rsqrtf(tot[tid] / (float)p.K + p.eps);
-  __syncthreads();
+  consumer_sync(kThreads);
 }
 
 // Normalise eight activations of batch row b at column 8*cg and pack them as
@@ -250,7 +254,7 @@ __device__ bool prologue_stage_fused(const GemvParams& p, float* stats, float* r
       if (tid < p.B) stats[2 * tid] = rsqrtf(tot[tid] / (float)p.K + p.eps);
     } else {
       if (tid < p.B) stats[2 * tid] = tot[tid] / (float)p.K;
-      __syncthreads();
+      consumer_sync(kThreads);
 #pragma unroll
       for (int b = 0; b < BT; ++b) s[b] = 0.f;
 #pragma unroll
@@ -267,7 +271,7 @@ __device__ bool prologue_stage_fused(const GemvParams& p, float* stats, float* r
       block_sum<BT>(s, red, tot, p.B, tid);
       if (tid < p.B) stats[2 * tid + 1] = rsqrtf(tot[tid] / (float)p.K + p.eps);
     }
-    __syncthreads();
+    consumer_sync(kThreads);
   }
 #pragma unroll
   for (int i = 0; i < kMaxChunks; ++i) {
@@ -334,6 +338,62 @@ __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, i
 
 // Issue the bulk copies of piece j (columns [k0 + j*PC, ...)) of row group rg
 // into ring slot `slot`.
+// Dot products of one ring piece against the staged activations: the piece
+// holds NMAT x RT rows of nc 8-column chunks, rows rs chunks apart; xs points
+// at the activations' chunk matching the piece's first column, batch rows
+// nchx chunks apart.  Lane l takes chunks l, l + 32, ...  Each output keeps
+// ACC partial sums (word k of a chunk feeds partial k % ACC), so that a warp
+// always has at least eight independent fma chains; the partials are folded
+// into acc at the end of the piece.  Rows past the end of the matrix hold
+// stale bytes; their sums are never written out.
+template <int BT, int NMAT, int RT>
+__device__ __forceinline__ void dot_piece(float (&acc)[2][4][BT], const uint4* st,
+                                          const uint4* xs, int nc, int rs, int nchx, int lane) {
+  constexpr int CH = NMAT * RT * BT;
+  constexpr int ACC = CH >= 8 ? 1 : (CH >= 4 ? 2 : 4);
+  float part[ACC][NMAT][RT][BT];
+#pragma unroll
+  for (int a = 0; a < ACC; ++a)
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) part[a][m][r][b] = 0.f;
+#pragma unroll 2
+  for (int c = lane; c < nc; c += 32) {
+    uint4 w[NMAT][RT];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) w[m][r] = st[(m * RT + r) * rs + c];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const uint4 xv = xs[b * nchx + c];
+#pragma unroll
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          part[0][m][r][b] = fma_bf16x2(w[m][r].x, xv.x, part[0][m][r][b]);
+          part[1 % ACC][m][r][b] = fma_bf16x2(w[m][r].y, xv.y, part[1 % ACC][m][r][b]);
+          part[2 % ACC][m][r][b] = fma_bf16x2(w[m][r].z, xv.z, part[2 % ACC][m][r][b]);
+          part[3 % ACC][m][r][b] = fma_bf16x2(w[m][r].w, xv.w, part[3 % ACC][m][r][b]);
+        }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int b = 0; b < BT; ++b) {
+        float t = part[0][m][r][b];
+#pragma unroll
+        for (int a = 1; a < ACC; ++a) t += part[a][m][r][b];
+        acc[m][r][b] += t;
+      }
+}
+
 template <int NMAT, int RT>
 __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, int slot, int k0,
                                             uint8_t* ring, uint64_t* full, uint64_t pol) {
@@ -363,7 +423,7 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
 }
 
 template <int BT, int NMAT, int RT>
-__global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant__ GemvParams p) {
+__global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Sched& sc = p.sc;
   const int tid = threadIdx.x;
@@ -418,7 +478,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
   int best_i = 0x7fffffff;
   bool abort = false;
 
-  float acc[NMAT][RT][BT];
+  float acc[2][4][BT];  // [matrix][row][batch]; NMAT x RT used
 #pragma unroll
   for (int m = 0; m < NMAT; ++m)
 #pragma unroll
@@ -442,34 +502,9 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
       if (lane == 0) raise_device_error(p.err, DERR_TIMEOUT);
     }
 
+    // a piece's rows sit PC columns apart, also in a task's shorter last piece
     const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.piece_bytes);
-    const int xoff = j * ncp;
-#pragma unroll 2
-    for (int c = lane; c < (len >> 3); c += 32) {
-      float wf[NMAT][RT][8];
-#pragma unroll
-      for (int r = 0; r < RT; ++r)
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint4 w = r < rows ? st[(size_t)(m * RT + r) * ncp + c] : make_uint4(0, 0, 0, 0);
-          wf[m][r][0] = bf16lo(w.x); wf[m][r][1] = bf16hi(w.x);
-          wf[m][r][2] = bf16lo(w.y); wf[m][r][3] = bf16hi(w.y);
-          wf[m][r][4] = bf16lo(w.z); wf[m][r][5] = bf16hi(w.z);
-          wf[m][r][6] = bf16lo(w.w); wf[m][r][7] = bf16hi(w.w);
-        }
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        const uint4 xv = xs4[(size_t)b * nchx + xoff + c];
-        const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
-                             bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[m][r][b] = fmaf(wf[m][r][e], xf[e], acc[m][r][b]);
-      }
-    }
+    dot_piece<BT, NMAT, RT>(acc, st, xs4 + j * ncp, len >> 3, ncp, nchx, lane);
     // Every lane's shared-memory reads of this slot have returned (their
     // values fed the FMAs above, and issue is in order): refill the slot.
     __syncwarp();
@@ -481,34 +516,30 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
     }
 
     if (j == NP - 1) {
-      // task complete: sum over lanes (every lane ends with every sum)
+      // task complete: sum over lanes; output o = r * BT + b ends in the
+      // lanes of group o, whose first lane runs its epilogue
+      constexpr int V = RT * BT, G = 32 / V;
+      float v[NMAT][V];
 #pragma unroll
       for (int m = 0; m < NMAT; ++m)
 #pragma unroll
         for (int r = 0; r < RT; ++r)
 #pragma unroll
-          for (int b = 0; b < BT; ++b) acc[m][r][b] = warp_sum(acc[m][r][b]);
+          for (int b = 0; b < BT; ++b) v[m][r * BT + b] = acc[m][r][b];
+      warp_reduce_scatter<NMAT, V>(v, lane);
+      const int o = lane / G, r = o / BT, b = o - (o / BT) * BT;
+      const bool mine = lane % G == 0 && r < rows && b < p.B;
       const int rowg = p.seg[seg].row_base + row0;
       if (sc.S == 1) {
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int b = 0; b < BT; ++b)
-            if (lane == r * BT + b && r < rows && b < p.B)
-              apply_epilogue(p, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v,
-                             best_i);
+        if (mine) apply_epilogue(p, seg, row0 + r, b, v[0][0], v[NMAT - 1][0], best_v, best_i);
       } else {
         // split-K: write this split's partials; the last split of the row
         // group adds all splits in split order and runs the epilogue
+        if (mine) {
 #pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int b = 0; b < BT; ++b)
-            if (lane == r * BT + b && r < rows && b < p.B) {
-#pragma unroll
-              for (int m = 0; m < NMAT; ++m)
-                p.part[((size_t)(ks * NMAT + m) * p.B + b) * p.M_total + rowg + r] = acc[m][r][b];
-            }
+          for (int m = 0; m < NMAT; ++m)
+            p.part[((size_t)(ks * NMAT + m) * p.B + b) * p.M_total + rowg + r] = v[m][0];
+        }
         __threadfence();
         __syncwarp();
         int last = 0;
@@ -556,8 +587,8 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
   }
 
   if (p.epilogue == EPI_ARGMAX) {
-    // per batch row: lanes r*BT + b hold a running best; combine the warps,
-    // then the last CTA (ticket) combines all CTAs
+    // per batch row b: the first lanes of groups r*BT + b hold a running
+    // best; combine the warps, then the last CTA (ticket) combines all CTAs
     argv[warp * 32 + lane] = best_v;
     argi[warp * 32 + lane] = best_i;
     __syncthreads();
@@ -566,7 +597,7 @@ __global__ void __launch_bounds__(kThreads) k_stream_gemv(const __grid_constant_
       int bi = 0x7fffffff;
       for (int w = 0; w < kWarps; ++w)
         for (int r = 0; r < RT; ++r) {
-          const int l = r * BT + tid;
+          const int l = (r * BT + tid) * (32 / (RT * BT));
           if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
             bv = argv[w * 32 + l];
             bi = argi[w * 32 + l];

@@ -40,6 +40,7 @@
 namespace ws {
 
 constexpr int kBars = 8;  // mbarriers (pieces in flight) per warp
+constexpr int kPersistThreads = (kWarps + 1) * 32;  // eight compute warps + the producer
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
@@ -47,7 +48,8 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Units of op sc for global warp gw: u = gw, gw + GW, ...
+// The units of op sc that global warp gw runs: gw, gw + GW, ... (dealt
+// round-robin over every warp of the grid).
 __device__ __forceinline__ int warp_units(const Sched& sc, int gw, int GW) {
   const int U = sc.RG * sc.S;
   return U > gw ? (U - gw + GW - 1) / GW : 0;
@@ -132,7 +134,7 @@ __device__ __forceinline__ int cursor_piece_bytes(const IssueCursor& c) {
 __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor& c, int gw, int GW,
                                            uint8_t* ring, uint64_t* bars, uint64_t pol) {
   const int u = gw + c.ui * GW;
-  const int rg = u / c.S;
+  const int rg = c.S == 1 ? u : u / c.S;
   const int ks = u - rg * c.S;
   const bool s1 = c.nseg > 1 && rg >= c.rgb[1];
   const bool s2 = c.nseg > 2 && rg >= c.rgb[2];
@@ -169,27 +171,48 @@ __device__ __forceinline__ void issue_next(const PersistParams& pp, IssueCursor&
   cursor_seek(pp, c, gw, GW);
 }
 
+// Prefetch the cursor's next piece into L2 (no shared memory, no barrier)
+// and advance the cursor: the producer's look-ahead, so that weights keep
+// streaming from HBM while the rings are full, e.g. across grid barriers.
+__device__ __forceinline__ void prefetch_next(const PersistParams& pp, IssueCursor& c, int gw,
+                                              int GW) {
+  const int u = gw + c.ui * GW;
+  const int rg = c.S == 1 ? u : u / c.S;
+  const int ks = u - rg * c.S;
+  const bool s1 = c.nseg > 1 && rg >= c.rgb[1];
+  const bool s2 = c.nseg > 2 && rg >= c.rgb[2];
+  const int rgb = s2 ? c.rgb[2] : (s1 ? c.rgb[1] : c.rgb[0]);
+  const int Mseg = s2 ? c.M[2] : (s1 ? c.M[1] : c.M[0]);
+  const uint16_t* W0 = s2 ? c.W0[2] : (s1 ? c.W0[1] : c.W0[0]);
+  const uint16_t* W1 = s2 ? c.W1[2] : (s1 ? c.W1[1] : c.W1[0]);
+  const int RT = c.RT, K = c.K;
+  const int row0 = (rg - rgb) * RT;
+  const int rows = min(RT, Mseg - row0);
+  const int c0 = ks * c.KS + c.j * c.PC;
+  const int len = min(c.PC, c.KS - c.j * c.PC);
+  for (int mat = 0; mat < c.nmat; ++mat) {
+    const uint16_t* W = mat == 0 ? W0 : W1;
+    if (len == K) {
+      bulk_prefetch_l2(W + (size_t)row0 * K, (uint32_t)(rows * K * 2));
+    } else {
+      for (int r = 0; r < rows; ++r)
+        bulk_prefetch_l2(W + (size_t)(row0 + r) * K + c0, (uint32_t)(len * 2));
+    }
+  }
+  ++c.q;
+  if (++c.j == c.NP) {
+    c.j = 0;
+    ++c.ui;
+  }
+  cursor_seek(pp, c, gw, GW);
+}
+
 // The consumer's view of the ring, the same in every lane.
 struct ConsumeState {
   int n;          // pieces consumed
   RingPos pos;    // ring position of the next piece
   bool abort;
 };
-
-// Issue pieces while a barrier is free and the next piece fits behind the
-// consumer (lane 0 only).
-__device__ __forceinline__ void refill(const PersistParams& pp, IssueCursor& ic,
-                                       const ConsumeState& cs, int gw, int GW, uint8_t* ring,
-                                       uint64_t* bars, uint64_t pol) {
-  const int R = pp.slot_bytes;
-  while (ic.f < pp.nops && ic.n - cs.n < kBars) {
-    const int sz = cursor_piece_bytes(ic);
-    RingPos end = ic.pos;
-    ring_place(end, sz, R);
-    if (end.lin - cs.pos.lin > R) break;
-    issue_next(pp, ic, gw, GW, ring, bars, pol);
-  }
-}
 
 // Asynchronous 16-byte copies of an op descriptor into shared memory (the
 // next op's, fetched while the current op computes).
@@ -208,101 +231,136 @@ __device__ __forceinline__ void wait_descriptor() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// The (matrices, rows per unit) shape of an op, as one of six kinds, and its
+// per-kind inner loop and lane reduction.  Only these two are specialised per
+// kind; the rest of a unit's code (waits, ring refills, epilogue) exists once,
+// which keeps the kernel's instruction footprint small.
+__host__ __device__ inline int unit_kind(int nmat, int RT) {
+  return (nmat - 1) * 3 + (RT == 1 ? 0 : (RT == 2 ? 1 : 2));
+}
+
+template <int BT>
+__device__ __forceinline__ void dot_kind(int kind, float (&acc)[2][4][BT], const uint4* st,
+                                         const uint4* xs, int nc, int nchx, int lane) {
+  switch (kind) {
+    case 0: dot_piece<BT, 1, 1>(acc, st, xs, nc, nc, nchx, lane); break;
+    case 1: dot_piece<BT, 1, 2>(acc, st, xs, nc, nc, nchx, lane); break;
+    case 2: dot_piece<BT, 1, 4>(acc, st, xs, nc, nc, nchx, lane); break;
+    case 3: dot_piece<BT, 2, 1>(acc, st, xs, nc, nc, nchx, lane); break;
+    case 4: dot_piece<BT, 2, 2>(acc, st, xs, nc, nc, nchx, lane); break;
+    default: dot_piece<BT, 2, 4>(acc, st, xs, nc, nc, nchx, lane); break;
+  }
+}
+
+template <int BT, int NMAT, int RT>
+__device__ __forceinline__ void reduce_t(float (&acc)[2][4][BT], int lane, float& v0, float& v1) {
+  constexpr int V = RT * BT;
+  float v[NMAT][V];
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int b = 0; b < BT; ++b) v[m][r * BT + b] = acc[m][r][b];
+  warp_reduce_scatter<NMAT, V>(v, lane);
+  v0 = v[0][0];
+  v1 = v[NMAT - 1][0];
+}
+
+// Warp totals of a unit: lane group o = r * BT + b (of 32 / (RT * BT) lanes)
+// ends with output (row r, batch b) in v0 (first matrix) and v1 (second).
+template <int BT>
+__device__ __forceinline__ void reduce_kind(int kind, float (&acc)[2][4][BT], int lane, float& v0,
+                                            float& v1) {
+  switch (kind) {
+    case 0: reduce_t<BT, 1, 1>(acc, lane, v0, v1); break;
+    case 1: reduce_t<BT, 1, 2>(acc, lane, v0, v1); break;
+    case 2: reduce_t<BT, 1, 4>(acc, lane, v0, v1); break;
+    case 3: reduce_t<BT, 2, 1>(acc, lane, v0, v1); break;
+    case 4: reduce_t<BT, 2, 2>(acc, lane, v0, v1); break;
+    default: reduce_t<BT, 2, 4>(acc, lane, v0, v1); break;
+  }
+}
+
+// Per-op constants of the unit loop.
+struct UnitShape {
+  int kind, RT, nmat, NP, PC, KS, S, nchx;
+  int lg;  // log2 of the lanes per output group, 32 / (RT * BT)
+};
+
 // One unit (RT rows x one K split) of op P: consume its NP pieces (refilling
 // the ring as they free up), reduce over lanes, then run the epilogue -- or,
 // for a split, publish the partial sums and let the last split finish.
-template <int BT, int NMAT, int RT>
-__device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvParams& P, int u,
-                                         uint8_t* ring, uint64_t* bars, const uint4* xs4,
-                                         ConsumeState& cs, IssueCursor& ic, uint64_t pol,
-                                         float& best_v, int& best_i, int gw, int GW, int lane,
-                                         unsigned long long* land_stamp) {
-  const int S = P.sc.S;
-  const int rg = u / S;
+template <int BT>
+__device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvParams& P,
+                                         const UnitShape& us, int u, uint8_t* ring,
+                                         uint64_t* bars, uint64_t* empty, const uint4* xs4,
+                                         ConsumeState& cs, volatile int* flags,
+                                         float& best_v, int& best_i, int lane,
+                                         unsigned long long* land_stamp,
+                                         unsigned long long* tacc) {
+  const int S = us.S, RT = us.RT;
+  const int rg = S == 1 ? u : u / S;
   const int ks = u - rg * S;
   int seg, rgl;
   decode_rg(P, rg, seg, rgl);
   const int row0 = rgl * RT;
   const int rows = min(RT, P.seg[seg].M - row0);
-  const int NP = P.sc.NP, PC = P.sc.PC, KS = P.sc.KS, nchx = P.K >> 3;
   const int R = pp.slot_bytes;
-  float acc[NMAT][RT][BT];
+  float acc[2][4][BT];
 #pragma unroll
-  for (int m = 0; m < NMAT; ++m)
+  for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int r = 0; r < RT; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int b = 0; b < BT; ++b) acc[m][r][b] = 0.f;
 
-  for (int j = 0; j < NP; ++j) {
-    const int len = min(PC, KS - j * PC);
+  for (int j = 0; j < us.NP; ++j) {
+    const int len = min(us.PC, us.KS - j * us.PC);
     const int ncp = len >> 3;
-    const int off = ring_place(cs.pos, piece_size(NMAT, RT, len), R);
+    const int off = ring_place(cs.pos, piece_size(us.nmat, RT, len), R);
+    unsigned long long tw = tacc ? global_ns() : 0;
     const bool ok = cs.abort || mbar_wait_bounded(&bars[cs.n & (kBars - 1)],
                                                   (uint32_t)((cs.n / kBars) & 1), pp.timeout_ns);
+    if (tacc) {
+      const unsigned long long t = global_ns();
+      tacc[0] += t - tw;
+      tw = t;
+    }
     if (land_stamp && j == 0 && lane == 0) *land_stamp = global_ns();
     if (__any_sync(0xffffffffu, !ok) && !cs.abort) {
       cs.abort = true;
-      if (lane == 0) raise_device_error(pp.err, DERR_TIMEOUT);
-    }
-    const uint4* st = reinterpret_cast<const uint4*>(ring + off);
-    const int xoff = (ks * KS + j * PC) >> 3;
-#pragma unroll 2
-    for (int c = lane; c < ncp; c += 32) {
-      float wf[NMAT][RT][8];
-#pragma unroll
-      for (int r = 0; r < RT; ++r)
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint4 w = r < rows ? st[(size_t)(m * RT + r) * ncp + c] : make_uint4(0, 0, 0, 0);
-          wf[m][r][0] = bf16lo(w.x); wf[m][r][1] = bf16hi(w.x);
-          wf[m][r][2] = bf16lo(w.y); wf[m][r][3] = bf16hi(w.y);
-          wf[m][r][4] = bf16lo(w.z); wf[m][r][5] = bf16hi(w.z);
-          wf[m][r][6] = bf16lo(w.w); wf[m][r][7] = bf16hi(w.w);
-        }
-#pragma unroll
-      for (int b = 0; b < BT; ++b) {
-        const uint4 xv = xs4[(size_t)b * nchx + xoff + c];
-        const float xf[8] = {bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y),
-                             bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w)};
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[m][r][b] = fmaf(wf[m][r][e], xf[e], acc[m][r][b]);
+      if (lane == 0) {
+        raise_device_error(pp.err, DERR_TIMEOUT);
+        flags[2] = 1;  // the producer stops issuing
       }
     }
+    // rows of a piece are packed at its own length
+    dot_kind<BT>(us.kind, acc, reinterpret_cast<const uint4*>(ring + off),
+                 xs4 + ((ks * us.KS + j * us.PC) >> 3), ncp, us.nchx, lane);
     // every lane's reads of this piece have returned: its bytes are free
     __syncwarp();
+    if (tacc) tacc[2] += global_ns() - tw;
+    if (lane == 0) mbar_arrive(&empty[cs.n & (kBars - 1)]);
     ++cs.n;
-    if (lane == 0 && !cs.abort) refill(pp, ic, cs, gw, GW, ring, bars, pol);
   }
-#pragma unroll
-  for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-    for (int r = 0; r < RT; ++r)
-#pragma unroll
-      for (int b = 0; b < BT; ++b) acc[m][r][b] = warp_sum(acc[m][r][b]);
+  const unsigned long long te = tacc ? global_ns() : 0;
+  float v0, v1;
+  reduce_kind<BT>(us.kind, acc, lane, v0, v1);
+  const int o = lane >> us.lg;
+  const int r = o / BT, b = o - (o / BT) * BT;
+  const bool mine = (lane & ((1 << us.lg) - 1)) == 0 && r < rows && b < P.B;
   if (S == 1) {
-#pragma unroll
-    for (int r = 0; r < RT; ++r)
-#pragma unroll
-      for (int b = 0; b < BT; ++b)
-        if (lane == r * BT + b && r < rows && b < P.B)
-          apply_epilogue(P, seg, row0 + r, b, acc[0][r][b], acc[NMAT - 1][r][b], best_v, best_i);
+    if (mine) apply_epilogue(P, seg, row0 + r, b, v0, v1, best_v, best_i);
+    if (tacc) tacc[3] += global_ns() - te;
     return;
   }
+  const int nmat = us.nmat;
   const int rowg = P.seg[seg].row_base + row0;
-#pragma unroll
-  for (int r = 0; r < RT; ++r)
-#pragma unroll
-    for (int b = 0; b < BT; ++b)
-      if (lane == r * BT + b && r < rows && b < P.B) {
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-          P.part[((size_t)(ks * NMAT + m) * P.B + b) * P.M_total + rowg + r] = acc[m][r][b];
-      }
+  if (mine) {
+    P.part[((size_t)(ks * nmat) * P.B + b) * P.M_total + rowg + r] = v0;
+    if (nmat == 2) P.part[((size_t)(ks * nmat + 1) * P.B + b) * P.M_total + rowg + r] = v1;
+  }
   __threadfence();
   __syncwarp();
   int last = 0;
@@ -314,26 +372,24 @@ __device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvPara
   last = __shfl_sync(0xffffffffu, last, 0);
   if (last) {
     __threadfence();
-    for (int o = lane; o < rows * P.B; o += 32) {
-      const int rr = o / P.B;
-      const int b = o - rr * P.B;
-      float v[NMAT];
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        float t = 0.f;
-        for (int s = 0; s < S; ++s)
-          t += __ldcg(&P.part[((size_t)(s * NMAT + m) * P.B + b) * P.M_total + rowg + rr]);
-        v[m] = t;
+    for (int q = lane; q < rows * P.B; q += 32) {
+      const int rr = q / P.B;
+      const int bb = q - rr * P.B;
+      float t0 = 0.f, t1 = 0.f;
+      for (int s2 = 0; s2 < S; ++s2) {
+        t0 += __ldcg(&P.part[((size_t)(s2 * nmat) * P.B + bb) * P.M_total + rowg + rr]);
+        if (nmat == 2)
+          t1 += __ldcg(&P.part[((size_t)(s2 * nmat + 1) * P.B + bb) * P.M_total + rowg + rr]);
       }
       float dv = -INFINITY;
       int di = 0x7fffffff;
-      apply_epilogue(P, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di);
+      apply_epilogue(P, seg, row0 + rr, bb, t0, nmat == 2 ? t1 : t0, dv, di);
     }
   }
 }
 
-// Wait until every CTA has finished op f (bounded).  Thread 0 spins; all
-// threads leave together.
+// Wait until every CTA has finished op f (bounded).  Thread 0 spins; the
+// compute threads leave together.
 __device__ __forceinline__ void grid_wait(const PersistParams& pp, int f, volatile int* flags,
                                           int tid) {
   if (tid == 0) {
@@ -350,7 +406,7 @@ __device__ __forceinline__ void grid_wait(const PersistParams& pp, int f, volati
     }
     __threadfence();
   }
-  __syncthreads();
+  consumer_sync(kThreads);
 }
 
 // CTA 0 copies an op's output ([B][M], fp32 or bf16) to its trace slot.
@@ -364,28 +420,28 @@ __device__ __forceinline__ void copy_trace(const GemvParams* op, int tid) {
   for (int i = tid; i < nwords; i += kThreads) dst[i] = __ldcg(src + i);
 }
 
-template <int BT>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_chain_persistent(const __grid_constant__ PersistParams pp) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
+// The copy producer (the last warp of each CTA).  Lane w < kWarps streams
+// compute warp w's pieces of every op, in order, into that warp's ring: a
+// piece goes out once one of the warp's eight barriers is free and the piece
+// fits behind the last piece the warp has released (its "empty" barrier gets
+// one arrival per consumed piece).  The producer never waits for activations,
+// so it runs ahead across op boundaries as far as the ring allows.  It polls
+// without blocking, so its lanes never wait on each other; if it makes no
+// progress for timeout_ns it raises the error flag and stops.
+__device__ __noinline__ void produce(const PersistParams& pp, uint8_t* smem, int lane,
+                                     volatile int* flags) {
   const int GW = gridDim.x * kWarps;
-  const int gw = blockIdx.x * kWarps + warp;
-  GemvParams* Ps = reinterpret_cast<GemvParams*>(smem + pp.off_op);  // two buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pp.off_bar) + warp * kBars;
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + pp.off_flags);
-  float* stats = reinterpret_cast<float*>(smem + pp.off_stats);
-  float* red = reinterpret_cast<float*>(smem + pp.off_red);
-  float* argv = reinterpret_cast<float*>(smem + pp.off_arg);
-  int* argi = reinterpret_cast<int*>(argv + kWarps * 32);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + pp.off_xs);
-  const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
-  uint8_t* ring = smem + pp.off_ring + (size_t)warp * pp.slot_bytes;
-
+  const bool active = lane < kWarps;
+  const int w = active ? lane : 0;
+  const int gw = blockIdx.x * kWarps + w;
+  const int R = pp.slot_bytes;
+  uint8_t* ring = smem + pp.off_ring + (size_t)w * R;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pp.off_bar) + w * kBars;
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + pp.off_empty) + w * kBars;
+  long long* ends = reinterpret_cast<long long*>(smem + pp.off_ends) + w * kBars;
+  const uint64_t pol = pp.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   IssueCursor ic;
-  ic.f = -1;
+  ic.f = active ? -1 : pp.nops;
   ic.q = 0;
   ic.npw = 0;
   ic.ui = 0;
@@ -393,118 +449,212 @@ __global__ void __launch_bounds__(kThreads, 1)
   ic.n = 0;
   ic.pos.lin = 0;
   ic.pos.off = 0;
-  ConsumeState cs;
-  cs.n = 0;
-  cs.pos.lin = 0;
-  cs.pos.off = 0;
-  cs.abort = false;
-  uint64_t pol = 0;
-  if (tid == 0) flags[1] = 0;
-  if (lane == 0) {
-    for (int s = 0; s < kBars; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-    pol = pp.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-    cursor_seek(pp, ic, gw, GW);
-    refill(pp, ic, cs, gw, GW, ring, bars, pol);
-  }
-  prefetch_descriptor(pp.ops, Ps, tid);
-
-  for (int f = 0; f < pp.nops; ++f) {
-    if (f > 0) {
-      grid_wait(pp, f - 1, flags, tid);
-      copy_trace(pp.ops + (f - 1), tid);
-    }
-    wait_descriptor();
-    __syncthreads();
-    unsigned long long* stamp =
-        pp.stamps ? pp.stamps + ((size_t)blockIdx.x * pp.nops + f) * 4 : nullptr;
-    if (stamp && tid == 0) stamp[0] = global_ns();
-    const GemvParams& P = Ps[f & 1];
-    // the next op's descriptor streams in while this op runs
-    if (f + 1 < pp.nops) prefetch_descriptor(pp.ops + f + 1, &Ps[(f + 1) & 1], tid);
-    // all K columns: units of every split index into them
-    if (!prologue_stage_fused<BT>(P, stats, red, xs, tid)) {
-      prologue_stats<BT>(P, stats, red, tid);
-      stage_x<BT>(P, stats, xs, 0, P.K >> 3, tid);
-    }
-    __syncthreads();
-    if (stamp && tid == 0) stamp[1] = global_ns();
-
-    const int nunits = warp_units(P.sc, gw, GW);
-    float best_v = -INFINITY;
-    int best_i = 0x7fffffff;
-    const int kind = (P.nmat - 1) * 3 + (P.sc.RT == 1 ? 0 : (P.sc.RT == 2 ? 1 : 2));
-    for (int t = 0; t < nunits; ++t) {
-      const int u = gw + t * GW;
-      unsigned long long* land = (stamp && warp == 0 && t == 0) ? stamp + 3 : nullptr;
-      switch (kind) {
-        case 0: run_unit<BT, 1, 1>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
-        case 1: run_unit<BT, 1, 2>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
-        case 2: run_unit<BT, 1, 4>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
-        case 3: run_unit<BT, 2, 1>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
-        case 4: run_unit<BT, 2, 2>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
-        default: run_unit<BT, 2, 4>(pp, P, u, ring, bars, xs4, cs, ic, pol, best_v, best_i, gw, GW, lane, land); break;
+  if (active) cursor_seek(pp, ic, gw, GW);
+  // look-ahead cursor: up to l2_ahead pieces in front of ic, prefetched to L2
+  IssueCursor pf = ic;
+  int pf_n = 0;  // pieces prefetched so far
+  int consumed = 0;    // pieces this warp is known to have released
+  long long freed = 0;  // ring bytes (linear) released so far
+  uint64_t idle_since = 0;
+  for (;;) {
+    bool progress = false;
+    const bool stop = flags[2] != 0;
+    if (!stop && ic.f < pp.nops) {
+      while (consumed < ic.n &&
+             mbar_test(&empty[consumed & (kBars - 1)], (uint32_t)((consumed / kBars) & 1))) {
+        freed = ends[consumed & (kBars - 1)];
+        ++consumed;
+        progress = true;
+      }
+      while (ic.f < pp.nops && ic.n - consumed < kBars) {
+        RingPos end = ic.pos;
+        ring_place(end, cursor_piece_bytes(ic), R);
+        if (end.lin - freed > R) break;
+        ends[ic.n & (kBars - 1)] = end.lin;
+        issue_next(pp, ic, gw, GW, ring, full, pol);
+        progress = true;
+      }
+      while (pp.l2_ahead > 0 && pf.f < pp.nops && pf_n < ic.n + pp.l2_ahead) {
+        if (pf_n < ic.n) {
+          // the copies caught up with the look-ahead: skip to them
+          pf = ic;
+          pf_n = ic.n;
+          continue;
+        }
+        prefetch_next(pp, pf, gw, GW);
+        ++pf_n;
+        progress = true;
       }
     }
+    if (__all_sync(0xffffffffu, stop || ic.f >= pp.nops)) break;
+    if (__any_sync(0xffffffffu, progress)) {
+      idle_since = 0;
+    } else {
+      const uint64_t t = global_ns();
+      if (idle_since == 0) {
+        idle_since = t;
+      } else if (t - idle_since > pp.timeout_ns) {
+        if (lane == 0) {
+          raise_device_error(pp.err, DERR_TIMEOUT);
+          flags[2] = 1;
+        }
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  if (flags[2] && active) {
+    // stopped early: let this warp's copies still in flight land before exit
+    for (int q = consumed; q < ic.n; ++q)
+      mbar_wait_bounded(&full[q & (kBars - 1)], (uint32_t)((q / kBars) & 1), pp.timeout_ns);
+  }
+}
 
-    if (P.epilogue == EPI_ARGMAX) {
-      const int RT = P.sc.RT;
-      argv[warp * 32 + lane] = best_v;
-      argi[warp * 32 + lane] = best_i;
-      __syncthreads();
-      if (tid < P.B) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int w = 0; w < kWarps; ++w)
-          for (int r = 0; r < RT; ++r) {
-            const int l = r * BT + tid;
-            if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
-              bv = argv[w * 32 + l];
-              bi = argi[w * 32 + l];
+template <int BT>
+__global__ void __launch_bounds__(kPersistThreads, 1)
+    k_chain_persistent(const __grid_constant__ PersistParams pp) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + pp.off_flags);
+  if (tid == 0) {
+    flags[1] = 0;
+    flags[2] = 0;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + pp.off_bar);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + pp.off_empty);
+    for (int s = 0; s < kWarps * kBars; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    produce(pp, smem, lane, flags);
+  } else {
+    const int GW = gridDim.x * kWarps;
+    const int gw = blockIdx.x * kWarps + warp;
+    GemvParams* Ps = reinterpret_cast<GemvParams*>(smem + pp.off_op);  // two buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pp.off_bar) + warp * kBars;
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + pp.off_empty) + warp * kBars;
+    float* stats = reinterpret_cast<float*>(smem + pp.off_stats);
+    float* red = reinterpret_cast<float*>(smem + pp.off_red);
+    float* argv = reinterpret_cast<float*>(smem + pp.off_arg);
+    int* argi = reinterpret_cast<int*>(argv + kWarps * 32);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + pp.off_xs);
+    const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
+    uint8_t* ring = smem + pp.off_ring + (size_t)warp * pp.slot_bytes;
+    ConsumeState cs;
+    cs.n = 0;
+    cs.pos.lin = 0;
+    cs.pos.off = 0;
+    cs.abort = false;
+    prefetch_descriptor(pp.ops, Ps, tid);
+
+    for (int f = 0; f < pp.nops; ++f) {
+      if (f > 0) {
+        grid_wait(pp, f - 1, flags, tid);
+        copy_trace(pp.ops + (f - 1), tid);
+      }
+      wait_descriptor();
+      consumer_sync(kThreads);
+      unsigned long long* stamp =
+          pp.stamps ? pp.stamps + ((size_t)blockIdx.x * pp.nops + f) * kStampsPerOp : nullptr;
+      if (stamp && tid == 0) stamp[0] = global_ns();
+      const GemvParams& P = Ps[f & 1];
+      // the next op's descriptor streams in while this op runs
+      if (f + 1 < pp.nops) prefetch_descriptor(pp.ops + f + 1, &Ps[(f + 1) & 1], tid);
+      // all K columns: units of every split index into them
+      if (!prologue_stage_fused<BT>(P, stats, red, xs, tid)) {
+        prologue_stats<BT>(P, stats, red, tid);
+        stage_x<BT>(P, stats, xs, 0, P.K >> 3, tid);
+      }
+      consumer_sync(kThreads);
+      if (stamp && tid == 0) stamp[1] = global_ns();
+
+      const int nunits = warp_units(P.sc, gw, GW);
+      // diagnostics: this warp's time waiting for pieces, in dot products
+      // and in the reduction and epilogue, in this op
+      unsigned long long tacc_v[4] = {0, 0, 0, 0};
+      unsigned long long* wwait = stamp ? tacc_v : nullptr;
+      float best_v = -INFINITY;
+      int best_i = 0x7fffffff;
+      UnitShape us;
+      us.kind = unit_kind(P.nmat, P.sc.RT);
+      us.RT = P.sc.RT;
+      us.nmat = P.nmat;
+      us.NP = P.sc.NP;
+      us.PC = P.sc.PC;
+      us.KS = P.sc.KS;
+      us.S = P.sc.S;
+      us.nchx = P.K >> 3;
+      us.lg = __ffs(32 / (us.RT * BT)) - 1;
+      for (int t = 0; t < nunits; ++t) {
+        unsigned long long* land = (stamp && warp == 0 && t == 0) ? stamp + 3 : nullptr;
+        run_unit<BT>(pp, P, us, gw + t * GW, ring, bars, empty, xs4, cs, flags, best_v, best_i,
+                     lane, land, wwait);
+      }
+
+      if (stamp && lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) stamp[4 + 5 * warp + i] = tacc_v[i];
+        stamp[8 + 5 * warp] = (unsigned long long)nunits;
+      }
+      if (P.epilogue == EPI_ARGMAX) {
+        const int RT = P.sc.RT;
+        argv[warp * 32 + lane] = best_v;
+        argi[warp * 32 + lane] = best_i;
+        consumer_sync(kThreads);
+        if (tid < P.B) {
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
+          for (int w = 0; w < kWarps; ++w)
+            for (int r = 0; r < RT; ++r) {
+              const int l = (r * BT + tid) * (32 / (RT * BT));
+              if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
+                bv = argv[w * 32 + l];
+                bi = argi[w * 32 + l];
+              }
+            }
+          P.arg_val[(size_t)blockIdx.x * P.B + tid] = bv;
+          P.arg_idx[(size_t)blockIdx.x * P.B + tid] = bi;
+          __threadfence();
+        }
+        consumer_sync(kThreads);
+        if (tid == 0) {
+          const unsigned old = atomicAdd(P.arg_ticket, 1u);
+          const int last = old == gridDim.x - 1;
+          if (last) atomicExch(P.arg_ticket, 0u);
+          flags[0] = last;
+        }
+        consumer_sync(kThreads);
+        if (flags[0] && tid < P.B) {
+          __threadfence();
+          float bv = -INFINITY;
+          int bi = 0x7fffffff;
+          for (int c = 0; c < (int)gridDim.x; ++c) {
+            const float v = __ldcg(&P.arg_val[(size_t)c * P.B + tid]);
+            const int ix = __ldcg(&P.arg_idx[(size_t)c * P.B + tid]);
+            if (arg_better(v, ix, bv, bi)) {
+              bv = v;
+              bi = ix;
             }
           }
-        P.arg_val[(size_t)blockIdx.x * P.B + tid] = bv;
-        P.arg_idx[(size_t)blockIdx.x * P.B + tid] = bi;
-        __threadfence();
-      }
-      __syncthreads();
-      if (tid == 0) {
-        const unsigned old = atomicAdd(P.arg_ticket, 1u);
-        const int last = old == gridDim.x - 1;
-        if (last) atomicExch(P.arg_ticket, 0u);
-        flags[0] = last;
-      }
-      __syncthreads();
-      if (flags[0] && tid < P.B) {
-        __threadfence();
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int c = 0; c < (int)gridDim.x; ++c) {
-          const float v = __ldcg(&P.arg_val[(size_t)c * P.B + tid]);
-          const int ix = __ldcg(&P.arg_idx[(size_t)c * P.B + tid]);
-          if (arg_better(v, ix, bv, bi)) {
-            bv = v;
-            bi = ix;
-          }
+          P.argmax_idx[tid] = bi;
         }
-        P.argmax_idx[tid] = bi;
       }
+      // this CTA is done with op f: its outputs are written
+      __threadfence();
+      consumer_sync(kThreads);
+      if (stamp && tid == 0) stamp[2] = global_ns();
+      if (tid == 0) atomicAdd(pp.bar + f, 1u);
     }
-    // this CTA is done with op f: its outputs are written
-    __threadfence();
-    __syncthreads();
-    if (stamp && tid == 0) stamp[2] = global_ns();
-    if (tid == 0) atomicAdd(pp.bar + f, 1u);
-  }
-  if (pp.nops > 0 && pp.ops[pp.nops - 1].trace_out) {
-    grid_wait(pp, pp.nops - 1, flags, tid);
-    copy_trace(pp.ops + (pp.nops - 1), tid);
-  }
-
-  if (cs.abort && lane == 0) {
-    // a wait ran out: let the copies still in flight land before exit
-    for (int q = cs.n; q < ic.n; ++q)
-      mbar_wait_bounded(&bars[q & (kBars - 1)], (uint32_t)((q / kBars) & 1), pp.timeout_ns);
+    if (pp.nops > 0 && pp.ops[pp.nops - 1].trace_out) {
+      grid_wait(pp, pp.nops - 1, flags, tid);
+      copy_trace(pp.ops + (pp.nops - 1), tid);
+    }
   }
   // the last CTA out resets the barrier counters for the next launch
   __syncthreads();
@@ -534,7 +684,11 @@ static bool layout_persistent(PersistParams& pp, int B, int kmax, char* why, siz
   int off = 0;
   pp.off_op = off;
   off += 2 * align_up_p((int)sizeof(GemvParams), 128);
-  pp.off_bar = off;
+  pp.off_bar = off;  // "full" barriers: a piece landed
+  off += kWarps * kBars * 8;
+  pp.off_empty = off;  // "empty" barriers: a piece was consumed
+  off += kWarps * kBars * 8;
+  pp.off_ends = off;  // producer's record of its pieces' ring ends
   off += kWarps * kBars * 8;
   pp.off_flags = off;
   off += 128;
@@ -582,11 +736,14 @@ bool plan_gemv_persistent(GemvParams& p, int ring_bytes, char* why, size_t why_l
     }
     return RG;
   };
-  int RT = 4;
+  // rows per unit: 4 only where every warp gets many units (the LM head);
+  // else 2 (measured faster than 1 for the decode-chain ops, even where some
+  // warps then get no unit: pieces are larger and per-unit work halves)
+  int RT = 2;
   if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
     RT = tu.force_rt;
-  } else {
-    while (RT > 1 && rgs(RT) < 2 * GW) RT /= 2;
+  } else if (rgs(4) >= 8 * GW) {
+    RT = 4;
   }
   const int RG = rgs(RT);
   // No K split unless asked for: inside one launch every split unit would pay
@@ -659,6 +816,7 @@ bool plan_persistent(PersistParams& pp, const GemvParams* ops, int nops, int B, 
   pp.nops = nops;
   pp.timeout_ns = tu.timeout_ns;
   pp.evict_first = tu.evict_first;
+  pp.l2_ahead = tu.l2_ahead;
   pp.err = device_error_ptr();
   return true;
 }
@@ -696,7 +854,7 @@ cudaError_t launch_persistent(const PersistParams& pp, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(pp.grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kPersistThreads);
   cfg.dynamicSmemBytes = pp.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
