@@ -34,7 +34,7 @@ METRIC = "decode-chain µs/step and achieved HBM GB/s (fraction of GB300 rooflin
 WORKLOAD = ("Qwen2.5-1.5B-shaped decode weight chain: 28 blocks (H 1536, KV 256, MLP 8960, "
             "SwiGLU) + final RMSNorm + LM head 151936x1536 + argmax, one CUDA graph")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ws_gemv.cu", "ws_common.cuh", "ws_device.cuh"]
+KERNEL_SOURCES = ["ws_gemv_kernel.cuh", "ws_gemv_host.cu", "ws_common.cuh", "ws_device.cuh"]
 
 
 def parse():
@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--mode", choices=["chain", "kernel"], default="chain")
+    ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
+                    help="graph: one launch per op, PDL edges, one CUDA graph; persistent: "
+                         "the whole step as one cooperative kernel")
     return ap.parse_args()
 
 
@@ -291,9 +294,12 @@ def run_ours(args):
 
     read_gbs = read_roofline(torch, wb)
 
+    persistent = args.chain_mode == "persistent"
+
     def make_chain(prefetch, decoy=False):
         return wc.qwen_chain(dblocks, dhead, dattn, dh0, eps=sh.eps, use_pdl=True,
-                             prefetch=prefetch, decoy=decoy, tune_pairs=30, min_gain=0.01)
+                             prefetch=prefetch, decoy=decoy, tune_pairs=30, min_gain=0.01,
+                             persistent=persistent)
 
     t_tune = time.perf_counter()
     main = make_chain(1 if args.prefetch == "tuned" else 0)
@@ -342,7 +348,7 @@ def run_ours(args):
     # controls: no prefetch, and a decoy of the same traffic (when a plan was kept)
     variants = {}
     ksteps = max(10, min(args.steps, 500))
-    if rank == 0:
+    if rank == 0 and not main.chain.persistent:
         off = make_chain(0)
         off.chain.capture()
         variants["no_prefetch_us"] = round(timed(off, ksteps, 5) / ksteps * 1e6, 2)
@@ -400,6 +406,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) bf16 weights)",
         "config": {"workload": WORKLOAD, "batch": B, "layers": sh.layers,
                    "bytes_per_step": step_bytes, "prefetch": args.prefetch, "pdl": True,
+                   "chain_mode": "persistent" if main.chain.persistent else "graph",
                    "l2": "inputs larger than L2 (3.09 GB of weights per step, no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "frac_of_copy_peak": round(value / world / hbm, 4),
@@ -408,7 +415,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": int(args.steps * (n_ops + n_prefetch_launches)),
+        "gpu_launches": int(args.steps * (1 if main.chain.persistent else n_ops + n_prefetch_launches)),
         "clocks": clk,
         "prefetch_plans": {"kept": sum(1 for p in plans if p[0][0] != 0), "ops": len(plans),
                            "tune_seconds": round(t_tune, 2),
