@@ -298,15 +298,19 @@ ws_status ws_chain_step_host(ws_chain *c, const void *in_host, const void *attn_
 int ws_chain_num_ops(const ws_chain *c);
 /* 1 if the chain runs as one persistent kernel per step, else 0. */
 int ws_chain_is_persistent(const ws_chain *c);
-/* Diagnostics of a persistent chain: CTAs per launch (0 if not persistent),
- * and a device buffer (uint64 [grid][ops][44], or NULL to stop) where every
- * later-captured step records, per CTA and op, globaltimer ns at the op's
- * start (after its grid barrier), after its activations are staged, when its
- * tasks are done, and when warp 0's first weight piece of the op landed;
- * then for each of the CTA's 8 compute warps the ns it spent waiting for
- * weight pieces, 0 (unused), the ns in dot products and in the reduction and
- * epilogue, and the units it ran.  Call ws_chain_capture again after setting
- * it. */
+/* Diagnostics.  ws_chain_grid: the CTA dimension of the stamp buffer (the
+ * persistent kernel's grid, else the SM count, the largest grid of any op).
+ * ws_chain_debug_stamps: a device buffer (uint64 [grid][ops][44], or NULL to
+ * stop) where every later-captured step records globaltimer ns per CTA and
+ * op.  Persistent chains: at the op's start (after its grid barrier), after
+ * its activations are staged, when its tasks are done, and when warp 0's
+ * first weight piece of the op landed; then for each of the CTA's 8 compute
+ * warps the ns it spent waiting for weight pieces, 0 (unused), the ns in dot
+ * products and in the reduction and epilogue, and the units it ran.  Graphs
+ * of launches: at the CTA's entry, after its dependency on the previous op
+ * was released, after its activations were staged, and when its tasks were
+ * done; the rest 0 (CTAs beyond an op's grid are not written).  Call
+ * ws_chain_capture again after setting it. */
 int ws_chain_grid(const ws_chain *c);
 ws_status ws_chain_debug_stamps(ws_chain *c, unsigned long long *stamps, size_t n);
 /* Plan and measured gain (95% CI lower bound, mean) of each op; n entries. */
@@ -346,6 +350,8 @@ typedef struct {
   int evict_first;     /* stream weights with an L2 evict-first hint           */
   int piece_bytes;     /* target bytes of one ring stage                       */
   unsigned long long timeout_ns; /* bound of every device wait                 */
+  int pre_pieces;      /* pieces per warp a GEMV issues before waiting for the
+                          previous op in a chain (0: its whole ring)          */
   int l2_ahead;        /* persistent chain: weight pieces per warp the copy
                           producer prefetches into L2 ahead of its copies     */
 } ws_tuning;

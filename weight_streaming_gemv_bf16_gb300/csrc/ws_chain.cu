@@ -106,6 +106,8 @@ struct ws_chain {
   // persistent mode: all ops in one cooperative kernel per step
   bool persistent = false;
   PersistParams persist;
+  // diagnostics: per-CTA, per-op stamps of the graph-of-launches mode
+  unsigned long long* dbg_stamps = nullptr;
   GemvParams* d_ops = nullptr;
   unsigned* d_bar = nullptr;
 };
@@ -477,6 +479,13 @@ static ws_status capture_graph(ws_chain* c, const std::vector<GemvParams>& ps,
 static std::vector<GemvParams> chain_params(const ws_chain* c) {
   std::vector<GemvParams> ps;
   for (const ChainOp& op : c->ops) ps.push_back(op.p);
+  if (c->dbg_stamps) {
+    const int nops = (int)ps.size();
+    for (int i = 0; i < nops; ++i) {
+      ps[i].stamps = c->dbg_stamps + (size_t)i * kStampsPerOp;
+      ps[i].stamp_stride = nops * kStampsPerOp;
+    }
+  }
   return ps;
 }
 
@@ -927,22 +936,25 @@ int ws_chain_num_ops(const ws_chain* c) { return c ? (int)c->ops.size() : 0; }
 int ws_chain_is_persistent(const ws_chain* c) { return c && c->persistent ? 1 : 0; }
 
 ws_status ws_chain_debug_stamps(ws_chain* c, unsigned long long* stamps, size_t n) {
-  if (!c || !c->persistent) {
-    set_error("stamps are recorded by persistent chains only");
-    return WS_ERR_STATE;
+  if (!c) {
+    set_error("null chain");
+    return WS_ERR_ARG;
   }
-  const size_t need = (size_t)c->persist.grid * c->ops.size() * kStampsPerOp;
+  const size_t need = (size_t)ws_chain_grid(c) * c->ops.size() * kStampsPerOp;
   if (stamps && n < need) {
     set_error("stamp buffer too small: need %zu entries", need);
     return WS_ERR_ARG;
   }
-  c->persist.stamps = stamps;
+  if (c->persistent)
+    c->persist.stamps = stamps;
+  else
+    c->dbg_stamps = stamps;
   return WS_OK;
 }
 
 int ws_chain_grid(const ws_chain* c) {
   if (!c) return 0;
-  return c->persistent ? c->persist.grid : 0;
+  return c->persistent ? c->persist.grid : device_sm_count();
 }
 
 ws_status ws_chain_plans(const ws_chain* c, ws_prefetch_plan* plans, float* gain_lo,

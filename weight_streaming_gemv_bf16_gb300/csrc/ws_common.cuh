@@ -65,6 +65,8 @@ struct Sched {
   int BT;           // batch the kernel is instantiated for (>= B)
   int smem_bytes;
   int off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
+  int off_res;   // residual rows of the CTA in shared memory (0: read at the epilogue)
+  int res_rows;  // rows reserved there per batch row
 };
 
 struct alignas(16) GemvParams {
@@ -92,7 +94,13 @@ struct alignas(16) GemvParams {
   int* err;
   unsigned long long timeout_ns;
   int evict_first;
+  int pre_pieces;    // pieces per warp issued before the dependency wait (0: all stages)
   float* trace_out;  // persistent chain: copy seg[0].out ([B][M] fp32) here after the op
+  // optional diagnostics of a launch inside a chain: globaltimer ns per CTA at
+  // stamps[cta * stamp_stride + i], i = 0 entry, 1 dependency released,
+  // 2 activations staged, 3 end
+  unsigned long long* stamps;
+  int stamp_stride;
   Sched sc;
 };
 
@@ -151,6 +159,7 @@ struct Tuning {
   int evict_first;   // weights streamed with an L2 evict-first policy
   int piece_bytes;   // target bytes per ring stage
   unsigned long long timeout_ns;
+  int pre_pieces;    // pieces per warp issued before the dependency wait (0: all stages)
   int l2_ahead;      // persistent chain: pieces per warp prefetched into L2 ahead of the copies
 };
 

@@ -33,7 +33,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 0};
   return t;
 }
 
@@ -202,6 +202,19 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   if (Gs > RG) Gs = RG;
   sc.Gs = Gs;
   sc.grid = S * Gs;
+  // residual epilogues: the CTA's rows of the residual input are read into
+  // shared memory while the activations are staged, off the epilogue's path
+  sc.off_res = 0;
+  sc.res_rows = 0;
+  if (p.epilogue == EPI_RESID && p.nseg == 1) {
+    const int rows = (RG + Gs - 1) / Gs * RT;
+    const int off_res = align_up(sc.smem_bytes, 16);
+    if (off_res + rows * sc.BT * 4 <= kSmemMax) {
+      sc.off_res = off_res;
+      sc.res_rows = rows;
+      sc.smem_bytes = off_res + rows * sc.BT * 4;
+    }
+  }
   p.sc = sc;
   p.M_total = 0;
   for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
@@ -310,6 +323,7 @@ void init_gemv_params(GemvParams& p, int K, int B) {
   p.err = device_error_ptr();
   p.timeout_ns = tuning().timeout_ns;
   p.evict_first = tuning().evict_first;
+  p.pre_pieces = tuning().pre_pieces;
 }
 
 }  // namespace ws
@@ -611,6 +625,7 @@ void ws_get_tuning(ws_tuning* t) {
   t->evict_first = tu.evict_first;
   t->piece_bytes = tu.piece_bytes;
   t->timeout_ns = tu.timeout_ns;
+  t->pre_pieces = tu.pre_pieces;
   t->l2_ahead = tu.l2_ahead;
 }
 
@@ -618,7 +633,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   if (!t || t->ring_bytes < 0 || t->ring_bytes > kSmemMax || t->grid_cap < 0 ||
       t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt == 3 || t->force_rt > 4 ||
       t->piece_bytes < 0 ||
-      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
+      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->pre_pieces < 0 || t->l2_ahead < 0 ||
       t->l2_ahead > 64) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
@@ -631,6 +646,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.evict_first = t->evict_first;
   tu.piece_bytes = t->piece_bytes;
   tu.timeout_ns = t->timeout_ns;
+  tu.pre_pieces = t->pre_pieces;
   tu.l2_ahead = t->l2_ahead;
   return WS_OK;
 }

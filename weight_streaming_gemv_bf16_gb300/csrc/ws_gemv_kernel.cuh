@@ -51,8 +51,12 @@ __device__ __forceinline__ void raise_device_error(int* err, int code) {
 
 // Epilogue for one output element (segment seg, row m, batch row b).  v0 is
 // the dot product with the first matrix, v1 with the second (SwiGLU up).
+// res_s, when given, holds the residual input of rows res_row0 .. res_row0 +
+// res_n - 1 (batch row b at b * res_n), read ahead into shared memory.
 __device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int m, int b,
-                                               float v0, float v1, float& best_v, int& best_i) {
+                                               float v0, float v1, float& best_v, int& best_i,
+                                               const float* res_s = nullptr, int res_row0 = 0,
+                                               int res_n = 0) {
   const Seg& S = p.seg[seg];
   const size_t o = (size_t)b * S.M + m;
   switch (p.epilogue) {
@@ -64,7 +68,8 @@ __device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int
       break;
     case EPI_RESID: {
       const float* src = p.res_in ? p.res_in : static_cast<const float*>(S.out);
-      static_cast<float*>(S.out)[o] = __ldcg(src + o) + v0;
+      const float r = res_s ? res_s[b * res_n + (m - res_row0)] : __ldcg(src + o);
+      static_cast<float*>(S.out)[o] = r + v0;
       break;
     }
     case EPI_BIAS_GELU: {
@@ -424,6 +429,9 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
 
 template <int BT, int NMAT, int RT>
 __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_constant__ GemvParams p) {
+  unsigned long long* stamp =
+      p.stamps ? p.stamps + (size_t)blockIdx.x * p.stamp_stride : nullptr;
+  if (stamp && threadIdx.x == 0) stamp[0] = global_ns();
   extern __shared__ __align__(128) uint8_t smem[];
   const Sched& sc = p.sc;
   const int tid = threadIdx.x;
@@ -453,8 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     fence_mbar_init();
     pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
     // Weights do not depend on the previous kernel: start streaming them
-    // before waiting for it.
-    while (iq < NSW && iq < npw) {
+    // before waiting for it (pre_pieces of them: the activations' loads
+    // after the wait queue behind whatever is still in flight).
+    const int pre = p.pre_pieces > 0 && p.pre_pieces < NSW ? p.pre_pieces : NSW;
+    while (iq < pre && iq < npw) {
       issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
@@ -463,13 +473,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   }
   pdl_launch_dependents();
   pdl_wait();
+  if (stamp && tid == 0) stamp[1] = global_ns();
 
-  // the activations of this CTA's split, [BT][KS]
-  if (sc.KS != p.K || !prologue_stage_fused<BT>(p, stats, red, xs, tid)) {
-    prologue_stats<BT>(p, stats, red, tid);
-    stage_x<BT>(p, stats, xs, k0 >> 3, sc.KS >> 3, tid);
+  // the residual input of this CTA's rows, read while the activations stage
+  float* res_s = sc.off_res ? reinterpret_cast<float*>(smem + sc.off_res) : nullptr;
+  const int res_row0 = rg0 * RT;
+  if (res_s) {
+    const float* src = p.res_in ? p.res_in : static_cast<const float*>(p.seg[0].out);
+    const int nr = min(rg1 * RT, p.seg[0].M) - res_row0;
+    for (int i = tid; i < p.B * nr; i += kThreads) {
+      const int b = i / nr, r = i - (i / nr) * nr;
+      res_s[b * sc.res_rows + r] = __ldcg(src + (size_t)b * p.seg[0].M + res_row0 + r);
+    }
   }
+  // the activations of this CTA's split, [BT][KS].  Two passes (statistics,
+  // then normalise and store) rather than the one-round fused path: the
+  // fused code is 24 KB, and a launch of a chain starts with cold
+  // instruction caches (measured: 817 vs 897 us per Qwen chain step).
+  prologue_stats<BT>(p, stats, red, tid);
+  stage_x<BT>(p, stats, xs, k0 >> 3, sc.KS >> 3, tid);
   __syncthreads();
+  if (stamp && tid == 0) stamp[2] = global_ns();
+  if (lane == 0) {
+    while (iq < NSW && iq < npw) {  // the rest of the ring
+      issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      ++iq;
+      if (++ij == NP) { ij = 0; ++iti; }
+      if (++islot == NSW) islot = 0;
+    }
+  }
 
   const int nchx = sc.KS >> 3;  // chunks of x in shared memory
   const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
@@ -531,7 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
       const bool mine = lane % G == 0 && r < rows && b < p.B;
       const int rowg = p.seg[seg].row_base + row0;
       if (sc.S == 1) {
-        if (mine) apply_epilogue(p, seg, row0 + r, b, v[0][0], v[NMAT - 1][0], best_v, best_i);
+        if (mine)
+          apply_epilogue(p, seg, row0 + r, b, v[0][0], v[NMAT - 1][0], best_v, best_i, res_s,
+                         res_row0, sc.res_rows);
       } else {
         // split-K: write this split's partials; the last split of the row
         // group adds all splits in split order and runs the epilogue
@@ -564,7 +598,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
             }
             float dv = -INFINITY;
             int di = 0x7fffffff;
-            apply_epilogue(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di);
+            apply_epilogue(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di, res_s, res_row0,
+                           sc.res_rows);
           }
         }
       }
@@ -584,6 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     // last NSW pieces issued are the only ones that can be in flight
     for (int q = iq - NSW; q < iq; ++q)
       if (q >= 0) mbar_wait_bounded(&full[q % NSW], (q / NSW) & 1, p.timeout_ns);
+  }
+
+  if (stamp) {  // the same for every thread of the grid
+    __syncthreads();
+    if (tid == 0) stamp[3] = global_ns();
   }
 
   if (p.epilogue == EPI_ARGMAX) {

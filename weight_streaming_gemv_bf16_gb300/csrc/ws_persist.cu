@@ -645,11 +645,15 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
           P.argmax_idx[tid] = bi;
         }
       }
-      // this CTA is done with op f: its outputs are written
-      __threadfence();
+      // this CTA is done with op f: its outputs are written.  The CTA barrier
+      // orders every thread's stores before thread 0's fence, which makes
+      // them visible GPU-wide before the arrival is counted.
       consumer_sync(kThreads);
       if (stamp && tid == 0) stamp[2] = global_ns();
-      if (tid == 0) atomicAdd(pp.bar + f, 1u);
+      if (tid == 0) {
+        __threadfence();
+        atomicAdd(pp.bar + f, 1u);
+      }
     }
     if (pp.nops > 0 && pp.ops[pp.nops - 1].trace_out) {
       grid_wait(pp, pp.nops - 1, flags, tid);
