@@ -289,6 +289,32 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   for (int o = n + tid; o < BT * nch; o += kThreads) xs4[o] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Staging without a prologue, bf16 activations: a copy into shared memory,
+// with each thread's loads (up to eight 16-byte chunks) all in flight before
+// its first store, so K = 8960 costs one round of latency, not five.
+template <int BT>
+__device__ void stage_copy_bf16(const GemvParams& p, uint16_t* xs, int c0, int nch, int tid) {
+  const int n = BT * nch;
+  uint4* xs4 = reinterpret_cast<uint4*>(xs);
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x));
+  const int rs = p.K >> 3;  // chunks per activation row in global memory
+  for (int base = tid; base < n; base += 8 * kThreads) {
+    uint4 t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int o = base + i * kThreads;
+      const int b = o / nch;
+      t[i] = (o < n && b < p.B) ? __ldcg(src + (size_t)b * rs + c0 + (o - b * nch))
+                                : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int o = base + i * kThreads;
+      if (o < n) xs4[o] = t[i];
+    }
+  }
+}
+
 // Prologue and staging in one pass: every thread loads all of its chunks of
 // the activations first (one round of memory latency), the CTA reduces the
 // statistics from registers, and the normalised bf16 rows -- all K columns --
@@ -571,6 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // instruction caches (measured: 817 vs 897 us per Qwen chain step).
   if (one_round) {
     stage_rms_one_round<BT>(p, stats, red, xs, tid, gpre);
+  } else if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16) {
+    stage_copy_bf16<BT>(p, xs, k0 >> 3, sc.KS >> 3, tid);
   } else {
     prologue_stats<BT>(p, stats, red, tid);
     stage_x<BT>(p, stats, xs, k0 >> 3, sc.KS >> 3, tid);
