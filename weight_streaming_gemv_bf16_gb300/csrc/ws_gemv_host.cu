@@ -74,7 +74,7 @@ static int batch_template(int B) {
 
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-static constexpr int kXsMax = 64 * 1024;
+static constexpr int kXsMax = 96 * 1024;  // activations in shared memory without a K split
 static constexpr int kSmemMax = 227 * 1024;
 
 static int row_groups(GemvParams& p, int RT) {
@@ -98,14 +98,30 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   sc.BT = batch_template(p.B);
   const int K = p.K, nmat = p.nmat;
 
-  // rows per task: as many as the accumulators allow (4 up to batch 4, 2 up
-  // to batch 8, else 1) while there are still two tasks per warp
+  // rows per task, up to what the accumulators allow (4 up to batch 4, 2 up
+  // to batch 8, else 1): the heaviest warp's rows, ceil(tasks / warps) x RT,
+  // as low as possible (ties within 10%); among those, the largest RT whose
+  // piece still holds whole rows (one contiguous copy per matrix), else the
+  // largest.  Measured on the decode chain: QKV, Wo and Wd get 2 rows (a
+  // task each, 6 KB or longer pieces), the LM head 4 (12 KB pieces).
   const int rt_max = sc.BT <= 4 ? 4 : (sc.BT <= 8 ? 2 : 1);
+  const int target_bytes = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
   int RT = rt_max;
   if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
     RT = tu.force_rt < rt_max ? tu.force_rt : rt_max;
   } else {
-    while (RT > 1 && row_groups(p, RT) < 2 * warps_total) RT /= 2;
+    auto load = [&](int rt) {
+      return (long)((row_groups(p, rt) + warps_total - 1) / warps_total) * rt;
+    };
+    long best = load(1);
+    for (int rt = 2; rt <= rt_max; rt *= 2) best = load(rt) < best ? load(rt) : best;
+    int pick = 0, pick_whole = 0;
+    for (int rt = 1; rt <= rt_max; rt *= 2) {
+      if (load(rt) * 10 > best * 11) continue;
+      pick = rt;
+      if ((long)nmat * rt * K * 2 <= target_bytes) pick_whole = rt;
+    }
+    RT = pick_whole ? pick_whole : pick;
   }
   sc.RT = RT;
   const int RG = row_groups(p, RT);
@@ -156,8 +172,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   sc.KS = K / S;
 
   // pieces: about piece_bytes each, evenly sized, multiples of 8 columns
-  const int target = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
-  int pc = target / (nmat * RT * 2);
+  int pc = target_bytes / (nmat * RT * 2);
   pc = pc < 256 ? 256 : pc;
   if (pc >= sc.KS) {
     sc.PC = sc.KS;
@@ -188,12 +203,20 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   int NSW = ring_budget / (kWarps * sc.piece_bytes);
   if (NSW > kMaxStages) NSW = kMaxStages;
   if (NSW < 2) {
-    if (sc.off_ring + 2 * kWarps * sc.piece_bytes <= kSmemMax) {
-      NSW = 2;
-    } else {
-      snprintf(why, why_len, "pieces of %d bytes do not fit twice per warp", sc.piece_bytes);
-      return false;
+    if (sc.off_ring + 2 * kWarps * sc.piece_bytes > kSmemMax) {
+      // smaller pieces, so that two stages per warp fit beside the activations
+      const int pc_fit = ((kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * 2)) & ~7;
+      if (pc_fit < 8) {
+        snprintf(why, why_len, "no two ring stages per warp fit beside %d bytes of activations",
+                 sc.BT * sc.KS * 2);
+        return false;
+      }
+      sc.NP = (sc.KS + pc_fit - 1) / pc_fit;
+      sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 8);
+      sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
+      sc.piece_bytes = align_up(nmat * RT * sc.PC * 2, 128);
     }
+    NSW = 2;
   }
   sc.NSW = NSW;
   sc.smem_bytes = sc.off_ring + kWarps * NSW * sc.piece_bytes;
