@@ -98,26 +98,31 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   sc.BT = batch_template(p.B);
   const int K = p.K, nmat = p.nmat;
 
-  // rows per task, up to what the accumulators allow (4 up to batch 4, 2 up
-  // to batch 8, else 1): the heaviest warp's rows, ceil(tasks / warps) x RT,
-  // as low as possible (ties within 10%); among those, the largest RT whose
-  // piece still holds whole rows (one contiguous copy per matrix), else the
-  // largest.  Measured on the decode chain: QKV, Wo and Wd get 2 rows (a
-  // task each, 6 KB or longer pieces), the LM head 4 (12 KB pieces).
-  const int rt_max = sc.BT <= 4 ? 4 : (sc.BT <= 8 ? 2 : 1);
+  // rows per task: up to 4, and RT x BT <= 32 (one output per lane group).  Cost of a choice: the heaviest warp's rows,
+  // ceil(tasks / warps) x RT, times the shared-memory time per weight row when
+  // it exceeds the HBM time: each 16-byte weight chunk takes BT activation
+  // chunks shared by the task's RT rows, and shared memory reads about 5.5x
+  // an SM's share of HBM (0.18 = 1 / 5.5).  Lowest cost wins (ties within
+  // 10%); among those, the largest RT whose piece still holds whole rows (one
+  // contiguous copy per matrix), else the largest.  Measured on the decode
+  // chain: QKV, Wo and Wd get 2 rows (a task each, 6 KB or longer pieces),
+  // the LM head 4 (12 KB pieces).
+  const int rt_max = sc.BT <= 8 ? 4 : 2;
   const int target_bytes = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
   int RT = rt_max;
   if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
     RT = tu.force_rt < rt_max ? tu.force_rt : rt_max;
   } else {
     auto load = [&](int rt) {
-      return (long)((row_groups(p, rt) + warps_total - 1) / warps_total) * rt;
+      const double rows = (double)((row_groups(p, rt) + warps_total - 1) / warps_total) * rt;
+      const double smem = 0.18 * (1.0 + (double)sc.BT / rt);
+      return rows * (smem > 1.0 ? smem : 1.0);
     };
-    long best = load(1);
+    double best = load(1);
     for (int rt = 2; rt <= rt_max; rt *= 2) best = load(rt) < best ? load(rt) : best;
     int pick = 0, pick_whole = 0;
     for (int rt = 1; rt <= rt_max; rt *= 2) {
-      if (load(rt) * 10 > best * 11) continue;
+      if (load(rt) > best * 1.1) continue;
       pick = rt;
       if ((long)nmat * rt * K * 2 <= target_bytes) pick_whole = rt;
     }
@@ -293,16 +298,17 @@ bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes) {
 static GemvKernel pick_kernel(int BT, int nmat, int RT) {
   if (BT <= 2) return pick_kernel_b12(BT, nmat, RT);
   if (BT == 4) return pick_kernel_b4(BT, nmat, RT);
-  return pick_kernel_b816(BT, nmat, RT);
+  if (BT == 8) return pick_kernel_b816(BT, nmat, RT);
+  return pick_kernel_b16(BT, nmat, RT);
 }
 
 static bool ensure_smem_attr(GemvKernel k) {
   static std::mutex mu;
-  static unsigned long long done[64][32] = {{0}};
+  static unsigned long long done[64][64] = {{0}};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   std::lock_guard<std::mutex> lk(mu);
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 64; ++i) {
     if (done[dev][i] == (unsigned long long)(uintptr_t)k) return true;
     if (done[dev][i] == 0) {
       if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,

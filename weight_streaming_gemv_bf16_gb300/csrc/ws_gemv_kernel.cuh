@@ -787,5 +787,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
 GemvKernel pick_kernel_b12(int BT, int nmat, int RT);
 GemvKernel pick_kernel_b4(int BT, int nmat, int RT);
 GemvKernel pick_kernel_b816(int BT, int nmat, int RT);
+GemvKernel pick_kernel_b16(int BT, int nmat, int RT);
 
 }  // namespace ws
