@@ -228,7 +228,9 @@ def test_full_chain_28_blocks_matches_oracle(persistent):
     assert ch.chain.persistent == persistent
     ch.chain.capture()
     ch.run()
+    ch.run()  # a replay computes the same step again from the same inputs
     torch.cuda.synchronize()
+    assert wb.device_error() == 0
     eligible = _check_chain(ch, blocks, head, attn, h0)
     assert eligible == 1
 
