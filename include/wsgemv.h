@@ -350,10 +350,14 @@ typedef struct {
   int evict_first;     /* stream weights with an L2 evict-first hint           */
   int piece_bytes;     /* target bytes of one ring stage                       */
   unsigned long long timeout_ns; /* bound of every device wait                 */
-  int pre_pieces;      /* pieces per warp a GEMV issues before waiting for the
-                          previous op in a chain (0: its whole ring)          */
   int l2_ahead;        /* persistent chain: weight pieces per warp the copy
                           producer prefetches into L2 ahead of its copies     */
+  int forms;           /* 1 (default): a launch whose shape is one of a decode
+                          chain's op forms (RMSNorm + fp32 out, RMSNorm +
+                          SwiGLU, RMSNorm + argmax, bf16 x + residual; no K
+                          split; batch <= 4) runs a kernel built for that form
+                          alone; 0: every launch runs the general kernel.
+                          Both compute the same values.                      */
 } ws_tuning;
 
 void ws_get_tuning(ws_tuning *t);

@@ -143,6 +143,37 @@ def test_graph_eager_and_pdl_are_bit_identical():
             assert torch.equal(a, b)
 
 
+def _set_tuning(**kw):
+    base = wb.get_tuning()
+    t = wb.Tuning()
+    for f, _ in wb.Tuning._fields_:
+        setattr(t, f, getattr(base, f))
+    for k, v in kw.items():
+        setattr(t, k, v)
+    wb.set_tuning(t)
+    return base
+
+
+@pytest.mark.parametrize("B", [1, 2, 4])
+def test_form_kernels_match_general_kernel_bitwise(B):
+    """The per-form kernels (each holding only its op's staging path and
+    epilogue) compute exactly what the general kernel computes."""
+    outs = []
+    for forms in (0, 1):
+        base = _set_tuning(forms=forms)
+        try:
+            ch, *_ = _make(SMALL, B, 24, trace=True, logits=True, keep_qkv=True)
+            ch.chain.capture()
+            ch.run()
+            torch.cuda.synchronize()
+            outs.append((ch.h_out.cpu(), ch.logits.cpu(), ch.idx.cpu(), ch.h_trace.cpu(),
+                         *[t.cpu() for t in ch.qkv[-1]]))
+        finally:
+            wb.set_tuning(base)
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("mode,stride", [(1, 128), (2, 128), (3, 16384)])
 def test_prefetch_and_decoy_leave_outputs_bit_identical(mode, stride):
     B = 1

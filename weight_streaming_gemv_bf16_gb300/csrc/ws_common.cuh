@@ -94,7 +94,6 @@ struct alignas(16) GemvParams {
   int* err;
   unsigned long long timeout_ns;
   int evict_first;
-  int pre_pieces;    // pieces per warp issued before the dependency wait (0: all stages)
   float* trace_out;  // persistent chain: copy seg[0].out ([B][M] fp32) here after the op
   // optional diagnostics of a launch inside a chain: globaltimer ns per CTA at
   // stamps[cta * stamp_stride + i], i = 0 entry, 1 dependency released,
@@ -151,6 +150,68 @@ __host__ __device__ inline void decode_rg(const GemvParams& p, int rg, int& seg,
   rgl = rg - p.seg[seg].rg_begin;
 }
 
+// One-round RMSNorm staging (fp32 activations, the whole K in one CTA): each
+// thread holds at most kOneRound 8-column chunks of the B x K activations.
+constexpr int kOneRound = 4;
+
+__host__ __device__ inline bool one_round_rms(const GemvParams& p) {
+  return p.prologue == PRO_RMSNORM && p.x_dtype == DT_F32 && p.sc.KS == p.K &&
+         p.B * (p.K >> 3) <= kOneRound * kThreads;
+}
+
+// Compile-time form of a launch.  The ops of a decode chain each run a kernel
+// holding only the code of their own form (staging path, epilogue, no K
+// split); F_ANY reads all of it from the parameters.  Every launch of a chain
+// starts with cold instruction caches, so code that a launch never runs
+// still costs time.
+enum KernelForm {
+  F_ANY = 0,
+  F_RMS_F32 = 1,     // one-round RMSNorm of fp32 x; fp32 outputs (QKV)
+  F_RMS_SWIGLU = 2,  // one-round RMSNorm; SwiGLU of a gate/up pair (bf16 out)
+  F_RMS_ARGMAX = 3,  // one-round RMSNorm; logits and argmax (LM head)
+  F_BF16_RESID = 4,  // bf16 x without prologue; fp32 residual add (Wo, Wd)
+  kNumForms = 5
+};
+
+template <int F>
+struct FormTraits {
+  static constexpr int epi = -1;  // epilogue, or -1: read from the parameters
+  static constexpr bool rms1 = false, copy_bf16 = false, no_split = false;
+};
+template <>
+struct FormTraits<F_RMS_F32> {
+  static constexpr int epi = EPI_F32;
+  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true;
+};
+template <>
+struct FormTraits<F_RMS_SWIGLU> {
+  static constexpr int epi = EPI_SWIGLU;
+  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true;
+};
+template <>
+struct FormTraits<F_RMS_ARGMAX> {
+  static constexpr int epi = EPI_ARGMAX;
+  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true;
+};
+template <>
+struct FormTraits<F_BF16_RESID> {
+  static constexpr int epi = EPI_RESID;
+  static constexpr bool rms1 = false, copy_bf16 = true, no_split = true;
+};
+
+// The form a planned launch can run as.
+inline int kernel_form(const GemvParams& p) {
+  if (p.sc.S != 1) return F_ANY;
+  if (one_round_rms(p)) {
+    if (p.epilogue == EPI_F32) return F_RMS_F32;
+    if (p.epilogue == EPI_SWIGLU && p.nmat == 2) return F_RMS_SWIGLU;
+    if (p.epilogue == EPI_ARGMAX) return F_RMS_ARGMAX;
+    return F_ANY;
+  }
+  if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_RESID) return F_BF16_RESID;
+  return F_ANY;
+}
+
 struct Tuning {
   int ring_bytes;    // shared-memory ring budget per CTA (all warps)
   int grid_cap;      // max CTAs (0: one per SM)
@@ -159,8 +220,8 @@ struct Tuning {
   int evict_first;   // weights streamed with an L2 evict-first policy
   int piece_bytes;   // target bytes per ring stage
   unsigned long long timeout_ns;
-  int pre_pieces;    // pieces per warp issued before the dependency wait (0: all stages)
   int l2_ahead;      // persistent chain: pieces per warp prefetched into L2 ahead of the copies
+  int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

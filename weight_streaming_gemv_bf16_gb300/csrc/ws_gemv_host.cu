@@ -33,7 +33,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 0};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1};
   return t;
 }
 
@@ -295,7 +295,16 @@ bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes) {
   return true;
 }
 
-static GemvKernel pick_kernel(int BT, int nmat, int RT) {
+// The kernel of a planned launch: the one of its chain form where one is
+// built for its batch tile, else the general one.
+static GemvKernel pick_kernel(const GemvParams& p) {
+  const int BT = p.sc.BT, nmat = p.nmat, RT = p.sc.RT;
+  const int F = tuning().forms ? kernel_form(p) : F_ANY;
+  if (F != F_ANY) {
+    GemvKernel k = BT == 1 ? pick_form_b1(BT, nmat, RT, F)
+                           : (BT <= 4 ? pick_form_b24(BT, nmat, RT, F) : nullptr);
+    if (k) return k;
+  }
   if (BT <= 2) return pick_kernel_b12(BT, nmat, RT);
   if (BT == 4) return pick_kernel_b4(BT, nmat, RT);
   if (BT == 8) return pick_kernel_b816(BT, nmat, RT);
@@ -322,12 +331,12 @@ static bool ensure_smem_attr(GemvKernel k) {
 }
 
 bool prepare_gemv(const GemvParams& p) {
-  GemvKernel k = pick_kernel(p.sc.BT, p.nmat, p.sc.RT);
+  GemvKernel k = pick_kernel(p);
   return k && ensure_smem_attr(k);
 }
 
 cudaError_t launch_gemv(const GemvParams& p, cudaStream_t stream, bool pdl) {
-  GemvKernel k = pick_kernel(p.sc.BT, p.nmat, p.sc.RT);
+  GemvKernel k = pick_kernel(p);
   if (!k) return cudaErrorInvalidValue;
   if (!ensure_smem_attr(k)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg;
@@ -352,7 +361,6 @@ void init_gemv_params(GemvParams& p, int K, int B) {
   p.err = device_error_ptr();
   p.timeout_ns = tuning().timeout_ns;
   p.evict_first = tuning().evict_first;
-  p.pre_pieces = tuning().pre_pieces;
 }
 
 }  // namespace ws
@@ -654,16 +662,16 @@ void ws_get_tuning(ws_tuning* t) {
   t->evict_first = tu.evict_first;
   t->piece_bytes = tu.piece_bytes;
   t->timeout_ns = tu.timeout_ns;
-  t->pre_pieces = tu.pre_pieces;
   t->l2_ahead = tu.l2_ahead;
+  t->forms = tu.forms;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
   if (!t || t->ring_bytes < 0 || t->ring_bytes > kSmemMax || t->grid_cap < 0 ||
       t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt == 3 || t->force_rt > 4 ||
       t->piece_bytes < 0 ||
-      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->pre_pieces < 0 || t->l2_ahead < 0 ||
-      t->l2_ahead > 64) {
+      t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
+      t->l2_ahead > 64 || t->forms < 0 || t->forms > 1) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -675,8 +683,8 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.evict_first = t->evict_first;
   tu.piece_bytes = t->piece_bytes;
   tu.timeout_ns = t->timeout_ns;
-  tu.pre_pieces = t->pre_pieces;
   tu.l2_ahead = t->l2_ahead;
+  tu.forms = t->forms;
   return WS_OK;
 }
 

@@ -4,7 +4,7 @@
 namespace ws {
 
 #define WS_INST(bt, nm, rt) \
-  if (BT == bt && nmat == nm && RT == rt) return (GemvKernel)k_stream_gemv<bt, nm, rt>;
+  if (BT == bt && nmat == nm && RT == rt) return (GemvKernel)k_stream_gemv<bt, nm, rt, F_ANY>;
 
 GemvKernel pick_kernel_b12(int BT, int nmat, int RT) {
   WS_INST(1, 1, 1) WS_INST(1, 1, 2) WS_INST(1, 1, 4)

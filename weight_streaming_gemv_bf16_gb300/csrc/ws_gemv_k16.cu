@@ -5,7 +5,7 @@
 namespace ws {
 
 #define WS_INST(bt, nm, rt) \
-  if (BT == bt && nmat == nm && RT == rt) return (GemvKernel)k_stream_gemv<bt, nm, rt>;
+  if (BT == bt && nmat == nm && RT == rt) return (GemvKernel)k_stream_gemv<bt, nm, rt, F_ANY>;
 
 GemvKernel pick_kernel_b16(int BT, int nmat, int RT) {
   WS_INST(16, 1, 1) WS_INST(16, 1, 2)

@@ -53,13 +53,14 @@ __device__ __forceinline__ void raise_device_error(int* err, int code) {
 // the dot product with the first matrix, v1 with the second (SwiGLU up).
 // res_s, when given, holds the residual input of rows res_row0 .. res_row0 +
 // res_n - 1 (batch row b at b * res_n), read ahead into shared memory.
+template <int EPI>  // the epilogue kind, or -1: p.epilogue
 __device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int m, int b,
                                                float v0, float v1, float& best_v, int& best_i,
                                                const float* res_s = nullptr, int res_row0 = 0,
                                                int res_n = 0) {
   const Seg& S = p.seg[seg];
   const size_t o = (size_t)b * S.M + m;
-  switch (p.epilogue) {
+  switch (EPI >= 0 ? EPI : p.epilogue) {
     case EPI_F32:
       static_cast<float*>(S.out)[o] = v0;
       break;
@@ -222,22 +223,31 @@ __device__ __forceinline__ uint4 normalise8(const GemvParams& p, const float* st
 // depend on the previous op): one round of activation latency instead of the
 // two of prologue_stats + stage_x, in compact code.  Same arithmetic: fp32
 // sums of squares, x * r * gamma rounded once to bf16.
-constexpr int kOneRound = 4;
 
-__device__ __forceinline__ bool one_round_rms(const GemvParams& p) {
-  return p.prologue == PRO_RMSNORM && p.x_dtype == DT_F32 && p.sc.KS == p.K &&
-         p.B * (p.K >> 3) <= kOneRound * kThreads;
+// Row b[i] and chunk c[i] of the chunks o0 + i * step (i < N) of a [rows][nch]
+// array of 8-column chunks, stepped without a division per chunk (integer
+// division is long code, and these run once per launch with cold caches).
+template <int N>
+__device__ __forceinline__ void chunk_coords(int o0, int step, int nch, int (&b)[N], int (&c)[N]) {
+  int bb = 0, cc = o0;
+  while (cc >= nch) { cc -= nch; ++bb; }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    b[i] = bb;
+    c[i] = cc;
+    cc += step;
+    while (cc >= nch) { cc -= nch; ++bb; }
+  }
 }
 
 __device__ __forceinline__ void gamma_preload(const GemvParams& p, int tid,
                                               uint4 (&g)[kOneRound]) {
-  const int nch = p.K >> 3;
+  int b[kOneRound], c[kOneRound];
+  chunk_coords<kOneRound>(tid, kThreads, p.K >> 3, b, c);
 #pragma unroll
-  for (int i = 0; i < kOneRound; ++i) {
-    const int o = tid + i * kThreads;
-    g[i] = o < p.B * nch ? *reinterpret_cast<const uint4*>(p.gamma + (o % nch) * 8)
-                         : make_uint4(0u, 0u, 0u, 0u);
-  }
+  for (int i = 0; i < kOneRound; ++i)
+    g[i] = b[i] < p.B ? *reinterpret_cast<const uint4*>(p.gamma + c[i] * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
 }
 
 template <int BT>
@@ -247,14 +257,19 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   float* tot = red + kWarps * BT;
   float v[kOneRound][8];
   float s[BT];
+  int rb[kOneRound], rc[kOneRound];
+  chunk_coords<kOneRound>(tid, kThreads, nch, rb, rc);
 #pragma unroll
   for (int b = 0; b < BT; ++b) s[b] = 0.f;
 #pragma unroll
   for (int i = 0; i < kOneRound; ++i) {
     const int o = tid + i * kThreads;
     if (o < n) {
-      const int b = o / nch;
-      load_x8(p, b, o - b * nch, v[i]);
+      const int b = rb[i];
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x)) + 2 * o;
+      const float4 lo4 = __ldcg(src), hi4 = __ldcg(src + 1);  // fp32, rows K apart: o = b*nch + c
+      v[i][0] = lo4.x; v[i][1] = lo4.y; v[i][2] = lo4.z; v[i][3] = lo4.w;
+      v[i][4] = hi4.x; v[i][5] = hi4.y; v[i][6] = hi4.z; v[i][7] = hi4.w;
       float t = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) t = fmaf(v[i][e], v[i][e], t);
@@ -271,7 +286,7 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   for (int i = 0; i < kOneRound; ++i) {
     const int o = tid + i * kThreads;
     if (o < n) {
-      const float r = stats[2 * (o / nch)];
+      const float r = stats[2 * rb[i]];
       const float gf[8] = {bf16lo(g[i].x), bf16hi(g[i].x), bf16lo(g[i].y), bf16hi(g[i].y),
                            bf16lo(g[i].z), bf16hi(g[i].z), bf16lo(g[i].w), bf16hi(g[i].w)};
       uint32_t w[4];
@@ -300,13 +315,12 @@ __device__ void stage_copy_bf16(const GemvParams& p, uint16_t* xs, int c0, int n
   const int rs = p.K >> 3;  // chunks per activation row in global memory
   for (int base = tid; base < n; base += 8 * kThreads) {
     uint4 t[8];
+    int b[8], c[8];
+    chunk_coords<8>(base, kThreads, nch, b, c);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int o = base + i * kThreads;
-      const int b = o / nch;
-      t[i] = (o < n && b < p.B) ? __ldcg(src + (size_t)b * rs + c0 + (o - b * nch))
-                                : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int i = 0; i < 8; ++i)
+      t[i] = (b[i] < BT && b[i] < p.B) ? __ldcg(src + (size_t)b[i] * rs + c0 + c[i])
+                                       : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int o = base + i * kThreads;
@@ -528,8 +542,11 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
   }
 }
 
-template <int BT, int NMAT, int RT>
+template <int BT, int NMAT, int RT, int F>
 __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_constant__ GemvParams p) {
+  using FT = FormTraits<F>;
+  constexpr int EPI = FT::epi;
+  const int epi = EPI >= 0 ? EPI : p.epilogue;
   unsigned long long* stamp =
       p.stamps ? p.stamps + (size_t)blockIdx.x * p.stamp_stride : nullptr;
   if (stamp && threadIdx.x == 0) stamp[0] = global_ns();
@@ -561,11 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     for (int s = 0; s < NSW; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
     pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
-    // Weights do not depend on the previous kernel: start streaming them
-    // before waiting for it (pre_pieces of them: the activations' loads
-    // after the wait queue behind whatever is still in flight).
-    const int pre = p.pre_pieces > 0 && p.pre_pieces < NSW ? p.pre_pieces : NSW;
-    while (iq < pre && iq < npw) {
+    // Weights do not depend on the previous kernel: fill the whole ring
+    // before waiting for it.
+    while (iq < NSW && iq < npw) {
       issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
@@ -573,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     }
   }
   // gamma does not depend on the previous op either
-  const bool one_round = one_round_rms(p);
+  const bool one_round = FT::rms1 || (!FT::copy_bf16 && one_round_rms(p));
   uint4 gpre[kOneRound];
   if (one_round) gamma_preload(p, tid, gpre);
   pdl_launch_dependents();
@@ -581,11 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   if (stamp && tid == 0) stamp[1] = global_ns();
 
   // the residual input of this CTA's rows, read while the activations stage
-  float* res_s = sc.off_res ? reinterpret_cast<float*>(smem + sc.off_res) : nullptr;
+  float* res_s = (EPI < 0 || EPI == EPI_RESID) && sc.off_res
+                     ? reinterpret_cast<float*>(smem + sc.off_res)
+                     : nullptr;
   const int res_row0 = rg0 * RT;
   if (res_s) {
     const float* src = p.res_in ? p.res_in : static_cast<const float*>(p.seg[0].out);
     const int nr = min(rg1 * RT, p.seg[0].M) - res_row0;
+#pragma unroll 1  // one pass when B x rows <= threads; compact code
     for (int i = tid; i < p.B * nr; i += kThreads) {
       const int b = i / nr, r = i - (i / nr) * nr;
       res_s[b * sc.res_rows + r] = __ldcg(src + (size_t)b * p.seg[0].M + res_row0 + r);
@@ -595,7 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // then normalise and store) rather than the one-round fused path: the
   // fused code is 24 KB, and a launch of a chain starts with cold
   // instruction caches (measured: 817 vs 897 us per Qwen chain step).
-  if (one_round) {
+  if constexpr (FT::rms1) {
+    stage_rms_one_round<BT>(p, stats, red, xs, tid, gpre);
+  } else if constexpr (FT::copy_bf16) {
+    stage_copy_bf16<BT>(p, xs, k0 >> 3, sc.KS >> 3, tid);
+  } else if (one_round) {
     stage_rms_one_round<BT>(p, stats, red, xs, tid, gpre);
   } else if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16) {
     stage_copy_bf16<BT>(p, xs, k0 >> 3, sc.KS >> 3, tid);
@@ -605,14 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   }
   __syncthreads();
   if (stamp && tid == 0) stamp[2] = global_ns();
-  if (lane == 0) {
-    while (iq < NSW && iq < npw) {  // the rest of the ring
-      issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
-      ++iq;
-      if (++ij == NP) { ij = 0; ++iti; }
-      if (++islot == NSW) islot = 0;
-    }
-  }
 
   const int nchx = sc.KS >> 3;  // chunks of x in shared memory
   const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
@@ -673,9 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
       const int o = lane / G, r = o / BT, b = o - (o / BT) * BT;
       const bool mine = lane % G == 0 && r < rows && b < p.B;
       const int rowg = p.seg[seg].row_base + row0;
-      if (sc.S == 1) {
+      if (FT::no_split || sc.S == 1) {
         if (mine)
-          apply_epilogue(p, seg, row0 + r, b, v[0][0], v[NMAT - 1][0], best_v, best_i, res_s,
+          apply_epilogue<EPI>(p, seg, row0 + r, b, v[0][0], v[NMAT - 1][0], best_v, best_i, res_s,
                          res_row0, sc.res_rows);
       } else {
         // split-K: write this split's partials; the last split of the row
@@ -709,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
             }
             float dv = -INFINITY;
             int di = 0x7fffffff;
-            apply_epilogue(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di, res_s, res_row0,
+            apply_epilogue<EPI>(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di, res_s, res_row0,
                            sc.res_rows);
           }
         }
@@ -737,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     if (tid == 0) stamp[3] = global_ns();
   }
 
-  if (p.epilogue == EPI_ARGMAX) {
+  if (epi == EPI_ARGMAX) {
     // per batch row b: the first lanes of groups r*BT + b hold a running
     // best; combine the warps, then the last CTA (ticket) combines all CTAs
     argv[warp * 32 + lane] = best_v;
@@ -783,10 +797,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   }
 }
 
-// Instantiation tables, one per translation unit (compiled in parallel).
+// Instantiation tables, one per translation unit (compiled in parallel):
+// the F_ANY kernels per batch tile, and the chain forms per batch tile.
 GemvKernel pick_kernel_b12(int BT, int nmat, int RT);
 GemvKernel pick_kernel_b4(int BT, int nmat, int RT);
 GemvKernel pick_kernel_b816(int BT, int nmat, int RT);
 GemvKernel pick_kernel_b16(int BT, int nmat, int RT);
+GemvKernel pick_form_b1(int BT, int nmat, int RT, int F);
+GemvKernel pick_form_b24(int BT, int nmat, int RT, int F);
 
 }  // namespace ws

@@ -351,7 +351,7 @@ __device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvPara
   const int r = o / BT, b = o - (o / BT) * BT;
   const bool mine = (lane & ((1 << us.lg) - 1)) == 0 && r < rows && b < P.B;
   if (S == 1) {
-    if (mine) apply_epilogue(P, seg, row0 + r, b, v0, v1, best_v, best_i);
+    if (mine) apply_epilogue<-1>(P, seg, row0 + r, b, v0, v1, best_v, best_i);
     if (tacc) tacc[3] += global_ns() - te;
     return;
   }
@@ -383,7 +383,7 @@ __device__ __forceinline__ void run_unit(const PersistParams& pp, const GemvPara
       }
       float dv = -INFINITY;
       int di = 0x7fffffff;
-      apply_epilogue(P, seg, row0 + rr, bb, t0, nmat == 2 ? t1 : t0, dv, di);
+      apply_epilogue<-1>(P, seg, row0 + rr, bb, t0, nmat == 2 ? t1 : t0, dv, di);
     }
   }
 }
