@@ -133,9 +133,10 @@ constexpr int kStampsPerOp = 4 + 5 * kWarps;
 // The split and the row-group range of CTA `cta`.
 __host__ __device__ inline void cta_range(const Sched& sc, int cta, int& ks, int& rg0, int& rg1) {
   ks = cta / sc.Gs;
-  const int g = cta - ks * sc.Gs;
-  rg0 = (int)((long long)g * sc.RG / sc.Gs);
-  rg1 = (int)((long long)(g + 1) * sc.RG / sc.Gs);
+  // 32-bit products: the planner keeps Gs * RG below 2^32
+  const unsigned g = (unsigned)(cta - ks * sc.Gs);
+  rg0 = (int)(g * (unsigned)sc.RG / (unsigned)sc.Gs);
+  rg1 = (int)((g + 1) * (unsigned)sc.RG / (unsigned)sc.Gs);
 }
 
 // Tasks of warp `w` in a CTA whose row groups are [rg0, rg1): rg0 + w + t * kWarps.
@@ -176,27 +177,27 @@ enum KernelForm {
 template <int F>
 struct FormTraits {
   static constexpr int epi = -1;  // epilogue, or -1: read from the parameters
-  static constexpr bool rms1 = false, copy_bf16 = false, no_split = false;
+  static constexpr bool rms1 = false, copy_bf16 = false, no_split = false, one_seg = false;
 };
 template <>
 struct FormTraits<F_RMS_F32> {
   static constexpr int epi = EPI_F32;
-  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true;
+  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true, one_seg = false;
 };
 template <>
 struct FormTraits<F_RMS_SWIGLU> {
   static constexpr int epi = EPI_SWIGLU;
-  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true;
+  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true, one_seg = true;
 };
 template <>
 struct FormTraits<F_RMS_ARGMAX> {
   static constexpr int epi = EPI_ARGMAX;
-  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true;
+  static constexpr bool rms1 = true, copy_bf16 = false, no_split = true, one_seg = true;
 };
 template <>
 struct FormTraits<F_BF16_RESID> {
   static constexpr int epi = EPI_RESID;
-  static constexpr bool rms1 = false, copy_bf16 = true, no_split = true;
+  static constexpr bool rms1 = false, copy_bf16 = true, no_split = true, one_seg = true;
 };
 
 // The form a planned launch can run as.
@@ -204,11 +205,12 @@ inline int kernel_form(const GemvParams& p) {
   if (p.sc.S != 1) return F_ANY;
   if (one_round_rms(p)) {
     if (p.epilogue == EPI_F32) return F_RMS_F32;
-    if (p.epilogue == EPI_SWIGLU && p.nmat == 2) return F_RMS_SWIGLU;
-    if (p.epilogue == EPI_ARGMAX) return F_RMS_ARGMAX;
+    if (p.epilogue == EPI_SWIGLU && p.nmat == 2 && p.nseg == 1) return F_RMS_SWIGLU;
+    if (p.epilogue == EPI_ARGMAX && p.nseg == 1) return F_RMS_ARGMAX;
     return F_ANY;
   }
-  if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_RESID) return F_BF16_RESID;
+  if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_RESID && p.nseg == 1)
+    return F_BF16_RESID;
   return F_ANY;
 }
 

@@ -228,6 +228,10 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   int Gs = grid_target / S;
   if (Gs < 1) Gs = 1;
   if (Gs > RG) Gs = RG;
+  if ((unsigned long long)Gs * (unsigned long long)RG >= (1ull << 32)) {
+    snprintf(why, why_len, "%d row groups over %d CTAs exceed the 32-bit row arithmetic", RG, Gs);
+    return false;
+  }
   sc.Gs = Gs;
   sc.grid = S * Gs;
   // residual epilogues: the CTA's rows of the residual input are read into

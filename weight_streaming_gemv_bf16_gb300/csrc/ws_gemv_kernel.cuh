@@ -514,12 +514,12 @@ __device__ __forceinline__ void dot_piece(float (&acc)[2][4][BT], const uint4* s
       }
 }
 
-template <int NMAT, int RT>
+template <int NMAT, int RT, bool ONE_SEG>
 __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, int slot, int k0,
                                             uint8_t* ring, uint64_t* full, uint64_t pol) {
   const Sched& sc = p.sc;
-  int seg, rgl;
-  decode_rg(p, rg, seg, rgl);
+  int seg = 0, rgl = rg;
+  if (!ONE_SEG) decode_rg(p, rg, seg, rgl);
   const Seg& S = p.seg[seg];
   const int row0 = rgl * RT;
   const int rows = min(RT, S.M - row0);
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     // Weights do not depend on the previous kernel: fill the whole ring
     // before waiting for it.
     while (iq < NSW && iq < npw) {
-      issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      issue_piece<NMAT, RT, FT::one_seg>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
       if (++islot == NSW) islot = 0;
@@ -648,8 +648,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   uint32_t phase = 0;
   for (int q = 0; q < npw; ++q) {
     const int rg = rgw + ti * kWarps;
-    int seg, rgl;
-    decode_rg(p, rg, seg, rgl);
+    int seg = 0, rgl = rg;
+    if (!FT::one_seg) decode_rg(p, rg, seg, rgl);
     const int row0 = rgl * RT;
     const int rows = min(RT, p.seg[seg].M - row0);
     const int len = min(sc.PC, sc.KS - j * sc.PC);
@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     // values fed the FMAs above, and issue is in order): refill the slot.
     __syncwarp();
     if (lane == 0 && !abort && iq < npw) {
-      issue_piece<NMAT, RT>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      issue_piece<NMAT, RT, FT::one_seg>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
       if (++islot == NSW) islot = 0;
