@@ -153,11 +153,14 @@ __host__ __device__ inline void decode_rg(const GemvParams& p, int rg, int& seg,
 
 // One-round RMSNorm staging (fp32 activations, the whole K in one CTA): each
 // thread holds at most kOneRound 8-column chunks of the B x K activations.
+// The chain forms hold min(BT, kOneRound) chunks (K <= 2048 at any BT).
 constexpr int kOneRound = 4;
 
-__host__ __device__ inline bool one_round_rms(const GemvParams& p) {
+__host__ __device__ constexpr int form_round_chunks(int BT) { return BT < kOneRound ? BT : kOneRound; }
+
+__host__ __device__ inline bool one_round_rms(const GemvParams& p, int chunks = kOneRound) {
   return p.prologue == PRO_RMSNORM && p.x_dtype == DT_F32 && p.sc.KS == p.K &&
-         p.B * (p.K >> 3) <= kOneRound * kThreads;
+         p.B * (p.K >> 3) <= chunks * kThreads;
 }
 
 // Compile-time form of a launch.  The ops of a decode chain each run a kernel
@@ -203,7 +206,7 @@ struct FormTraits<F_BF16_RESID> {
 // The form a planned launch can run as.
 inline int kernel_form(const GemvParams& p) {
   if (p.sc.S != 1) return F_ANY;
-  if (one_round_rms(p)) {
+  if (one_round_rms(p, form_round_chunks(p.sc.BT))) {
     if (p.epilogue == EPI_F32) return F_RMS_F32;
     if (p.epilogue == EPI_SWIGLU && p.nmat == 2 && p.nseg == 1) return F_RMS_SWIGLU;
     if (p.epilogue == EPI_ARGMAX && p.nseg == 1) return F_RMS_ARGMAX;

@@ -45,6 +45,13 @@ __device__ __forceinline__ float bf16_round(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// Two fp32 values rounded to bf16 (round to nearest even) and packed, lo in
+// the low half: one conversion instruction for the pair.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ void raise_device_error(int* err, int code) {
   if (err) atomicExch(err, code);
 }
@@ -207,11 +214,7 @@ __device__ __forceinline__ uint4 normalise8(const GemvParams& p, const float* st
   }
   uint32_t w[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e]));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e + 1]));
-    w[e] = lo | (hi << 16);
-  }
+  for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -240,29 +243,29 @@ __device__ __forceinline__ void chunk_coords(int o0, int step, int nch, int (&b)
   }
 }
 
-__device__ __forceinline__ void gamma_preload(const GemvParams& p, int tid,
-                                              uint4 (&g)[kOneRound]) {
-  int b[kOneRound], c[kOneRound];
-  chunk_coords<kOneRound>(tid, kThreads, p.K >> 3, b, c);
+template <int NR>  // chunks per thread
+__device__ __forceinline__ void gamma_preload(const GemvParams& p, int tid, uint4 (&g)[NR]) {
+  int b[NR], c[NR];
+  chunk_coords<NR>(tid, kThreads, p.K >> 3, b, c);
 #pragma unroll
-  for (int i = 0; i < kOneRound; ++i)
+  for (int i = 0; i < NR; ++i)
     g[i] = b[i] < p.B ? *reinterpret_cast<const uint4*>(p.gamma + c[i] * 8)
                       : make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int BT>
+template <int BT, int NR>  // NR chunks per thread
 __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* red, uint16_t* xs,
-                                    int tid, const uint4 (&g)[kOneRound]) {
+                                    int tid, const uint4 (&g)[NR]) {
   const int nch = p.K >> 3, n = p.B * nch;
   float* tot = red + kWarps * BT;
-  float v[kOneRound][8];
+  float v[NR][8];
   float s[BT];
-  int rb[kOneRound], rc[kOneRound];
-  chunk_coords<kOneRound>(tid, kThreads, nch, rb, rc);
+  int rb[NR], rc[NR];
+  chunk_coords<NR>(tid, kThreads, nch, rb, rc);
 #pragma unroll
   for (int b = 0; b < BT; ++b) s[b] = 0.f;
 #pragma unroll
-  for (int i = 0; i < kOneRound; ++i) {
+  for (int i = 0; i < NR; ++i) {
     const int o = tid + i * kThreads;
     if (o < n) {
       const int b = rb[i];
@@ -283,7 +286,7 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   consumer_sync(kThreads);
   uint4* xs4 = reinterpret_cast<uint4*>(xs);
 #pragma unroll
-  for (int i = 0; i < kOneRound; ++i) {
+  for (int i = 0; i < NR; ++i) {
     const int o = tid + i * kThreads;
     if (o < n) {
       const float r = stats[2 * rb[i]];
@@ -291,12 +294,8 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
                            bf16lo(g[i].z), bf16hi(g[i].z), bf16lo(g[i].w), bf16hi(g[i].w)};
       uint32_t w[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[i][2 * e] * r * gf[2 * e]));
-        const uint32_t hi =
-            __bfloat16_as_ushort(__float2bfloat16_rn(v[i][2 * e + 1] * r * gf[2 * e + 1]));
-        w[e] = lo | (hi << 16);
-      }
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2(v[i][2 * e] * r * gf[2 * e], v[i][2 * e + 1] * r * gf[2 * e + 1]);
       xs4[o] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
@@ -444,11 +443,7 @@ __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, i
         }
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e]));
-          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e + 1]));
-          w[e] = lo | (hi << 16);
-        }
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
         out = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
@@ -531,14 +526,10 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
 #pragma unroll
   for (int mat = 0; mat < NMAT; ++mat) {
     const uint16_t* W = mat == 0 ? S.W0 : S.W1;
-    if (len == K) {  // whole rows: one contiguous copy
-      bulk_copy_g2s(dst + (size_t)mat * RT * sc.PC * 2, W + (size_t)row0 * K,
-                    (uint32_t)(rows * K * 2), &full[slot], pol);
-    } else {
-      for (int r = 0; r < rows; ++r)
-        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * sc.PC * 2, W + (size_t)(row0 + r) * K + c0,
-                      (uint32_t)(len * 2), &full[slot], pol);
-    }
+    // one copy per row (also for whole rows: one code path is shorter code)
+    for (int r = 0; r < rows; ++r)
+      bulk_copy_g2s(dst + ((size_t)mat * RT + r) * sc.PC * 2, W + (size_t)(row0 + r) * K + c0,
+                    (uint32_t)(len * 2), &full[slot], pol);
   }
 }
 
@@ -589,8 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   }
   // gamma does not depend on the previous op either
   const bool one_round = FT::rms1 || (!FT::copy_bf16 && one_round_rms(p));
-  uint4 gpre[kOneRound];
-  if (one_round) gamma_preload(p, tid, gpre);
+  constexpr int NR = FT::rms1 ? form_round_chunks(BT) : kOneRound;
+  uint4 gpre[NR];
+  if (one_round) gamma_preload<NR>(p, tid, gpre);
   pdl_launch_dependents();
   pdl_wait();
   if (stamp && tid == 0) stamp[1] = global_ns();
@@ -614,11 +606,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // fused code is 24 KB, and a launch of a chain starts with cold
   // instruction caches (measured: 817 vs 897 us per Qwen chain step).
   if constexpr (FT::rms1) {
-    stage_rms_one_round<BT>(p, stats, red, xs, tid, gpre);
+    stage_rms_one_round<BT, NR>(p, stats, red, xs, tid, gpre);
   } else if constexpr (FT::copy_bf16) {
     stage_copy_bf16<BT>(p, xs, k0 >> 3, sc.KS >> 3, tid);
   } else if (one_round) {
-    stage_rms_one_round<BT>(p, stats, red, xs, tid, gpre);
+    stage_rms_one_round<BT, NR>(p, stats, red, xs, tid, gpre);
   } else if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16) {
     stage_copy_bf16<BT>(p, xs, k0 >> 3, sc.KS >> 3, tid);
   } else {
@@ -752,21 +744,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   }
 
   if (epi == EPI_ARGMAX) {
-    // per batch row b: the first lanes of groups r*BT + b hold a running
-    // best; combine the warps, then the last CTA (ticket) combines all CTAs
-    argv[warp * 32 + lane] = best_v;
-    argi[warp * 32 + lane] = best_i;
+    // per batch row b the lanes of output groups r*BT + b hold a running
+    // best: a warp butterfly per batch row, then thread b combines the warps,
+    // then the last CTA (ticket) combines all CTAs with a warp per batch row
+    constexpr int G = 32 / (RT * BT);
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const bool has = (lane / G) % BT == b;
+      float v = has ? best_v : -INFINITY;
+      int i = has ? best_i : 0x7fffffff;
+      warp_argmax(v, i);
+      if (lane == 0) {
+        argv[warp * BT + b] = v;
+        argi[warp * BT + b] = i;
+      }
+    }
     __syncthreads();
     if (tid < p.B) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int w = 0; w < kWarps; ++w)
-        for (int r = 0; r < RT; ++r) {
-          const int l = (r * BT + tid) * (32 / (RT * BT));
-          if (arg_better(argv[w * 32 + l], argi[w * 32 + l], bv, bi)) {
-            bv = argv[w * 32 + l];
-            bi = argi[w * 32 + l];
-          }
+      float bv = argv[tid];
+      int bi = argi[tid];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w)
+        if (arg_better(argv[w * BT + tid], argi[w * BT + tid], bv, bi)) {
+          bv = argv[w * BT + tid];
+          bi = argi[w * BT + tid];
         }
       p.arg_val[(size_t)blockIdx.x * p.B + tid] = bv;
       p.arg_idx[(size_t)blockIdx.x * p.B + tid] = bi;
@@ -780,19 +781,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
       flags[0] = last;
     }
     __syncthreads();
-    if (flags[0] && tid < p.B) {
+    if (flags[0]) {
       __threadfence();
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int c = 0; c < (int)gridDim.x; ++c) {
-        const float v = __ldcg(&p.arg_val[(size_t)c * p.B + tid]);
-        const int ix = __ldcg(&p.arg_idx[(size_t)c * p.B + tid]);
-        if (arg_better(v, ix, bv, bi)) {
-          bv = v;
-          bi = ix;
+      for (int b = warp; b < p.B; b += kWarps) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int c = lane; c < (int)gridDim.x; c += 32) {
+          const float v = __ldcg(&p.arg_val[(size_t)c * p.B + b]);
+          const int ix = __ldcg(&p.arg_idx[(size_t)c * p.B + b]);
+          if (arg_better(v, ix, bv, bi)) {
+            bv = v;
+            bi = ix;
+          }
         }
+        warp_argmax(bv, bi);
+        if (lane == 0) p.argmax_idx[b] = bi;
       }
-      p.argmax_idx[tid] = bi;
     }
   }
 }
