@@ -461,10 +461,11 @@ __device__ void stage_x(const GemvParams& p, const float* stats, uint16_t* xs, i
 // always has at least eight independent fma chains; the partials are folded
 // into acc at the end of the piece.  Rows past the end of the matrix hold
 // stale bytes; their sums are never written out.
-template <int BT, int NMAT, int RT>
+template <int BT, int NMAT, int RT, int UNROLL = 2>
 __device__ __forceinline__ void dot_piece(float (&acc)[2][4][BT], const uint4* st,
                                           const uint4* xs, int nc, int rs, int nchx, int lane) {
   constexpr int CH = NMAT * RT * BT;
+  constexpr int kUnroll = UNROLL;
   constexpr int ACC = CH >= 8 ? 1 : (CH >= 4 ? 2 : 4);
   float part[ACC][NMAT][RT][BT];
 #pragma unroll
@@ -475,7 +476,7 @@ __device__ __forceinline__ void dot_piece(float (&acc)[2][4][BT], const uint4* s
       for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int b = 0; b < BT; ++b) part[a][m][r][b] = 0.f;
-#pragma unroll 2
+#pragma unroll kUnroll
   for (int c = lane; c < nc; c += 32) {
     uint4 w[NMAT][RT];
 #pragma unroll
@@ -653,7 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
 
     // a piece's rows sit PC columns apart, also in a task's shorter last piece
     const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.piece_bytes);
-    dot_piece<BT, NMAT, RT>(acc, st, xs4 + j * ncp, len >> 3, ncp, nchx, lane);
+    // batch 1 in a chain form keeps the loop rolled: shorter code, and one
+    // iteration per 16-byte chunk is far from the issue limit (measured: it
+    // is not at batch 4)
+    dot_piece<BT, NMAT, RT, (F != F_ANY && BT == 1) ? 1 : 2>(acc, st, xs4 + j * ncp, len >> 3, ncp,
+                                                              nchx, lane);
     // Every lane's shared-memory reads of this slot have returned (their
     // values fed the FMAs above, and issue is in order): refill the slot.
     __syncwarp();
