@@ -358,6 +358,14 @@ typedef struct {
                           split; batch <= 4) runs a kernel built for that form
                           alone; 0: every launch runs the general kernel.
                           Both compute the same values.                      */
+  int launch_pdl;      /* 1: the standalone GEMV entry points launch with the
+                          programmatic-dependent-launch attribute, so that a
+                          GEMV following another one on the stream streams
+                          its first weights while the previous one finishes
+                          (every kernel here waits for the previous grid
+                          before reading its activations; its weights and γ
+                          it reads before, so they must not be outputs of
+                          the GEMV launched just before it).  Default 0.     */
 } ws_tuning;
 
 void ws_get_tuning(ws_tuning *t);

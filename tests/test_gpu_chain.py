@@ -231,6 +231,15 @@ def test_step_host_matches_device_run():
     ch.run()
     torch.cuda.synchronize()
     assert np.array_equal(out.numpy(), ch.idx.cpu().numpy())
+    # the same host buffers with new contents (the step's graph reads them anew)
+    h3 = synth.qwen_hidden(SMALL, B, 99)
+    h_host.copy_(torch.from_numpy(h3))
+    out.fill_(-1)
+    ch.chain.step_host(h_host, attn_host, out)
+    ch.h_in.copy_(torch.from_numpy(h3))
+    ch.run()
+    torch.cuda.synchronize()
+    assert np.array_equal(out.numpy(), ch.idx.cpu().numpy())
 
 
 @pytest.mark.parametrize("persistent", [False, True])

@@ -101,6 +101,10 @@ struct ws_chain {
   cudaEvent_t join_ev = nullptr;
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;
+  // ws_chain_step_host's graph: the input copies, the step and the result
+  // copy for one set of host buffers (host_key), captured on first use
+  cudaGraphExec_t host_exec = nullptr;
+  const void* host_key[3] = {nullptr, nullptr, nullptr};
   std::vector<const void*> attn_dev;
   int32_t* idx = nullptr;
   // persistent mode: all ops in one cooperative kernel per step
@@ -114,6 +118,7 @@ struct ws_chain {
 
 static void free_chain_buffers(ws_chain* c) {
   if (c->exec) cudaGraphExecDestroy(c->exec);
+  if (c->host_exec) cudaGraphExecDestroy(c->host_exec);
   if (c->graph) cudaGraphDestroy(c->graph);
   for (cudaEvent_t e : c->fork_ev)
     if (e) cudaEventDestroy(e);
@@ -126,6 +131,7 @@ static void free_chain_buffers(ws_chain* c) {
   for (void* q : c->pp)
     if (q) cudaFree(q);
   c->exec = nullptr;
+  c->host_exec = nullptr;
   c->graph = nullptr;
   c->fork_ev.clear();
   c->join_ev = nullptr;
@@ -448,18 +454,35 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
   return WS_OK;
 }
 
+// Host buffers of one ws_chain_step_host graph.
+struct HostIO {
+  const void* in;
+  const void* attn;
+  void* out;
+};
+
+static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st);
+static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st);
+
+// Capture the ops (with prefetches and trace copies) into *out; with io, the
+// copies of ws_chain_step_host's inputs come first and its result copy last.
 static ws_status capture_graph(ws_chain* c, const std::vector<GemvParams>& ps,
                                const std::vector<std::vector<std::pair<const void*, size_t>>>& reads,
                                const std::vector<ws_prefetch_plan>& plans, bool decoy,
-                               const std::vector<int>& trace, cudaGraphExec_t* out) {
+                               const std::vector<int>& trace, cudaGraphExec_t* out,
+                               const HostIO* io = nullptr) {
   cudaGraph_t g = nullptr;
   cudaStream_t stream = c->cap;
   if (cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
     set_error("cudaStreamBeginCapture failed");
     return WS_ERR_CUDA;
   }
-  const ws_status s = enqueue_ops(c, ps, reads, plans, c->o.distance, decoy, stream, trace,
-                                  c->o.use_pdl != 0);
+  ws_status s = io ? enqueue_host_in(c, *io, stream) : WS_OK;
+  if (s == WS_OK)
+    s = c->persistent ? (launch_persistent(c->persist, stream) == cudaSuccess ? WS_OK : WS_ERR_CUDA)
+                      : enqueue_ops(c, ps, reads, plans, c->o.distance, decoy, stream, trace,
+                                    c->o.use_pdl != 0);
+  if (s == WS_OK && io) s = enqueue_host_out(c, *io, stream);
   const cudaError_t e = cudaStreamEndCapture(stream, &g);
   if (s != WS_OK || e != cudaSuccess) {
     if (g) cudaGraphDestroy(g);
@@ -493,6 +516,52 @@ static std::vector<std::vector<std::pair<const void*, size_t>>> chain_reads(cons
   std::vector<std::vector<std::pair<const void*, size_t>>> r;
   for (const ChainOp& op : c->ops) r.push_back(op.reads);
   return r;
+}
+
+// The copies of one step's inputs from host buffers to the chain's device
+// inputs (Qwen: fp32 h and, if given, the bf16 attention stand-ins of every
+// block; MLP: bf16 x), and of its result back.
+static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st) {
+  const int B = c->o.batch, H = c->o.hidden;
+  if (c->n_mlp)
+    return cudaMemcpyAsync(const_cast<void*>(c->o.x_in), io.in, (size_t)B * H * 2,
+                           cudaMemcpyHostToDevice, st) == cudaSuccess
+               ? WS_OK
+               : WS_ERR_CUDA;
+  if (cudaMemcpyAsync(const_cast<float*>(c->o.h_in), io.in, (size_t)B * H * 4,
+                      cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return WS_ERR_CUDA;
+  if (io.attn && !c->attn_dev.empty()) {
+    const size_t blk = (size_t)B * H * 2;
+    bool contiguous = true;
+    for (size_t l = 0; l < c->attn_dev.size(); ++l)
+      if (static_cast<const char*>(c->attn_dev[l]) !=
+          static_cast<const char*>(c->attn_dev[0]) + l * blk)
+        contiguous = false;
+    if (contiguous)
+      return cudaMemcpyAsync(const_cast<void*>(c->attn_dev[0]), io.attn,
+                             blk * c->attn_dev.size(), cudaMemcpyHostToDevice, st) == cudaSuccess
+                 ? WS_OK
+                 : WS_ERR_CUDA;
+    for (size_t l = 0; l < c->attn_dev.size(); ++l)
+      if (cudaMemcpyAsync(const_cast<void*>(c->attn_dev[l]),
+                          static_cast<const char*>(io.attn) + l * blk, blk,
+                          cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return WS_ERR_CUDA;
+  }
+  return WS_OK;
+}
+
+static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st) {
+  const int B = c->o.batch, H = c->o.hidden;
+  cudaError_t e;
+  if (c->n_mlp)
+    e = cudaMemcpyAsync(io.out, c->o.y_out, (size_t)B * H * 2, cudaMemcpyDeviceToHost, st);
+  else if (c->idx)
+    e = cudaMemcpyAsync(io.out, c->idx, (size_t)B * 4, cudaMemcpyDeviceToHost, st);
+  else
+    e = cudaMemcpyAsync(io.out, c->o.h_out, (size_t)B * H * 4, cudaMemcpyDeviceToHost, st);
+  return e == cudaSuccess ? WS_OK : WS_ERR_CUDA;
 }
 
 extern "C" {
@@ -786,6 +855,10 @@ ws_status ws_chain_capture(ws_chain* c, ws_stream_t stream) {
     cudaGraphExecDestroy(c->exec);
     c->exec = nullptr;
   }
+  if (c->host_exec) {  // recaptured on its next use, with the new ops and plans
+    cudaGraphExecDestroy(c->host_exec);
+    c->host_exec = nullptr;
+  }
   std::vector<ws_prefetch_plan> plans;
   for (const ChainOp& op : c->ops) plans.push_back(c->o.prefetch ? op.plan : kNoPlan);
   std::vector<int> trace;
@@ -879,49 +952,41 @@ ws_status ws_chain_step_host(ws_chain* c, const void* in_host, const void* attn_
     return WS_ERR_STATE;
   }
   cudaStream_t st = (cudaStream_t)stream;
-  const int B = c->o.batch, H = c->o.hidden;
-  if (c->n_mlp) {
-    if (cudaMemcpyAsync(const_cast<void*>(c->o.x_in), in_host, (size_t)B * H * 2,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return WS_ERR_CUDA;
-  } else {
-    if (cudaMemcpyAsync(const_cast<float*>(c->o.h_in), in_host, (size_t)B * H * 4,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return WS_ERR_CUDA;
-    if (attn_host && !c->attn_dev.empty()) {
-      const size_t blk = (size_t)B * H * 2;
-      bool contiguous = true;
-      for (size_t l = 0; l < c->attn_dev.size(); ++l)
-        if (static_cast<const char*>(c->attn_dev[l]) !=
-            static_cast<const char*>(c->attn_dev[0]) + l * blk)
-          contiguous = false;
-      if (contiguous) {
-        if (cudaMemcpyAsync(const_cast<void*>(c->attn_dev[0]), attn_host,
-                            blk * c->attn_dev.size(), cudaMemcpyHostToDevice, st) != cudaSuccess)
-          return WS_ERR_CUDA;
-      } else {
-        for (size_t l = 0; l < c->attn_dev.size(); ++l)
-          if (cudaMemcpyAsync(const_cast<void*>(c->attn_dev[l]),
-                              static_cast<const char*>(attn_host) + l * blk, blk,
-                              cudaMemcpyHostToDevice, st) != cudaSuccess)
-            return WS_ERR_CUDA;
-      }
+  const HostIO io = {in_host, attn_host, out_host};
+  // one graph launch per step: the copies in, the step, the copy out.  It is
+  // captured for these host buffers on first use (pinned memory; a capture
+  // that fails, e.g. on pageable buffers, leaves the copies outside)
+  if (c->host_exec && (c->host_key[0] != in_host || c->host_key[1] != attn_host ||
+                       c->host_key[2] != out_host)) {
+    cudaGraphExecDestroy(c->host_exec);
+    c->host_exec = nullptr;
+  }
+  if (!c->host_exec) {
+    std::vector<ws_prefetch_plan> plans;
+    for (const ChainOp& op : c->ops) plans.push_back(c->o.prefetch ? op.plan : kNoPlan);
+    std::vector<int> trace;
+    if (c->o.h_trace && !c->persistent)
+      for (const ChainOp& op : c->ops) trace.push_back(op.trace_block);
+    if (capture_graph(c, chain_params(c), chain_reads(c), plans, c->o.decoy != 0, trace,
+                      &c->host_exec, &io) == WS_OK) {
+      c->host_key[0] = in_host;
+      c->host_key[1] = attn_host;
+      c->host_key[2] = out_host;
+    } else {
+      c->host_exec = nullptr;
+      cudaGetLastError();
     }
   }
-  ws_status s = ws_chain_run(c, stream);
-  if (s != WS_OK) return s;
-  if (c->n_mlp) {
-    if (cudaMemcpyAsync(out_host, c->o.y_out, (size_t)B * H * 2, cudaMemcpyDeviceToHost, st) !=
-        cudaSuccess)
+  if (c->host_exec) {
+    if (cudaGraphLaunch(c->host_exec, st) != cudaSuccess) {
+      set_error("graph launch failed");
       return WS_ERR_CUDA;
-  } else if (c->idx) {
-    if (cudaMemcpyAsync(out_host, c->idx, (size_t)B * 4, cudaMemcpyDeviceToHost, st) !=
-        cudaSuccess)
-      return WS_ERR_CUDA;
+    }
   } else {
-    if (cudaMemcpyAsync(out_host, c->o.h_out, (size_t)B * H * 4, cudaMemcpyDeviceToHost, st) !=
-        cudaSuccess)
-      return WS_ERR_CUDA;
+    ws_status s = enqueue_host_in(c, io, st);
+    if (s == WS_OK) s = ws_chain_run(c, stream);
+    if (s == WS_OK) s = enqueue_host_out(c, io, st);
+    if (s != WS_OK) return s;
   }
   const cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) {

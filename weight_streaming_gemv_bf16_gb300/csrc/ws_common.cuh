@@ -227,6 +227,7 @@ struct Tuning {
   unsigned long long timeout_ns;
   int l2_ahead;      // persistent chain: pieces per warp prefetched into L2 ahead of the copies
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
+  int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

@@ -33,7 +33,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0};
   return t;
 }
 
@@ -422,7 +422,7 @@ static ws_status plan_bind_launch(GemvParams& p, void* ws, size_t ws_bytes, cuda
       return WS_ERR_ARG;
     }
   }
-  const cudaError_t e = launch_gemv(p, st, false);
+  const cudaError_t e = launch_gemv(p, st, tuning().launch_pdl != 0);
   if (e != cudaSuccess) {
     set_error("launch failed: %s", cudaGetErrorString(e));
     return WS_ERR_CUDA;
@@ -668,6 +668,7 @@ void ws_get_tuning(ws_tuning* t) {
   t->timeout_ns = tu.timeout_ns;
   t->l2_ahead = tu.l2_ahead;
   t->forms = tu.forms;
+  t->launch_pdl = tu.launch_pdl;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
@@ -675,7 +676,8 @@ ws_status ws_set_tuning(const ws_tuning* t) {
       t->force_ksplit < 0 || t->force_rt < 0 || t->force_rt == 3 || t->force_rt > 4 ||
       t->piece_bytes < 0 ||
       t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
-      t->l2_ahead > 64 || t->forms < 0 || t->forms > 1) {
+      t->l2_ahead > 64 || t->forms < 0 || t->forms > 1 || t->launch_pdl < 0 ||
+      t->launch_pdl > 1) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -689,6 +691,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.timeout_ns = t->timeout_ns;
   tu.l2_ahead = t->l2_ahead;
   tu.forms = t->forms;
+  tu.launch_pdl = t->launch_pdl;
   return WS_OK;
 }
 

@@ -120,7 +120,7 @@ extern "C" ws_status ws_gemv_bf16_noalloc(const void* W, const void* x, float* y
       return WS_ERR_CUDA;
     }
   }
-  const cudaError_t e = launch_gemv(p, st, false);
+  const cudaError_t e = launch_gemv(p, st, tuning().launch_pdl != 0);
   if (e != cudaSuccess) {
     set_error("launch failed: %s", cudaGetErrorString(e));
     return WS_ERR_CUDA;
