@@ -154,7 +154,7 @@ def _set_tuning(**kw):
     return base
 
 
-@pytest.mark.parametrize("B", [1, 2, 4])
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 16])
 def test_form_kernels_match_general_kernel_bitwise(B):
     """The per-form kernels (each holding only its op's staging path and
     epilogue) compute exactly what the general kernel computes."""

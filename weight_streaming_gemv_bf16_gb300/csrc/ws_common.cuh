@@ -153,10 +153,11 @@ __host__ __device__ inline void decode_rg(const GemvParams& p, int rg, int& seg,
 
 // One-round RMSNorm staging (fp32 activations, the whole K in one CTA): each
 // thread holds at most kOneRound 8-column chunks of the B x K activations.
-// The chain forms hold min(BT, kOneRound) chunks (K <= 2048 at any BT).
+// The chain forms hold BT chunks up to batch tile 8 (K <= 2048) and 12 at
+// batch tile 16 (K <= 1536).
 constexpr int kOneRound = 4;
 
-__host__ __device__ constexpr int form_round_chunks(int BT) { return BT < kOneRound ? BT : kOneRound; }
+__host__ __device__ constexpr int form_round_chunks(int BT) { return BT <= 8 ? BT : 12; }
 
 __host__ __device__ inline bool one_round_rms(const GemvParams& p, int chunks = kOneRound) {
   return p.prologue == PRO_RMSNORM && p.x_dtype == DT_F32 && p.sc.KS == p.K &&

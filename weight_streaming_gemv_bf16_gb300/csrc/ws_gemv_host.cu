@@ -305,8 +305,10 @@ static GemvKernel pick_kernel(const GemvParams& p) {
   const int BT = p.sc.BT, nmat = p.nmat, RT = p.sc.RT;
   const int F = tuning().forms ? kernel_form(p) : F_ANY;
   if (F != F_ANY) {
-    GemvKernel k = BT == 1 ? pick_form_b1(BT, nmat, RT, F)
-                           : (BT <= 4 ? pick_form_b24(BT, nmat, RT, F) : nullptr);
+    GemvKernel k = BT == 1   ? pick_form_b1(BT, nmat, RT, F)
+                   : BT <= 4 ? pick_form_b24(BT, nmat, RT, F)
+                   : BT == 8 ? pick_form_b8(BT, nmat, RT, F)
+                             : pick_form_b16(BT, nmat, RT, F);
     if (k) return k;
   }
   if (BT <= 2) return pick_kernel_b12(BT, nmat, RT);

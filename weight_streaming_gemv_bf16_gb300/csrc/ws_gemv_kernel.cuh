@@ -814,5 +814,7 @@ GemvKernel pick_kernel_b816(int BT, int nmat, int RT);
 GemvKernel pick_kernel_b16(int BT, int nmat, int RT);
 GemvKernel pick_form_b1(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b24(int BT, int nmat, int RT, int F);
+GemvKernel pick_form_b8(int BT, int nmat, int RT, int F);
+GemvKernel pick_form_b16(int BT, int nmat, int RT, int F);
 
 }  // namespace ws
