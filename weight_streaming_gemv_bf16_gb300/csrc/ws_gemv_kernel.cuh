@@ -230,8 +230,16 @@ __device__ __forceinline__ uint4 normalise8(const GemvParams& p, const float* st
 // Row b[i] and chunk c[i] of the chunks o0 + i * step (i < N) of a [rows][nch]
 // array of 8-column chunks, stepped without a division per chunk (integer
 // division is long code, and these run once per launch with cold caches).
-template <int N>
+template <int N, int BT = 2>
 __device__ __forceinline__ void chunk_coords(int o0, int step, int nch, int (&b)[N], int (&c)[N]) {
+  if constexpr (BT == 1) {  // one row: the callers only use chunks o < nch
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      b[i] = o0 + i * step < nch ? 0 : 1;
+      c[i] = o0 + i * step;
+    }
+    return;
+  }
   int bb = 0, cc = o0;
   while (cc >= nch) { cc -= nch; ++bb; }
 #pragma unroll
@@ -243,10 +251,10 @@ __device__ __forceinline__ void chunk_coords(int o0, int step, int nch, int (&b)
   }
 }
 
-template <int NR>  // chunks per thread
+template <int NR, int BT>  // chunks per thread, batch tile
 __device__ __forceinline__ void gamma_preload(const GemvParams& p, int tid, uint4 (&g)[NR]) {
   int b[NR], c[NR];
-  chunk_coords<NR>(tid, kThreads, p.K >> 3, b, c);
+  chunk_coords<NR, BT>(tid, kThreads, p.K >> 3, b, c);
 #pragma unroll
   for (int i = 0; i < NR; ++i)
     g[i] = b[i] < p.B ? *reinterpret_cast<const uint4*>(p.gamma + c[i] * 8)
@@ -261,7 +269,7 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   float v[NR][8];
   float s[BT];
   int rb[NR], rc[NR];
-  chunk_coords<NR>(tid, kThreads, nch, rb, rc);
+  chunk_coords<NR, BT>(tid, kThreads, nch, rb, rc);
 #pragma unroll
   for (int b = 0; b < BT; ++b) s[b] = 0.f;
 #pragma unroll
@@ -315,7 +323,7 @@ __device__ void stage_copy_bf16(const GemvParams& p, uint16_t* xs, int c0, int n
   for (int base = tid; base < n; base += 8 * kThreads) {
     uint4 t[8];
     int b[8], c[8];
-    chunk_coords<8>(base, kThreads, nch, b, c);
+    chunk_coords<8, BT>(base, kThreads, nch, b, c);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       t[i] = (b[i] < BT && b[i] < p.B) ? __ldcg(src + (size_t)b[i] * rs + c0 + c[i])
@@ -583,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   const bool one_round = FT::rms1 || (!FT::copy_bf16 && one_round_rms(p));
   constexpr int NR = FT::rms1 ? form_round_chunks(BT) : kOneRound;
   uint4 gpre[NR];
-  if (one_round) gamma_preload<NR>(p, tid, gpre);
+  if (one_round) gamma_preload<NR, BT>(p, tid, gpre);
   pdl_launch_dependents();
   pdl_wait();
   if (stamp && tid == 0) stamp[1] = global_ns();
