@@ -90,13 +90,17 @@ def _check_chain(ch, blocks, head, attn, h0, eps=1e-6):
 
 
 SMALL_SPLIT = synth.QwenShape(hidden=256, kv_dim=64, inter=2048, vocab=1000, layers=2)
+# gate/up and the LM head large enough (8 Mi weights) for the tensor-core kernel
+MID = synth.QwenShape(hidden=512, kv_dim=128, inter=8192, vocab=16384, layers=2)
 
 
 @pytest.mark.parametrize("persistent", [False, True])
-@pytest.mark.parametrize("B,shape", [(1, SMALL), (3, SMALL), (16, SMALL), (1, SMALL_SPLIT),
-                                     (4, SMALL_SPLIT)])
+@pytest.mark.parametrize("B,shape", [(1, SMALL), (3, SMALL), (8, SMALL), (12, SMALL), (16, SMALL),
+                                     (1, SMALL_SPLIT), (4, SMALL_SPLIT), (16, SMALL_SPLIT),
+                                     (5, MID), (12, MID), (16, MID)])
 def test_small_chain_matches_oracle(B, shape, persistent):
-    """SMALL_SPLIT's down projection (K = 2048 over 256 rows) is split in K."""
+    """SMALL_SPLIT's down projection (K = 2048 over 256 rows) is split in K.
+    MID's gate/up and LM head run the tensor-core kernels above batch 4."""
     ch, blocks, head, attn, h0 = _make(shape, B, 21, trace=True, keep_qkv=True, logits=True,
                                        persistent=persistent)
     # the persistent kernel takes batch <= 4; larger batches run op by op
@@ -160,7 +164,7 @@ def test_form_kernels_match_general_kernel_bitwise(B):
     epilogue) compute exactly what the general kernel computes."""
     outs = []
     for forms in (0, 1):
-        base = _set_tuning(forms=forms)
+        base = _set_tuning(forms=forms, mma=0)  # the CUDA-core forms
         try:
             ch, *_ = _make(SMALL, B, 24, trace=True, logits=True, keep_qkv=True)
             ch.chain.capture()
@@ -257,6 +261,20 @@ def test_one_full_size_block_matches_oracle(persistent):
     for name, t in zip("qkv", ch.qkv[0]):
         assert_fp32(t.cpu().numpy(), ref[name], what=name)
     assert_fp32(ch.h_out.cpu().numpy(), ref["h"], what="h")
+
+
+@pytest.mark.parametrize("B", [8, 16])
+def test_one_full_size_block_tensor_cores_match_oracle(B):
+    """One full-size block at batch 8 and 16: the tensor-core kernels at the
+    real shapes (Wd's K = 8960 split), then the LM head and its argmax."""
+    shape = synth.QwenShape(layers=1)
+    ch, blocks, head, attn, h0 = _make(shape, B, 3, trace=True, keep_qkv=True, logits=True)
+    ch.chain.capture()
+    ch.run()
+    ch.run()
+    torch.cuda.synchronize()
+    assert wb.device_error() == 0
+    _check_chain(ch, blocks, head, attn, h0)
 
 
 @pytest.mark.parametrize("persistent", [False, True])

@@ -28,6 +28,9 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxSeg = 3;
 constexpr int kMaxStages = 8;  // ring stages per warp
+// tensor-core kernel: the warps of a CTA that stream and multiply (the others
+// only stage): fewer rows in flight per CTA, so that each row's copy is longer
+constexpr int kMmaWarps = 4;
 constexpr int kMaxBatch = 16;
 
 enum Prologue { PRO_NONE = 0, PRO_RMSNORM = 1, PRO_LAYERNORM = 2 };
@@ -67,6 +70,11 @@ struct Sched {
   int off_bar, off_flags, off_stats, off_red, off_arg, off_xs, off_ring;
   int off_res;   // residual rows of the CTA in shared memory (0: read at the epilogue)
   int res_rows;  // rows reserved there per batch row
+  // tensor-core kernel (mma = 1): tasks of 16 rows, piece rows prow bytes
+  // apart in the ring and activation rows xrs 16-byte chunks apart in shared
+  // memory (both odd multiples of 16 bytes: ldmatrix rows in distinct banks)
+  int mma, prow, xrs;
+  int form;      // its chain form (F_ANY for none)
 };
 
 struct alignas(16) GemvParams {
@@ -229,6 +237,7 @@ struct Tuning {
   int l2_ahead;      // persistent chain: pieces per warp prefetched into L2 ahead of the copies
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
   int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
+  int mma;           // 1: chain forms at batch tiles 8 and 16 run on the tensor cores (mma.sync)
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

@@ -33,7 +33,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 1};
   return t;
 }
 
@@ -86,6 +86,124 @@ static int row_groups(GemvParams& p, int RT) {
   return RG;
 }
 
+static constexpr int kMmaTaskRows = 16;  // one m16 tile per warp task
+
+// The chain form of a launch for the tensor-core kernel (any K split), or
+// F_ANY.  The one-round RMSNorm reads the whole K: B x K / 8 chunks within
+// form_round_chunks(BT) per thread.
+static int mma_form(const GemvParams& p, int BT) {
+  if (p.prologue == PRO_RMSNORM && p.x_dtype == DT_F32 &&
+      p.B * (p.K >> 3) <= form_round_chunks(BT) * kThreads) {
+    if (p.epilogue == EPI_F32) return F_RMS_F32;
+    if (p.epilogue == EPI_SWIGLU && p.nmat == 2 && p.nseg == 1) return F_RMS_SWIGLU;
+    if (p.epilogue == EPI_ARGMAX && p.nseg == 1) return F_RMS_ARGMAX;
+    return F_ANY;
+  }
+  if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_RESID && p.nseg == 1)
+    return F_BF16_RESID;
+  return F_ANY;
+}
+
+// Schedule for the tensor-core kernel (batch tiles 8 and 16, chain forms,
+// at least 8 Mi weights): 16-row tasks; a K split until the tasks cover most
+// streaming warps (none for the argmax, which needs whole rows) and the
+// split's activations fit; pieces of about 16 KB; rows an odd number of
+// 16-byte units apart.  Smaller ops (QKV, Wo of a 1.5B model) keep the
+// CUDA-core kernels: measured at batch 16, 16-row tasks leave too few tasks
+// and too long a split-K tail for them (Wo 15.9 vs 6.9 us) while gate/up, Wd
+// and the LM head run faster (24 vs 37, 21 vs 31, 105 vs 201 us).  False when
+// the launch does not qualify.
+static bool plan_gemv_mma(GemvParams& p, int force_S, int grid_target) {
+  const int BT = batch_template(p.B);
+  const int K = p.K, nmat = p.nmat;
+  if (BT < 8 || K % 16 != 0) return false;
+  long long weights = 0;
+  for (int s = 0; s < p.nseg; ++s) weights += (long long)p.seg[s].M * K * nmat;
+  if (weights < (8ll << 20)) return false;
+  const int F = mma_form(p, BT);
+  if (F == F_ANY) return false;
+  Sched sc;
+  memset(&sc, 0, sizeof sc);
+  sc.BT = BT;
+  sc.RT = kMmaTaskRows;
+  const int RG = row_groups(p, kMmaTaskRows);
+  sc.RG = RG;
+  const int warps_total = grid_target * kMmaWarps;
+  auto valid = [&](int S) { return S >= 1 && K % (16 * S) == 0; };
+  auto xs_bytes = [&](int S) { return BT * (((K / S) >> 3) | 1) * 16; };
+  int S = 1;
+  if (F == F_RMS_ARGMAX || force_S < 0) {
+    if (xs_bytes(1) > kXsMax) return false;
+  } else if (force_S > 0) {
+    S = force_S;
+    if (!valid(S) || xs_bytes(S) > kXsMax) return false;
+  } else {
+    while (S <= 64 && !(valid(S) && xs_bytes(S) <= kXsMax)) ++S;
+    if (S > 64) return false;
+    for (int s = S + 1; s <= 32 && RG * S < (warps_total * 3) / 4; ++s)
+      if (valid(s) && K / s >= 128) S = s;
+  }
+  sc.S = S;
+  sc.KS = K / S;
+  sc.xrs = (sc.KS >> 3) | 1;
+  // pieces of about 16 KB over all matrices, 16-column multiples
+  int pc = 16384 / (nmat * kMmaTaskRows * 2);
+  if (pc >= sc.KS) {
+    sc.PC = sc.KS;
+    sc.NP = 1;
+  } else {
+    sc.NP = (sc.KS + pc - 1) / pc;
+    sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 16);
+    sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
+  }
+  int u = (sc.PC * 2 + 15) / 16;
+  if (u % 2 == 0) ++u;
+  sc.prow = u * 16;
+  sc.piece_bytes = align_up(nmat * kMmaTaskRows * sc.prow, 128);
+
+  int off = 0;
+  sc.off_bar = off;
+  off += kWarps * kMaxStages * 8;
+  sc.off_flags = off;
+  off += 128;
+  sc.off_stats = off;
+  off += align_up(sc.BT * 2 * 4, 16);
+  sc.off_red = off;
+  off += align_up((kWarps + 1) * sc.BT * 4, 16);
+  sc.off_arg = off;
+  off += kWarps * 32 * 8;
+  sc.off_xs = align_up(off, 128);
+  off = sc.off_xs + align_up(xs_bytes(S), 128);
+  sc.off_ring = align_up(off, 128);
+  int Gs = grid_target / S;
+  if (Gs < 1) Gs = 1;
+  if (Gs > RG) Gs = RG;
+  if ((unsigned long long)Gs * (unsigned long long)RG >= (1ull << 32)) return false;
+  sc.Gs = Gs;
+  sc.grid = S * Gs;
+  // residual rows of the CTA, read ahead (unsplit K only: a split's last
+  // CTA reads them at the epilogue)
+  const int res_bytes = (p.epilogue == EPI_RESID && S == 1)
+                            ? (RG + Gs - 1) / Gs * kMmaTaskRows * BT * 4
+                            : 0;
+  int NSW = (kSmemMax - sc.off_ring - res_bytes - 16) / (kMmaWarps * sc.piece_bytes);
+  if (NSW > kMaxStages) NSW = kMaxStages;
+  if (NSW < 2) return false;
+  sc.NSW = NSW;
+  sc.smem_bytes = sc.off_ring + kMmaWarps * NSW * sc.piece_bytes;
+  if (res_bytes) {
+    sc.off_res = align_up(sc.smem_bytes, 16);
+    sc.res_rows = (RG + Gs - 1) / Gs * kMmaTaskRows;
+    sc.smem_bytes = sc.off_res + res_bytes;
+  }
+  sc.mma = 1;
+  sc.form = F;
+  p.sc = sc;
+  p.M_total = 0;
+  for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
+  return true;
+}
+
 // Choose the schedule.  force_S > 0 fixes the K split; force_S == 0 lets the
 // heuristic split skinny shapes; force_S < 0 forbids splitting.
 bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
@@ -93,6 +211,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   const int nsm = device_sm_count();
   const int grid_target = tu.grid_cap > 0 ? tu.grid_cap : nsm;
   const int warps_total = grid_target * kWarps;
+  if (tu.mma && tu.forms && plan_gemv_mma(p, force_S, grid_target)) return true;
   Sched sc;
   memset(&sc, 0, sizeof sc);
   sc.BT = batch_template(p.B);
@@ -299,10 +418,12 @@ bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes) {
   return true;
 }
 
-// The kernel of a planned launch: the one of its chain form where one is
-// built for its batch tile, else the general one.
+// The kernel of a planned launch: the tensor-core one of its chain form when
+// planned for it, else the CUDA-core one of its chain form where one is built
+// for its batch tile, else the general one.
 static GemvKernel pick_kernel(const GemvParams& p) {
   const int BT = p.sc.BT, nmat = p.nmat, RT = p.sc.RT;
+  if (p.sc.mma) return pick_kernel_mma(BT, nmat, p.sc.form);
   const int F = tuning().forms ? kernel_form(p) : F_ANY;
   if (F != F_ANY) {
     GemvKernel k = BT == 1   ? pick_form_b1(BT, nmat, RT, F)
@@ -620,17 +741,30 @@ ws_status ws_lmhead_argmax(const void* h, int h_dtype, const void* gamma, const 
   return plan_bind_launch(p, workspace, workspace_bytes, (cudaStream_t)stream, false);
 }
 
-static bool plan_for_op(int op, int M, int K, int B, GemvParams& p) {
+// variant: 0 plain bf16 x; 1 RMSNorm of fp32 x; 2 bf16 x with a residual
+// epilogue (the entry points an op id covers plan differently: the tensor-
+// core schedule takes the chain forms only)
+static bool plan_for_op(int op, int M, int K, int B, GemvParams& p, int variant = 0) {
   init_gemv_params(p, K, B);
   p.nseg = 1;
   p.seg[0].M = M;
   p.epilogue = EPI_F32;
+  p.x_dtype = DT_BF16;
+  if (variant == 1) {
+    p.prologue = PRO_RMSNORM;
+    p.x_dtype = DT_F32;
+  } else if (variant == 2) {
+    p.epilogue = EPI_RESID;
+  }
   if (op == WS_OP_SWIGLU_GEMV) {
     p.nmat = 2;
     p.epilogue = EPI_SWIGLU;
   } else if (op == WS_OP_LMHEAD_ARGMAX) {
     p.epilogue = EPI_ARGMAX;
   } else if (op != WS_OP_GEMV && op != WS_OP_QKV_GEMV) {
+    return false;
+  }
+  if (variant == 2 && op != WS_OP_GEMV) {
     return false;
   }
   char why[256];
@@ -640,9 +774,17 @@ static bool plan_for_op(int op, int M, int K, int B, GemvParams& p) {
 size_t ws_workspace_bytes(int op, int M, int K, int B) {
   if (op == WS_OP_ARGMAX_ROWS) return argmax_rows_workspace(M, K);
   if (M <= 0 || K <= 0 || K % 8 != 0 || B < 1 || B > kMaxBatch) return 0;
-  GemvParams p;
-  if (!plan_for_op(op, M, K, B, p)) return 0;
-  return workspace_layout(p, nullptr, nullptr, nullptr, nullptr, nullptr);
+  // the largest workspace of the schedules the op id's entry points can take
+  size_t need = 0;
+  bool any = false;
+  for (int variant = 0; variant < 3; ++variant) {
+    GemvParams p;
+    if (!plan_for_op(op, M, K, B, p, variant)) continue;
+    any = true;
+    const size_t w = workspace_layout(p, nullptr, nullptr, nullptr, nullptr, nullptr);
+    need = w > need ? w : need;
+  }
+  return any ? need : 0;
 }
 
 int ws_device_error(int reset) {
@@ -671,6 +813,7 @@ void ws_get_tuning(ws_tuning* t) {
   t->l2_ahead = tu.l2_ahead;
   t->forms = tu.forms;
   t->launch_pdl = tu.launch_pdl;
+  t->mma = tu.mma;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
@@ -679,7 +822,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
       t->piece_bytes < 0 ||
       t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
       t->l2_ahead > 64 || t->forms < 0 || t->forms > 1 || t->launch_pdl < 0 ||
-      t->launch_pdl > 1) {
+      t->launch_pdl > 1 || t->mma < 0 || t->mma > 1) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -694,6 +837,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.l2_ahead = t->l2_ahead;
   tu.forms = t->forms;
   tu.launch_pdl = t->launch_pdl;
+  tu.mma = t->mma;
   return WS_OK;
 }
 

@@ -518,6 +518,33 @@ __device__ __forceinline__ void dot_piece(float (&acc)[2][4][BT], const uint4* s
       }
 }
 
+// The last split of a row group: the sums over all splits, in split order,
+// of the outputs o0 + 32 u (u < U) of this lane, n_out outputs in all.  The
+// loads of U outputs and two splits are in flight together (the partials
+// come from L2, one round trip each).
+template <int NMAT, int U>
+__device__ __forceinline__ void split_sums(const GemvParams& p, int rowg, int n_out, int o0,
+                                           float (&v)[NMAT][U], int (&rr)[U], int (&bb)[U]) {
+  bool ok[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int o = o0 + 32 * u;
+    ok[u] = o < n_out;
+    rr[u] = o / p.B;
+    bb[u] = o - rr[u] * p.B;
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) v[m][u] = 0.f;
+  }
+#pragma unroll 2
+  for (int s = 0; s < p.sc.S; ++s)
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (ok[u])
+          v[m][u] += __ldcg(&p.part[((size_t)(s * NMAT + m) * p.B + bb[u]) * p.M_total + rowg + rr[u]]);
+}
+
 template <int NMAT, int RT, bool ONE_SEG>
 __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, int slot, int k0,
                                             uint8_t* ring, uint64_t* full, uint64_t pol) {
@@ -715,21 +742,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          for (int o = lane; o < rows * p.B; o += 32) {
-            const int rr = o / p.B;
-            const int b = o - rr * p.B;
-            float v[NMAT];
+          constexpr int U = 4;
+          for (int o0 = lane; o0 < rows * p.B; o0 += 32 * U) {
+            float v[NMAT][U];
+            int rr[U], bb[U];
+            split_sums<NMAT, U>(p, rowg, rows * p.B, o0, v, rr, bb);
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-              float t = 0.f;
-              for (int s = 0; s < sc.S; ++s)
-                t += __ldcg(&p.part[((size_t)(s * NMAT + m) * p.B + b) * p.M_total + rowg + rr]);
-              v[m] = t;
-            }
-            float dv = -INFINITY;
-            int di = 0x7fffffff;
-            apply_epilogue<EPI>(p, seg, row0 + rr, b, v[0], v[NMAT - 1], dv, di, res_s, res_row0,
-                           sc.res_rows);
+            for (int u = 0; u < U; ++u)
+              if (o0 + 32 * u < rows * p.B) {
+                float dv = -INFINITY;
+                int di = 0x7fffffff;
+                apply_epilogue<EPI>(p, seg, row0 + rr[u], bb[u], v[0][u], v[NMAT - 1][u], dv, di,
+                                    res_s, res_row0, sc.res_rows);
+              }
           }
         }
       }
@@ -824,5 +849,6 @@ GemvKernel pick_form_b1(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b24(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b8(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b16(int BT, int nmat, int RT, int F);
+GemvKernel pick_kernel_mma(int BT, int nmat, int F);
 
 }  // namespace ws
