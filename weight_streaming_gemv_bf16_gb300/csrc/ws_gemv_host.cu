@@ -107,7 +107,7 @@ static int mma_form(const GemvParams& p, int BT) {
 // Schedule for the tensor-core kernel (batch tiles 8 and 16, chain forms,
 // at least 8 Mi weights): 16-row tasks; a K split until the tasks cover most
 // streaming warps (none for the argmax, which needs whole rows) and the
-// split's activations fit; pieces of about 16 KB; rows an odd number of
+// split's activations fit; pieces of 8-24 KB; rows an odd number of
 // 16-byte units apart.  Smaller ops (QKV, Wo of a 1.5B model) keep the
 // CUDA-core kernels: measured at batch 16, 16-row tasks leave too few tasks
 // and too long a split-K tail for them (Wo 15.9 vs 6.9 us) while gate/up, Wd
@@ -146,21 +146,6 @@ static bool plan_gemv_mma(GemvParams& p, int force_S, int grid_target) {
   sc.S = S;
   sc.KS = K / S;
   sc.xrs = (sc.KS >> 3) | 1;
-  // pieces of about 16 KB over all matrices, 16-column multiples
-  int pc = 16384 / (nmat * kMmaTaskRows * 2);
-  if (pc >= sc.KS) {
-    sc.PC = sc.KS;
-    sc.NP = 1;
-  } else {
-    sc.NP = (sc.KS + pc - 1) / pc;
-    sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 16);
-    sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
-  }
-  int u = (sc.PC * 2 + 15) / 16;
-  if (u % 2 == 0) ++u;
-  sc.prow = u * 16;
-  sc.piece_bytes = align_up(nmat * kMmaTaskRows * sc.prow, 128);
-
   int off = 0;
   sc.off_bar = off;
   off += kWarps * kMaxStages * 8;
@@ -186,7 +171,29 @@ static bool plan_gemv_mma(GemvParams& p, int force_S, int grid_target) {
   const int res_bytes = (p.epilogue == EPI_RESID && S == 1)
                             ? (RG + Gs - 1) / Gs * kMmaTaskRows * BT * 4
                             : 0;
-  int NSW = (kSmemMax - sc.off_ring - res_bytes - 16) / (kMmaWarps * sc.piece_bytes);
+  // pieces (16-column multiples) of about 24 KB over all matrices at batch
+  // tile 8 and 16 KB at 16, else smaller, with two ring stages per streaming
+  // warp (measured on the chain: batch 8 24 KB 1249 vs 16 KB 1387 vs 8 KB
+  // 1845 us; batch 16 16 KB 1873 vs 24 KB 1909 us)
+  int NSW = 0;
+  for (const int target : {24576, 16384, 8192}) {
+    if (BT == 16 && target > 16384) continue;
+    const int pc = target / (nmat * kMmaTaskRows * 2);
+    if (pc >= sc.KS) {
+      sc.PC = sc.KS;
+      sc.NP = 1;
+    } else {
+      sc.NP = (sc.KS + pc - 1) / pc;
+      sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 16);
+      sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
+    }
+    int u = (sc.PC * 2 + 15) / 16;
+    if (u % 2 == 0) ++u;
+    sc.prow = u * 16;
+    sc.piece_bytes = align_up(nmat * kMmaTaskRows * sc.prow, 128);
+    NSW = (kSmemMax - sc.off_ring - res_bytes - 16) / (kMmaWarps * sc.piece_bytes);
+    if (NSW >= 2) break;
+  }
   if (NSW > kMaxStages) NSW = kMaxStages;
   if (NSW < 2) return false;
   sc.NSW = NSW;
