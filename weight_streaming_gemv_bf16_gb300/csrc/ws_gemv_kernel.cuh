@@ -28,7 +28,9 @@
 //  * the activations are normalised once per CTA (RMSNorm or LayerNorm
 //    prologue in fp32, all threads, vector loads) and rounded once to bf16
 //    into shared memory.
-// There are no tensor cores here: at batch <= 16 this is a vector product.
+// This kernel multiplies on CUDA cores: at batch <= 4 the product is bound by
+// HBM.  From batch 5 the chain forms with at least 8 Mi weights run the
+// warp-level tensor-core kernel of ws_gemv_mma.cuh instead.
 #pragma once
 
 #include <cuda_bf16.h>
