@@ -48,7 +48,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--mode", choices=["chain", "kernel"], default="chain")
+    ap.add_argument("--mode", choices=["chain", "kernel", "sweep"], default="chain",
+                    help="chain: the decode step (the metric); kernel: gate/up alone (profiler "
+                         "captures); sweep: the batch GEMV sweep, fp16 RMSNorm and the "
+                         "LayerNorm block chain, one JSON line")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
                     help="graph: one launch per op, PDL edges, one CUDA graph; persistent: "
                          "the whole step as one cooperative kernel")
@@ -504,12 +507,121 @@ def run_kernel_only(args):
     return 0
 
 
+def run_sweep(args):
+    """The standalone workloads of the batch sweep and of the LayerNorm block
+    chain, one JSON line: each GEMV shape of the decode step at batch 1..16
+    (launched back to back with programmatic dependent launch over rotating
+    weight copies larger than L2, one CUDA graph, CUDA events around it), the
+    fp16 RMSNorm on [R, 896] rows, and the 72-block LayerNorm + GEMV + bias +
+    GELU chain (768 x 768) at batch 4 and 16."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+    from weight_streaming_gemv_bf16_gb300 import synth
+    torch.cuda.set_device(0)
+    gen = torch.Generator(device="cuda").manual_seed(args.seed)
+    st = torch.cuda.current_stream()
+
+    def graph_time(fn, n_inner, reps=10):
+        side = torch.cuda.Stream()
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            fn(side)  # plans, workspaces and kernel attributes before capture
+        st.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / (reps * n_inner)
+
+    base = wb.get_tuning()
+    t = wb.Tuning()
+    for f, _ in wb.Tuning._fields_:
+        setattr(t, f, getattr(base, f))
+    t.launch_pdl = 1
+    wb.set_tuning(t)
+    gemv = []
+    try:
+        for M, K in [(8960, 1536), (1536, 8960), (256, 1536), (151936, 1536)]:
+            ncopy = max(2, -(-(256 << 20) // (M * K * 2)))
+            Ws = [(torch.randn((M, K), device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+                  for _ in range(ncopy)]
+            for B in (1, 2, 4, 8, 16):
+                x = torch.randn((B, K), device="cuda", generator=gen).to(torch.bfloat16)
+                y = torch.empty((B, M), device="cuda")
+                nws = wb.workspace_bytes(wb.OP_GEMV, M, K, B)
+                ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+
+                def fn(s, Ws=Ws, x=x, y=y, ws=ws):
+                    for W in Ws:
+                        wb.gemv_bf16(W, x, y, workspace=ws, stream=s)
+                dur = graph_time(fn, len(Ws))
+                nbytes = M * K * 2 + B * K * 2 + B * M * 4
+                gemv.append({"M": M, "K": K, "B": B, "us": round(dur * 1e6, 2),
+                             "gbs": round(nbytes / dur / 1e9, 1)})
+            del Ws
+    finally:
+        wb.set_tuning(base)
+    rms = []
+    N = 896
+    for R in (1, 128, 4096):
+        xs = [torch.randn((R, N), device="cuda", generator=gen).to(torch.float16) for _ in range(8)]
+        gmm = (torch.rand((N,), device="cuda", generator=gen) + 0.5).to(torch.float16)
+        ys = [torch.empty_like(v) for v in xs]
+
+        def fn(s, xs=xs, ys=ys, gmm=gmm):
+            for v, o in zip(xs, ys):
+                wb.rmsnorm(v, gmm, o, 1e-6, stream=s)
+        dur = graph_time(fn, len(xs))
+        rms.append({"R": R, "N": N, "us": round(dur * 1e6, 2),
+                    "gbs": round(2 * R * N * 2 / dur / 1e9, 1)})
+    mlp = []
+    sh = synth.MlpShape()
+    hb = [synth.mlp_block_weights(sh, args.seed, l) for l in range(sh.blocks)]
+    db = [{k: to_dev(v, torch) for k, v in b.items()} for b in hb]
+    for B in (4, 16):
+        x_in = to_dev(synth.mlp_input(sh, B, args.seed), torch)
+        ch = wc.mlp_chain(db, x_in, eps=sh.eps)
+        ch.chain.capture()
+        for _ in range(5):
+            ch.run(st)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 200
+        e0.record(st)
+        for _ in range(reps):
+            ch.run(st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        dur = e0.elapsed_time(e1) * 1e-3 / reps
+        nbytes = sh.blocks * sh.block_bytes()
+        mlp.append({"B": B, "blocks": sh.blocks, "us_per_step": round(dur * 1e6, 2),
+                    "gbs": round(nbytes / dur / 1e9, 1)})
+        ch.chain.close()
+    print(json.dumps({"mode": "sweep", "gemv_back_to_back": gemv, "rmsnorm_fp16": rms,
+                      "mlp_chain": mlp}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.mode == "kernel":
         return run_kernel_only(args)
+    if args.mode == "sweep":
+        return run_sweep(args)
     return run_ours(args)
 
 

@@ -366,12 +366,13 @@ typedef struct {
                           before reading its activations; its weights and γ
                           it reads before, so they must not be outputs of
                           the GEMV launched just before it).  Default 0.     */
-  int mma;             /* 1 (default): launches of a chain form (with forms
-                          = 1) at batch 5..16 run a warp-level tensor-core
-                          kernel (bf16 m16n8k16 MMA, fp32 accumulation, 16-row
-                          tasks); 0: the CUDA-core kernels.  Sums are ordered
-                          differently; both stay within the fp32 tolerance
-                          of the oracle.                                     */
+  int mma;             /* 1: launches of a chain form (with forms = 1) with
+                          at least 8 Mi weights at batch 5..16 run a warp-
+                          level tensor-core kernel (bf16 m16n8k16 MMA, fp32
+                          accumulation, 16-row tasks); 0 (default): every
+                          launch runs on CUDA cores, the vector-product
+                          design.  Sums are ordered differently; both stay
+                          within the fp32 tolerance of the oracle.           */
 } ws_tuning;
 
 void ws_get_tuning(ws_tuning *t);

@@ -90,7 +90,8 @@ def _check_chain(ch, blocks, head, attn, h0, eps=1e-6):
 
 
 SMALL_SPLIT = synth.QwenShape(hidden=256, kv_dim=64, inter=2048, vocab=1000, layers=2)
-# gate/up and the LM head large enough (8 Mi weights) for the tensor-core kernel
+# gate/up and the LM head large enough (8 Mi weights) for the optional
+# tensor-core kernel
 MID = synth.QwenShape(hidden=512, kv_dim=128, inter=8192, vocab=16384, layers=2)
 
 
@@ -99,8 +100,7 @@ MID = synth.QwenShape(hidden=512, kv_dim=128, inter=8192, vocab=16384, layers=2)
                                      (1, SMALL_SPLIT), (4, SMALL_SPLIT), (16, SMALL_SPLIT),
                                      (5, MID), (12, MID), (16, MID)])
 def test_small_chain_matches_oracle(B, shape, persistent):
-    """SMALL_SPLIT's down projection (K = 2048 over 256 rows) is split in K.
-    MID's gate/up and LM head run the tensor-core kernels above batch 4."""
+    """SMALL_SPLIT's down projection (K = 2048 over 256 rows) is split in K."""
     ch, blocks, head, attn, h0 = _make(shape, B, 21, trace=True, keep_qkv=True, logits=True,
                                        persistent=persistent)
     # the persistent kernel takes batch <= 4; larger batches run op by op
@@ -265,15 +265,35 @@ def test_one_full_size_block_matches_oracle(persistent):
 
 @pytest.mark.parametrize("B", [8, 16])
 def test_one_full_size_block_tensor_cores_match_oracle(B):
-    """One full-size block at batch 8 and 16: the tensor-core kernels at the
-    real shapes (Wd's K = 8960 split), then the LM head and its argmax."""
-    shape = synth.QwenShape(layers=1)
-    ch, blocks, head, attn, h0 = _make(shape, B, 3, trace=True, keep_qkv=True, logits=True)
-    ch.chain.capture()
-    ch.run()
-    ch.run()
-    torch.cuda.synchronize()
+    """One full-size block at batch 8 and 16 with the optional tensor-core
+    kernel (gate/up, Wd with its K = 8960 split, the LM head and its
+    argmax), against the oracle."""
+    base = _set_tuning(mma=1)
+    try:
+        shape = synth.QwenShape(layers=1)
+        ch, blocks, head, attn, h0 = _make(shape, B, 3, trace=True, keep_qkv=True, logits=True)
+        ch.chain.capture()
+        ch.run()
+        ch.run()
+        torch.cuda.synchronize()
+    finally:
+        wb.set_tuning(base)
     assert wb.device_error() == 0
+    _check_chain(ch, blocks, head, attn, h0)
+
+
+@pytest.mark.parametrize("B", [5, 12, 16])
+def test_mid_chain_tensor_cores_match_oracle(B):
+    """The optional tensor-core kernel on MID (gate/up and the LM head large
+    enough for it), batch tiles 8 and 16 with padded batch rows."""
+    base = _set_tuning(mma=1)
+    try:
+        ch, blocks, head, attn, h0 = _make(MID, B, 21, trace=True, keep_qkv=True, logits=True)
+        ch.chain.capture()
+        ch.run()
+        torch.cuda.synchronize()
+    finally:
+        wb.set_tuning(base)
     _check_chain(ch, blocks, head, attn, h0)
 
 

@@ -183,37 +183,59 @@ enum KernelForm {
   F_RMS_SWIGLU = 2,  // one-round RMSNorm; SwiGLU of a gate/up pair (bf16 out)
   F_RMS_ARGMAX = 3,  // one-round RMSNorm; logits and argmax (LM head)
   F_BF16_RESID = 4,  // bf16 x without prologue; fp32 residual add (Wo, Wd)
-  kNumForms = 5
+  F_BF16_F32 = 5,    // bf16 x without prologue; fp32 outputs (the plain GEMV)
+  F_LN_GELU = 6,     // one-round LayerNorm of bf16 x; bias + GELU (the MLP block), K split allowed
+  kNumForms = 7
 };
 
 template <int F>
 struct FormTraits {
   static constexpr int epi = -1;  // epilogue, or -1: read from the parameters
   static constexpr bool rms1 = false, copy_bf16 = false, no_split = false, one_seg = false;
+  static constexpr bool ln1 = false;  // one-round LayerNorm staging
 };
 template <>
 struct FormTraits<F_RMS_F32> {
   static constexpr int epi = EPI_F32;
   static constexpr bool rms1 = true, copy_bf16 = false, no_split = true, one_seg = false;
+  static constexpr bool ln1 = false;
 };
 template <>
 struct FormTraits<F_RMS_SWIGLU> {
   static constexpr int epi = EPI_SWIGLU;
   static constexpr bool rms1 = true, copy_bf16 = false, no_split = true, one_seg = true;
+  static constexpr bool ln1 = false;
 };
 template <>
 struct FormTraits<F_RMS_ARGMAX> {
   static constexpr int epi = EPI_ARGMAX;
   static constexpr bool rms1 = true, copy_bf16 = false, no_split = true, one_seg = true;
+  static constexpr bool ln1 = false;
 };
 template <>
 struct FormTraits<F_BF16_RESID> {
   static constexpr int epi = EPI_RESID;
   static constexpr bool rms1 = false, copy_bf16 = true, no_split = true, one_seg = true;
+  static constexpr bool ln1 = false;
+};
+template <>
+struct FormTraits<F_BF16_F32> {
+  static constexpr int epi = EPI_F32;
+  static constexpr bool rms1 = false, copy_bf16 = true, no_split = true, one_seg = true;
+  static constexpr bool ln1 = false;
+};
+template <>
+struct FormTraits<F_LN_GELU> {
+  static constexpr int epi = EPI_BIAS_GELU;
+  static constexpr bool rms1 = false, copy_bf16 = false, no_split = false, one_seg = true;
+  static constexpr bool ln1 = true;
 };
 
 // The form a planned launch can run as.
 inline int kernel_form(const GemvParams& p) {
+  if (p.prologue == PRO_LAYERNORM && p.x_dtype == DT_BF16 && p.epilogue == EPI_BIAS_GELU &&
+      p.nseg == 1 && p.B * (p.K >> 3) <= form_round_chunks(p.sc.BT) * kThreads)
+    return F_LN_GELU;
   if (p.sc.S != 1) return F_ANY;
   if (one_round_rms(p, form_round_chunks(p.sc.BT))) {
     if (p.epilogue == EPI_F32) return F_RMS_F32;
@@ -223,6 +245,8 @@ inline int kernel_form(const GemvParams& p) {
   }
   if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_RESID && p.nseg == 1)
     return F_BF16_RESID;
+  if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_F32 && p.nseg == 1)
+    return F_BF16_F32;
   return F_ANY;
 }
 
@@ -237,7 +261,7 @@ struct Tuning {
   int l2_ahead;      // persistent chain: pieces per warp prefetched into L2 ahead of the copies
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
   int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
-  int mma;           // 1: chain forms at batch tiles 8 and 16 run on the tensor cores (mma.sync)
+  int mma;           // 1: large chain-form ops at batch tiles 8 and 16 run on tensor cores (mma.sync)
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

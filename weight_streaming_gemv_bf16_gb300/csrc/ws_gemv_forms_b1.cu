@@ -8,7 +8,8 @@ namespace ws {
   if (BT == bt && nmat == nm && RT == rt && F == f) return (GemvKernel)k_stream_gemv<bt, nm, rt, f>;
 #define WS_FORMS(bt, rt)                                                           \
   WS_FORM(bt, 1, rt, F_RMS_F32) WS_FORM(bt, 2, rt, F_RMS_SWIGLU)                  \
-  WS_FORM(bt, 1, rt, F_RMS_ARGMAX) WS_FORM(bt, 1, rt, F_BF16_RESID)
+  WS_FORM(bt, 1, rt, F_RMS_ARGMAX) WS_FORM(bt, 1, rt, F_BF16_RESID)                \
+  WS_FORM(bt, 1, rt, F_BF16_F32) WS_FORM(bt, 1, rt, F_LN_GELU)
 
 GemvKernel pick_form_b1(int BT, int nmat, int RT, int F) {
   WS_FORMS(1, 1) WS_FORMS(1, 2) WS_FORMS(1, 4)

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
+#include <set>
 
 #include "wsgemv.h"
 #include "ws_common.cuh"
@@ -33,7 +34,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 1};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 0};
   return t;
 }
 
@@ -101,6 +102,8 @@ static int mma_form(const GemvParams& p, int BT) {
   }
   if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_RESID && p.nseg == 1)
     return F_BF16_RESID;
+  if (p.prologue == PRO_NONE && p.x_dtype == DT_BF16 && p.epilogue == EPI_F32 && p.nseg == 1)
+    return F_BF16_F32;
   return F_ANY;
 }
 
@@ -246,9 +249,18 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
     };
     double best = load(1);
     for (int rt = 2; rt <= rt_max; rt *= 2) best = load(rt) < best ? load(rt) : best;
+    // candidates whose row groups cover half the warps without a K split
+    // first: a split's partial sums and ticket cost an op about 2 us (the
+    // 768 x 768 LayerNorm block at batch 16: 1 row per task and no split,
+    // 811 vs 1009 us per 72-block chain)
+    const bool allow_split = force_S == 0 && tu.force_ksplit == 0;
+    bool any_unsplit = false;
+    for (int rt = 1; rt <= rt_max; rt *= 2)
+      if (load(rt) <= best * 1.1 && row_groups(p, rt) >= warps_total / 2) any_unsplit = true;
     int pick = 0, pick_whole = 0;
     for (int rt = 1; rt <= rt_max; rt *= 2) {
       if (load(rt) > best * 1.1) continue;
+      if (allow_split && any_unsplit && row_groups(p, rt) < warps_total / 2) continue;
       pick = rt;
       if ((long)nmat * rt * K * 2 <= target_bytes) pick_whole = rt;
     }
@@ -445,23 +457,21 @@ static GemvKernel pick_kernel(const GemvParams& p) {
   return pick_kernel_b16(BT, nmat, RT);
 }
 
+// The dynamic shared-memory limit of a kernel, raised once per device (a set
+// of (device, kernel) pairs: the library holds a few hundred instantiations).
 static bool ensure_smem_attr(GemvKernel k) {
   static std::mutex mu;
-  static unsigned long long done[64][64] = {{0}};
+  static std::set<std::pair<int, uintptr_t>> done;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lk(mu);
-  for (int i = 0; i < 64; ++i) {
-    if (done[dev][i] == (unsigned long long)(uintptr_t)k) return true;
-    if (done[dev][i] == 0) {
-      if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemMax) != cudaSuccess)
-        return false;
-      done[dev][i] = (unsigned long long)(uintptr_t)k;
-      return true;
-    }
-  }
-  return false;
+  const std::pair<int, uintptr_t> key(dev, (uintptr_t)k);
+  if (done.count(key)) return true;
+  if (cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemMax) != cudaSuccess)
+    return false;
+  done.insert(key);
+  return true;
 }
 
 bool prepare_gemv(const GemvParams& p) {

@@ -313,6 +313,95 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   for (int o = n + tid; o < BT * nch; o += kThreads) xs4[o] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// LayerNorm per column chunk as in gamma_preload, for beta.
+template <int NR, int BT>
+__device__ __forceinline__ void beta_preload(const GemvParams& p, int tid, uint4 (&g)[NR]) {
+  int b[NR], c[NR];
+  chunk_coords<NR, BT>(tid, kThreads, p.K >> 3, b, c);
+#pragma unroll
+  for (int i = 0; i < NR; ++i)
+    g[i] = b[i] < p.B ? *reinterpret_cast<const uint4*>(p.beta + c[i] * 8)
+                      : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// One-round LayerNorm staging on bf16 activations (NR 8-column chunks per
+// thread over the whole K, read once and kept in registers): the mean, then
+// the variance about it from the same registers (two CTA reductions, one
+// round of memory latency), then (x - mean) * rstd * gamma + beta rounded once
+// to bf16 for this split's columns [c0, c0 + nch).  The arithmetic of
+// prologue_stats + stage_x, with the sums grouped by thread.
+template <int BT, int NR>
+__device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red, uint16_t* xs,
+                                   int c0, int nch, int tid, const uint4 (&g)[NR],
+                                   const uint4 (&bt)[NR]) {
+  const int kch = p.K >> 3, n = p.B * kch;
+  float* tot = red + kWarps * BT;
+  float v[NR][8];
+  float s[BT];
+  int rb[NR], rc[NR];
+  chunk_coords<NR, BT>(tid, kThreads, kch, rb, rc);
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x));
+#pragma unroll
+  for (int b = 0; b < BT; ++b) s[b] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int o = tid + i * kThreads;
+    if (o < n) {
+      const uint4 u = __ldcg(src + o);  // rows K apart: o = b * kch + c
+      v[i][0] = bf16lo(u.x); v[i][1] = bf16hi(u.x); v[i][2] = bf16lo(u.y); v[i][3] = bf16hi(u.y);
+      v[i][4] = bf16lo(u.z); v[i][5] = bf16hi(u.z); v[i][6] = bf16lo(u.w); v[i][7] = bf16hi(u.w);
+      float t = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) t += v[i][e];
+#pragma unroll
+      for (int bb = 0; bb < BT; ++bb)
+        if (bb == rb[i]) s[bb] += t;
+    }
+  }
+  block_sum<BT>(s, red, tot, p.B, tid);
+  if (tid < p.B) stats[2 * tid] = tot[tid] / (float)p.K;
+  consumer_sync(kThreads);
+#pragma unroll
+  for (int b = 0; b < BT; ++b) s[b] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int o = tid + i * kThreads;
+    if (o < n) {
+      const float mean = stats[2 * rb[i]];
+      float t = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) t = fmaf(v[i][e] - mean, v[i][e] - mean, t);
+#pragma unroll
+      for (int bb = 0; bb < BT; ++bb)
+        if (bb == rb[i]) s[bb] += t;
+    }
+  }
+  block_sum<BT>(s, red, tot, p.B, tid);
+  if (tid < p.B) stats[2 * tid + 1] = rsqrtf(tot[tid] / (float)p.K + p.eps);
+  consumer_sync(kThreads);
+  uint4* xs4 = reinterpret_cast<uint4*>(xs);
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int o = tid + i * kThreads;
+    const int c = rc[i] - c0;
+    if (o < n && c >= 0 && c < nch) {
+      const float mean = stats[2 * rb[i]], rstd = stats[2 * rb[i] + 1];
+      const float gf[8] = {bf16lo(g[i].x), bf16hi(g[i].x), bf16lo(g[i].y), bf16hi(g[i].y),
+                           bf16lo(g[i].z), bf16hi(g[i].z), bf16lo(g[i].w), bf16hi(g[i].w)};
+      const float bf[8] = {bf16lo(bt[i].x), bf16hi(bt[i].x), bf16lo(bt[i].y), bf16hi(bt[i].y),
+                           bf16lo(bt[i].z), bf16hi(bt[i].z), bf16lo(bt[i].w), bf16hi(bt[i].w)};
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        w[e] = pack_bf16x2((v[i][2 * e] - mean) * rstd * gf[2 * e] + bf[2 * e],
+                           (v[i][2 * e + 1] - mean) * rstd * gf[2 * e + 1] + bf[2 * e + 1]);
+      xs4[rb[i] * nch + c] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  // batch rows the kernel computes past B read zeros
+  for (int o = p.B * nch + tid; o < BT * nch; o += kThreads) xs4[o] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Staging without a prologue, bf16 activations: a copy into shared memory,
 // with each thread's loads (up to eight 16-byte chunks) all in flight before
 // its first store, so K = 8960 costs one round of latency, not five.
@@ -617,10 +706,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     }
   }
   // gamma does not depend on the previous op either
-  const bool one_round = FT::rms1 || (!FT::copy_bf16 && one_round_rms(p));
-  constexpr int NR = FT::rms1 ? form_round_chunks(BT) : kOneRound;
+  const bool one_round = FT::rms1 || (!FT::copy_bf16 && !FT::ln1 && one_round_rms(p));
+  constexpr int NR = (FT::rms1 || FT::ln1) ? form_round_chunks(BT) : kOneRound;
   uint4 gpre[NR];
-  if (one_round) gamma_preload<NR, BT>(p, tid, gpre);
+  uint4 bpre[FT::ln1 ? NR : 1];
+  if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
+  if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
   pdl_launch_dependents();
   pdl_wait();
   if (stamp && tid == 0) stamp[1] = global_ns();
@@ -645,6 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // instruction caches (measured: 817 vs 897 us per Qwen chain step).
   if constexpr (FT::rms1) {
     stage_rms_one_round<BT, NR>(p, stats, red, xs, tid, gpre);
+  } else if constexpr (FT::ln1) {
+    stage_ln_one_round<BT, NR>(p, stats, red, xs, k0 >> 3, sc.KS >> 3, tid, gpre, bpre);
   } else if constexpr (FT::copy_bf16) {
     stage_copy_bf16<BT>(p, xs, k0 >> 3, sc.KS >> 3, tid);
   } else if (one_round) {
