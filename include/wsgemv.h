@@ -292,7 +292,11 @@ ws_status ws_chain_run_eager(ws_chain *c, ws_stream_t stream);
  * h_in; MLP: bf16 [B][w] to x_in) and, if not NULL, attn_host (bf16
  * [L][B][H], block order) to the chain's device inputs, replays the graph,
  * copies the result (head: int32 idx [B]; MLP: bf16 [B][w]) to out_host and
- * waits for the stream. */
+ * waits for the stream.  The copies and the step are one graph launch,
+ * captured for these host buffers on first use.  Pinned host buffers that
+ * are mapped into the device's address space (cudaHostAlloc, torch's
+ * pin_memory) are copied by one word-copy kernel each way; other buffers by
+ * cudaMemcpyAsync. */
 ws_status ws_chain_step_host(ws_chain *c, const void *in_host, const void *attn_host,
                              void *out_host, ws_stream_t stream);
 int ws_chain_num_ops(const ws_chain *c);

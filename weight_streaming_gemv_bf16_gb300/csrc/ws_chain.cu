@@ -454,12 +454,35 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
   return WS_OK;
 }
 
-// Host buffers of one ws_chain_step_host graph.
+namespace ws {
+// word copies between device-accessible buffers (ws_misc.cu)
+cudaError_t launch_copy_words(void* d0, const void* s0, size_t b0, void* d1, const void* s1,
+                              size_t b1, cudaStream_t stream);
+}  // namespace ws
+
+// Host buffers of one ws_chain_step_host graph, and their device aliases
+// where the buffers are pinned host memory mapped into the device's address
+// space (else null: the copies then go through the copy engines).
 struct HostIO {
   const void* in;
   const void* attn;
   void* out;
+  const void* in_d = nullptr;
+  const void* attn_d = nullptr;
+  void* out_d = nullptr;
 };
+
+// The device alias of a pinned, mapped host buffer (4-byte aligned), or null.
+static void* mapped_alias(const void* p) {
+  if (!p || ((uintptr_t)p & 3u)) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  return ((uintptr_t)a.devicePointer & 3u) ? nullptr : a.devicePointer;
+}
 
 static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st);
 static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st);
@@ -523,21 +546,37 @@ static std::vector<std::vector<std::pair<const void*, size_t>>> chain_reads(cons
 // block; MLP: bf16 x), and of its result back.
 static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st) {
   const int B = c->o.batch, H = c->o.hidden;
-  if (c->n_mlp)
+  if (c->n_mlp) {
+    if (io.in_d)  // one word-copy launch reading the mapped host buffer
+      return launch_copy_words(const_cast<void*>(c->o.x_in), io.in_d, (size_t)B * H * 2, nullptr,
+                               nullptr, 0, st) == cudaSuccess
+                 ? WS_OK
+                 : WS_ERR_CUDA;
     return cudaMemcpyAsync(const_cast<void*>(c->o.x_in), io.in, (size_t)B * H * 2,
                            cudaMemcpyHostToDevice, st) == cudaSuccess
                ? WS_OK
                : WS_ERR_CUDA;
+  }
+  const size_t blk = (size_t)B * H * 2;
+  bool contiguous = !c->attn_dev.empty();
+  for (size_t l = 0; l < c->attn_dev.size(); ++l)
+    if (static_cast<const char*>(c->attn_dev[l]) !=
+        static_cast<const char*>(c->attn_dev[0]) + l * blk)
+      contiguous = false;
+  const bool with_attn = io.attn && !c->attn_dev.empty();
+  if (io.in_d && (!with_attn || (io.attn_d && contiguous))) {
+    // h and every block's attention input in one word-copy launch
+    return launch_copy_words(const_cast<float*>(c->o.h_in), io.in_d, (size_t)B * H * 4,
+                             with_attn ? const_cast<void*>(c->attn_dev[0]) : nullptr,
+                             with_attn ? io.attn_d : nullptr,
+                             with_attn ? blk * c->attn_dev.size() : 0, st) == cudaSuccess
+               ? WS_OK
+               : WS_ERR_CUDA;
+  }
   if (cudaMemcpyAsync(const_cast<float*>(c->o.h_in), io.in, (size_t)B * H * 4,
                       cudaMemcpyHostToDevice, st) != cudaSuccess)
     return WS_ERR_CUDA;
-  if (io.attn && !c->attn_dev.empty()) {
-    const size_t blk = (size_t)B * H * 2;
-    bool contiguous = true;
-    for (size_t l = 0; l < c->attn_dev.size(); ++l)
-      if (static_cast<const char*>(c->attn_dev[l]) !=
-          static_cast<const char*>(c->attn_dev[0]) + l * blk)
-        contiguous = false;
+  if (with_attn) {
     if (contiguous)
       return cudaMemcpyAsync(const_cast<void*>(c->attn_dev[0]), io.attn,
                              blk * c->attn_dev.size(), cudaMemcpyHostToDevice, st) == cudaSuccess
@@ -554,14 +593,25 @@ static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st)
 
 static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st) {
   const int B = c->o.batch, H = c->o.hidden;
-  cudaError_t e;
-  if (c->n_mlp)
-    e = cudaMemcpyAsync(io.out, c->o.y_out, (size_t)B * H * 2, cudaMemcpyDeviceToHost, st);
-  else if (c->idx)
-    e = cudaMemcpyAsync(io.out, c->idx, (size_t)B * 4, cudaMemcpyDeviceToHost, st);
-  else
-    e = cudaMemcpyAsync(io.out, c->o.h_out, (size_t)B * H * 4, cudaMemcpyDeviceToHost, st);
-  return e == cudaSuccess ? WS_OK : WS_ERR_CUDA;
+  const void* src;
+  size_t bytes;
+  if (c->n_mlp) {
+    src = c->o.y_out;
+    bytes = (size_t)B * H * 2;
+  } else if (c->idx) {
+    src = c->idx;
+    bytes = (size_t)B * 4;
+  } else {
+    src = c->o.h_out;
+    bytes = (size_t)B * H * 4;
+  }
+  if (io.out_d)  // written through the mapped host buffer by one word-copy launch
+    return launch_copy_words(io.out_d, src, bytes, nullptr, nullptr, 0, st) == cudaSuccess
+               ? WS_OK
+               : WS_ERR_CUDA;
+  return cudaMemcpyAsync(io.out, src, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess
+             ? WS_OK
+             : WS_ERR_CUDA;
 }
 
 extern "C" {
@@ -952,7 +1002,10 @@ ws_status ws_chain_step_host(ws_chain* c, const void* in_host, const void* attn_
     return WS_ERR_STATE;
   }
   cudaStream_t st = (cudaStream_t)stream;
-  const HostIO io = {in_host, attn_host, out_host};
+  HostIO io = {in_host, attn_host, out_host};
+  io.in_d = mapped_alias(in_host);
+  io.attn_d = mapped_alias(attn_host);
+  io.out_d = mapped_alias(out_host);
   // one graph launch per step: the copies in, the step, the copy out.  It is
   // captured for these host buffers on first use (pinned memory; a capture
   // that fails, e.g. on pageable buffers, leaves the copies outside)

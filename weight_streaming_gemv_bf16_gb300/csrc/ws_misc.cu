@@ -239,6 +239,34 @@ __global__ void k_test_bounded_wait(unsigned long long timeout_ns, int* err) {
     atomicExch(err, DERR_TIMEOUT);
 }
 
+// Word copies between device-accessible buffers, for a step's inputs read
+// from pinned host memory and its result written back (the host buffers
+// reached through their device mapping): up to two (dst, src, bytes) pairs,
+// bytes a multiple of 4, 4-byte aligned.  SMs move the few kilobytes of a
+// decode step's inputs with one launch instead of a copy-engine transfer
+// per buffer.
+__global__ void __launch_bounds__(256) k_copy_words(uint32_t* d0, const uint32_t* s0, long long n0,
+                                                    uint32_t* d1, const uint32_t* s1, long long n1) {
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = t; i < n0; i += stride) d0[i] = s0[i];
+  for (long long i = t; i < n1; i += stride) d1[i] = s1[i];
+}
+
+cudaError_t launch_copy_words(void* d0, const void* s0, size_t b0, void* d1, const void* s1,
+                              size_t b1, cudaStream_t stream) {
+  const long long n0 = (long long)(b0 / 4), n1 = (long long)(b1 / 4);
+  const long long n = n0 > n1 ? n0 : n1;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks < 1) blocks = 1;
+  if (blocks > 148) blocks = 148;
+  k_copy_words<<<blocks, 256, 0, stream>>>(static_cast<uint32_t*>(d0),
+                                           static_cast<const uint32_t*>(s0), n0,
+                                           static_cast<uint32_t*>(d1),
+                                           static_cast<const uint32_t*>(s1), n1);
+  return cudaGetLastError();
+}
+
 size_t argmax_rows_workspace(int rows, int cols) {
   if (rows <= 0 || cols <= 0) return 0;
   const size_t cb = (size_t)argmax_cols_per_row_blocks(cols);
