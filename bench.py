@@ -48,10 +48,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--mode", choices=["chain", "kernel", "sweep"], default="chain",
+    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs"], default="chain",
                     help="chain: the decode step (the metric); kernel: gate/up alone (profiler "
                          "captures); sweep: the batch GEMV sweep, fp16 RMSNorm and the "
-                         "LayerNorm block chain, one JSON line")
+                         "LayerNorm block chain; configs: the fused 256x256 op beside the launch "
+                         "floor, one block warm and cold, the LayerNorm chain with and without "
+                         "prefetch (one JSON line each)")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
                     help="graph: one launch per op, PDL edges, one CUDA graph; persistent: "
                          "the whole step as one cooperative kernel")
@@ -614,6 +616,131 @@ def run_sweep(args):
     return 0
 
 
+def run_configs(args):
+    """The small configurations, one JSON line:
+    - the fused RMSNorm + GEMV 256 x 256 at batch 1 (latency-bound) beside the
+      on-box launch floor (an empty kernel, and one with a DRAM round trip),
+      each as back-to-back launches in one CUDA graph;
+    - one Qwen2.5-1.5B-shaped block at batch 1 (93.6 MB): L2-warm (the same
+      block replayed) and cold (six blocks with their own weights, 562 MB,
+      replayed in turn);
+    - the 72-block LayerNorm chain at batch 4 and 16: the measured prefetch
+      plans against none (with the tuner's kept plans and best lower CI),
+      warm (one chain, 85 MB) and cold (six chains in turn)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+    from weight_streaming_gemv_bf16_gb300 import synth
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream()
+
+    def events(fn, reps):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e-3 / reps
+
+    def graph_of(fn, n):
+        side = torch.cuda.Stream()
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            fn(side)
+        st.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                fn(torch.cuda.current_stream())
+        return g
+
+    out = {"mode": "configs"}
+    # config 1 and the launch floor
+    n = 100
+    x = to_dev(synth.normal_bf16((1, 256), 1.0, args.seed, "c1/x"), torch)
+    gm = to_dev(synth.uniform_bf16((256,), 0.5, 1.5, args.seed, "c1/g"), torch)
+    W = to_dev(synth.normal_bf16((256, 256), 0.02, args.seed, "c1/W"), torch)
+    y = torch.empty((1, 256), device="cuda")
+    ws = torch.empty(max(wb.workspace_bytes(wb.OP_GEMV, 256, 256, 1), 16), dtype=torch.uint8,
+                     device="cuda")
+    g1 = graph_of(lambda s: wb.rmsnorm_gemv(x, gm, W, y, 1e-6, workspace=ws, stream=s), n)
+    sink = torch.zeros(16, dtype=torch.int32, device="cuda")
+    probe = torch.zeros(1 << 20, dtype=torch.int32, device="cuda")
+    ge = graph_of(lambda s: wb.empty_probe(0, probe, sink, stream=s), n)
+    gt = graph_of(lambda s: wb.empty_probe(1, probe, sink, stream=s), n)
+    out["config1_rmsnorm_gemv_256"] = {
+        "us_per_launch": round(events(g1.replay, 20) / n * 1e6, 3),
+        "empty_kernel_us": round(events(ge.replay, 20) / n * 1e6, 3),
+        "one_dram_round_trip_us": round(events(gt.replay, 20) / n * 1e6, 3)}
+    # config 2: one block, warm and cold
+    sh = synth.QwenShape(layers=1)
+    chains = []
+    for c in range(6):
+        blk = synth.qwen_block_weights(sh, args.seed + c, 0)
+        dblk = {k: to_dev(v, torch) for k, v in blk.items()}
+        dattn = to_dev(synth.qwen_attn(sh, 1, args.seed + c, 0), torch)[None]
+        dh = torch.from_numpy(synth.qwen_hidden(sh, 1, args.seed + c)).cuda()
+        ch = wc.qwen_chain([dblk], None, dattn, dh, eps=sh.eps, prefetch=0)
+        ch.chain.capture()
+        chains.append(ch)
+    warm = events(lambda: chains[0].run(st), 200)
+
+    def cold_round():
+        for ch in chains:
+            ch.run(st)
+    cold = events(cold_round, 50) / len(chains)
+    bb = sh.block_weight_bytes()
+    out["config2_one_block_b1"] = {"warm_us": round(warm * 1e6, 2),
+                                   "warm_gbs": round(bb / warm / 1e9, 1),
+                                   "cold_us": round(cold * 1e6, 2),
+                                   "cold_gbs": round(bb / cold / 1e9, 1), "bytes": bb}
+    for ch in chains:
+        ch.chain.close()
+    del chains
+    # config 4: prefetch plans vs none, warm and cold
+    msh = synth.MlpShape()
+    mout = []
+    sets = []
+    for c in range(6):
+        hb = [synth.mlp_block_weights(msh, args.seed + c, l) for l in range(msh.blocks)]
+        sets.append([{k: to_dev(v, torch) for k, v in b.items()} for b in hb])
+    for B in (4, 16):
+        x_in = to_dev(synth.mlp_input(msh, B, args.seed), torch)
+        res = {"B": B}
+        for pf in (0, 1):
+            chs = []
+            for c in range(6):
+                ch = wc.mlp_chain(sets[c], x_in, eps=msh.eps, prefetch=pf)
+                if pf:
+                    ch.chain.tune()
+                ch.chain.capture()
+                chs.append(ch)
+            key = "tuned" if pf else "none"
+            res[key + "_warm_us"] = round(events(lambda: chs[0].run(st), 200) * 1e6, 2)
+
+            def rnd(chs=chs):
+                for ch in chs:
+                    ch.run(st)
+            res[key + "_cold_us"] = round(events(rnd, 30) / len(chs) * 1e6, 2)
+            if pf:
+                pl = chs[0].chain.plans()
+                res["plans_kept"] = sum(1 for p in pl if p[0][0] != 0)
+                res["best_lower_ci"] = round(max(p[1] for p in pl), 4)
+            for ch in chs:
+                ch.chain.close()
+        mout.append(res)
+    out["config4_mlp_chain"] = mout
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -622,6 +749,8 @@ def main():
         return run_kernel_only(args)
     if args.mode == "sweep":
         return run_sweep(args)
+    if args.mode == "configs":
+        return run_configs(args)
     return run_ours(args)
 
 
