@@ -314,6 +314,55 @@ def rmsnorm_rows(x_bits, gamma_bits, eps: float, dtype: str = "fp16") -> np.ndar
     return enc(rmsnorm(dec(x_bits), dec(gamma_bits), eps))
 
 
+# --------------------------------------------------------------------------
+# decode attention with a key-value cache
+# --------------------------------------------------------------------------
+
+def decode_attention(q, k_new, v_new, k_cache_bits, v_cache_bits, pos, n_kv_heads: int,
+                     head_dim: int) -> dict:
+    """One decode step of grouped-query attention over a key-value cache, in
+    double ("Making small PyTorch ops faster on a laptop GPU", "A full decode
+    step is a different story": the new key and value are appended to the
+    cache and the softmax is taken over every cached position; "One Token,
+    Kernel by Kernel", "The fix: Part 10's split-KV kernel": the cache layout
+    (batch, key-value head, slot, dimension), the valid length read at run
+    time, one key-value head serving n_heads / n_kv_heads query heads).
+
+    q: [B, n_heads * d] (fp32 values); k_new, v_new: [B, n_kv * d]; the
+    caches: bf16 bits [B, n_kv, S, d]; pos: [B] slot of the new token.
+    Steps, per batch row b:
+      1. the new key and value, rounded to bf16 (the cache's type), are
+         written at slot pos[b] of their head;
+      2. for query head h, with key-value head g = h // (n_heads / n_kv):
+         s_j = (q_h . k_j) / sqrt(d) for slots j = 0 .. pos[b],
+         p = exp(s - max s) / sum exp(s - max s),
+         out_h = sum_j p_j v_j.
+    Returns the output [B, n_heads * d] (double) and the updated caches."""
+    q = np.asarray(q, np.float64)
+    B = q.shape[0]
+    d = head_dim
+    nh = q.shape[1] // d
+    group = nh // n_kv_heads
+    kc = _u16(k_cache_bits).copy()
+    vc = _u16(v_cache_bits).copy()
+    kn = f64_to_bf16(np.asarray(k_new, np.float64))
+    vn = f64_to_bf16(np.asarray(v_new, np.float64))
+    out = np.zeros((B, nh * d), np.float64)
+    for b in range(B):
+        p_b = int(pos[b])
+        for g in range(n_kv_heads):
+            kc[b, g, p_b] = kn[b, g * d:(g + 1) * d]
+            vc[b, g, p_b] = vn[b, g * d:(g + 1) * d]
+        for h in range(nh):
+            g = h // group
+            K = bf16_to_f64(kc[b, g, :p_b + 1])      # [n, d]
+            V = bf16_to_f64(vc[b, g, :p_b + 1])
+            s = K @ q[b, h * d:(h + 1) * d] / np.sqrt(d)
+            e = np.exp(s - s.max())
+            out[b, h * d:(h + 1) * d] = (e / e.sum()) @ V
+    return {"out": out, "k_cache": kc, "v_cache": vc}
+
+
 def openmp_threads() -> int:
     return int(_load().ws_oracle_openmp_threads())
 

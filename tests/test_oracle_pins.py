@@ -337,3 +337,121 @@ def test_workload_shapes_reproduce_the_pages_byte_counts():
     assert close(2 * s.kv_dim * s.hidden, "kv_proj_bytes")
     assert close(7 * s.layers + 1, "gemv_count")
     assert close(s.vocab, "lm_head_rows") and close(s.hidden, "lm_head_cols")
+
+
+# --------------------------------------------------------------------------
+# decode attention over a key-value cache
+# --------------------------------------------------------------------------
+
+def _attn_case(rng, B, nkv, S, d, nh, ints=False):
+    def draw(shape):
+        v = rng.integers(-8, 9, size=shape).astype(np.float64) if ints else rng.standard_normal(shape)
+        return v
+    q = draw((B, nh * d))
+    kn, vn = draw((B, nkv * d)), draw((B, nkv * d))
+    kc = oracle.f64_to_bf16(draw((B, nkv, S, d)))
+    vc = oracle.f64_to_bf16(draw((B, nkv, S, d)))
+    return q, kn, vn, kc, vc
+
+
+def test_attention_single_slot_returns_the_new_value():
+    """pos = 0: the softmax has one term, so every query head returns its
+    group's new value, rounded to bf16 (the cache's type), exactly."""
+    rng = np.random.default_rng(1)
+    B, nkv, S, d, nh = 2, 2, 8, 16, 6
+    q, kn, vn, kc, vc = _attn_case(rng, B, nkv, S, d, nh)
+    r = oracle.decode_attention(q, kn, vn, kc, vc, np.zeros(B, np.int32), nkv, d)
+    group = nh // nkv
+    for b in range(B):
+        for h in range(nh):
+            g = h // group
+            want = oracle.bf16_to_f64(oracle.f64_to_bf16(vn[b, g * d:(g + 1) * d]))
+            assert np.array_equal(r["out"][b, h * d:(h + 1) * d], want)
+
+
+def test_attention_appends_at_pos_and_leaves_other_slots():
+    rng = np.random.default_rng(2)
+    B, nkv, S, d, nh = 3, 2, 16, 8, 4
+    q, kn, vn, kc, vc = _attn_case(rng, B, nkv, S, d, nh)
+    pos = np.array([0, 7, 15])
+    r = oracle.decode_attention(q, kn, vn, kc, vc, pos, nkv, d)
+    for b in range(B):
+        for g in range(nkv):
+            assert np.array_equal(r["k_cache"][b, g, pos[b]], oracle.f64_to_bf16(kn[b, g * d:(g + 1) * d]))
+            assert np.array_equal(r["v_cache"][b, g, pos[b]], oracle.f64_to_bf16(vn[b, g * d:(g + 1) * d]))
+            keep = np.arange(S) != pos[b]
+            assert np.array_equal(r["k_cache"][b, g][keep], kc[b, g][keep])
+            assert np.array_equal(r["v_cache"][b, g][keep], vc[b, g][keep])
+
+
+def test_attention_zero_query_averages_the_values():
+    """q = 0: every score is 0, the weights are uniform and the output is the
+    mean of the group's value rows over slots 0 .. pos."""
+    rng = np.random.default_rng(3)
+    B, nkv, S, d, nh = 2, 2, 32, 8, 4
+    _, kn, vn, kc, vc = _attn_case(rng, B, nkv, S, d, nh)
+    q = np.zeros((B, nh * d))
+    pos = np.array([9, 31])
+    r = oracle.decode_attention(q, kn, vn, kc, vc, pos, nkv, d)
+    for b in range(B):
+        for h in range(nh):
+            g = h // (nh // nkv)
+            V = oracle.bf16_to_f64(r["v_cache"][b, g, :pos[b] + 1])
+            assert np.allclose(r["out"][b, h * d:(h + 1) * d], V.mean(axis=0), rtol=0, atol=1e-12)
+
+
+def test_attention_two_slots_closed_form():
+    """Two slots: the weight of slot 0 is the logistic function of the score
+    difference divided by sqrt(d) (pins the scale and the sign)."""
+    d = 16
+    q = np.zeros((1, d)); q[0, 0] = 2.0
+    k0 = np.zeros(d); k0[0] = 1.5
+    k1 = np.zeros(d); k1[0] = -0.5
+    v0 = np.arange(d, dtype=np.float64)
+    v1 = -2.0 * np.ones(d)
+    kc = oracle.f64_to_bf16(np.stack([k0, np.zeros(d)])[None, None])
+    vc = oracle.f64_to_bf16(np.stack([v0, np.zeros(d)])[None, None])
+    r = oracle.decode_attention(q, k1[None], v1[None], kc, vc, np.array([1]), 1, d)
+    s0, s1 = q[0] @ k0, q[0] @ k1
+    p0 = 1.0 / (1.0 + math.exp((s1 - s0) / math.sqrt(d)))
+    assert np.allclose(r["out"][0], p0 * v0 + (1 - p0) * v1, rtol=0, atol=1e-12)
+
+
+def test_attention_slot_order_does_not_matter():
+    rng = np.random.default_rng(4)
+    B, nkv, S, d, nh = 1, 2, 24, 8, 6
+    q, kn, vn, kc, vc = _attn_case(rng, B, nkv, S, d, nh)
+    pos = np.array([20])
+    r1 = oracle.decode_attention(q, kn, vn, kc, vc, pos, nkv, d)
+    perm = np.concatenate([rng.permutation(20), np.arange(20, S)])
+    r2 = oracle.decode_attention(q, kn, vn, kc[:, :, perm], vc[:, :, perm], pos, nkv, d)
+    assert np.allclose(r1["out"], r2["out"], rtol=0, atol=1e-12)
+
+
+def test_attention_is_linear_in_the_values():
+    """With integer-valued caches (exact in bf16) the output for V1 + V2 is
+    the sum of the outputs for V1 and V2 (same keys, same weights)."""
+    rng = np.random.default_rng(5)
+    B, nkv, S, d, nh = 2, 2, 16, 8, 4
+    q, kn, vn1, kc, vc1 = _attn_case(rng, B, nkv, S, d, nh, ints=True)
+    _, _, vn2, _, vc2 = _attn_case(rng, B, nkv, S, d, nh, ints=True)
+    pos = np.array([5, 15])
+    vc12 = oracle.f64_to_bf16(oracle.bf16_to_f64(vc1) + oracle.bf16_to_f64(vc2))
+    r1 = oracle.decode_attention(q, kn, vn1, kc, vc1, pos, nkv, d)
+    r2 = oracle.decode_attention(q, kn, vn2, kc, vc2, pos, nkv, d)
+    r12 = oracle.decode_attention(q, kn, vn1 + vn2, kc, vc12, pos, nkv, d)
+    assert np.allclose(r12["out"], r1["out"] + r2["out"], rtol=0, atol=1e-9)
+
+
+def test_attention_query_heads_share_their_group():
+    """Query heads of one group with equal queries give equal outputs; heads
+    of another group read the other key-value head."""
+    rng = np.random.default_rng(6)
+    B, nkv, S, d, nh = 1, 2, 16, 8, 4   # groups of 2 heads
+    q, kn, vn, kc, vc = _attn_case(rng, B, nkv, S, d, nh)
+    q[0, d:2 * d] = q[0, 0:d]            # heads 0 and 1 (group 0) equal
+    q[0, 2 * d:3 * d] = q[0, 0:d]        # head 2 (group 1) equal too
+    r = oracle.decode_attention(q, kn, vn, kc, vc, np.array([10]), nkv, d)
+    o = r["out"][0].reshape(nh, d)
+    assert np.array_equal(o[0], o[1])
+    assert not np.allclose(o[0], o[2])
