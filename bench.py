@@ -48,12 +48,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs"], default="chain",
+    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs", "attention"],
+                    default="chain",
                     help="chain: the decode step (the metric); kernel: gate/up alone (profiler "
                          "captures); sweep: the batch GEMV sweep, fp16 RMSNorm and the "
                          "LayerNorm block chain; configs: the fused 256x256 op beside the launch "
                          "floor, one block warm and cold, the LayerNorm chain with and without "
-                         "prefetch (one JSON line each)")
+                         "prefetch (one JSON line each); attention: decode attention over "
+                         "a key-value cache at batch 1/4/16 and 1k-32k cached slots")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
                     help="graph: one launch per op, PDL edges, one CUDA graph; persistent: "
                          "the whole step as one cooperative kernel")
@@ -741,6 +743,76 @@ def run_configs(args):
     return 0
 
 
+def run_attention(args):
+    """Decode attention with the key-value append, Qwen2.5-1.5B heads (12 query
+    heads over 2 key-value heads of 128), one JSON line: per (batch, cached
+    slots) the time per launch over rotating caches larger than L2 (launched
+    back to back in one CUDA graph, CUDA events around it), and the
+    algorithmic bytes per launch (the key and value rows of slots 0..pos read,
+    the new rows written, q read and the fp32 output written) over that time
+    against the measured copy peak."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda").manual_seed(args.seed)
+    hbm = peaks()[0]
+    nh, nkv, d = 12, 2, 128
+    rows = []
+    for B in (1, 4, 16):
+        for n in (1024, 4096, 32768):
+            S = n
+            cache_b = B * nkv * S * d * 2
+            ncopy = max(2, -(-(256 << 20) // (2 * cache_b)))
+            ks = [torch.randn((B, nkv, S, d), device="cuda", generator=gen).to(torch.bfloat16)
+                  for _ in range(ncopy)]
+            vs = [torch.randn((B, nkv, S, d), device="cuda", generator=gen).to(torch.bfloat16)
+                  for _ in range(ncopy)]
+            q = torch.randn((B, nh * d), device="cuda", generator=gen)
+            kn = torch.randn((B, nkv * d), device="cuda", generator=gen)
+            vn = torch.randn((B, nkv * d), device="cuda", generator=gen)
+            pos = torch.full((B,), n - 1, dtype=torch.int32, device="cuda")
+            ws = torch.zeros(wb.attention_workspace_bytes(B, nh, nkv, S), dtype=torch.uint8,
+                             device="cuda")
+            out = torch.empty((B, nh * d), device="cuda")
+
+            def fn(s):
+                for c in range(ncopy):
+                    wb.decode_attention(q, kn, vn, ks[c], vs[c], pos, ws, out, None, stream=s)
+            side = torch.cuda.Stream()
+            side.wait_stream(st)
+            with torch.cuda.stream(side):
+                fn(side)
+            st.wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(torch.cuda.current_stream())
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            reps = max(3, min(50, (400 << 20) // (ncopy * 2 * cache_b)))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(reps):
+                g.replay()
+            e1.record(st)
+            torch.cuda.synchronize()
+            dt = e0.elapsed_time(e1) * 1e-3 / (reps * ncopy)
+            nbytes = B * nkv * (2 * n * d * 2 + 2 * d * 2) + B * nh * d * 4 * 2
+            rows.append({"batch": B, "cached_slots": n, "us_per_launch": round(dt * 1e6, 2),
+                         "algorithmic_bytes": nbytes, "GB_s": round(nbytes / dt / 1e9, 1),
+                         "frac_of_measured_hbm": round(nbytes / dt / 1e9 / hbm, 3)})
+            del ks, vs
+            torch.cuda.empty_cache()
+    assert wb.device_error() == 0
+    print(json.dumps({"mode": "attention", "heads": [nh, nkv, d], "hbm_peak_gbs": hbm,
+                      "l2": "rotating caches, at least 256 MB per graph replay", "rows": rows}))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -751,6 +823,8 @@ def main():
         return run_sweep(args)
     if args.mode == "configs":
         return run_configs(args)
+    if args.mode == "attention":
+        return run_attention(args)
     return run_ours(args)
 
 

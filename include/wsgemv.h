@@ -154,6 +154,32 @@ ws_status ws_lmhead_argmax(const void *h, int h_dtype, const void *gamma, const 
                            int32_t *idx, float *logits, int V, int K, int B, float eps,
                            void *workspace, size_t workspace_bytes, ws_stream_t stream);
 
+/* One decode step of grouped-query attention over a key-value cache
+ * ("Making small PyTorch ops faster on a laptop GPU", "A full decode step is
+ * a different story"; "One Token, Kernel by Kernel", "The fix: Part 10's
+ * split-KV kernel").  Per batch row b: the new key and value (k_new, v_new
+ * fp32 [B][n_kv_heads * 128], rounded to bf16) are written at slot pos[b] of
+ * the caches (bf16 [B][n_kv_heads][s_max][128], 16-byte aligned; the caller
+ * owns them); query head h (q fp32 [B][n_heads * 128]) attends over slots
+ * 0 .. pos[b] of key-value head h / (n_heads / n_kv_heads) with scores
+ * q.k / sqrt(128) and an fp32 softmax.  Output: out_f32 [B][n_heads * 128]
+ * and/or out_bf16 (bf16, the same shape); either may be NULL, not both.
+ * pos: int32 [B] in device memory, read when the kernel runs (a captured
+ * graph replays with the current positions); a position outside
+ * 0 .. s_max - 1 skips that row and raises the device error flag (2).
+ * head_dim must be 128, n_heads / n_kv_heads one of 1, 2, 4, 6, 8, s_max a
+ * multiple of 128, 1 <= B <= 16.  The cache is split into chunks of 128
+ * slots, one CTA each; the last chunk of a (row, key-value head) merges the
+ * chunks' partial softmax results.  Workspace (zero-filled before its first
+ * use, left zeroed by every call):
+ * ws_attention_workspace_bytes(B, n_heads, n_kv_heads, 128, s_max). */
+size_t ws_attention_workspace_bytes(int B, int n_heads, int n_kv_heads, int head_dim, int s_max);
+ws_status ws_decode_attention(const float *q, const float *k_new, const float *v_new,
+                              void *k_cache, void *v_cache, const int32_t *pos, float *out_f32,
+                              void *out_bf16, int B, int n_heads, int n_kv_heads, int head_dim,
+                              int s_max, void *workspace, size_t workspace_bytes,
+                              ws_stream_t stream);
+
 /* idx[r] = the lowest j with v[r][j] == max_j v[r][j] for fp32 rows
  * [rows][cols] ("One Token, Kernel by Kernel", "The whole step").  Workspace
  * required: ws_workspace_bytes(WS_OP_ARGMAX_ROWS, rows, cols, 1). */

@@ -78,6 +78,30 @@ def test_other_entry_points_validate(lib):
     assert lib.ws_set_tuning(wb.ctypes.byref(t)) == -1
 
 
+@pytest.mark.parametrize("B,nh,nkv,d,S,kc,wsb,status", [
+    (2, 12, 2, 64, 256, A, 1 << 20, -3),     # head_dim != 128
+    (2, 12, 4, 128, 256, A, 1 << 20, -3),    # 3 query heads per key-value head
+    (2, 12, 5, 128, 256, A, 1 << 20, -3),    # n_heads not a multiple of n_kv_heads
+    (2, 12, 2, 128, 200, A, 1 << 20, -3),    # s_max not a multiple of 128
+    (17, 12, 2, 128, 256, A, 1 << 20, -3),   # B > 16
+    (0, 12, 2, 128, 256, A, 1 << 20, -3),    # B = 0
+    (2, 12, 2, 128, 256, MIS + 2, 1 << 20, -2),  # misaligned cache
+    (2, 12, 2, 128, 256, A, 64, -1),         # workspace too small
+])
+def test_decode_attention_validation(lib, B, nh, nkv, d, S, kc, wsb, status):
+    assert lib.ws_decode_attention(A, A, A, kc, A, A, A, None, B, nh, nkv, d, S, A, wsb,
+                                   None) == status
+    assert lib.ws_last_error()
+
+
+def test_decode_attention_workspace(lib):
+    # tickets [B][n_kv] (256-byte aligned), then per (row, head, chunk) G x 130 floats
+    assert wb.attention_workspace_bytes(1, 12, 2, 1024) == 256 + 2 * 8 * 6 * 130 * 4
+    assert wb.attention_workspace_bytes(16, 12, 2, 32768) == 256 + 32 * 256 * 6 * 130 * 4
+    assert wb.attention_workspace_bytes(1, 12, 2, 1000) == 0
+    assert wb.attention_workspace_bytes(1, 12, 2, 1024, head_dim=64) == 0
+
+
 def test_chain_create_rejects_bad_block_lists(lib):
     opts = wb.ChainOpts(batch=1, hidden=64, kv_dim=16, inter=128, vocab=100, eps=1e-6,
                         h_in=A, h_out=A + 4096)

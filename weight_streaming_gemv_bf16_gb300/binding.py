@@ -96,6 +96,7 @@ _SIGS = {
     "ws_ln_gemv_gelu": [P, P, P, P, P, P, I32, I32, I32, F32, P, SZ, P],
     "ws_lmhead_argmax": [P, I32, P, P, P, P, I32, I32, I32, F32, P, SZ, P],
     "ws_argmax_rows": [P, P, I32, I32, P, SZ, P],
+    "ws_decode_attention": [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P],
     "ws_rmsnorm": [P, P, P, I32, I32, I32, F32, P],
     "ws_l2_prefetch": [P, SZ, PrefetchPlan, P],
     "ws_chain_create": [P, I32, P, P],
@@ -114,6 +115,7 @@ _SIGS = {
 }
 _OTHER = {
     "ws_workspace_bytes": ([I32, I32, I32, I32], SZ),
+    "ws_attention_workspace_bytes": ([I32, I32, I32, I32, I32], SZ),
     "ws_last_error": ([], C.c_char_p),
     "ws_device_error": ([I32], I32),
     "ws_chain_num_ops": ([P], I32),
@@ -272,6 +274,22 @@ def argmax_rows(logits, idx, workspace, stream=None):
     rows, cols = logits.shape
     wp, wb = _ws(workspace)
     _check(load().ws_argmax_rows(_ptr(logits), _ptr(idx), rows, cols, wp, wb, _stream(stream)))
+
+
+def attention_workspace_bytes(B, n_heads, n_kv_heads, s_max, head_dim=128) -> int:
+    return int(load().ws_attention_workspace_bytes(B, n_heads, n_kv_heads, head_dim, s_max))
+
+
+def decode_attention(q, k_new, v_new, k_cache, v_cache, pos, workspace, out_f32=None,
+                     out_bf16=None, stream=None):
+    """q [B, n_heads*128] fp32, k_new/v_new [B, n_kv*128] fp32, caches bf16
+    [B, n_kv, s_max, 128] (updated in place at pos), pos int32 [B] on the device."""
+    B, n_kv, s_max, d = k_cache.shape
+    n_heads = q.shape[1] // d
+    wp, wb = _ws(workspace)
+    _check(load().ws_decode_attention(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(pos), _ptr(out_f32), _ptr(out_bf16),
+                                      B, n_heads, n_kv, d, s_max, wp, wb, _stream(stream)))
 
 
 def rmsnorm(x, gamma, y, eps, stream=None):
