@@ -95,9 +95,18 @@ def test_decode_attention_validation(lib, B, nh, nkv, d, S, kc, wsb, status):
 
 
 def test_decode_attention_workspace(lib):
-    # tickets [B][n_kv] (256-byte aligned), then per (row, head, chunk) G x 130 floats
-    assert wb.attention_workspace_bytes(1, 12, 2, 1024) == 256 + 2 * 8 * 6 * 130 * 4
-    assert wb.attention_workspace_bytes(16, 12, 2, 32768) == 256 + 32 * 256 * 6 * 130 * 4
+    def expect(B, nh, nkv, S):
+        # tickets per group of 16 chunks, per (row, head); G x 130 floats per
+        # chunk and per group; each part 256-byte aligned
+        a = lambda v: -(-v // 256) * 256
+        G, chunks = nh // nkv, S // 128
+        groups = -(-chunks // 16)
+        bg = B * nkv
+        return (a(bg * groups * 4) + a(bg * 4) + a(bg * chunks * G * 130 * 4)
+                + bg * groups * G * 130 * 4)
+    for shape in [(1, 12, 2, 1024), (16, 12, 2, 32768), (3, 8, 8, 128), (2, 16, 2, 2176)]:
+        assert wb.attention_workspace_bytes(*shape) == expect(*shape), shape
+    assert wb.attention_workspace_bytes(1, 12, 2, 1024) == 256 + 256 + 2 * 8 * 6 * 520 + 2 * 6 * 520
     assert wb.attention_workspace_bytes(1, 12, 2, 1000) == 0
     assert wb.attention_workspace_bytes(1, 12, 2, 1024, head_dim=64) == 0
 

@@ -155,3 +155,11 @@ def test_position_outside_the_cache_raises_the_device_flag():
     assert_fp32(o32[:1].cpu().numpy(), ref["out"], what="valid row")
     assert np.array_equal(host_bits(dk)[1], kc[1]) and np.array_equal(host_bits(dv)[1], vc[1])
     assert torch.isnan(o32[1]).all()
+
+
+def test_group_merges():
+    """17 chunks (a group of 16 and a group of 1, merged by the last group),
+    exactly 16 chunks (one group), and 33 chunks, across three rows."""
+    B, nh, nkv, S = 3, 12, 2, 4224
+    args = _inputs(B, nh, nkv, S, seed=21)
+    _check(*args, [2175, 2047, 4223], nkv, "groups")
