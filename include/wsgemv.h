@@ -162,16 +162,20 @@ ws_status ws_lmhead_argmax(const void *h, int h_dtype, const void *gamma, const 
  * the caches (bf16 [B][n_kv_heads][s_max][128], 16-byte aligned; the caller
  * owns them); query head h (q fp32 [B][n_heads * 128]) attends over slots
  * 0 .. pos[b] of key-value head h / (n_heads / n_kv_heads) with scores
- * q.k / sqrt(128) and an fp32 softmax.  Output: out_f32 [B][n_heads * 128]
+ * q.k / sqrt(128) and an fp32 softmax.  The two products run on warp-level
+ * bf16 tensor-core MMAs with fp32 accumulators; q and the probabilities
+ * enter as bf16 hi + lo pairs (relative error 2^-17).  Output: out_f32 [B][n_heads * 128]
  * and/or out_bf16 (bf16, the same shape); either may be NULL, not both.
  * pos: int32 [B] in device memory, read when the kernel runs (a captured
  * graph replays with the current positions); a position outside
  * 0 .. s_max - 1 skips that row and raises the device error flag (2).
- * head_dim must be 128, n_heads / n_kv_heads one of 1, 2, 4, 6, 8, s_max a
- * multiple of 128, 1 <= B <= 16.  The cache is split into chunks of 128
- * slots, one CTA each; the last chunk of a (row, key-value head) merges the
- * chunks' partial softmax results.  Workspace (zero-filled before its first
- * use, left zeroed by every call):
+ * head_dim must be 128, n_heads / n_kv_heads at most 8, s_max a multiple
+ * of 64, 1 <= B <= 16; caches, k_new and v_new 16-byte aligned, q 8-byte
+ * aligned.  Slots after pos are never read (they may hold anything).  Each
+ * (row, key-value head) is cut into splits of whole 64-slot runs, as many as
+ * fill one wave of CTAs; the last split of each group of 16 merges the
+ * group's partial softmax results and the last group merges the groups.
+ * Workspace (zero-filled before its first use, left zeroed by every call):
  * ws_attention_workspace_bytes(B, n_heads, n_kv_heads, 128, s_max). */
 size_t ws_attention_workspace_bytes(int B, int n_heads, int n_kv_heads, int head_dim, int s_max);
 ws_status ws_decode_attention(const float *q, const float *k_new, const float *v_new,

@@ -80,9 +80,9 @@ def test_other_entry_points_validate(lib):
 
 @pytest.mark.parametrize("B,nh,nkv,d,S,kc,wsb,status", [
     (2, 12, 2, 64, 256, A, 1 << 20, -3),     # head_dim != 128
-    (2, 12, 4, 128, 256, A, 1 << 20, -3),    # 3 query heads per key-value head
+    (2, 12, 1, 128, 256, A, 1 << 20, -3),    # 12 query heads per key-value head (> 8)
     (2, 12, 5, 128, 256, A, 1 << 20, -3),    # n_heads not a multiple of n_kv_heads
-    (2, 12, 2, 128, 200, A, 1 << 20, -3),    # s_max not a multiple of 128
+    (2, 12, 2, 128, 200, A, 1 << 20, -3),    # s_max not a multiple of 64
     (17, 12, 2, 128, 256, A, 1 << 20, -3),   # B > 16
     (0, 12, 2, 128, 256, A, 1 << 20, -3),    # B = 0
     (2, 12, 2, 128, 256, MIS + 2, 1 << 20, -2),  # misaligned cache
@@ -96,18 +96,19 @@ def test_decode_attention_validation(lib, B, nh, nkv, d, S, kc, wsb, status):
 
 def test_decode_attention_workspace(lib):
     def expect(B, nh, nkv, S):
-        # tickets per group of 16 chunks, per (row, head); G x 130 floats per
-        # chunk and per group; each part 256-byte aligned
+        # tickets per group of 16 splits, per (row, head); G x 130 floats per
+        # split (at most one per 64 slots) and per group; each part 256-byte aligned
         a = lambda v: -(-v // 256) * 256
-        G, chunks = nh // nkv, S // 128
+        G, chunks = nh // nkv, S // 64
         groups = -(-chunks // 16)
         bg = B * nkv
         return (a(bg * groups * 4) + a(bg * 4) + a(bg * chunks * G * 130 * 4)
                 + bg * groups * G * 130 * 4)
     for shape in [(1, 12, 2, 1024), (16, 12, 2, 32768), (3, 8, 8, 128), (2, 16, 2, 2176)]:
         assert wb.attention_workspace_bytes(*shape) == expect(*shape), shape
-    assert wb.attention_workspace_bytes(1, 12, 2, 1024) == 256 + 256 + 2 * 8 * 6 * 520 + 2 * 6 * 520
+    assert wb.attention_workspace_bytes(1, 12, 2, 1024) == 256 + 256 + 2 * 16 * 6 * 520 + 2 * 6 * 520
     assert wb.attention_workspace_bytes(1, 12, 2, 1000) == 0
+    assert wb.attention_workspace_bytes(1, 12, 1, 1024) == 0
     assert wb.attention_workspace_bytes(1, 12, 2, 1024, head_dim=64) == 0
 
 

@@ -5,7 +5,8 @@ kernel of "One Token, Kernel by Kernel"), the bf16 output (the kernel's own
 fp32 result rounded to nearest even), cache lengths on and around the
 128-slot chunk boundary up to the full cache, every supported group size,
 ragged positions across the batch, graph replay with advancing positions, and
-an out-of-range position turned into the device error flag."""
+an out-of-range position turned into the device error flag, and stale
+non-finite values in the cache past the new token (never read)."""
 import numpy as np
 import pytest
 import torch
@@ -85,7 +86,7 @@ def test_ragged_positions_across_the_batch(B):
     _check(*args, pos, nkv, f"B={B}")
 
 
-@pytest.mark.parametrize("nh,nkv", [(4, 4), (8, 4), (8, 2), (12, 2), (16, 2)])
+@pytest.mark.parametrize("nh,nkv", [(4, 4), (8, 4), (12, 4), (8, 2), (12, 2), (16, 2)])
 def test_group_sizes(nh, nkv):
     B, S = 3, 384
     args = _inputs(B, nh, nkv, S, seed=nh * 10 + nkv)
@@ -163,3 +164,15 @@ def test_group_merges():
     B, nh, nkv, S = 3, 12, 2, 4224
     args = _inputs(B, nh, nkv, S, seed=21)
     _check(*args, [2175, 2047, 4223], nkv, "groups")
+
+
+def test_slots_past_the_token_are_never_read():
+    """Cache slots after pos hold NaN and infinity bit patterns (stale or
+    uninitialised memory): the output is the oracle's over slots 0..pos."""
+    B, nh, nkv, S = 2, 12, 2, 512
+    q, kn, vn, kc, vc = _inputs(B, nh, nkv, S, seed=13)
+    pos = [200, 37]
+    for b, p in enumerate(pos):
+        kc[b, :, p + 1:] = 0x7FC0  # NaN
+        vc[b, :, p + 1:] = 0x7F80  # +inf
+    _check(q, kn, vn, kc, vc, pos, nkv, "stale tail")

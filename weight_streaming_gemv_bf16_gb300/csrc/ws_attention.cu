@@ -7,22 +7,29 @@
 // valid length read on the GPU at run time so that a CUDA graph can be
 // replayed, one key-value head read once for all of its query heads).
 //
-// Design for GB300: one CTA of 256 threads per (chunk of 128 cached slots,
-// key-value head, batch row).  The chunk's key and value rows (32 KB each,
-// contiguous in the cache) land in shared memory by two bulk async copies on
-// one mbarrier, so a CTA has its whole chunk in flight at once; the new
-// token's row is written to the cache and to shared memory by the CTA's
-// threads (the copies stop short of it).  Scores: two threads per slot (one
-// per half of the head dimension, in different warps), reading the key row
-// by 16-byte columns in a per-slot rotated order and the queries from a
-// padded copy, so neither read has bank conflicts.  Softmax over the chunk in
-// fp32.  Values: warp w takes slots 16w..16w+15, lane l dimensions 4l..4l+3,
-// all G heads; the eight warps' sums are added in shared memory.  A chunk
-// writes (acc, max, sum) per head; the last chunk of each group of 16 to
-// finish (an atomic ticket, reset by that chunk for the next replay) merges
-// the group in chunk order, and with more than one group the last group
-// merges the groups.  A (row, head) with a single chunk writes its output
-// directly.  Chunks past the valid length exit at once.
+// Design for GB300: the group's G <= 8 query heads make the scores a
+// product [16 slots x 128] x [128 x 8 heads] and the output a product
+// [128 x 16 slots] x [16 slots x 8 heads] per tile of 16 cached slots, done
+// with warp-level bf16 tensor-core MMAs (m16n8k16, fp32 accumulators).  The
+// fp32 queries and probabilities enter as a pair of bf16 terms (hi + lo,
+// relative error 2^-17), the keys and values are bf16 already, so the
+// products match an fp32 computation to well under the fp32 test bound.
+// Softmax is online and in fp32, per warp, over its tiles.
+//
+// One CTA of four warps per (split, key-value head, batch row).  A split is a
+// run of tiles sized on the device from the actual length so that the grid's
+// CTAs share the cache evenly; warp w takes tiles w, w + 4, ... of its split.
+// Each warp streams its tiles through its own two-stage ring: 32 row copies
+// of 256 bytes (16 key rows, 16 value rows, one 1-D bulk async copy per lane)
+// into rows of 272 bytes, so the ldmatrix reads of 8 rows hit 8 different
+// bank groups.  The new token's row is written to the cache and to the ring
+// by the warp whose tile holds it (the copies stop short of it); rows past it
+// are zero-filled, so a tile never reads a slot it does not own.  At the end
+// the four warps' (max, sum, acc) are combined in shared memory; a single
+// split writes the output, otherwise the split writes a partial result, the
+// last split of each group of 16 (an atomic ticket, reset by that split for
+// the next replay) merges the group in split order, and with more than one
+// group the last group merges the groups.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,13 +42,21 @@
 
 namespace ws {
 
-constexpr int kAttnChunk = 128;           // cached slots per CTA
-constexpr int kAttnDim = 128;             // head dimension
-constexpr int kAttnThreads = 256;
-constexpr int kAttnGroup = 16;            // chunks merged by one first-level merge
+constexpr int kAttnDim = 128;              // head dimension
+constexpr int kAttnTile = 16;              // slots per tile (one MMA's rows)
+constexpr int kAttnWarps = 4;
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kAttnStages = 2;             // ring stages per warp
+constexpr int kAttnPitch = kAttnDim * 2 + 16;  // bytes per staged row
+constexpr int kAttnStageBytes = 2 * kAttnTile * kAttnPitch;  // keys then values
+constexpr int kAttnMaxG = 8;               // query heads per key-value head (MMA columns)
+constexpr int kAttnGroup = 16;             // splits merged by one first-level merge
 constexpr int kPartStride = kAttnDim + 2;  // one partial result: acc[128], max, sum
-constexpr int kQPad = kAttnDim + kAttnDim / 8;  // padded query row: 16 bytes after every 128
-constexpr int kDerrBadPos = 2;            // device error flag: a position outside the cache
+constexpr int kDerrBadPos = 2;             // device error flag: a position outside the cache
+
+// ring, then per barrier one mbarrier per (warp, stage)
+constexpr int kAttnSmem = kAttnWarps * kAttnStages * kAttnStageBytes;
+static_assert(kAttnSmem >= kAttnWarps * kAttnMaxG * kAttnDim * 4, "combine area fits the ring");
 
 struct AttnParams {
   const float* q;      // [B][nh * 128]
@@ -52,10 +67,10 @@ struct AttnParams {
   const int* pos;      // [B]: slot of the new token
   float* out_f32;      // optional [B][nh * 128]
   uint16_t* out_bf16;  // optional bf16 [B][nh * 128]
-  int nh, nkv, S;
+  int nh, nkv, S, G;
   float scale;         // 1 / sqrt(128)
-  float* part0;        // [B][nkv][S / 128][G][130]: per chunk
-  float* part1;        // [B][nkv][groups][G][130]: per group of 16 chunks
+  float* part0;        // [B][nkv][max splits][G][130]: per split
+  float* part1;        // [B][nkv][groups][G][130]: per group of 16 splits
   unsigned* tick0;     // [B][nkv][groups]
   unsigned* tick1;     // [B][nkv]
   int* err;
@@ -66,254 +81,301 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-template <int G>
-struct AttnSmem {
-  static constexpr int kKV = kAttnChunk * kAttnDim * 2;  // bytes of one chunk of keys
-  static constexpr int kQ = G * kQPad * 4;
-  static constexpr int kS = 2 * G * kAttnChunk * 4;      // half-dimension scores, then p
-  static constexpr int bytes = 2 * kKV + kQ + kS;
-};
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
-// Online merge of n partial results (acc, max, sum) in entry order for the
-// heads hp, hp + 2, ... and dimension d: M = max m_c, L = sum e^(m_c - M) l_c,
-// O = sum e^(m_c - M) acc_c.
-template <int G>
-__device__ __forceinline__ void merge_partials(const float* src, int n, int d, int hp,
-                                               float (&O)[(G + 1) / 2], float (&M)[(G + 1) / 2],
-                                               float (&L)[(G + 1) / 2]) {
-#pragma unroll
-  for (int i = 0; i < (G + 1) / 2; ++i) {
-    const int h = hp + 2 * i;
-    float m_run = -INFINITY, l_run = 0.f, o_run = 0.f;
-    if (h < G) {
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi), two values per word
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = bf16x2_bits(a - __low2float(h), b - __high2float(h));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// Online merge of n partial results (acc, max, sum) in entry order, head h,
+// dimension d: M = max m_c, L = sum e^(m_c - M) l_c, O = sum e^(m_c - M) acc_c.
+__device__ __forceinline__ void merge_partials(const float* src, int n, int G, int h, int d,
+                                               float& O, float& M, float& L) {
+  float m_run = -INFINITY, l_run = 0.f, o_run = 0.f;
 #pragma unroll 8
-      for (int c = 0; c < n; ++c) {
-        const float* e = src + ((size_t)c * G + h) * kPartStride;
-        const float m = __ldcg(e + kAttnDim), l = __ldcg(e + kAttnDim + 1), x = __ldcg(e + d);
-        const float mn = fmaxf(m_run, m);
-        const float r = expf(m_run - mn), w = expf(m - mn);
-        l_run = fmaf(l_run, r, w * l);
-        o_run = fmaf(o_run, r, w * x);
-        m_run = mn;
-      }
-    }
-    O[i] = o_run;
-    M[i] = m_run;
-    L[i] = l_run;
+  for (int c = 0; c < n; ++c) {
+    const float* e = src + ((size_t)c * G + h) * kPartStride;
+    const float m = __ldcg(e + kAttnDim), l = __ldcg(e + kAttnDim + 1), x = __ldcg(e + d);
+    const float mn = fmaxf(m_run, m);
+    const float r = expf(m_run - mn), w = expf(m - mn);
+    l_run = fmaf(l_run, r, w * l);
+    o_run = fmaf(o_run, r, w * x);
+    m_run = mn;
   }
+  O = o_run;
+  M = m_run;
+  L = l_run;
 }
 
-template <int G>
-__device__ __forceinline__ void write_output(const AttnParams& a, int b, int g, int d, int hp,
-                                             const float (&O)[(G + 1) / 2],
-                                             const float (&L)[(G + 1) / 2]) {
+// Stage tile `tile` (slots 16 tile .. 16 tile + 15) of one (row, head) into a
+// warp's ring stage: lane l copies key row l (l < 16) or value row l - 16 of
+// the slots before pos; the slot pos comes from the new key and value (the
+// whole warp, 4 dimensions a lane, also written to the cache); later slots
+// are zero.
+__device__ __forceinline__ void stage_tile(const AttnParams& a, size_t row0, size_t kvn, int tile,
+                                           int pos, unsigned char* st, uint64_t* bar, int lane,
+                                           uint64_t pol) {
+  const int slot0 = tile * kAttnTile;
+  const int ncopy = max(0, min(kAttnTile, pos - slot0));  // cached rows of this tile
+  if (lane == 0) mbar_arrive_expect_tx(bar, 2u * ncopy * kAttnDim * 2);
+  __syncwarp();
+  const int r = lane & (kAttnTile - 1);
+  const bool is_v = lane >= kAttnTile;
+  unsigned char* dst = st + (is_v ? kAttnTile * kAttnPitch : 0) + r * kAttnPitch;
+  if (r < ncopy) {
+    fence_proxy_async_smem();  // earlier generic writes of this stage before the copy
+    const uint16_t* src = (is_v ? a.v_cache : a.k_cache) + (row0 + slot0 + r) * kAttnDim;
+    bulk_copy_g2s(dst, src, kAttnDim * 2, bar, pol);
+  } else if (slot0 + r > pos) {
+    uint4* z = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < (G + 1) / 2; ++i) {
-    const int h = hp + 2 * i;
-    if (h >= G) break;
-    const float o = O[i] / L[i];
-    const size_t oi = ((size_t)b * a.nh + g * G + h) * kAttnDim + d;
-    if (a.out_f32) a.out_f32[oi] = o;
-    if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(o);
+    for (int i = 0; i < kAttnDim * 2 / 16; ++i) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
+  if (pos >= slot0 && pos < slot0 + kAttnTile) {
+    const int rp = pos - slot0;
+    const float4 kf = *reinterpret_cast<const float4*>(a.k_new + kvn + lane * 4);
+    const float4 vf = *reinterpret_cast<const float4*>(a.v_new + kvn + lane * 4);
+    const uint2 ku = make_uint2(bf16x2_bits(kf.x, kf.y), bf16x2_bits(kf.z, kf.w));
+    const uint2 vu = make_uint2(bf16x2_bits(vf.x, vf.y), bf16x2_bits(vf.z, vf.w));
+    *reinterpret_cast<uint2*>(st + rp * kAttnPitch + lane * 8) = ku;
+    *reinterpret_cast<uint2*>(st + (kAttnTile + rp) * kAttnPitch + lane * 8) = vu;
+    *reinterpret_cast<uint2*>(a.k_cache + (row0 + pos) * kAttnDim + lane * 4) = ku;
+    *reinterpret_cast<uint2*>(a.v_cache + (row0 + pos) * kAttnDim + lane * 4) = vu;
+  }
+  __syncwarp();  // generic rows visible to the warp's ldmatrix
 }
 
-template <int G>
-__device__ __forceinline__ void write_partial(float* dst, int d, int hp,
-                                              const float (&O)[(G + 1) / 2],
-                                              const float (&M)[(G + 1) / 2],
-                                              const float (&L)[(G + 1) / 2]) {
-#pragma unroll
-  for (int i = 0; i < (G + 1) / 2; ++i) {
-    const int h = hp + 2 * i;
-    if (h >= G) break;
-    dst[h * kPartStride + d] = O[i];
-    if (d == 0) {
-      dst[h * kPartStride + kAttnDim] = M[i];
-      dst[h * kPartStride + kAttnDim + 1] = L[i];
-    }
-  }
-}
-
-template <int G>
 __global__ void __launch_bounds__(kAttnThreads)
     k_decode_attention(const __grid_constant__ AttnParams a) {
-  constexpr int HPT = (G + 1) / 2;  // heads per thread in the combine and merge steps
-  const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int g = blockIdx.y, b = blockIdx.z, G = a.G;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int pos = a.pos[b];
   if (pos < 0 || pos >= a.S) {  // no access outside the cache
-    if (t == 0 && chunk == 0) atomicExch(a.err, kDerrBadPos);
+    if (t == 0 && blockIdx.x == 0) atomicExch(a.err, kDerrBadPos);
     return;
   }
-  const int n_valid = pos + 1;
-  const int nchunks = (n_valid + kAttnChunk - 1) / kAttnChunk;
-  if (chunk >= nchunks) return;
+  // splits: tiles per split a multiple of the warps, at most gridDim.x splits
+  const int ntiles = (pos + kAttnTile) / kAttnTile;
+  int tps = (ntiles + gridDim.x - 1) / gridDim.x;
+  tps = (tps + kAttnWarps - 1) / kAttnWarps * kAttnWarps;
+  const int nsplits = (ntiles + tps - 1) / tps;
+  const int split = blockIdx.x;
+  if (split >= nsplits) return;
+  const int t0 = split * tps, t1 = min(t0 + tps, ntiles);
+  const int nt = t1 - t0 > warp ? (t1 - t0 - warp + kAttnWarps - 1) / kAttnWarps : 0;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* Ks = smem;
-  unsigned char* Vs = smem + AttnSmem<G>::kKV;
-  float* qs = reinterpret_cast<float*>(smem + 2 * AttnSmem<G>::kKV);
-  float* sp = reinterpret_cast<float*>(smem + 2 * AttnSmem<G>::kKV + AttnSmem<G>::kQ);
-  __shared__ uint64_t bar;
-  __shared__ float red[kAttnThreads / 32][G];
-  __shared__ float mx[G], sm[G];
+  __shared__ uint64_t full[kAttnWarps][kAttnStages];
+  __shared__ float cm[kAttnWarps][kAttnMaxG], cl[kAttnWarps][kAttnMaxG];
   __shared__ int last;
+  unsigned char* ring = smem + warp * kAttnStages * kAttnStageBytes;
 
-  const int c0 = chunk * kAttnChunk;
-  const int nv = min(kAttnChunk, n_valid - c0);  // valid slots of this chunk
-  const int nk = min(kAttnChunk, pos - c0);      // of them already cached (all but pos)
-  const size_t row0 = (size_t)(b * a.nkv + g) * a.S + c0;  // first slot of the chunk
-  if (t == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    if (nk > 0) {
-      const uint64_t pol = l2_policy_evict_normal();
-      mbar_arrive_expect_tx(&bar, 2u * nk * kAttnDim * 2);
-      bulk_copy_g2s(Ks, a.k_cache + row0 * kAttnDim, nk * kAttnDim * 2, &bar, pol);
-      bulk_copy_g2s(Vs, a.v_cache + row0 * kAttnDim, nk * kAttnDim * 2, &bar, pol);
-    }
-  }
-  // the new token's key and value: slot pos of the cache and row nk of the chunk
-  if (nk < kAttnChunk) {
-    const int d = t & (kAttnDim - 1);
-    const bool is_v = t >= kAttnDim;
-    const float* src = is_v ? a.v_new : a.k_new;
-    const uint16_t u = to_bf16_bits(src[(size_t)(b * a.nkv + g) * kAttnDim + d]);
-    (is_v ? a.v_cache : a.k_cache)[(row0 + nk) * kAttnDim + d] = u;
-    reinterpret_cast<uint16_t*>(is_v ? Vs : Ks)[nk * kAttnDim + d] = u;
-  }
-  for (int i = t; i < G * kAttnDim; i += kAttnThreads) {
-    const int h = i / kAttnDim, d = i % kAttnDim;
-    qs[h * kQPad + d + (d / 32) * 4] = a.q[((size_t)b * a.nh + g * G + h) * kAttnDim + d];
-  }
-  __syncthreads();  // mbarrier initialised, queries and the new row visible
-  bool ok = nk == 0 || mbar_wait_bounded(&bar, 0, a.timeout_ns);
-  if (__syncthreads_or(!ok)) {
-    if (t == 0) {
-      atomicExch(a.err, (int)DERR_TIMEOUT);
-      mbar_wait_bounded(&bar, 0, a.timeout_ns);  // no copy may land after the CTA exits
-    }
-    return;
-  }
-
-  // scores: warp w, lane l -> slot 32 (w % 4) + l, dimension half w / 4
-  {
-    const int p = warp >> 2, s = ((warp & 3) << 5) | lane;
-    float acc[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.f;
-    if (s < nv) {
-      const unsigned char* kr = Ks + s * kAttnDim * 2;
-      const float4* q4 = reinterpret_cast<const float4*>(qs);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int col = p * 8 + ((c + s) & 7);  // 16-byte column: 8 dimensions
-        const uint4 u = *reinterpret_cast<const uint4*>(kr + col * 16);
-        const float kv[8] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y),
-                             bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
-        const int qi = (col * 8 + (col >> 2) * 4) >> 2;  // padded float4 index
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 qa = q4[h * (kQPad / 4) + qi], qb = q4[h * (kQPad / 4) + qi + 1];
-          acc[h] = fmaf(kv[0], qa.x, acc[h]);
-          acc[h] = fmaf(kv[1], qa.y, acc[h]);
-          acc[h] = fmaf(kv[2], qa.z, acc[h]);
-          acc[h] = fmaf(kv[3], qa.w, acc[h]);
-          acc[h] = fmaf(kv[4], qb.x, acc[h]);
-          acc[h] = fmaf(kv[5], qb.y, acc[h]);
-          acc[h] = fmaf(kv[6], qb.z, acc[h]);
-          acc[h] = fmaf(kv[7], qb.w, acc[h]);
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h) sp[(p * G + h) * kAttnChunk + s] = acc[h];
-  }
-  __syncthreads();
-
-  // softmax over the chunk: warps 0..3, thread t = slot t
-  float sc[G];
-  if (t < kAttnChunk) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      sc[h] = t < nv ? (sp[h * kAttnChunk + t] + sp[(G + h) * kAttnChunk + t]) * a.scale
-                     : -INFINITY;
-      float m = sc[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) red[warp][h] = m;
-    }
-  }
-  __syncthreads();
-  if (t < G) mx[t] = fmaxf(fmaxf(red[0][t], red[1][t]), fmaxf(red[2][t], red[3][t]));
-  __syncthreads();
-  float* ps = sp;  // p[slot][G] over the scores, all of which are read
-  if (t < kAttnChunk) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float pj = t < nv ? expf(sc[h] - mx[h]) : 0.f;
-      ps[t * G + h] = pj;
-      const float w = warp_sum(pj);
-      if (lane == 0) red[warp][h] = w;
-    }
-  }
-  __syncthreads();
-  if (t < G) sm[t] = (red[0][t] + red[1][t]) + (red[2][t] + red[3][t]);
-
-  // values: warp w takes slots 16w..16w+15, lane l dimensions 4l..4l+3
-  float av[G][4];
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) av[h][e] = 0.f;
-  {
-    const int s1 = min(warp * 16 + 16, nv);
-#pragma unroll 4
-    for (int s = warp * 16; s < s1; ++s) {
-      const uint2 u = *reinterpret_cast<const uint2*>(Vs + s * kAttnDim * 2 + lane * 8);
-      const float v[4] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y)};
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pj = ps[s * G + h];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) av[h][e] = fmaf(pj, v[e], av[h][e]);
-      }
-    }
-  }
-  // the eight warps' sums: through the key buffer, no longer read
-  float* racc = reinterpret_cast<float*>(Ks);  // [8][G][128]
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-    *reinterpret_cast<float4*>(racc + (warp * G + h) * kAttnDim + lane * 4) =
-        make_float4(av[h][0], av[h][1], av[h][2], av[h][3]);
-  __syncthreads();  // also: sm written
-  const int d = t & (kAttnDim - 1), hp = t >> 7;
-  float O[HPT], M[HPT], L[HPT];
-#pragma unroll
-  for (int i = 0; i < HPT; ++i) {
-    const int h = hp + 2 * i;
-    float o = 0.f;
-    if (h < G) {
-#pragma unroll
-      for (int w = 0; w < kAttnThreads / 32; ++w) o += racc[(w * G + h) * kAttnDim + d];
-    }
-    O[i] = o;
-    M[i] = h < G ? mx[h] : 0.f;
-    L[i] = h < G ? sm[h] : 1.f;
-  }
-  if (nchunks == 1) {
-    write_output<G>(a, b, g, d, hp, O, L);
-    return;
-  }
-
-  // this chunk's partials, then the ticket of its group
-  const int maxc = a.S / kAttnChunk, maxg = (maxc + kAttnGroup - 1) / kAttnGroup;
   const size_t bg = (size_t)b * a.nkv + g;
-  float* base0 = a.part0 + bg * maxc * G * kPartStride;
-  write_partial<G>(base0 + (size_t)chunk * G * kPartStride, d, hp, O, M, L);
-  const int grp = chunk / kAttnGroup, ngroups = (nchunks + kAttnGroup - 1) / kAttnGroup;
-  const int gsize = min(kAttnGroup, nchunks - grp * kAttnGroup);
+  const size_t row0 = bg * a.S;           // slot 0 of this head's cache
+  const size_t kvn = bg * kAttnDim;       // this head's new key and value
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kAttnStages; ++s) mbar_init(&full[warp][s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t pol = l2_policy_evict_normal();
+#pragma unroll
+  for (int s = 0; s < kAttnStages; ++s)
+    if (s < nt)
+      stage_tile(a, row0, kvn, t0 + warp + s * kAttnWarps, pos, ring + s * kAttnStageBytes,
+                 &full[warp][s], lane, pol);
+
+  // the queries as the MMA's B operand: lane holds head lane / 4, dimensions
+  // 16 k + 2 (lane % 4) + {0, 1} and + 8, as hi and lo bf16 terms
+  uint32_t qh[8][2], ql[8][2];
+  {
+    const int h = lane >> 2, c = (lane & 3) * 2;
+    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+      if (h < G) {
+        x0 = *reinterpret_cast<const float2*>(qr + k * 16 + c);
+        x1 = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
+      }
+      split_bf16x2(x0.x, x0.y, qh[k][0], ql[k][0]);
+      split_bf16x2(x1.x, x1.y, qh[k][1], ql[k][1]);
+    }
+  }
+
+  // per lane: heads c, c + 1 of the accumulators (c = 2 (lane % 4)), dims
+  // 16 mt + lane / 4 and + 8
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[mt][e] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool abort = false;
+  const int rq = lane >> 2;  // this lane's slot rows rq, rq + 8 of a tile
+
+  for (int i = 0; i < nt; ++i) {
+    const int s = i % kAttnStages;
+    const uint32_t par = (i / kAttnStages) & 1;
+    const bool ok = abort || mbar_wait_bounded(&full[warp][s], par, a.timeout_ns);
+    if (__any_sync(0xffffffffu, !ok) && !abort) {
+      abort = true;
+      if (lane == 0) atomicExch(a.err, (int)DERR_TIMEOUT);
+    }
+    if (abort) continue;
+    const int tile = t0 + warp + i * kAttnWarps;
+    const unsigned char* st = ring + s * kAttnStageBytes;
+    const uint32_t sK = smem_addr(st), sV = sK + kAttnTile * kAttnPitch;
+
+    // scores S[slot][head] over the 8 k-steps of 16 dimensions
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const uint32_t base = sK + ((lane & 7) + ((lane >> 3) & 1) * 8) * kAttnPitch + (lane >> 4) * 16;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(base + k * 32, a0, a1, a2, a3);
+        mma_bf16_16816(sc, a0, a1, a2, a3, qh[k][0], qh[k][1]);
+        mma_bf16_16816(sc, a0, a1, a2, a3, ql[k][0], ql[k][1]);
+      }
+    }
+    const int sl = tile * kAttnTile + rq;
+    const bool v0 = sl <= pos, v1 = sl + 8 <= pos;
+    sc[0] = v0 ? sc[0] * a.scale : -INFINITY;
+    sc[1] = v0 ? sc[1] * a.scale : -INFINITY;
+    sc[2] = v1 ? sc[2] * a.scale : -INFINITY;
+    sc[3] = v1 ? sc[3] * a.scale : -INFINITY;
+    float t0m = fmaxf(sc[0], sc[2]), t1m = fmaxf(sc[1], sc[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      t0m = fmaxf(t0m, __shfl_xor_sync(0xffffffffu, t0m, off));
+      t1m = fmaxf(t1m, __shfl_xor_sync(0xffffffffu, t1m, off));
+    }
+    const float n0 = fmaxf(m0, t0m), n1 = fmaxf(m1, t1m);
+    const float r0 = expf(m0 - n0), r1 = expf(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    const float p0 = expf(sc[0] - n0), p1 = expf(sc[1] - n1);
+    const float p2 = expf(sc[2] - n0), p3 = expf(sc[3] - n1);
+    l0 = fmaf(l0, r0, p0 + p2);
+    l1 = fmaf(l1, r1, p1 + p3);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= r0;
+      o[mt][1] *= r1;
+      o[mt][2] *= r0;
+      o[mt][3] *= r1;
+    }
+    // P as the B operand [16 slots][8 heads]: the score fragment transposed
+    uint32_t h01, l01, h23, l23;
+    split_bf16x2(p0, p1, h01, l01);
+    split_bf16x2(p2, p3, h23, l23);
+    const uint32_t bh0 = movmatrix_t(h01), bh1 = movmatrix_t(h23);
+    const uint32_t bl0 = movmatrix_t(l01), bl1 = movmatrix_t(l23);
+    {
+      const uint32_t base = sV + ((lane & 7) + (lane >> 4) * 8) * kAttnPitch + ((lane >> 3) & 1) * 16;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(base + mt * 32, a0, a1, a2, a3);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, bh0, bh1);
+        mma_bf16_16816(o[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+    // every lane's reads of this stage fed the MMAs above: refill it
+    __syncwarp();
+    if (i + kAttnStages < nt)
+      stage_tile(a, row0, kvn, tile + kAttnStages * kAttnWarps, pos, ring + s * kAttnStageBytes,
+                 &full[warp][s], lane, pol);
+  }
+  if (abort && lane == 0) {
+    // no copy may land after the CTA exits: wait (bounded) for the stages
+    for (int i = max(0, nt - kAttnStages); i < nt; ++i)
+      mbar_wait_bounded(&full[warp][i % kAttnStages], (i / kAttnStages) & 1, a.timeout_ns);
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  if (__syncthreads_or(abort)) return;
+
+  // the four warps' results through the ring (no longer read)
+  float* co = reinterpret_cast<float*>(smem);  // [warp][head][128]
+  {
+    const int c = (lane & 3) * 2;
+    if (lane < 4) {
+      cm[warp][c] = m0;
+      cm[warp][c + 1] = m1;
+      cl[warp][c] = l0;
+      cl[warp][c + 1] = l1;
+    }
+    float* cw = co + (size_t)warp * kAttnMaxG * kAttnDim;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d = mt * 16 + rq;
+      cw[c * kAttnDim + d] = o[mt][0];
+      cw[(c + 1) * kAttnDim + d] = o[mt][1];
+      cw[c * kAttnDim + d + 8] = o[mt][2];
+      cw[(c + 1) * kAttnDim + d + 8] = o[mt][3];
+    }
+  }
+  __syncthreads();
+  const int d = t;  // one dimension per thread
+  const bool single = nsplits == 1;
+  const int maxs = a.S / (kAttnTile * kAttnWarps);
+  const int maxg = (maxs + kAttnGroup - 1) / kAttnGroup;
+  float* dst0 = a.part0 + (bg * maxs + split) * G * kPartStride;
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, cm[w][h]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float e = expf(cm[w][h] - M);  // 0 for a warp without tiles
+      L = fmaf(e, cl[w][h], L);
+      O = fmaf(e, co[((size_t)w * kAttnMaxG + h) * kAttnDim + d], O);
+    }
+    if (single) {
+      const float v = O / L;
+      const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
+      if (a.out_f32) a.out_f32[oi] = v;
+      if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
+    } else {
+      dst0[h * kPartStride + d] = O;
+      if (d == 0) {
+        dst0[h * kPartStride + kAttnDim] = M;
+        dst0[h * kPartStride + kAttnDim + 1] = L;
+      }
+    }
+  }
+  if (single) return;
+
+  // the ticket of this split's group
+  const int grp = split / kAttnGroup, ngroups = (nsplits + kAttnGroup - 1) / kAttnGroup;
+  const int gsize = min(kAttnGroup, nsplits - grp * kAttnGroup);
   __threadfence();
   __syncthreads();
   if (t == 0) {
@@ -325,15 +387,27 @@ __global__ void __launch_bounds__(kAttnThreads)
   __syncthreads();
   if (!last) return;
   __threadfence();
-  merge_partials<G>(base0 + (size_t)grp * kAttnGroup * G * kPartStride, gsize, d, hp, O, M, L);
-  if (ngroups == 1) {
-    write_output<G>(a, b, g, d, hp, O, L);
-    return;
+  const float* src0 = a.part0 + (bg * maxs + (size_t)grp * kAttnGroup) * G * kPartStride;
+  float* dst1 = a.part1 + (bg * maxg + grp) * G * kPartStride;
+  for (int h = 0; h < G; ++h) {
+    float O, M, L;
+    merge_partials(src0, gsize, G, h, d, O, M, L);
+    if (ngroups == 1) {
+      const float v = O / L;
+      const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
+      if (a.out_f32) a.out_f32[oi] = v;
+      if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
+    } else {
+      dst1[h * kPartStride + d] = O;
+      if (d == 0) {
+        dst1[h * kPartStride + kAttnDim] = M;
+        dst1[h * kPartStride + kAttnDim + 1] = L;
+      }
+    }
   }
+  if (ngroups == 1) return;
 
-  // the group's merged result, then the ticket of the (row, head)
-  float* base1 = a.part1 + bg * maxg * G * kPartStride;
-  write_partial<G>(base1 + (size_t)grp * G * kPartStride, d, hp, O, M, L);
+  // the ticket of the (row, head)
   __threadfence();
   __syncthreads();
   if (t == 0) {
@@ -345,23 +419,15 @@ __global__ void __launch_bounds__(kAttnThreads)
   __syncthreads();
   if (!last) return;
   __threadfence();
-  merge_partials<G>(base1, ngroups, d, hp, O, M, L);
-  write_output<G>(a, b, g, d, hp, O, L);
-}
-
-typedef void (*AttnKernel)(const AttnParams);
-
-template <int G>
-static cudaError_t launch_attention(const AttnParams& a, dim3 grid, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        k_decode_attention<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnSmem<G>::bytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+  const float* src1 = a.part1 + bg * maxg * G * kPartStride;
+  for (int h = 0; h < G; ++h) {
+    float O, M, L;
+    merge_partials(src1, ngroups, G, h, d, O, M, L);
+    const float v = O / L;
+    const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
+    if (a.out_f32) a.out_f32[oi] = v;
+    if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
   }
-  k_decode_attention<G><<<grid, kAttnThreads, AttnSmem<G>::bytes, st>>>(a);
-  return cudaGetLastError();
 }
 
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
@@ -370,18 +436,44 @@ struct AttnLayout {
   size_t tick1, part0, part1, total;
 };
 
-// Workspace: tickets per group [B][nkv][groups], tickets per (row, head)
-// [B][nkv], partials per chunk, partials per group (each 256-byte aligned).
+// Workspace: tickets per group of 16 splits [B][nkv][groups], tickets per
+// (row, head) [B][nkv], partials per split (at most s_max / 64 splits: four
+// tiles of 16 slots each), partials per group; each part 256-byte aligned.
 static AttnLayout attention_workspace(int B, int nh, int nkv, int s_max) {
-  const int G = nh / nkv, maxc = s_max / kAttnChunk;
-  const int maxg = (maxc + kAttnGroup - 1) / kAttnGroup;
+  const int G = nh / nkv, maxs = s_max / (kAttnTile * kAttnWarps);
+  const int maxg = (maxs + kAttnGroup - 1) / kAttnGroup;
   const size_t bg = (size_t)B * nkv;
   AttnLayout l;
   l.tick1 = align256(bg * maxg * 4);
   l.part0 = l.tick1 + align256(bg * 4);
-  l.part1 = l.part0 + align256(bg * maxc * G * kPartStride * 4);
+  l.part1 = l.part0 + align256(bg * maxs * G * kPartStride * 4);
   l.total = l.part1 + bg * maxg * G * kPartStride * 4;
   return l;
+}
+
+// Splits per (row, head): one wave of resident CTAs over all rows and heads,
+// at most one split per four tiles.
+static int attention_splits(int B, int nkv, int s_max, cudaError_t* err) {
+  static int ctas_per_sm = 0, nsm = 0;
+  if (!ctas_per_sm) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_decode_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kAttnSmem);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm, k_decode_attention,
+                                                        kAttnThreads, kAttnSmem);
+    if (e != cudaSuccess || ctas_per_sm < 1) {
+      *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+      ctas_per_sm = 0;
+      return 0;
+    }
+  }
+  const int maxs = s_max / (kAttnTile * kAttnWarps);
+  const int fill = ctas_per_sm * nsm / (B * nkv);
+  return fill < 1 ? 1 : (fill < maxs ? fill : maxs);
 }
 
 }  // namespace ws
@@ -392,7 +484,8 @@ extern "C" {
 
 size_t ws_attention_workspace_bytes(int B, int n_heads, int n_kv_heads, int head_dim, int s_max) {
   if (B < 1 || B > kMaxBatch || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim != kAttnDim ||
-      s_max < kAttnChunk || s_max % kAttnChunk)
+      s_max < kAttnTile * kAttnWarps || s_max % (kAttnTile * kAttnWarps) ||
+      n_heads / n_kv_heads > kAttnMaxG)
     return 0;
   return attention_workspace(B, n_heads, n_kv_heads, s_max).total;
 }
@@ -408,24 +501,31 @@ ws_status ws_decode_attention(const float* q, const float* k_new, const float* v
     return WS_ERR_ARG;
   }
   if (B < 1 || B > kMaxBatch || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim != kAttnDim ||
-      s_max < kAttnChunk || s_max % kAttnChunk) {
+      s_max < kAttnTile * kAttnWarps || s_max % (kAttnTile * kAttnWarps)) {
     set_error("decode attention: B 1..%d, head_dim %d, n_heads a multiple of n_kv_heads, "
-              "s_max a multiple of %d", kMaxBatch, kAttnDim, kAttnChunk);
+              "s_max a multiple of %d", kMaxBatch, kAttnDim, kAttnTile * kAttnWarps);
     return WS_ERR_SHAPE;
   }
   const int G = n_heads / n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 6 && G != 8) {
-    set_error("decode attention: %d query heads per key-value head (1, 2, 4, 6 or 8)", G);
+  if (G < 1 || G > kAttnMaxG) {
+    set_error("decode attention: %d query heads per key-value head (1 to %d)", G, kAttnMaxG);
     return WS_ERR_SHAPE;
   }
-  if (((uintptr_t)k_cache & 15u) || ((uintptr_t)v_cache & 15u)) {
-    set_error("decode attention: caches must be 16-byte aligned");
+  if (((uintptr_t)k_cache & 15u) || ((uintptr_t)v_cache & 15u) || ((uintptr_t)q & 7u) ||
+      ((uintptr_t)k_new & 15u) || ((uintptr_t)v_new & 15u)) {
+    set_error("decode attention: caches and new rows 16-byte aligned, q 8-byte aligned");
     return WS_ERR_ALIGN;
   }
   const AttnLayout lay = attention_workspace(B, n_heads, n_kv_heads, s_max);
   if (workspace_bytes < lay.total) {
     set_error("workspace too small: need %zu bytes, got %zu", lay.total, workspace_bytes);
     return WS_ERR_ARG;
+  }
+  cudaError_t e = cudaSuccess;
+  const int splits = attention_splits(B, n_kv_heads, s_max, &e);
+  if (!splits) {
+    set_error("decode attention setup failed: %s", cudaGetErrorString(e));
+    return WS_ERR_CUDA;
   }
   AttnParams a;
   memset(&a, 0, sizeof a);
@@ -440,6 +540,7 @@ ws_status ws_decode_attention(const float* q, const float* k_new, const float* v
   a.nh = n_heads;
   a.nkv = n_kv_heads;
   a.S = s_max;
+  a.G = G;
   a.scale = 1.0f / sqrtf((float)kAttnDim);
   char* w = static_cast<char*>(workspace);
   a.tick0 = reinterpret_cast<unsigned*>(w);
@@ -450,16 +551,9 @@ ws_status ws_decode_attention(const float* q, const float* k_new, const float* v
   a.timeout_ns = tuning().timeout_ns;
   // the tickets are zero on entry (a zero-filled workspace; the last arrival
   // at every ticket resets it, rows with a bad position take none)
-  const dim3 grid(s_max / kAttnChunk, n_kv_heads, B);
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = cudaSuccess;
-  switch (G) {
-    case 1: e = launch_attention<1>(a, grid, st); break;
-    case 2: e = launch_attention<2>(a, grid, st); break;
-    case 4: e = launch_attention<4>(a, grid, st); break;
-    case 6: e = launch_attention<6>(a, grid, st); break;
-    default: e = launch_attention<8>(a, grid, st); break;
-  }
+  const dim3 grid(splits, n_kv_heads, B);
+  k_decode_attention<<<grid, kAttnThreads, kAttnSmem, (cudaStream_t)stream>>>(a);
+  e = cudaGetLastError();
   if (e != cudaSuccess) {
     set_error("launch failed: %s", cudaGetErrorString(e));
     return WS_ERR_CUDA;
