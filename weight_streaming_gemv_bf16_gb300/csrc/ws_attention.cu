@@ -56,7 +56,8 @@ constexpr int kDerrBadPos = 2;             // device error flag: a position outs
 
 // ring, then per barrier one mbarrier per (warp, stage)
 constexpr int kAttnSmem = kAttnWarps * kAttnStages * kAttnStageBytes;
-static_assert(kAttnSmem >= kAttnWarps * kAttnMaxG * kAttnDim * 4, "combine area fits the ring");
+static_assert(kAttnSmem >= kAttnWarps * kAttnMaxG * kAttnDim * 4 + 256 * kAttnMaxG * 4,
+              "combine area and merge weights fit the ring");
 
 struct AttnParams {
   const float* q;      // [B][nh * 128]
@@ -107,24 +108,80 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
   return d;
 }
 
-// Online merge of n partial results (acc, max, sum) in entry order, head h,
-// dimension d: M = max m_c, L = sum e^(m_c - M) l_c, O = sum e^(m_c - M) acc_c.
-__device__ __forceinline__ void merge_partials(const float* src, int n, int G, int h, int d,
-                                               float& O, float& M, float& L) {
-  float m_run = -INFINITY, l_run = 0.f, o_run = 0.f;
-#pragma unroll 8
-  for (int c = 0; c < n; ++c) {
-    const float* e = src + ((size_t)c * G + h) * kPartStride;
-    const float m = __ldcg(e + kAttnDim), l = __ldcg(e + kAttnDim + 1), x = __ldcg(e + d);
-    const float mn = fmaxf(m_run, m);
-    const float r = expf(m_run - mn), w = expf(m - mn);
-    l_run = fmaf(l_run, r, w * l);
-    o_run = fmaf(o_run, r, w * x);
-    m_run = mn;
+// Merge of n partial results (acc, max, sum) for the G heads, by the whole
+// CTA, thread t = dimension t: M = max m_c, L = sum e^(m_c - M) l_c,
+// O = sum e^(m_c - M) acc_c.  Warp 0 forms M, L and the weights e^(m_c - M)
+// from one pass of loads (each lane an online max and sum over its entries,
+// combined across the warp) while every thread already has its first eight
+// entries' values in flight.  wsm holds n x 8 weights, hsm M then L per head.
+constexpr int kMergeBatch = 8;
+constexpr int kMergeMax = 256;  // entries one merge takes (weights buffer)
+
+__device__ __forceinline__ void merge_cta(const float* src, int n, int G, int t, float* wsm,
+                                          float* hsm, float (&O)[kAttnMaxG]) {
+  const int lane = t & 31;
+  float x[kMergeBatch][kAttnMaxG];
+#pragma unroll
+  for (int c = 0; c < kMergeBatch; ++c)
+#pragma unroll
+    for (int h = 0; h < kAttnMaxG; ++h)
+      x[c][h] = (c < n && h < G) ? __ldcg(src + ((size_t)c * G + h) * kPartStride + t) : 0.f;
+  if (t < 32) {
+    float mr[kAttnMaxG], lr[kAttnMaxG];
+#pragma unroll
+    for (int h = 0; h < kAttnMaxG; ++h) {
+      mr[h] = -INFINITY;
+      lr[h] = 0.f;
+    }
+    for (int c = lane; c < n; c += 32) {
+#pragma unroll
+      for (int h = 0; h < kAttnMaxG; ++h) {
+        if (h < G) {
+          const float* e = src + ((size_t)c * G + h) * kPartStride + kAttnDim;
+          const float m = __ldcg(e), l = __ldcg(e + 1);
+          wsm[c * kAttnMaxG + h] = m;
+          const float mn = fmaxf(mr[h], m);
+          lr[h] = fmaf(lr[h], expf(mr[h] - mn), l * expf(m - mn));
+          mr[h] = mn;
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kAttnMaxG; ++h) {
+      if (h < G) {
+        float M = mr[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = lr[h] * expf(mr[h] - M);  // 0 for a lane without entries
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (lane == 0) {
+          hsm[h] = M;
+          hsm[kAttnMaxG + h] = L;
+        }
+        for (int c = lane; c < n; c += 32) wsm[c * kAttnMaxG + h] = expf(wsm[c * kAttnMaxG + h] - M);
+      }
+    }
   }
-  O = o_run;
-  M = m_run;
-  L = l_run;
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < kAttnMaxG; ++h) O[h] = 0.f;
+  for (int c0 = 0; c0 < n; c0 += kMergeBatch) {
+    if (c0 > 0) {
+#pragma unroll
+      for (int c = 0; c < kMergeBatch; ++c)
+#pragma unroll
+        for (int h = 0; h < kAttnMaxG; ++h)
+          x[c][h] = (c0 + c < n && h < G)
+                        ? __ldcg(src + ((size_t)(c0 + c) * G + h) * kPartStride + t)
+                        : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < kMergeBatch; ++c)
+      if (c0 + c < n)
+#pragma unroll
+        for (int h = 0; h < kAttnMaxG; ++h) O[h] = fmaf(wsm[(c0 + c) * kAttnMaxG + h], x[c][h], O[h]);
+  }
 }
 
 // Stage tile `tile` (slots 16 tile .. 16 tile + 15) of one (row, head) into a
@@ -165,10 +222,43 @@ __device__ __forceinline__ void stage_tile(const AttnParams& a, size_t row0, siz
   __syncwarp();  // generic rows visible to the warp's ldmatrix
 }
 
+// out[h][d] = O[h] / L[h] for the G heads of key-value head g (L in hsm[8..15])
+__device__ __forceinline__ void write_heads(const AttnParams& a, int b, int g, int d,
+                                            const float (&O)[kAttnMaxG], const float* hsm) {
+#pragma unroll
+  for (int h = 0; h < kAttnMaxG; ++h) {
+    if (h < a.G) {
+      const float v = O[h] / hsm[kAttnMaxG + h];
+      const size_t oi = ((size_t)b * a.nh + (size_t)g * a.G + h) * kAttnDim + d;
+      if (a.out_f32) a.out_f32[oi] = v;
+      if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kAttnThreads)
     k_decode_attention(const __grid_constant__ AttnParams a) {
   const int g = blockIdx.y, b = blockIdx.z, G = a.G;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  // (loaded before the position, which they do not depend on)
+  // the queries as the MMA's B operand: lane holds head lane / 4, dimensions
+  // 16 k + 2 (lane % 4) + {0, 1} and + 8, as hi and lo bf16 terms
+  uint32_t qh[8][2], ql[8][2];
+  {
+    const int h = lane >> 2, c = (lane & 3) * 2;
+    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+      if (h < G) {
+        x0 = *reinterpret_cast<const float2*>(qr + k * 16 + c);
+        x1 = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
+      }
+      split_bf16x2(x0.x, x0.y, qh[k][0], ql[k][0]);
+      split_bf16x2(x1.x, x1.y, qh[k][1], ql[k][1]);
+    }
+  }
+
   const int pos = a.pos[b];
   if (pos < 0 || pos >= a.S) {  // no access outside the cache
     if (t == 0 && blockIdx.x == 0) atomicExch(a.err, kDerrBadPos);
@@ -205,24 +295,6 @@ __global__ void __launch_bounds__(kAttnThreads)
     if (s < nt)
       stage_tile(a, row0, kvn, t0 + warp + s * kAttnWarps, pos, ring + s * kAttnStageBytes,
                  &full[warp][s], lane, pol);
-
-  // the queries as the MMA's B operand: lane holds head lane / 4, dimensions
-  // 16 k + 2 (lane % 4) + {0, 1} and + 8, as hi and lo bf16 terms
-  uint32_t qh[8][2], ql[8][2];
-  {
-    const int h = lane >> 2, c = (lane & 3) * 2;
-    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
-      if (h < G) {
-        x0 = *reinterpret_cast<const float2*>(qr + k * 16 + c);
-        x1 = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
-      }
-      split_bf16x2(x0.x, x0.y, qh[k][0], ql[k][0]);
-      split_bf16x2(x1.x, x1.y, qh[k][1], ql[k][1]);
-    }
-  }
 
   // per lane: heads c, c + 1 of the accumulators (c = 2 (lane % 4)), dims
   // 16 mt + lane / 4 and + 8
@@ -387,25 +459,26 @@ __global__ void __launch_bounds__(kAttnThreads)
   __syncthreads();
   if (!last) return;
   __threadfence();
+  float* wsm = reinterpret_cast<float*>(smem + kAttnWarps * kAttnMaxG * kAttnDim * 4);
+  float* hsm = cm[0];  // M then L per head (the warp maxima are no longer read)
+  float O[kAttnMaxG];
   const float* src0 = a.part0 + (bg * maxs + (size_t)grp * kAttnGroup) * G * kPartStride;
+  merge_cta(src0, gsize, G, t, wsm, hsm, O);
+  if (ngroups == 1) {
+    write_heads(a, b, g, d, O, hsm);
+    return;
+  }
   float* dst1 = a.part1 + (bg * maxg + grp) * G * kPartStride;
-  for (int h = 0; h < G; ++h) {
-    float O, M, L;
-    merge_partials(src0, gsize, G, h, d, O, M, L);
-    if (ngroups == 1) {
-      const float v = O / L;
-      const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
-      if (a.out_f32) a.out_f32[oi] = v;
-      if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
-    } else {
-      dst1[h * kPartStride + d] = O;
+#pragma unroll
+  for (int h = 0; h < kAttnMaxG; ++h) {
+    if (h < G) {
+      dst1[h * kPartStride + d] = O[h];
       if (d == 0) {
-        dst1[h * kPartStride + kAttnDim] = M;
-        dst1[h * kPartStride + kAttnDim + 1] = L;
+        dst1[h * kPartStride + kAttnDim] = hsm[h];
+        dst1[h * kPartStride + kAttnDim + 1] = hsm[kAttnMaxG + h];
       }
     }
   }
-  if (ngroups == 1) return;
 
   // the ticket of the (row, head)
   __threadfence();
@@ -419,15 +492,8 @@ __global__ void __launch_bounds__(kAttnThreads)
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const float* src1 = a.part1 + bg * maxg * G * kPartStride;
-  for (int h = 0; h < G; ++h) {
-    float O, M, L;
-    merge_partials(src1, ngroups, G, h, d, O, M, L);
-    const float v = O / L;
-    const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
-    if (a.out_f32) a.out_f32[oi] = v;
-    if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
-  }
+  merge_cta(a.part1 + bg * maxg * G * kPartStride, ngroups, G, t, wsm, hsm, O);
+  write_heads(a, b, g, d, O, hsm);
 }
 
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
@@ -473,7 +539,10 @@ static int attention_splits(int B, int nkv, int s_max, cudaError_t* err) {
   }
   const int maxs = s_max / (kAttnTile * kAttnWarps);
   const int fill = ctas_per_sm * nsm / (B * nkv);
-  return fill < 1 ? 1 : (fill < maxs ? fill : maxs);
+  int splits = fill < 1 ? 1 : (fill < maxs ? fill : maxs);
+  // a merge takes at most kMergeMax entries: groups of the splits included
+  if (splits > kAttnGroup * kMergeMax) splits = kAttnGroup * kMergeMax;
+  return splits;
 }
 
 }  // namespace ws
