@@ -94,6 +94,15 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
   lo = bf16x2_bits(a - __low2float(h), b - __high2float(h));
 }
 
+// Ticket of a merge: the CTA's writes precede thread 0's release (they come
+// before a CTA barrier), and the last arrival's acquire precedes the merge's
+// reads (they come after the next barrier), so one thread fences, not all.
+__device__ __forceinline__ unsigned ticket_acq_rel(unsigned* p) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
                                           uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -119,13 +128,18 @@ constexpr int kMergeMax = 256;  // entries one merge takes (weights buffer)
 
 __device__ __forceinline__ void merge_cta(const float* src, int n, int G, int t, float* wsm,
                                           float* hsm, float (&O)[kAttnMaxG]) {
+  // every load is unconditional (entry and head indices clamped into range,
+  // the extra values unused), so a thread's loads are all in flight at once
   const int lane = t & 31;
+  int hc[kAttnMaxG];
+#pragma unroll
+  for (int h = 0; h < kAttnMaxG; ++h) hc[h] = min(h, G - 1);
   float x[kMergeBatch][kAttnMaxG];
 #pragma unroll
   for (int c = 0; c < kMergeBatch; ++c)
 #pragma unroll
     for (int h = 0; h < kAttnMaxG; ++h)
-      x[c][h] = (c < n && h < G) ? __ldcg(src + ((size_t)c * G + h) * kPartStride + t) : 0.f;
+      x[c][h] = __ldcg(src + ((size_t)min(c, n - 1) * G + hc[h]) * kPartStride + t);
   if (t < 32) {
     float mr[kAttnMaxG], lr[kAttnMaxG];
 #pragma unroll
@@ -133,35 +147,52 @@ __device__ __forceinline__ void merge_cta(const float* src, int n, int G, int t,
       mr[h] = -INFINITY;
       lr[h] = 0.f;
     }
-    for (int c = lane; c < n; c += 32) {
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int c = c0 + lane;
+      float m[kAttnMaxG], l[kAttnMaxG];
 #pragma unroll
       for (int h = 0; h < kAttnMaxG; ++h) {
-        if (h < G) {
-          const float* e = src + ((size_t)c * G + h) * kPartStride + kAttnDim;
-          const float m = __ldcg(e), l = __ldcg(e + 1);
-          wsm[c * kAttnMaxG + h] = m;
-          const float mn = fmaxf(mr[h], m);
-          lr[h] = fmaf(lr[h], expf(mr[h] - mn), l * expf(m - mn));
+        const float* e = src + ((size_t)min(c, n - 1) * G + hc[h]) * kPartStride + kAttnDim;
+        m[h] = __ldcg(e);
+        l[h] = __ldcg(e + 1);
+      }
+      if (c < n) {
+#pragma unroll
+        for (int h = 0; h < kAttnMaxG; ++h) {
+          wsm[c * kAttnMaxG + h] = m[h];
+          const float mn = fmaxf(mr[h], m[h]);
+          lr[h] = fmaf(lr[h], expf(mr[h] - mn), l[h] * expf(m[h] - mn));
           mr[h] = mn;
         }
       }
     }
+    float M[kAttnMaxG], L[kAttnMaxG];
 #pragma unroll
-    for (int h = 0; h < kAttnMaxG; ++h) {
-      if (h < G) {
-        float M = mr[h];
+    for (int h = 0; h < kAttnMaxG; ++h) M[h] = mr[h];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = lr[h] * expf(mr[h] - M);  // 0 for a lane without entries
+    for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        if (lane == 0) {
-          hsm[h] = M;
-          hsm[kAttnMaxG + h] = L;
+      for (int h = 0; h < kAttnMaxG; ++h) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+#pragma unroll
+    for (int h = 0; h < kAttnMaxG; ++h) L[h] = lr[h] * expf(mr[h] - M[h]);  // 0 without entries
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+      for (int h = 0; h < kAttnMaxG; ++h) L[h] += __shfl_xor_sync(0xffffffffu, L[h], off);
+    if (lane < kAttnMaxG) {
+      hsm[lane] = M[0];
+      hsm[kAttnMaxG + lane] = L[0];
+#pragma unroll
+      for (int h = 1; h < kAttnMaxG; ++h)
+        if (lane == h) {
+          hsm[lane] = M[h];
+          hsm[kAttnMaxG + lane] = L[h];
         }
-        for (int c = lane; c < n; c += 32) wsm[c * kAttnMaxG + h] = expf(wsm[c * kAttnMaxG + h] - M);
-      }
     }
+    for (int c = lane; c < n; c += 32)
+#pragma unroll
+      for (int h = 0; h < kAttnMaxG; ++h)
+        wsm[c * kAttnMaxG + h] = expf(wsm[c * kAttnMaxG + h] - M[h]);
   }
   __syncthreads();
 #pragma unroll
@@ -172,9 +203,7 @@ __device__ __forceinline__ void merge_cta(const float* src, int n, int G, int t,
       for (int c = 0; c < kMergeBatch; ++c)
 #pragma unroll
         for (int h = 0; h < kAttnMaxG; ++h)
-          x[c][h] = (c0 + c < n && h < G)
-                        ? __ldcg(src + ((size_t)(c0 + c) * G + h) * kPartStride + t)
-                        : 0.f;
+          x[c][h] = __ldcg(src + ((size_t)min(c0 + c, n - 1) * G + hc[h]) * kPartStride + t);
     }
 #pragma unroll
     for (int c = 0; c < kMergeBatch; ++c)
@@ -245,17 +274,21 @@ __global__ void __launch_bounds__(kAttnThreads)
   // 16 k + 2 (lane % 4) + {0, 1} and + 8, as hi and lo bf16 terms
   uint32_t qh[8][2], ql[8][2];
   {
+    // heads past G read head 0's row (all loads unconditional, in flight
+    // together) and are zeroed
     const int h = lane >> 2, c = (lane & 3) * 2;
-    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim;
+    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + (h < G ? h : 0)) * kAttnDim;
+    float2 x0[8], x1[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
-      if (h < G) {
-        x0 = *reinterpret_cast<const float2*>(qr + k * 16 + c);
-        x1 = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
-      }
-      split_bf16x2(x0.x, x0.y, qh[k][0], ql[k][0]);
-      split_bf16x2(x1.x, x1.y, qh[k][1], ql[k][1]);
+      x0[k] = *reinterpret_cast<const float2*>(qr + k * 16 + c);
+      x1[k] = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
+    }
+    const float z = h < G ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      split_bf16x2(x0[k].x * z, x0[k].y * z, qh[k][0], ql[k][0]);
+      split_bf16x2(x1[k].x * z, x1[k].y * z, qh[k][1], ql[k][1]);
     }
   }
 
@@ -264,10 +297,16 @@ __global__ void __launch_bounds__(kAttnThreads)
     if (t == 0 && blockIdx.x == 0) atomicExch(a.err, kDerrBadPos);
     return;
   }
-  // splits: tiles per split a multiple of the warps, at most gridDim.x splits
+  // splits: tiles per split a multiple of the warps, at most gridDim.x
+  // splits; at most one merge group (16 splits) while that keeps a split at
+  // 32 tiles or fewer, since a second merge level costs more (three more
+  // round trips to L2) than the longer splits
   const int ntiles = (pos + kAttnTile) / kAttnTile;
   int tps = (ntiles + gridDim.x - 1) / gridDim.x;
   tps = (tps + kAttnWarps - 1) / kAttnWarps * kAttnWarps;
+  int tps_one = (ntiles + kAttnGroup - 1) / kAttnGroup;
+  tps_one = (tps_one + kAttnWarps - 1) / kAttnWarps * kAttnWarps;
+  if (tps_one <= 8 * kAttnWarps && tps_one > tps) tps = tps_one;
   const int nsplits = (ntiles + tps - 1) / tps;
   const int split = blockIdx.x;
   if (split >= nsplits) return;
@@ -419,7 +458,11 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int maxs = a.S / (kAttnTile * kAttnWarps);
   const int maxg = (maxs + kAttnGroup - 1) / kAttnGroup;
   float* dst0 = a.part0 + (bg * maxs + split) * G * kPartStride;
-  for (int h = 0; h < G; ++h) {
+  // all heads at once (unrolled over 8, heads past G unused): the shared
+  // memory reads and exponentials of different heads overlap
+  float Mh[kAttnMaxG], Lh[kAttnMaxG], Oh[kAttnMaxG];
+#pragma unroll
+  for (int h = 0; h < kAttnMaxG; ++h) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, cm[w][h]);
@@ -430,16 +473,24 @@ __global__ void __launch_bounds__(kAttnThreads)
       L = fmaf(e, cl[w][h], L);
       O = fmaf(e, co[((size_t)w * kAttnMaxG + h) * kAttnDim + d], O);
     }
-    if (single) {
-      const float v = O / L;
-      const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
-      if (a.out_f32) a.out_f32[oi] = v;
-      if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
-    } else {
-      dst0[h * kPartStride + d] = O;
-      if (d == 0) {
-        dst0[h * kPartStride + kAttnDim] = M;
-        dst0[h * kPartStride + kAttnDim + 1] = L;
+    Mh[h] = M;
+    Lh[h] = L;
+    Oh[h] = O;
+  }
+#pragma unroll
+  for (int h = 0; h < kAttnMaxG; ++h) {
+    if (h < G) {
+      if (single) {
+        const float v = Oh[h] / Lh[h];
+        const size_t oi = ((size_t)b * a.nh + (size_t)g * G + h) * kAttnDim + d;
+        if (a.out_f32) a.out_f32[oi] = v;
+        if (a.out_bf16) a.out_bf16[oi] = to_bf16_bits(v);
+      } else {
+        dst0[h * kPartStride + d] = Oh[h];
+        if (d == 0) {
+          dst0[h * kPartStride + kAttnDim] = Mh[h];
+          dst0[h * kPartStride + kAttnDim + 1] = Lh[h];
+        }
       }
     }
   }
@@ -448,17 +499,15 @@ __global__ void __launch_bounds__(kAttnThreads)
   // the ticket of this split's group
   const int grp = split / kAttnGroup, ngroups = (nsplits + kAttnGroup - 1) / kAttnGroup;
   const int gsize = min(kAttnGroup, nsplits - grp * kAttnGroup);
-  __threadfence();
   __syncthreads();
   if (t == 0) {
     unsigned* tk = a.tick0 + bg * maxg + grp;
-    const unsigned old = atomicAdd(tk, 1u);
+    const unsigned old = ticket_acq_rel(tk);
     last = old == (unsigned)(gsize - 1);
     if (last) atomicExch(tk, 0u);
   }
   __syncthreads();
   if (!last) return;
-  __threadfence();
   float* wsm = reinterpret_cast<float*>(smem + kAttnWarps * kAttnMaxG * kAttnDim * 4);
   float* hsm = cm[0];  // M then L per head (the warp maxima are no longer read)
   float O[kAttnMaxG];
@@ -481,17 +530,15 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
 
   // the ticket of the (row, head)
-  __threadfence();
   __syncthreads();
   if (t == 0) {
     unsigned* tk = a.tick1 + bg;
-    const unsigned old = atomicAdd(tk, 1u);
+    const unsigned old = ticket_acq_rel(tk);
     last = old == (unsigned)(ngroups - 1);
     if (last) atomicExch(tk, 0u);
   }
   __syncthreads();
   if (!last) return;
-  __threadfence();
   merge_cta(a.part1 + bg * maxg * G * kPartStride, ngroups, G, t, wsm, hsm, O);
   write_heads(a, b, g, d, O, hsm);
 }
