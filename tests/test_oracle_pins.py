@@ -455,3 +455,138 @@ def test_attention_query_heads_share_their_group():
     o = r["out"][0].reshape(nh, d)
     assert np.array_equal(o[0], o[1])
     assert not np.allclose(o[0], o[2])
+
+
+# ---- 4-bit group-128 weights ("One Token, Kernel by Kernel", "4-bit weights")
+
+from oracle import q4 as oq4  # noqa: E402
+
+
+def _bf16_value(bits):
+    import struct
+    return struct.unpack("<f", struct.pack("<I", int(bits) << 16))[0]
+
+
+def test_q4_golden_group_layout_and_dequant():
+    """One group (K = 128) written byte by byte from the format: codes
+    q_k = k mod 16 give word 0x75316420 for k = 0..7 (even k in the low
+    half's nibbles 0..3, odd k in the high half's) and 0xFDB9ECA8 for
+    k = 8..15; scale 0.5 (0x3F00), zero -1.0 (0xBF80) right after the 64
+    bytes of codes, padded to 80 bytes.  Weight k is 0.5 (k mod 16 - 8) - 1."""
+    import struct
+    row = b"".join(struct.pack("<II", 0x75316420, 0xFDB9ECA8) for _ in range(8))
+    row += struct.pack("<HH", 0x3F00, 0xBF80) + bytes(12)
+    assert len(row) == 80 == oq4.row_bytes(128)
+    P = np.frombuffer(row, np.uint8)[None, :]
+    W = oq4.dequant(P, 128)
+    assert np.array_equal(W[0], [0.5 * (k % 16 - 8) - 1.0 for k in range(128)])
+
+
+def test_q4_super_group_and_tail_layout():
+    """K = 640: one super-group of four groups (4 x 64 bytes of codes, then
+    the four (s, z) pairs, 272 bytes) and a tail of one group (64 + 4 bytes
+    padded to 80).  All codes 8, so each weight is its group's zero, here
+    g + 1 for group g; scale 1."""
+    import struct
+    zero_bits = [0x3F80, 0x4000, 0x4040, 0x4080, 0x40A0]  # 1, 2, 3, 4, 5
+    codes8 = struct.pack("<I", 0x88888888) * 16
+    row = codes8 * 4 + b"".join(struct.pack("<HH", 0x3F80, z) for z in zero_bits[:4])
+    row += codes8 + struct.pack("<HH", 0x3F80, zero_bits[4]) + bytes(12)
+    assert len(row) == 352 == oq4.row_bytes(640)
+    W = oq4.dequant(np.frombuffer(row, np.uint8)[None, :], 640)
+    for g in range(5):
+        assert np.all(W[0, g * 128:(g + 1) * 128] == g + 1)
+    # the Qwen2.5-1.5B row lengths: 3 super-groups; 17 and a tail of two groups
+    assert oq4.row_bytes(1536) == 3 * 272
+    assert oq4.row_bytes(8960) == 17 * 272 + 144
+
+
+def _brute_q4_row(row_bytes, K):
+    """Weights of one packed row by plain loops over bytes (nibble m of a
+    32-bit word, m = 0..7 from the least significant bits, is weight 2m for
+    m < 4 and 2(m - 4) + 1 for m >= 4 of the word's eight)."""
+    out = [0.0] * K
+    ng = K // 128
+    off = 0
+    for g0 in range(0, ng, 4):
+        n = min(4, ng - g0)
+        for gi in range(n):
+            g = g0 + gi
+            sb = row_bytes[off + 64 * n + 4 * gi] | (row_bytes[off + 64 * n + 4 * gi + 1] << 8)
+            zb = row_bytes[off + 64 * n + 4 * gi + 2] | (row_bytes[off + 64 * n + 4 * gi + 3] << 8)
+            s, z = _bf16_value(sb), _bf16_value(zb)
+            for i in range(16):
+                b0 = off + 64 * gi + 4 * i
+                word = sum(row_bytes[b0 + t] << (8 * t) for t in range(4))
+                for m in range(8):
+                    q = (word >> (4 * m)) & 15
+                    kk = 2 * m if m < 4 else 2 * (m - 4) + 1
+                    out[g * 128 + 8 * i + kk] = s * (q - 8) + z
+        off += ((64 + 4) * n + 15) // 16 * 16
+    return out
+
+
+def test_q4_gemv_matches_brute_force():
+    rng = np.random.default_rng(5)
+    M, K, B = 3, 640, 2
+    codes = rng.integers(0, 16, size=(M, K), dtype=np.uint8)
+    s = oracle.f64_to_bf16(rng.uniform(0.001, 0.01, size=(M, K // 128)))
+    z = oracle.f64_to_bf16(rng.normal(0, 0.01, size=(M, K // 128)))
+    P = oq4.pack(codes, s, z)
+    x = oracle.bf16_to_f64(oracle.f64_to_bf16(rng.normal(size=(B, K))))
+    y = oq4.gemv(P, K, x)
+    for m in range(M):
+        w = _brute_q4_row([int(v) for v in P[m]], K)
+        for b in range(B):
+            ref = sum(w[k] * x[b, k] for k in range(K))
+            assert abs(y[b, m] - ref) <= 1e-12 * max(1.0, abs(ref))
+    cu, su, zu = oq4.unpack(P, K)
+    assert np.array_equal(cu, codes) and np.array_equal(su, s) and np.array_equal(zu, z)
+
+
+def test_q4_gemv_all_codes_eight_is_zero_times_group_sums():
+    rng = np.random.default_rng(6)
+    M, K = 4, 512
+    z = oracle.f64_to_bf16(rng.normal(0, 1, size=(M, K // 128)))
+    s = oracle.f64_to_bf16(rng.uniform(0.1, 1, size=(M, K // 128)))
+    P = oq4.pack(np.full((M, K), 8, np.uint8), s, z)
+    x = rng.normal(size=(1, K))
+    zg = oracle.bf16_to_f64(z)
+    ref = [sum(zg[m, g] * x[0, g * 128:(g + 1) * 128].sum() for g in range(K // 128))
+           for m in range(M)]
+    assert np.allclose(oq4.gemv(P, K, x)[0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_q4_quantizer_error_bound_and_special_groups():
+    rng = np.random.default_rng(7)
+    M, K = 6, 512
+    W = rng.normal(0, 0.02, size=(M, K))
+    W[1, :128] = 0.25            # a constant group: scale 0, codes 8, exact
+    W[2, 128:256] = np.linspace(-1, 1, 128)
+    Wb = oracle.f64_to_bf16(W)
+    codes, s, z = oq4.quantize(Wb)
+    assert codes.min() >= 0 and codes.max() <= 15
+    assert s[1, 0] == 0 and np.all(codes[1, :128] == 8)
+    Wq = oq4.dequant(oq4.pack(codes, s, z), K)
+    w = oracle.bf16_to_f64(Wb)
+    sg = np.repeat(oracle.bf16_to_f64(s), 128, axis=1)
+    zg = np.repeat(oracle.bf16_to_f64(z), 128, axis=1)
+    # half a step, plus what rounding s and z to bf16 moves the grid's ends by
+    bound = 0.5 * sg + 2.0 ** -8 * (np.abs(zg) + 8 * sg) + 1e-30
+    assert np.all(np.abs(Wq - w) <= bound)
+    assert np.all(Wq[1, :128] == 0.25)
+    # a group's minimum and maximum land on the end codes (within one step)
+    g = codes[2, 128:256]
+    assert g[0] <= 1 and g[-1] >= 14
+
+
+def test_q4_model_size_matches_the_pages():
+    """Qwen2.5-1.5B's linear layers and LM head: 3.09 GB in bf16, 0.82 GB in
+    this format, 3.76 times smaller (the pages' figures)."""
+    blk = [(1536, 1536), (256, 1536), (256, 1536), (1536, 1536), (8960, 1536),
+           (8960, 1536), (1536, 8960)]
+    bf16 = 28 * sum(M * K * 2 for M, K in blk) + 151936 * 1536 * 2
+    q4b = 28 * sum(M * oq4.row_bytes(K) for M, K in blk) + 151936 * oq4.row_bytes(1536)
+    assert round(bf16 / 1e9, 2) == 3.09
+    assert round(q4b / 1e9, 2) == 0.82
+    assert round(bf16 / q4b, 2) == 3.76
