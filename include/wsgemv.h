@@ -99,6 +99,32 @@ ws_status ws_gemv_bf16(const void *W, const void *x, float *y, int M, int K, int
 ws_status ws_gemv_bf16_noalloc(const void *W, const void *x, float *y, int M, int K, int B,
                                ws_stream_t stream);
 
+/* 4-bit group-128 weights ("One Token, Kernel by Kernel: A Decode Step on a
+ * Laptop GPU", "4-bit weights": every linear layer quantised to 4-bit
+ * integers in groups of 128, 0.82 GB instead of 3.09 for Qwen2.5-1.5B).  A
+ * group is 128 consecutive weights of a row with a bf16 scale s and zero z;
+ * code q (0..15) stands for s * (q - 8) + z.  A packed row (ws_q4_row_bytes(K)
+ * bytes, K a multiple of 128) is a run of super-groups of four groups: their
+ * codes, 64 bytes a group, in which 32-bit little-endian word i holds weights
+ * 8i .. 8i+7 (bits 4j..4j+3: weight 8i+2j; bits 16+4j..16+4j+3: weight
+ * 8i+2j+1), then their (s, z) pairs (4 bytes each, s first), zero-padded to
+ * 16 bytes: 272 bytes for four groups, 4.25 bits a weight.
+ *
+ * ws_q4_row_bytes: bytes of one packed row, or 0 when K is not a positive
+ * multiple of 128.
+ * ws_quantize_q4: W bf16 [M][K] -> Wq packed [M][ws_q4_row_bytes(K)], min-max
+ * per group with every decision in fp32: s = bf16((max - min) / 15),
+ * z = bf16(min + 8 s), q = clamp(rint((w - z) / s) + 8, 0, 15) (8 when s is
+ * 0).  Both pointers 16-byte aligned; finite weights.
+ * ws_gemv_q4: y[b][m] = sum_k w[m][k] * x[b][k] for the packed rows, x bf16
+ * [B][K], y fp32 [B][M], B <= 4, fp32 accumulation; the codes are expanded
+ * inside the GEMV (no dequantised copy is written).  Workspace as
+ * ws_gemv_bf16 (4-bit rows are never split along K, so none is needed). */
+size_t ws_q4_row_bytes(int K);
+ws_status ws_quantize_q4(const void *W, void *Wq, int M, int K, ws_stream_t stream);
+ws_status ws_gemv_q4(const void *Wq, const void *x, float *y, int M, int K, int B,
+                     void *workspace, size_t workspace_bytes, ws_stream_t stream);
+
 /* h_out[b][m] = h_in[b][m] + sum_k W[m][k] x[b][k]: the residual add of a
  * decoder block folded into the GEMV's epilogue ("One Token, Kernel by
  * Kernel", Step 1, "What one block launches").  x bf16 [B][K]; h_in, h_out
@@ -227,6 +253,7 @@ ws_status ws_l2_prefetch(const void *ptr, size_t bytes, ws_prefetch_plan plan,
  * Chain executor: a block list replayed as one CUDA graph.
  * ---------------------------------------------------------------------- */
 enum { WS_BLOCK_QWEN = 1, WS_BLOCK_MLP = 2, WS_BLOCK_HEAD = 3 };
+enum { WS_WEIGHTS_BF16 = 0, WS_WEIGHTS_Q4 = 1 };
 
 /* One decoder block of a Llama-style model at decode ("One Token, Kernel by
  * Kernel", Step 1): a = bf16(RMSNorm(h, gamma1)); q,k,v = a.W{q,k,v}^T;
@@ -291,6 +318,11 @@ typedef struct {
   int tune_pairs;       /* paired replays per candidate (>= 8)               */
   float tune_min_gain;  /* keep a plan only if the 95% CI lower bound of its
                            relative gain exceeds this (e.g. 0.01)            */
+  int weight_format;    /* WS_WEIGHTS_BF16 (0), or WS_WEIGHTS_Q4 (1): every
+                           weight matrix of the Qwen and head blocks (Wq, Wk,
+                           Wv, Wo, Wg, Wu, Wd, the LM head) is packed 4-bit
+                           rows as ws_quantize_q4 writes them (batch <= 4,
+                           one launch per op); the RMSNorm gammas stay bf16 */
   int persistent;       /* 1: run the whole step as one persistent kernel
                            (batch <= 4): each op is a phase of a cooperative
                            launch with one CTA per SM, phases separated by
@@ -427,6 +459,10 @@ ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind,
  * into the CTA's ring, bytes) triples.  Returns the count (host only). */
 long ws_debug_gemv_copies(int M, int K, int B, int nmat, int allow_split, int cta,
                           long long *triples, long max_triples);
+/* The same for packed 4-bit rows (source offsets into [nmat][M] rows of
+ * ws_q4_row_bytes(K) bytes); also returns the schedule in *sched (if given). */
+long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, long long *triples,
+                             long max_triples, ws_gemv_schedule *sched);
 
 /* Read-only streaming kernel over [ptr, ptr + bytes): a read-roofline probe.
  * Writes one checksum per CTA into sink (uint32 [blocks]). */

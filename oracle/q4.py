@@ -153,3 +153,24 @@ def quantize(W_bits):
     q = np.where(s_f[:, :, None] == 0, np.float32(8.0), q)
     q = np.clip(q, 0, 15).astype(np.uint8).reshape(M, K)
     return q, s_bits, z_bits
+
+
+def qwen_block(h, blk: dict, attn, eps: float) -> dict:
+    """One decoder block with 4-bit weights (the module docstring's reading),
+    the same steps as the bf16 block with every product over the dequantised
+    rows: blk holds bf16 bits gamma1, gamma2 and packed rows Wq, Wk, Wv, Wo,
+    Wg, Wu, Wd with their K in blk["K"] (hidden) and blk["KI"] (inter)."""
+    from . import bf16_to_f64, f64_to_bf16, rmsnorm, round_bf16, round_f32, swiglu
+    H, I = blk["K"], blk["KI"]
+    a = round_bf16(rmsnorm(h, bf16_to_f64(blk["gamma1"]), eps))
+    q, k, v = (gemv(blk[n], H, a) for n in ("Wq", "Wk", "Wv"))
+    h1 = round_f32(np.asarray(h, np.float64) + gemv(blk["Wo"], H, attn))
+    m = round_bf16(rmsnorm(h1, bf16_to_f64(blk["gamma2"]), eps))
+    s_bits = f64_to_bf16(swiglu(gemv(blk["Wg"], H, m), gemv(blk["Wu"], H, m)))
+    h2 = round_f32(h1 + gemv(blk["Wd"], I, bf16_to_f64(s_bits)))
+    return {"q": q, "k": k, "v": v, "h_mid": h1, "s": s_bits, "h": h2}
+
+
+def lmhead_logits(h, gamma_bits, Wlm, K: int, eps: float) -> np.ndarray:
+    from . import bf16_to_f64, rmsnorm, round_bf16
+    return gemv(Wlm, K, round_bf16(rmsnorm(h, bf16_to_f64(gamma_bits), eps)))

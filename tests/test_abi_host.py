@@ -172,6 +172,43 @@ def test_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, split):
     assert covered.min() == 1 and covered.max() == 1
 
 
+Q4_SHAPES = [
+    # (M, K, B, nmat): the Qwen2.5-1.5B products at 4 bits, ragged tails
+    (2048, 1536, 1, 1),    # merged QKV rows
+    (1536, 1536, 1, 1),    # Wo
+    (8960, 1536, 1, 2),    # gate/up pair
+    (1536, 8960, 1, 1),    # Wd: 17 super-groups and a tail of two groups
+    (1536, 8960, 4, 1),
+    (151936, 1536, 1, 1),  # LM head
+    (37, 640, 3, 1),       # ragged rows, a one-group tail
+    (1000, 1408, 2, 2),    # a three-group tail
+    (5, 128, 4, 1),        # one group
+]
+
+
+@pytest.mark.parametrize("M,K,B,nmat", Q4_SHAPES)
+def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat):
+    rb = wb.q4_row_bytes(K)
+    _, sc = wb.debug_gemv_copies_q4(M, K, B, nmat, 0)
+    assert sc["smem_bytes"] <= 227 * 1024 and 2 <= sc["NSW"] <= 8
+    assert sc["S"] == 1 and sc["KS"] == K
+    assert sc["PC"] == K or sc["PC"] % 512 == 0
+    assert sc["piece_bytes"] % 128 == 0
+    warp_ring = sc["NSW"] * sc["piece_bytes"]
+    covered = np.zeros(nmat * M * rb // 16, np.int32)
+    for cta in range(sc["grid"]):
+        copies, _ = wb.debug_gemv_copies_q4(M, K, B, nmat, cta)
+        for src, dst, n in copies:
+            assert n > 0 and n % 16 == 0 and src % 16 == 0 and dst % 16 == 0
+            assert 0 <= src and src + n <= nmat * M * rb
+            assert src // rb == (src + n - 1) // rb  # within one row
+            warp, rest = divmod(dst, warp_ring)
+            slot, off = divmod(rest, sc["piece_bytes"])
+            assert warp < 8 and slot < sc["NSW"] and off + n <= sc["piece_bytes"]
+            covered[src // 16:(src + n) // 16] += 1
+    assert covered.min() == 1 and covered.max() == 1
+
+
 def test_workspace_sizes(lib):
     assert wb.workspace_bytes(wb.OP_GEMV, 1536, 1536, 1) == 0  # no split needed
     assert wb.workspace_bytes(wb.OP_GEMV, 256, 1536, 1) > 0    # skinny: split

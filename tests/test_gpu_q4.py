@@ -1,0 +1,106 @@
+"""GPU parity of the 4-bit group-128 weight path ("One Token, Kernel by
+Kernel", "4-bit weights") against the oracle: the quantiser bit for bit (its
+decisions in fp32 on both sides), the GEMV over the packed rows within the
+fp32 bound (double oracle on the same bytes), the decode chain on 4-bit
+weights block by block (teacher-forced on the GPU's h trace) and its argmax."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import q4 as oq4
+from weight_streaming_gemv_bf16_gb300 import binding as wb
+from weight_streaming_gemv_bf16_gb300 import chain as wc
+from weight_streaming_gemv_bf16_gb300 import synth
+from _util import assert_fp32, dev_bf16, dev_f32, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    assert wb.device_error(reset=True) == 0
+    yield
+    torch.cuda.synchronize()
+    assert wb.device_error() == 0
+
+
+def _quantize_both(W_bits):
+    """(GPU packed rows, oracle packed rows); asserts they are the same bytes."""
+    M, K = W_bits.shape
+    Wq = torch.zeros((M, wb.q4_row_bytes(K)), dtype=torch.uint8, device="cuda")
+    wb.quantize_q4(dev_bf16(W_bits), Wq)
+    torch.cuda.synchronize()
+    ref = oq4.pack(*oq4.quantize(W_bits))
+    got = Wq.cpu().numpy()
+    assert got.shape == ref.shape
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:4].tolist()}"
+    return Wq, ref
+
+
+@pytest.mark.parametrize("M,K", [(37, 640), (64, 1536), (9, 8960), (5, 1408), (3, 128)])
+def test_quantizer_matches_oracle_bitwise(M, K):
+    W = synth.normal_bf16((M, K), 0.02, M * 7 + K, "q4/W")
+    W[0, :128] = W[0, 0]  # a constant group: scale 0
+    _quantize_both(W)
+
+
+@pytest.mark.parametrize("M,K,B", [(37, 640, 1), (37, 640, 3), (300, 1408, 2), (2048, 1536, 1),
+                                   (1536, 8960, 1), (1536, 8960, 4), (8960, 1536, 1),
+                                   (5, 128, 4)])
+def test_gemv_q4_matches_oracle(M, K, B):
+    W = synth.normal_bf16((M, K), 0.02, M + K + B, "q4/W")
+    Wq, ref = _quantize_both(W)
+    x = synth.normal_bf16((B, K), 1.0, M + K + B, "q4/x")
+    y = torch.full((B, M), float("nan"), device="cuda")
+    wb.gemv_q4(Wq, dev_bf16(x), y, K)
+    torch.cuda.synchronize()
+    assert_fp32(y.cpu().numpy(), oq4.gemv(ref, K, oracle.bf16_to_f64(x)), what=f"{M}x{K} B={B}")
+
+
+SMALL = synth.QwenShape(hidden=256, kv_dim=64, inter=512, vocab=1000, layers=3)
+MID = synth.QwenShape(hidden=512, kv_dim=128, inter=1408, vocab=4096, layers=2)
+
+
+@pytest.mark.parametrize("B,shape", [(1, SMALL), (2, SMALL), (4, SMALL), (1, MID), (3, MID)])
+def test_q4_chain_matches_oracle(B, shape):
+    seed = 11 * B + shape.hidden
+    blocks = [synth.qwen_block_weights(shape, seed, l) for l in range(shape.layers)]
+    head = synth.qwen_head_weights(shape, seed)
+    attn = np.stack([synth.qwen_attn(shape, B, seed, l) for l in range(shape.layers)])
+    h0 = synth.qwen_hidden(shape, B, seed)
+    mats = ("Wq", "Wk", "Wv", "Wo", "Wg", "Wu", "Wd")
+    dblocks, rblocks = [], []
+    for blk in blocks:
+        d = {n: dev_bf16(blk[n]) for n in ("gamma1", "gamma2")}
+        r = {n: blk[n] for n in ("gamma1", "gamma2")}
+        for n in mats:
+            d[n], r[n] = _quantize_both(blk[n])
+        r["K"], r["KI"] = shape.hidden, shape.inter
+        dblocks.append(d)
+        rblocks.append(r)
+    Wlm, Wlm_ref = _quantize_both(head["Wlm"])
+    dhead = {"gamma_f": dev_bf16(head["gamma_f"]), "Wlm": Wlm}
+    ch = wc.qwen_chain(dblocks, dhead, dev_bf16(attn), dev_f32(h0), eps=shape.eps, trace=True,
+                       logits=True, q4=True)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    trace = ch.h_trace.cpu().numpy().astype(np.float64)
+    h = h0.astype(np.float64)
+    for l in range(shape.layers):
+        out = oq4.qwen_block(h, rblocks[l], oracle.bf16_to_f64(attn[l]), shape.eps)
+        assert_fp32(trace[l], out["h"], what=f"block {l}")
+        h = trace[l]
+    logits = oq4.lmhead_logits(h, head["gamma_f"], Wlm_ref, shape.hidden, shape.eps)
+    assert_fp32(ch.logits.cpu().numpy(), logits, what="logits")
+    idx = ch.idx.cpu().numpy()
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    rms = np.sqrt(np.mean(logits * logits, axis=1))
+    clear = (top2[:, 1] - top2[:, 0]) > 2 * 2e-3 * np.maximum(np.abs(top2[:, 1]), rms)
+    ref_idx = oracle.argmax_rows(logits)
+    assert np.array_equal(idx[clear], ref_idx[clear])

@@ -71,7 +71,8 @@ class ChainOpts(C.Structure):
                 ("vocab", I32), ("eps", F32), ("h_in", P), ("h_out", P), ("x_in", P),
                 ("y_out", P), ("h_trace", P), ("use_pdl", I32), ("prefetch", I32),
                 ("fixed_plan", PrefetchPlan), ("distance", I32), ("decoy", I32),
-                ("tune_pairs", I32), ("tune_min_gain", F32), ("persistent", I32)]
+                ("tune_pairs", I32), ("tune_min_gain", F32), ("weight_format", I32),
+                ("persistent", I32)]
 
 
 class Tuning(C.Structure):
@@ -97,6 +98,8 @@ _SIGS = {
     "ws_lmhead_argmax": [P, I32, P, P, P, P, I32, I32, I32, F32, P, SZ, P],
     "ws_argmax_rows": [P, P, I32, I32, P, SZ, P],
     "ws_decode_attention": [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P],
+    "ws_quantize_q4": [P, P, I32, I32, P],
+    "ws_gemv_q4": [P, P, P, I32, I32, I32, P, SZ, P],
     "ws_rmsnorm": [P, P, P, I32, I32, I32, F32, P],
     "ws_l2_prefetch": [P, SZ, PrefetchPlan, P],
     "ws_chain_create": [P, I32, P, P],
@@ -116,6 +119,7 @@ _SIGS = {
 _OTHER = {
     "ws_workspace_bytes": ([I32, I32, I32, I32], SZ),
     "ws_attention_workspace_bytes": ([I32, I32, I32, I32, I32], SZ),
+    "ws_q4_row_bytes": ([I32], SZ),
     "ws_last_error": ([], C.c_char_p),
     "ws_device_error": ([I32], I32),
     "ws_chain_num_ops": ([P], I32),
@@ -125,6 +129,7 @@ _OTHER = {
     "ws_chain_destroy": ([P], None),
     "ws_get_tuning": ([P], None),
     "ws_debug_gemv_copies": ([I32, I32, I32, I32, I32, I32, P, C.c_long], C.c_long),
+    "ws_debug_gemv_copies_q4": ([I32, I32, I32, I32, I32, P, C.c_long, P], C.c_long),
     "ws_version": ([], C.c_char_p),
 }
 
@@ -276,6 +281,24 @@ def argmax_rows(logits, idx, workspace, stream=None):
     _check(load().ws_argmax_rows(_ptr(logits), _ptr(idx), rows, cols, wp, wb, _stream(stream)))
 
 
+def q4_row_bytes(K: int) -> int:
+    return int(load().ws_q4_row_bytes(K))
+
+
+def quantize_q4(W, Wq, stream=None):
+    """W bf16 [M, K] -> Wq uint8 [M, q4_row_bytes(K)] (4-bit groups of 128)."""
+    M, K = W.shape
+    _check(load().ws_quantize_q4(_ptr(W), _ptr(Wq), M, K, _stream(stream)))
+
+
+def gemv_q4(Wq, x, y, K, workspace=None, stream=None):
+    """y [B, M] fp32 = x [B, K] bf16 . W^T for packed 4-bit rows Wq [M, q4_row_bytes(K)]."""
+    M = Wq.shape[0]
+    B = x.shape[0]
+    wp, wb = _ws(workspace)
+    _check(load().ws_gemv_q4(_ptr(Wq), _ptr(x), _ptr(y), M, K, B, wp, wb, _stream(stream)))
+
+
 def attention_workspace_bytes(B, n_heads, n_kv_heads, s_max, head_dim=128) -> int:
     return int(load().ws_attention_workspace_bytes(B, n_heads, n_kv_heads, head_dim, s_max))
 
@@ -333,6 +356,19 @@ def gemv_plan(M, K, B, nmat=1, prologue=PRO_NONE, epilogue=EPI_F32, allow_split=
     _check(load().ws_gemv_plan(M, K, B, nmat, prologue, epilogue, 1 if allow_split else 0,
                                C.byref(s)))
     return {n: getattr(s, n) for n, _ in GemvSchedule._fields_}
+
+
+def debug_gemv_copies_q4(M, K, B, nmat, cta):
+    """(triples, schedule dict) of CTA `cta` for packed 4-bit rows."""
+    lib = load()
+    sc = GemvSchedule()
+    n = lib.ws_debug_gemv_copies_q4(M, K, B, nmat, cta, None, 0, C.byref(sc))
+    if n < 0:
+        raise WsError(-1, "bad arguments")
+    buf = (C.c_longlong * (3 * max(n, 1)))()
+    lib.ws_debug_gemv_copies_q4(M, K, B, nmat, cta, buf, n, None)
+    sched = {f: getattr(sc, f) for f, _ in GemvSchedule._fields_}
+    return [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n)], sched
 
 
 def debug_gemv_copies(M, K, B, nmat, allow_split, cta):

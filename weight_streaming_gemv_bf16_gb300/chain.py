@@ -65,10 +65,12 @@ def _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, t
 
 def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
                fixed_plan=None, distance=1, decoy=False, trace=False, keep_qkv=False,
-               logits=False, tune_pairs=30, min_gain=0.01, persistent=False) -> QwenChain:
+               logits=False, tune_pairs=30, min_gain=0.01, persistent=False,
+               q4=False) -> QwenChain:
     """blocks: list of dicts of bf16 device tensors gamma1, Wq, Wk, Wv, Wo, gamma2,
     Wg, Wu, Wd; head: dict gamma_f, Wlm (or None); attn: bf16 [L, B, H];
-    h_in: fp32 [B, H]."""
+    h_in: fp32 [B, H].  q4=True: the weight matrices are packed 4-bit rows
+    (uint8 [M, q4_row_bytes(K)], as binding.quantize_q4 writes them)."""
     B, H = h_in.shape
     L = len(blocks)
     KV = blocks[0]["Wk"].shape[0] if L else 0
@@ -106,6 +108,7 @@ def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
     o.h_in = h_in.data_ptr()
     o.h_out = h_out.data_ptr()
     o.h_trace = h_trace.data_ptr() if h_trace is not None else None
+    o.weight_format = 1 if q4 else 0
     keep += [h_out, h_trace, idx, lg, qkv]
     ch = wb.Chain(descs, o, keepalive=keep)
     return QwenChain(ch, h_in, h_out, attn, idx, lg, h_trace, qkv)

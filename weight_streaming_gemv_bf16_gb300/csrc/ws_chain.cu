@@ -311,6 +311,14 @@ static ws_status build_ops(ws_chain* c) {
     }
   }
 
+  // 4-bit weights: every op streams packed rows (q4_prefix(K) bytes a row)
+  if (o.weight_format == WS_WEIGHTS_Q4) {
+    for (auto& op : c->ops) {
+      op.p.wfmt = WF_Q4;
+      for (auto& r : op.reads) r.second = r.second / ((size_t)2 * op.p.K) * q4_prefix(op.p.K);
+    }
+  }
+
   // persistent mode when asked for and every op fits its stage layout
   c->persistent = false;
   if (o.persistent && B <= 4) {
@@ -696,6 +704,17 @@ ws_status ws_chain_create(const ws_block_desc* blocks, int n, const ws_chain_opt
   }
   if (nh && (o.vocab <= 0 || (!nq && (!o.h_in || !al16(o.h_in))))) {
     set_error("head needs vocab > 0 and an input h");
+    return WS_ERR_ARG;
+  }
+  if (o.weight_format != WS_WEIGHTS_BF16 && o.weight_format != WS_WEIGHTS_Q4) {
+    set_error("unknown weight format %d", o.weight_format);
+    return WS_ERR_ARG;
+  }
+  if (o.weight_format == WS_WEIGHTS_Q4 &&
+      (nm || o.batch > 4 || o.persistent || o.hidden % kQ4Group ||
+       (nq && o.inter % kQ4Group))) {
+    set_error("4-bit weights: Qwen and head blocks, batch <= 4, one launch per op, hidden "
+              "and inter multiples of 128");
     return WS_ERR_ARG;
   }
 

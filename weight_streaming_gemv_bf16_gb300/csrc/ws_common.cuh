@@ -45,8 +45,25 @@ enum Epilogue {
 enum DType { DT_F32 = 0, DT_BF16 = 1, DT_F16 = 2 };
 enum DeviceError { DERR_TIMEOUT = 1 };
 
+// 4-bit group-128 weights ("One Token, Kernel by Kernel", "4-bit weights"):
+// a group is 128 consecutive weights of a row with a bf16 scale s and zero z,
+// code q standing for s * (q - 8) + z.  A row is a run of super-groups of
+// four groups: their codes (64 bytes a group; 32-bit word i of a group holds
+// k = 8i .. 8i+7, even k in the low half's nibbles, odd k in the high half's),
+// then their (s, z) pairs, zero-padded to 16 bytes (272 bytes for four).
+constexpr int kQ4Group = 128;
+constexpr int kQ4Super = 512;       // columns of a full super-group
+constexpr int kQ4SuperBytes = 272;  // its bytes
+__host__ __device__ constexpr int q4_super_bytes(int groups) { return (groups * 68 + 15) & ~15; }
+// Bytes of a row before column k (k a multiple of 512, or the row's end).
+__host__ __device__ constexpr int q4_prefix(int k) {
+  return (k / kQ4Super) * kQ4SuperBytes +
+         ((k % kQ4Super) ? q4_super_bytes((k % kQ4Super) / kQ4Group) : 0);
+}
+enum WeightFormat { WF_BF16 = 0, WF_Q4 = 1 };
+
 struct Seg {
-  const uint16_t* W0;  // bf16 [M][K]
+  const uint16_t* W0;  // bf16 [M][K]; 4-bit rows (q4_prefix(K) bytes each) for WF_Q4
   const uint16_t* W1;  // second matrix read in lockstep (SwiGLU up), or null
   void* out;           // [B][M]
   int M;
@@ -75,12 +92,14 @@ struct Sched {
   // memory (both odd multiples of 16 bytes: ldmatrix rows in distinct banks)
   int mma, prow, xrs;
   int form;      // its chain form (F_ANY for none)
+  int off_xsum;  // 4-bit weights: sums of 32 staged activations, [BT][KS / 32] fp32
 };
 
 struct alignas(16) GemvParams {
   Seg seg[kMaxSeg];
   int nseg;
   int nmat;  // 1, or 2 for a gate/up pair
+  int wfmt;  // WeightFormat
   int K, B, M_total;
   const void* x;
   int x_dtype;

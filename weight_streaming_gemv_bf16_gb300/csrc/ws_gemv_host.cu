@@ -221,11 +221,19 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   const int nsm = device_sm_count();
   const int grid_target = tu.grid_cap > 0 ? tu.grid_cap : nsm;
   const int warps_total = grid_target * kWarps;
-  if (tu.mma && tu.forms && plan_gemv_mma(p, force_S, grid_target)) return true;
+  const bool q4 = p.wfmt == WF_Q4;
+  if (!q4 && tu.mma && tu.forms && plan_gemv_mma(p, force_S, grid_target)) return true;
   Sched sc;
   memset(&sc, 0, sizeof sc);
   sc.BT = batch_template(p.B);
   const int K = p.K, nmat = p.nmat;
+  // bytes of one weight row (4-bit rows: whole super-groups)
+  const long row_b = q4 ? q4_prefix(K) : (long)K * 2;
+  if (q4 && (K % kQ4Group != 0 || sc.BT > 4)) {
+    snprintf(why, why_len, "4-bit weights need K a multiple of 128 and B <= 4 (K=%d, B=%d)", K,
+             p.B);
+    return false;
+  }
 
   // rows per task: up to 4, and RT x BT <= 32 (one output per lane group).  Cost of a choice: the heaviest warp's rows,
   // ceil(tasks / warps) x RT, times the shared-memory time per weight row when
@@ -236,7 +244,8 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   // contiguous copy per matrix), else the largest.  Measured on the decode
   // chain: QKV, Wo and Wd get 2 rows (a task each, 6 KB or longer pieces),
   // the LM head 4 (12 KB pieces).
-  const int rt_max = sc.BT <= 8 ? 4 : 2;
+  // 4-bit rows: at most four rows a task in all (NMAT x RT code registers)
+  const int rt_max = q4 ? 4 / nmat : (sc.BT <= 8 ? 4 : 2);
   const int target_bytes = tu.piece_bytes > 0 ? tu.piece_bytes : 6144;
   int RT = rt_max;
   if (tu.force_rt == 1 || tu.force_rt == 2 || tu.force_rt == 4) {
@@ -262,7 +271,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
       if (load(rt) > best * 1.1) continue;
       if (allow_split && any_unsplit && row_groups(p, rt) < warps_total / 2) continue;
       pick = rt;
-      if ((long)nmat * rt * K * 2 <= target_bytes) pick_whole = rt;
+      if ((long)nmat * rt * row_b <= target_bytes) pick_whole = rt;
     }
     RT = pick_whole ? pick_whole : pick;
   }
@@ -273,7 +282,10 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   auto valid_split = [&](int S) { return S >= 1 && K % (8 * S) == 0; };
   auto xs_fits = [&](int S) { return (long)sc.BT * (K / S) * 2 <= kXsMax; };
   int S = 1;
-  if (force_S > 0) {
+  if (q4) {
+    // 4-bit rows are not split along K (a split would have to start on a
+    // super-group); the activations of the full K stay in shared memory
+  } else if (force_S > 0) {
     S = force_S;
   } else if (force_S == 0) {
     if (tu.force_ksplit > 0) {
@@ -294,7 +306,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
     return false;
   }
   if (!xs_fits(S)) {
-    if (force_S < 0) {
+    if (force_S < 0 || q4) {
       snprintf(why, why_len,
                "B=%d x K=%d activations exceed shared memory; pass a workspace", p.B, K);
       return false;
@@ -315,17 +327,21 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   sc.KS = K / S;
 
   // pieces: about piece_bytes each, evenly sized, multiples of 8 columns
-  int pc = target_bytes / (nmat * RT * 2);
-  pc = pc < 256 ? 256 : pc;
+  // (4-bit rows: of 512 columns, whole super-groups)
+  const int pc_unit = q4 ? kQ4Super : 8;
+  auto piece_row_bytes = [&](int pc_cols) { return q4 ? q4_prefix(pc_cols) : pc_cols * 2; };
+  int pc = q4 ? target_bytes / (nmat * RT * kQ4SuperBytes) * kQ4Super
+              : target_bytes / (nmat * RT * 2);
+  pc = pc < (q4 ? kQ4Super : 256) ? (q4 ? kQ4Super : 256) : pc;
   if (pc >= sc.KS) {
     sc.PC = sc.KS;
     sc.NP = 1;
   } else {
     sc.NP = (sc.KS + pc - 1) / pc;
-    sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 8);
+    sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, pc_unit);
     sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
   }
-  sc.piece_bytes = align_up(nmat * RT * sc.PC * 2, 128);
+  sc.piece_bytes = align_up(nmat * RT * piece_row_bytes(sc.PC), 128);
 
   int off = 0;
   sc.off_bar = off;
@@ -340,6 +356,10 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   off += kWarps * 32 * 8;
   sc.off_xs = align_up(off, 128);
   off = sc.off_xs + align_up(sc.BT * sc.KS * 2, 128);
+  if (q4) {
+    sc.off_xsum = off;
+    off += align_up(sc.BT * (sc.KS / 32) * 4, 128);
+  }
   sc.off_ring = align_up(off, 128);
   int ring_budget = tu.ring_bytes > 0 ? tu.ring_bytes : 96 * 1024;
   if (sc.off_ring + ring_budget > kSmemMax) ring_budget = kSmemMax - sc.off_ring;
@@ -348,16 +368,18 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   if (NSW < 2) {
     if (sc.off_ring + 2 * kWarps * sc.piece_bytes > kSmemMax) {
       // smaller pieces, so that two stages per warp fit beside the activations
-      const int pc_fit = ((kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * 2)) & ~7;
-      if (pc_fit < 8) {
+      const int pc_fit =
+          q4 ? (kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * kQ4SuperBytes) * kQ4Super
+             : ((kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * 2)) & ~7;
+      if (pc_fit < pc_unit) {
         snprintf(why, why_len, "no two ring stages per warp fit beside %d bytes of activations",
                  sc.BT * sc.KS * 2);
         return false;
       }
       sc.NP = (sc.KS + pc_fit - 1) / pc_fit;
-      sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, 8);
+      sc.PC = align_up((sc.KS + sc.NP - 1) / sc.NP, pc_unit);
       sc.NP = (sc.KS + sc.PC - 1) / sc.PC;
-      sc.piece_bytes = align_up(nmat * RT * sc.PC * 2, 128);
+      sc.piece_bytes = align_up(nmat * RT * piece_row_bytes(sc.PC), 128);
     }
     NSW = 2;
   }
@@ -444,6 +466,10 @@ static GemvKernel pick_kernel(const GemvParams& p) {
   const int BT = p.sc.BT, nmat = p.nmat, RT = p.sc.RT;
   if (p.sc.mma) return pick_kernel_mma(BT, nmat, p.sc.form);
   const int F = tuning().forms ? kernel_form(p) : F_ANY;
+  if (p.wfmt == WF_Q4) {
+    GemvKernel k = F != F_ANY ? pick_kernel_q4(BT, nmat, RT, F) : nullptr;
+    return k ? k : pick_kernel_q4(BT, nmat, RT, F_ANY);
+  }
   if (F != F_ANY) {
     GemvKernel k = BT == 1   ? pick_form_b1(BT, nmat, RT, F)
                    : BT <= 4 ? pick_form_b24(BT, nmat, RT, F)
@@ -496,6 +522,8 @@ cudaError_t launch_gemv(const GemvParams& p, cudaStream_t stream, bool pdl) {
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, k, p);
 }
+
+cudaError_t launch_quantize_q4(const void* W, void* out, int M, int K, cudaStream_t st);
 
 void init_gemv_params(GemvParams& p, int K, int B) {
   memset(&p, 0, sizeof p);
@@ -585,6 +613,49 @@ ws_status ws_gemv_bf16(const void* W, const void* x, float* y, int M, int K, int
   init_gemv_params(p, K, B);
   p.nseg = 1;
   p.seg[0].W0 = static_cast<const uint16_t*>(W);
+  p.seg[0].out = y;
+  p.seg[0].M = M;
+  p.x = x;
+  p.x_dtype = DT_BF16;
+  p.prologue = PRO_NONE;
+  p.epilogue = EPI_F32;
+  return plan_bind_launch(p, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+size_t ws_q4_row_bytes(int K) {
+  if (K <= 0 || K % kQ4Group) return 0;
+  return (size_t)q4_prefix(K);
+}
+
+ws_status ws_quantize_q4(const void* W, void* Wq, int M, int K, ws_stream_t stream) {
+  if (M <= 0 || K <= 0 || K % kQ4Group) {
+    set_error("bad shape M=%d K=%d (need M>0 and K a positive multiple of 128)", M, K);
+    return WS_ERR_SHAPE;
+  }
+  ws_status s = check_ptrs({W, Wq});
+  if (s) return s;
+  const cudaError_t e = launch_quantize_q4(W, Wq, M, K, (cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    set_error("quantize failed: %s", cudaGetErrorString(e));
+    return WS_ERR_CUDA;
+  }
+  return WS_OK;
+}
+
+ws_status ws_gemv_q4(const void* Wq, const void* x, float* y, int M, int K, int B,
+                     void* workspace, size_t workspace_bytes, ws_stream_t stream) {
+  ws_status s = check_common(M, K, B);
+  if (s) return s;
+  if (K % kQ4Group || B > 4) {
+    set_error("4-bit weights: K a multiple of 128 and B <= 4 (K=%d, B=%d)", K, B);
+    return WS_ERR_SHAPE;
+  }
+  if ((s = check_ptrs({Wq, x, y}))) return s;
+  GemvParams p;
+  init_gemv_params(p, K, B);
+  p.wfmt = WF_Q4;
+  p.nseg = 1;
+  p.seg[0].W0 = static_cast<const uint16_t*>(Wq);
   p.seg[0].out = y;
   p.seg[0].M = M;
   p.x = x;
@@ -890,6 +961,66 @@ ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind, i
   out->grid = sc.grid;
   out->smem_bytes = sc.smem_bytes;
   return WS_OK;
+}
+
+long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, long long* triples,
+                             long max_triples, ws_gemv_schedule* out) {
+  if (check_common(M, K, B) != WS_OK || K % kQ4Group || (nmat != 1 && nmat != 2)) return -1;
+  GemvParams p;
+  init_gemv_params(p, K, B);
+  p.wfmt = WF_Q4;
+  p.nseg = 1;
+  p.nmat = nmat;
+  p.seg[0].M = M;
+  p.epilogue = nmat == 2 ? EPI_SWIGLU : EPI_F32;
+  char why[256];
+  if (!plan_gemv(p, -1, why, sizeof why)) return -1;
+  const Sched& sc = p.sc;
+  if (out) {
+    out->RT = sc.RT;
+    out->S = sc.S;
+    out->KS = sc.KS;
+    out->PC = sc.PC;
+    out->NP = sc.NP;
+    out->NSW = sc.NSW;
+    out->piece_bytes = sc.piece_bytes;
+    out->RG = sc.RG;
+    out->grid = sc.grid;
+    out->smem_bytes = sc.smem_bytes;
+  }
+  if (cta < 0 || cta >= sc.grid) return -1;
+  int ks, rg0, rg1;
+  cta_range(sc, cta, ks, rg0, rg1);
+  const int k0 = ks * sc.KS;
+  const long long warp_ring = (long long)sc.NSW * sc.piece_bytes;
+  const long long rb = q4_prefix(K);
+  long n = 0;
+  // the same order and arithmetic as issue_piece's 4-bit path
+  for (int w = 0; w < kWarps; ++w) {
+    const int npw = warp_tasks(rg0, rg1, w) * sc.NP;
+    for (int q = 0; q < npw; ++q) {
+      const int ti = q / sc.NP;
+      const int j = q - ti * sc.NP;
+      int seg, rgl;
+      decode_rg(p, rg0 + w + ti * kWarps, seg, rgl);
+      const int row0 = rgl * sc.RT;
+      const int rows = (sc.RT < M - row0) ? sc.RT : M - row0;
+      const int c0 = k0 + j * sc.PC;
+      const int len = (sc.PC < sc.KS - j * sc.PC) ? sc.PC : sc.KS - j * sc.PC;
+      const int src0 = q4_prefix(c0), nb = q4_prefix(c0 + len) - src0, pst = q4_prefix(sc.PC);
+      const long long dst0 = w * warp_ring + (long long)(q % sc.NSW) * sc.piece_bytes;
+      for (int mat = 0; mat < nmat; ++mat)
+        for (int r = 0; r < rows; ++r) {
+          if (triples && n < max_triples) {
+            triples[3 * n] = (long long)mat * M * rb + (long long)(row0 + r) * rb + src0;
+            triples[3 * n + 1] = dst0 + ((long long)mat * sc.RT + r) * pst;
+            triples[3 * n + 2] = nb;
+          }
+          ++n;
+        }
+    }
+  }
+  return n;
 }
 
 long ws_debug_gemv_copies(int M, int K, int B, int nmat, int allow_split, int cta,

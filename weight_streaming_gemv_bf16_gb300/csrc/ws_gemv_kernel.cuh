@@ -609,6 +609,71 @@ __device__ __forceinline__ void dot_piece(float (&acc)[2][4][BT], const uint4* s
       }
 }
 
+// Two 4-bit codes of a word (bits 4j.. and 16 + 4j..) as a bf16 pair 128 + q:
+// 0x4300 is 128 in bf16 and the nibble lands in the low mantissa bits.
+__device__ __forceinline__ uint32_t q4_pair(uint32_t w, int j) {
+  return ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+}
+
+// Dot products of one ring piece of 4-bit rows against the staged
+// activations.  The piece holds NMAT x RT rows pst bytes apart, each len
+// columns of whole super-groups.  Lane l takes 32-column chunks l, l + 32,
+// ...: a 16-byte code chunk (four words, 32 weights) and its group's (s, z)
+// per row, four activation chunks and their sum X per batch row.  With
+// t = sum (128 + q) x (mixed fma: bf16 operands, exact products, fp32 sums),
+// s t + (z - 136 s) X = sum (s (q - 8) + z) x.
+template <int BT, int NMAT, int RT>
+__device__ __forceinline__ void dot_piece_q4(float (&acc)[2][4][BT], const uint8_t* st, int pst,
+                                             const uint4* xs, const float* xsum, int len,
+                                             int nchx, int nx32, int lane) {
+  const int nc = len >> 5, ngr = len >> 7;
+#pragma unroll 1
+  for (int c = lane; c < nc; c += 32) {
+    const int u = c >> 4, w = c & 15;
+    const int gu = min(4, ngr - 4 * u);  // groups of super-group u
+    const int off = u * kQ4SuperBytes + w * 16;
+    const int soff = u * kQ4SuperBytes + gu * 64 + (w >> 2) * 4;
+    uint32_t qp[NMAT][RT][16];
+    float sc[NMAT][RT], zc[NMAT][RT];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+      for (int r = 0; r < RT; ++r) {
+        const uint8_t* row = st + (size_t)(m * RT + r) * pst;
+        const uint4 q = *reinterpret_cast<const uint4*>(row + off);
+        const uint32_t sz = *reinterpret_cast<const uint32_t*>(row + soff);
+        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) qp[m][r][4 * i + jj] = q4_pair(qw[i], jj);
+        sc[m][r] = bf16lo(sz);
+        zc[m][r] = fmaf(-136.f, bf16lo(sz), bf16hi(sz));
+      }
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      const uint4* xb = xs + (size_t)b * nchx + 4 * c;
+      const uint4 x0 = xb[0], x1 = xb[1], x2 = xb[2], x3 = xb[3];
+      const uint32_t xw[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                               x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+      const float X = xsum[b * nx32 + c];
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            t0 = fma_bf16x2(qp[m][r][e], xw[e], t0);
+            t1 = fma_bf16x2(qp[m][r][e + 1], xw[e + 1], t1);
+          }
+          acc[m][r][b] = fmaf(sc[m][r], t0 + t1, acc[m][r][b]);
+          acc[m][r][b] = fmaf(zc[m][r], X, acc[m][r][b]);
+        }
+    }
+  }
+}
+
 // The last split of a row group: the sums over all splits, in split order,
 // of the outputs o0 + 32 u (u < U) of this lane, n_out outputs in all.  The
 // loads of U outputs and two splits are in flight together (the partials
@@ -636,9 +701,33 @@ __device__ __forceinline__ void split_sums(const GemvParams& p, int rowg, int n_
           v[m][u] += __ldcg(&p.part[((size_t)(s * NMAT + m) * p.B + bb[u]) * p.M_total + rowg + rr[u]]);
 }
 
-template <int NMAT, int RT, bool ONE_SEG>
+template <int NMAT, int RT, bool ONE_SEG, bool Q4 = false>
 __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, int slot, int k0,
                                             uint8_t* ring, uint64_t* full, uint64_t pol) {
+  if constexpr (Q4) {
+    // 4-bit rows: a piece is a run of whole super-groups (its columns start
+    // at a multiple of 512), q4_prefix(PC) bytes apart in the ring
+    const Sched& sc = p.sc;
+    int seg = 0, rgl = rg;
+    if (!ONE_SEG) decode_rg(p, rg, seg, rgl);
+    const Seg& S = p.seg[seg];
+    const int row0 = rgl * RT;
+    const int rows = min(RT, S.M - row0);
+    const int c0 = k0 + j * sc.PC;
+    const int len = min(sc.PC, sc.KS - j * sc.PC);
+    const int rb = q4_prefix(p.K), src0 = q4_prefix(c0);
+    const int nb = q4_prefix(c0 + len) - src0, pst = q4_prefix(sc.PC);
+    uint8_t* dst = ring + (size_t)slot * sc.piece_bytes;
+    mbar_arrive_expect_tx(&full[slot], (uint32_t)(NMAT * rows * nb));
+#pragma unroll
+    for (int mat = 0; mat < NMAT; ++mat) {
+      const uint8_t* W = reinterpret_cast<const uint8_t*>(mat == 0 ? S.W0 : S.W1);
+      for (int r = 0; r < rows; ++r)
+        bulk_copy_g2s(dst + ((size_t)mat * RT + r) * pst, W + (size_t)(row0 + r) * rb + src0,
+                      (uint32_t)nb, &full[slot], pol);
+    }
+    return;
+  }
   const Sched& sc = p.sc;
   int seg = 0, rgl = rg;
   if (!ONE_SEG) decode_rg(p, rg, seg, rgl);
@@ -660,7 +749,7 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
   }
 }
 
-template <int BT, int NMAT, int RT, int F>
+template <int BT, int NMAT, int RT, int F, bool Q4 = false>
 __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_constant__ GemvParams p) {
   using FT = FormTraits<F>;
   constexpr int EPI = FT::epi;
@@ -699,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     // Weights do not depend on the previous kernel: fill the whole ring
     // before waiting for it.
     while (iq < NSW && iq < npw) {
-      issue_piece<NMAT, RT, FT::one_seg>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      issue_piece<NMAT, RT, FT::one_seg, Q4>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
       if (++islot == NSW) islot = 0;
@@ -754,6 +843,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   const int nchx = sc.KS >> 3;  // chunks of x in shared memory
   const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
   const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
+  float* xsum = Q4 ? reinterpret_cast<float*>(smem + sc.off_xsum) : nullptr;
+  if constexpr (Q4) {
+    // per batch row the sum of every 32 staged (rounded) activations, in
+    // column order
+    const int n32 = sc.KS >> 5;
+    for (int o = tid; o < BT * n32; o += kThreads) {
+      const int b = o / n32, c = o - b * n32;
+      const uint4* src = xs4 + (size_t)b * nchx + 4 * c;
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = src[i];
+        sum += bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y);
+        sum += bf16lo(v.z) + bf16hi(v.z) + bf16lo(v.w) + bf16hi(v.w);
+      }
+      xsum[o] = sum;
+    }
+    __syncthreads();
+  }
   float best_v = -INFINITY;
   int best_i = 0x7fffffff;
   bool abort = false;
@@ -787,13 +895,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     // batch 1 in a chain form keeps the loop rolled: shorter code, and one
     // iteration per 16-byte chunk is far from the issue limit (measured: it
     // is not at batch 4)
-    dot_piece<BT, NMAT, RT, (F != F_ANY && BT == 1) ? 1 : 2>(acc, st, xs4 + j * ncp, len >> 3, ncp,
-                                                              nchx, lane);
+    if constexpr (Q4) {
+      dot_piece_q4<BT, NMAT, RT>(acc, reinterpret_cast<const uint8_t*>(st), q4_prefix(sc.PC),
+                                 xs4 + j * ncp, xsum + j * (sc.PC >> 5), len, nchx, sc.KS >> 5,
+                                 lane);
+    } else {
+      dot_piece<BT, NMAT, RT, (F != F_ANY && BT == 1) ? 1 : 2>(acc, st, xs4 + j * ncp, len >> 3,
+                                                                ncp, nchx, lane);
+    }
     // Every lane's shared-memory reads of this slot have returned (their
     // values fed the FMAs above, and issue is in order): refill the slot.
     __syncwarp();
     if (lane == 0 && !abort && iq < npw) {
-      issue_piece<NMAT, RT, FT::one_seg>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
+      issue_piece<NMAT, RT, FT::one_seg, Q4>(p, rgw + iti * kWarps, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
       if (++islot == NSW) islot = 0;
@@ -945,5 +1059,6 @@ GemvKernel pick_form_b24(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b8(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b16(int BT, int nmat, int RT, int F);
 GemvKernel pick_kernel_mma(int BT, int nmat, int F);
+GemvKernel pick_kernel_q4(int BT, int nmat, int RT, int F);
 
 }  // namespace ws
