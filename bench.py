@@ -48,14 +48,16 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs", "attention"],
+    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs", "attention", "q4"],
                     default="chain",
                     help="chain: the decode step (the metric); kernel: gate/up alone (profiler "
                          "captures); sweep: the batch GEMV sweep, fp16 RMSNorm and the "
                          "LayerNorm block chain; configs: the fused 256x256 op beside the launch "
                          "floor, one block warm and cold, the LayerNorm chain with and without "
                          "prefetch (one JSON line each); attention: decode attention over "
-                         "a key-value cache at batch 1/4/16 and 1k-32k cached slots")
+                         "a key-value cache at batch 1/4/16 and 1k-32k cached slots; q4: "
+                         "4-bit group-128 weights, each GEMV shape and the decode step "
+                         "beside bf16")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
                     help="graph: one launch per op, PDL edges, one CUDA graph; persistent: "
                          "the whole step as one cooperative kernel")
@@ -743,6 +745,133 @@ def run_configs(args):
     return 0
 
 
+def _graph_time(torch, fn, n_inner, reps=10):
+    """Seconds per inner launch of fn(stream) captured in one CUDA graph and
+    replayed `reps` times between CUDA events (after a warm call and three
+    warm replays)."""
+    st = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        fn(side)
+    st.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn(torch.cuda.current_stream())
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3 / (reps * n_inner)
+
+
+def run_q4(args):
+    """4-bit group-128 weights, one JSON line:
+    - each GEMV shape of the Qwen2.5-1.5B decode step at batch 1, 2 and 4
+      (packed rows quantised on the GPU from random bf16 weights, rotating
+      copies of at least 256 MB, launched back to back with programmatic
+      dependent launch in one CUDA graph): time per launch and the packed
+      bytes over it against the measured copy peak;
+    - the whole decode step (28 blocks and the LM head) on 4-bit weights
+      quantised from the same bf16 weights as the bf16 chain, both timed as
+      graph replays between CUDA events, at batch 1 and 4."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda").manual_seed(args.seed)
+    hbm = peaks()[0]
+    base = wb.get_tuning()
+    t = wb.Tuning()
+    for f, _ in wb.Tuning._fields_:
+        setattr(t, f, getattr(base, f))
+    t.launch_pdl = 1
+    wb.set_tuning(t)
+    gemv = []
+    try:
+        for M, K in [(2048, 1536), (1536, 1536), (8960, 1536), (1536, 8960), (151936, 1536)]:
+            rb = wb.q4_row_bytes(K)
+            nbytes = M * rb
+            ncopy = max(2, -(-(256 << 20) // nbytes))
+            W = (torch.randn((M, K), device="cuda", generator=gen) * 0.02).to(torch.bfloat16)
+            Wqs = []
+            for _ in range(ncopy):
+                Wq = torch.empty((M, rb), dtype=torch.uint8, device="cuda")
+                wb.quantize_q4(W, Wq)
+                Wqs.append(Wq)
+            del W
+            for B in (1, 2, 4):
+                x = torch.randn((B, K), device="cuda", generator=gen).to(torch.bfloat16)
+                y = torch.empty((B, M), device="cuda")
+
+                def fn(s, Wqs=Wqs, x=x, y=y, K=K):
+                    for Wq in Wqs:
+                        wb.gemv_q4(Wq, x, y, K, stream=s)
+                dt = _graph_time(torch, fn, ncopy)
+                gemv.append({"M": M, "K": K, "batch": B, "us_per_launch": round(dt * 1e6, 2),
+                             "packed_bytes": nbytes, "GB_s": round(nbytes / dt / 1e9, 1),
+                             "frac_of_measured_hbm": round(nbytes / dt / 1e9 / hbm, 3)})
+            del Wqs
+            torch.cuda.empty_cache()
+    finally:
+        wb.set_tuning(base)
+
+    sh, blocks, head, attn, h0 = make_host_inputs(4, args.seed)
+    dblocks = [{k: to_dev(v, torch) for k, v in b.items()} for b in blocks]
+    dhead = {k: to_dev(v, torch) for k, v in head.items()}
+    mats = ("Wq", "Wk", "Wv", "Wo", "Wg", "Wu", "Wd")
+
+    def packed(Wbf):
+        Wq = torch.empty((Wbf.shape[0], wb.q4_row_bytes(Wbf.shape[1])), dtype=torch.uint8,
+                         device="cuda")
+        wb.quantize_q4(Wbf, Wq)
+        return Wq
+    qblocks = [{k: (packed(v) if k in mats else v) for k, v in b.items()} for b in dblocks]
+    qhead = {"gamma_f": dhead["gamma_f"], "Wlm": packed(dhead["Wlm"])}
+    torch.cuda.synchronize()
+    q4_bytes = sum(v.numel() for b in qblocks for k, v in b.items() if k in mats)
+    q4_bytes += qhead["Wlm"].numel()
+    bf16_bytes = sh.chain_weight_bytes()
+    chain = {"weights_bf16_bytes": bf16_bytes, "weights_q4_bytes": q4_bytes,
+             "bytes_ratio": round(bf16_bytes / q4_bytes, 3)}
+    for B in (1, 4):
+        dattn = to_dev(attn[:, :B], torch)
+        dh0 = torch.from_numpy(np.ascontiguousarray(h0[:B])).cuda()
+        res = {}
+        for name, blks, hd, q4 in (("bf16", dblocks, dhead, False), ("q4", qblocks, qhead, True)):
+            ch = wc.qwen_chain(blks, hd, dattn, dh0, eps=sh.eps, use_pdl=True, q4=q4)
+            ch.chain.capture()
+            for _ in range(5):
+                ch.run(st)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 200
+            e0.record(st)
+            for _ in range(n):
+                ch.run(st)
+            e1.record(st)
+            torch.cuda.synchronize()
+            res[name] = e0.elapsed_time(e1) * 1e3 / n
+            del ch
+        chain[f"batch{B}"] = {
+            "bf16_us_per_step": round(res["bf16"], 1), "q4_us_per_step": round(res["q4"], 1),
+            "speedup": round(res["bf16"] / res["q4"], 2),
+            "q4_GB_s": round(q4_bytes / res["q4"] / 1e3, 1),
+            "q4_frac_of_measured_hbm": round(q4_bytes / res["q4"] / 1e3 / hbm, 3)}
+    assert wb.device_error() == 0
+    print(json.dumps({"mode": "q4", "hbm_peak_gbs": hbm, "gemv": gemv, "chain": chain}))
+    return 0
+
+
 def run_attention(args):
     """Decode attention with the key-value append, Qwen2.5-1.5B heads (12 query
     heads over 2 key-value heads of 128), one JSON line: per (batch, cached
@@ -825,6 +954,8 @@ def main():
         return run_configs(args)
     if args.mode == "attention":
         return run_attention(args)
+    if args.mode == "q4":
+        return run_q4(args)
     return run_ours(args)
 
 
