@@ -460,9 +460,12 @@ ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind,
 long ws_debug_gemv_copies(int M, int K, int B, int nmat, int allow_split, int cta,
                           long long *triples, long max_triples);
 /* The same for packed 4-bit rows (source offsets into [nmat][M] rows of
- * ws_q4_row_bytes(K) bytes); also returns the schedule in *sched (if given). */
-long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, long long *triples,
-                             long max_triples, ws_gemv_schedule *sched);
+ * ws_q4_row_bytes(K) bytes), for the CUDA-core kernel (mma = 0) or the
+ * tensor-core one (mma = 1: bf16 x for one matrix, RMSNorm + SwiGLU for a
+ * pair); also returns the schedule in *sched (if given); -1 when the launch
+ * would not take that kernel. */
+long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, int mma,
+                             long long *triples, long max_triples, ws_gemv_schedule *sched);
 
 /* Read-only streaming kernel over [ptr, ptr + bytes): a read-roofline probe.
  * Writes one checksum per CTA into sink (uint32 [blocks]). */

@@ -186,10 +186,11 @@ Q4_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("mma", [False, True])
 @pytest.mark.parametrize("M,K,B,nmat", Q4_SHAPES)
-def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat):
+def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, mma):
     rb = wb.q4_row_bytes(K)
-    _, sc = wb.debug_gemv_copies_q4(M, K, B, nmat, 0)
+    _, sc = wb.debug_gemv_copies_q4(M, K, B, nmat, 0, mma)
     assert sc["smem_bytes"] <= 227 * 1024 and 2 <= sc["NSW"] <= 8
     assert sc["S"] == 1 and sc["KS"] == K
     assert sc["PC"] == K or sc["PC"] % 512 == 0
@@ -197,7 +198,7 @@ def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat):
     warp_ring = sc["NSW"] * sc["piece_bytes"]
     covered = np.zeros(nmat * M * rb // 16, np.int32)
     for cta in range(sc["grid"]):
-        copies, _ = wb.debug_gemv_copies_q4(M, K, B, nmat, cta)
+        copies, _ = wb.debug_gemv_copies_q4(M, K, B, nmat, cta, mma)
         for src, dst, n in copies:
             assert n > 0 and n % 16 == 0 and src % 16 == 0 and dst % 16 == 0
             assert 0 <= src and src + n <= nmat * M * rb

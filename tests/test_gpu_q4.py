@@ -49,16 +49,33 @@ def test_quantizer_matches_oracle_bitwise(M, K):
     _quantize_both(W)
 
 
+def _with_forms(forms):
+    base = wb.get_tuning()
+    t = wb.Tuning()
+    for f, _ in wb.Tuning._fields_:
+        setattr(t, f, getattr(base, f))
+    t.forms = forms
+    wb.set_tuning(t)
+    return base
+
+
+@pytest.mark.parametrize("kernel", ["mma", "cuda_cores"])
 @pytest.mark.parametrize("M,K,B", [(37, 640, 1), (37, 640, 3), (300, 1408, 2), (2048, 1536, 1),
                                    (1536, 8960, 1), (1536, 8960, 4), (8960, 1536, 1),
-                                   (5, 128, 4)])
-def test_gemv_q4_matches_oracle(M, K, B):
+                                   (5, 128, 4), (151936 // 8, 1536, 2)])
+def test_gemv_q4_matches_oracle(M, K, B, kernel):
+    """Both 4-bit kernels: the tensor-core one (chain forms) and the CUDA-core
+    one (taken with the chain forms switched off)."""
     W = synth.normal_bf16((M, K), 0.02, M + K + B, "q4/W")
     Wq, ref = _quantize_both(W)
     x = synth.normal_bf16((B, K), 1.0, M + K + B, "q4/x")
     y = torch.full((B, M), float("nan"), device="cuda")
-    wb.gemv_q4(Wq, dev_bf16(x), y, K)
-    torch.cuda.synchronize()
+    base = _with_forms(1 if kernel == "mma" else 0)
+    try:
+        wb.gemv_q4(Wq, dev_bf16(x), y, K)
+        torch.cuda.synchronize()
+    finally:
+        wb.set_tuning(base)
     assert_fp32(y.cpu().numpy(), oq4.gemv(ref, K, oracle.bf16_to_f64(x)), what=f"{M}x{K} B={B}")
 
 

@@ -129,7 +129,7 @@ _OTHER = {
     "ws_chain_destroy": ([P], None),
     "ws_get_tuning": ([P], None),
     "ws_debug_gemv_copies": ([I32, I32, I32, I32, I32, I32, P, C.c_long], C.c_long),
-    "ws_debug_gemv_copies_q4": ([I32, I32, I32, I32, I32, P, C.c_long, P], C.c_long),
+    "ws_debug_gemv_copies_q4": ([I32, I32, I32, I32, I32, I32, P, C.c_long, P], C.c_long),
     "ws_version": ([], C.c_char_p),
 }
 
@@ -358,15 +358,15 @@ def gemv_plan(M, K, B, nmat=1, prologue=PRO_NONE, epilogue=EPI_F32, allow_split=
     return {n: getattr(s, n) for n, _ in GemvSchedule._fields_}
 
 
-def debug_gemv_copies_q4(M, K, B, nmat, cta):
+def debug_gemv_copies_q4(M, K, B, nmat, cta, mma=False):
     """(triples, schedule dict) of CTA `cta` for packed 4-bit rows."""
     lib = load()
     sc = GemvSchedule()
-    n = lib.ws_debug_gemv_copies_q4(M, K, B, nmat, cta, None, 0, C.byref(sc))
+    n = lib.ws_debug_gemv_copies_q4(M, K, B, nmat, cta, int(mma), None, 0, C.byref(sc))
     if n < 0:
         raise WsError(-1, "bad arguments")
     buf = (C.c_longlong * (3 * max(n, 1)))()
-    lib.ws_debug_gemv_copies_q4(M, K, B, nmat, cta, buf, n, None)
+    lib.ws_debug_gemv_copies_q4(M, K, B, nmat, cta, int(mma), buf, n, None)
     sched = {f: getattr(sc, f) for f, _ in GemvSchedule._fields_}
     return [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n)], sched
 

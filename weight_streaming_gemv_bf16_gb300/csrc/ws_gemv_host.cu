@@ -214,6 +214,95 @@ static bool plan_gemv_mma(GemvParams& p, int force_S, int grid_target) {
   return true;
 }
 
+// Schedule of the tensor-core kernel for 4-bit rows (chain forms, B <= 4,
+// every size): 16-row tasks over all eight warps, no K split, the B
+// activation rows staged once (padding rows of the fragments read a zero
+// row), pieces of whole super-groups of at most 24 KB over all matrices
+// (whole rows when they fit), rows an odd number of 16-byte units apart,
+// and as many ring stages as shared memory holds (up to eight).
+static bool plan_gemv_q4mma(GemvParams& p, int grid_target) {
+  const int K = p.K, nmat = p.nmat;
+  if (p.B > 4 || K % kQ4Group != 0) return false;
+  const int F = mma_form(p, 4);  // four activation rows staged
+  if (F == F_ANY || !pick_kernel_q4mma(nmat, F)) return false;
+  Sched sc;
+  memset(&sc, 0, sizeof sc);
+  sc.BT = 8;
+  sc.RT = kMmaTaskRows;
+  const int RG = row_groups(p, kMmaTaskRows);
+  sc.RG = RG;
+  sc.S = 1;
+  sc.KS = K;
+  sc.xrs = (K >> 3) | 1;
+  const int xs_bytes = 4 * sc.xrs * 16;
+  if (xs_bytes > kXsMax) return false;
+  int off = 0;
+  sc.off_bar = off;
+  off += kWarps * kMaxStages * 8;
+  sc.off_flags = off;
+  off += 128;
+  sc.off_stats = off;
+  off += align_up(sc.BT * 2 * 4, 16);
+  sc.off_red = off;
+  off += align_up((kWarps + 1) * sc.BT * 4, 16);
+  sc.off_arg = off;
+  off += kWarps * 32 * 8;
+  sc.off_xzero = off;
+  off += 16;
+  sc.off_xsum = off;
+  off += 8 * (K / kQ4Group) * 4;
+  sc.off_xs = align_up(off, 128);
+  off = sc.off_xs + align_up(xs_bytes, 128);
+  sc.off_ring = align_up(off, 128);
+  int Gs = grid_target;
+  if (Gs > RG) Gs = RG;
+  if ((unsigned long long)Gs * (unsigned long long)RG >= (1ull << 32)) return false;
+  sc.Gs = Gs;
+  sc.grid = Gs;
+  const int res_bytes =
+      p.epilogue == EPI_RESID ? (RG + Gs - 1) / Gs * kMmaTaskRows * sc.BT * 4 : 0;
+  // pieces: the largest run of whole super-groups (whole rows first) of at
+  // most 24 KB over all matrices that leaves every warp three ring stages,
+  // else two
+  const int avail = kSmemMax - sc.off_ring - res_bytes - 16;
+  int NSW = 0;
+  for (const int need : {3, 2}) {
+    for (int pc = K; pc >= kQ4Super || pc == K; pc = (pc == K ? (K - 1) / kQ4Super * kQ4Super
+                                                             : pc - kQ4Super)) {
+      if (pc <= 0) break;
+      int u = (q4_prefix(pc) + 15) / 16;
+      if (u % 2 == 0) ++u;
+      const int pb = align_up(nmat * kMmaTaskRows * u * 16, 128);
+      if (pb > 24576 && pc > kQ4Super) continue;
+      const int nsw = avail / (kWarps * pb);
+      if (nsw >= need) {
+        sc.PC = pc;
+        sc.prow = u * 16;
+        sc.piece_bytes = pb;
+        NSW = nsw;
+        break;
+      }
+    }
+    if (NSW) break;
+  }
+  if (NSW < 2) return false;
+  sc.NP = (K + sc.PC - 1) / sc.PC;
+  if (NSW > kMaxStages) NSW = kMaxStages;
+  sc.NSW = NSW;
+  sc.smem_bytes = sc.off_ring + kWarps * NSW * sc.piece_bytes;
+  if (res_bytes) {
+    sc.off_res = align_up(sc.smem_bytes, 16);
+    sc.res_rows = (RG + Gs - 1) / Gs * kMmaTaskRows;
+    sc.smem_bytes = sc.off_res + res_bytes;
+  }
+  sc.mma = 1;
+  sc.form = F;
+  p.sc = sc;
+  p.M_total = 0;
+  for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
+  return true;
+}
+
 // Choose the schedule.  force_S > 0 fixes the K split; force_S == 0 lets the
 // heuristic split skinny shapes; force_S < 0 forbids splitting.
 bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
@@ -223,6 +312,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   const int warps_total = grid_target * kWarps;
   const bool q4 = p.wfmt == WF_Q4;
   if (!q4 && tu.mma && tu.forms && plan_gemv_mma(p, force_S, grid_target)) return true;
+  if (q4 && tu.forms && plan_gemv_q4mma(p, grid_target)) return true;
   Sched sc;
   memset(&sc, 0, sizeof sc);
   sc.BT = batch_template(p.B);
@@ -464,7 +554,8 @@ bool bind_workspace(GemvParams& p, void* ws, size_t ws_bytes) {
 // for its batch tile, else the general one.
 static GemvKernel pick_kernel(const GemvParams& p) {
   const int BT = p.sc.BT, nmat = p.nmat, RT = p.sc.RT;
-  if (p.sc.mma) return pick_kernel_mma(BT, nmat, p.sc.form);
+  if (p.sc.mma) return p.wfmt == WF_Q4 ? pick_kernel_q4mma(nmat, p.sc.form)
+                                       : pick_kernel_mma(BT, nmat, p.sc.form);
   const int F = tuning().forms ? kernel_form(p) : F_ANY;
   if (p.wfmt == WF_Q4) {
     GemvKernel k = F != F_ANY ? pick_kernel_q4(BT, nmat, RT, F) : nullptr;
@@ -963,8 +1054,8 @@ ws_status ws_gemv_plan(int M_total, int K, int B, int nmat, int prologue_kind, i
   return WS_OK;
 }
 
-long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, long long* triples,
-                             long max_triples, ws_gemv_schedule* out) {
+long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, int mma,
+                             long long* triples, long max_triples, ws_gemv_schedule* out) {
   if (check_common(M, K, B) != WS_OK || K % kQ4Group || (nmat != 1 && nmat != 2)) return -1;
   GemvParams p;
   init_gemv_params(p, K, B);
@@ -973,9 +1064,14 @@ long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, long long* 
   p.nmat = nmat;
   p.seg[0].M = M;
   p.epilogue = nmat == 2 ? EPI_SWIGLU : EPI_F32;
+  if (mma) {  // the chain forms the tensor-core kernel takes
+    p.x_dtype = nmat == 2 ? DT_F32 : DT_BF16;
+    p.prologue = nmat == 2 ? PRO_RMSNORM : PRO_NONE;
+  }
   char why[256];
   if (!plan_gemv(p, -1, why, sizeof why)) return -1;
   const Sched& sc = p.sc;
+  if (sc.mma != (mma ? 1 : 0)) return -1;
   if (out) {
     out->RT = sc.RT;
     out->S = sc.S;
@@ -1007,7 +1103,8 @@ long ws_debug_gemv_copies_q4(int M, int K, int B, int nmat, int cta, long long* 
       const int rows = (sc.RT < M - row0) ? sc.RT : M - row0;
       const int c0 = k0 + j * sc.PC;
       const int len = (sc.PC < sc.KS - j * sc.PC) ? sc.PC : sc.KS - j * sc.PC;
-      const int src0 = q4_prefix(c0), nb = q4_prefix(c0 + len) - src0, pst = q4_prefix(sc.PC);
+      const int src0 = q4_prefix(c0), nb = q4_prefix(c0 + len) - src0;
+      const int pst = sc.mma ? sc.prow : q4_prefix(sc.PC);
       const long long dst0 = w * warp_ring + (long long)(q % sc.NSW) * sc.piece_bytes;
       for (int mat = 0; mat < nmat; ++mat)
         for (int r = 0; r < rows; ++r) {

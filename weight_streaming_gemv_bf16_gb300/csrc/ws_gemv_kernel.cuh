@@ -1060,5 +1060,6 @@ GemvKernel pick_form_b8(int BT, int nmat, int RT, int F);
 GemvKernel pick_form_b16(int BT, int nmat, int RT, int F);
 GemvKernel pick_kernel_mma(int BT, int nmat, int F);
 GemvKernel pick_kernel_q4(int BT, int nmat, int RT, int F);
+GemvKernel pick_kernel_q4mma(int nmat, int F);
 
 }  // namespace ws

@@ -103,10 +103,31 @@ __device__ void stage_copy_mma(const GemvParams& p, uint16_t* xs, int c0, int nc
 // One piece of a task: kMmaRows rows x len columns of every matrix, each row
 // a 1-D bulk copy to its prow-strided place in the ring slot (rows past the
 // segment's end are left as they are; their results are never stored).
-template <int NMAT>
+template <int NMAT, bool Q4 = false>
 __device__ __forceinline__ void issue_piece_mma(const GemvParams& p, int rg, int j, int slot, int k0,
                                                 uint8_t* ring, uint64_t* full, uint64_t pol) {
   const Sched& sc = p.sc;
+  if constexpr (Q4) {
+    // 4-bit rows: the piece's whole super-groups of each row
+    int seg, rgl;
+    decode_rg(p, rg, seg, rgl);
+    const Seg& S = p.seg[seg];
+    const int row0 = rgl * kMmaRows;
+    const int rows = min(kMmaRows, S.M - row0);
+    const int c0 = k0 + j * sc.PC;
+    const int len = min(sc.PC, sc.KS - j * sc.PC);
+    const int rb = q4_prefix(p.K), src0 = q4_prefix(c0), nb = q4_prefix(c0 + len) - src0;
+    uint8_t* dst = ring + (size_t)slot * sc.piece_bytes;
+    mbar_arrive_expect_tx(&full[slot], (uint32_t)(NMAT * rows * nb));
+#pragma unroll
+    for (int mat = 0; mat < NMAT; ++mat) {
+      const uint8_t* W = reinterpret_cast<const uint8_t*>(mat == 0 ? S.W0 : S.W1);
+      for (int r = 0; r < rows; ++r)
+        bulk_copy_g2s(dst + (size_t)(mat * kMmaRows + r) * sc.prow,
+                      W + (size_t)(row0 + r) * rb + src0, (uint32_t)nb, &full[slot], pol);
+    }
+    return;
+  }
   int seg, rgl;
   decode_rg(p, rg, seg, rgl);
   const Seg& S = p.seg[seg];
@@ -157,14 +178,86 @@ __device__ __forceinline__ void mma_piece(float (&d)[NMAT][BT / 8][4], uint32_t 
   }
 }
 
+// Two 4-bit codes of a word (bits 4j.. and 16 + 4j..) as a bf16 pair 128 + q
+// (0x4300 is 128 in bf16; the nibble lands in the low mantissa bits).
+__device__ __forceinline__ uint32_t q4_mma_pair(uint32_t w, int j) {
+  return ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+}
+
+// 4-bit rows (16 of each matrix, prow bytes apart in the ring) against the
+// staged activations over one piece, group by group.  Lane (g, t) builds the
+// A fragments of rows g and g + 8 from their code words (pair t of a word is
+// weights 2t and 2t + 1 of its eight, as 128 + q in bf16), one m16n8k16 MMA
+// per 16 columns into a fresh group accumulator (two chains), then
+// d += s * D + (z - 136 s) * X with the group's (s, z) per row and X the
+// batch column's sum of the group's 128 activations: the sum of
+// (s (q - 8) + z) x.  Batch rows past the staged ones read a zero row.
+template <int NMAT>
+__device__ __forceinline__ void mma_piece_q4(float (&d)[NMAT][1][4], const uint8_t* st,
+                                             uint32_t xa, uint32_t xzero, const float* xsg,
+                                             int len, int prow, int xrow, int nxg, int nb_rows,
+                                             int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const int ngr = len >> 7;
+  const int br = lane & 7;
+  const bool bz = br >= nb_rows;
+  const uint32_t bbase = bz ? xzero : xa + (uint32_t)(br * xrow + (lane >> 3) * 16);
+#pragma unroll 1
+  for (int gg = 0; gg < ngr; ++gg) {
+    const int u = gg >> 2, gi = gg & 3;
+    const int gu = min(4, ngr - 4 * u);
+    const int coff = u * kQ4SuperBytes + gi * 64;
+    const int soff = u * kQ4SuperBytes + gu * 64 + gi * 4;
+    float dg[NMAT][2][4];
+    uint32_t sz0[NMAT], sz1[NMAT];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dg[m][0][i] = dg[m][1][i] = 0.f;
+      sz0[m] = *reinterpret_cast<const uint32_t*>(st + (size_t)(m * kMmaRows + g) * prow + soff);
+      sz1[m] = *reinterpret_cast<const uint32_t*>(st + (size_t)(m * kMmaRows + g + 8) * prow + soff);
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {  // 32 columns: two MMA steps
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(bz ? bbase : bbase + (uint32_t)((gg * 128 + h * 32) * 2), b0, b1, b2, b3);
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        const uint4 w0 = *reinterpret_cast<const uint4*>(
+            st + (size_t)(m * kMmaRows + g) * prow + coff + h * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(
+            st + (size_t)(m * kMmaRows + g + 8) * prow + coff + h * 16);
+        mma_bf16_16816(dg[m][0], q4_mma_pair(w0.x, t), q4_mma_pair(w1.x, t),
+                       q4_mma_pair(w0.y, t), q4_mma_pair(w1.y, t), b0, b1);
+        mma_bf16_16816(dg[m][1], q4_mma_pair(w0.z, t), q4_mma_pair(w1.z, t),
+                       q4_mma_pair(w0.w, t), q4_mma_pair(w1.w, t), b2, b3);
+      }
+    }
+    const float x0 = xsg[(2 * t) * nxg + gg], x1 = xsg[(2 * t + 1) * nxg + gg];
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m) {
+      const float s0 = bf16lo(sz0[m]), z0 = fmaf(-136.f, s0, bf16hi(sz0[m]));
+      const float s1 = bf16lo(sz1[m]), z1 = fmaf(-136.f, s1, bf16hi(sz1[m]));
+      d[m][0][0] = fmaf(z0, x0, fmaf(s0, dg[m][0][0] + dg[m][1][0], d[m][0][0]));
+      d[m][0][1] = fmaf(z0, x1, fmaf(s0, dg[m][0][1] + dg[m][1][1], d[m][0][1]));
+      d[m][0][2] = fmaf(z1, x0, fmaf(s1, dg[m][0][2] + dg[m][1][2], d[m][0][2]));
+      d[m][0][3] = fmaf(z1, x1, fmaf(s1, dg[m][0][3] + dg[m][1][3], d[m][0][3]));
+    }
+  }
+}
+
 // The tensor-core kernel for the chain forms F at batch tile BT (8 or 16):
 // the same ring, waits, staging order, epilogues and split-K protocol as
 // k_stream_gemv; 16-row tasks and MMA fragments in place of the lane dot
 // products and the warp reduction.
-template <int BT, int NMAT, int F>
+template <int BT, int NMAT, int F, bool Q4 = false>
 __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_constant__ GemvParams p) {
   static_assert(BT == 8 || BT == 16, "tensor-core kernel: batch tile 8 or 16");
+  static_assert(!Q4 || BT == 8, "4-bit rows: one batch group (B <= 4 staged)");
   constexpr int NG = BT / 8;
+  // streaming warps: all of them for 4-bit rows (small pieces), else kMmaWarps
+  constexpr int NWS = Q4 ? kWarps : kMmaWarps;
+  constexpr int SBT = Q4 ? 4 : BT;  // activation rows staged
   using FT = FormTraits<F>;
   constexpr int EPI = FT::epi;
   static_assert(EPI >= 0, "tensor-core kernel: chain forms only");
@@ -191,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_co
   const int NP = sc.NP, NSW = sc.NSW;
   // pieces of this warp: row groups rg0 + warp + t * kMmaWarps
   const int npw =
-      (warp < kMmaWarps && rg1 - rg0 > warp) ? (rg1 - rg0 - warp + kMmaWarps - 1) / kMmaWarps * NP : 0;
+      (warp < NWS && rg1 - rg0 > warp) ? (rg1 - rg0 - warp + NWS - 1) / NWS * NP : 0;
   const int rgw = rg0 + warp;  // this warp's first row group
 
   int iq = 0, iti = 0, ij = 0, islot = 0;
@@ -201,15 +294,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_co
     fence_mbar_init();
     pol = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
     while (iq < NSW && iq < npw) {  // the whole ring before the dependency wait
-      issue_piece_mma<NMAT>(p, rgw + iti * kMmaWarps, ij, islot, k0, ring, full, pol);
+      issue_piece_mma<NMAT, Q4>(p, rgw + iti * NWS, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
       if (++islot == NSW) islot = 0;
     }
   }
-  constexpr int NR = form_round_chunks(BT);
+  constexpr int NR = form_round_chunks(SBT);
   uint4 gpre[NR];
-  if constexpr (FT::rms1) gamma_preload<NR, BT>(p, tid, gpre);
+  if constexpr (FT::rms1) gamma_preload<NR, SBT>(p, tid, gpre);
   pdl_launch_dependents();
   pdl_wait();
   if (stamp && tid == 0) stamp[1] = global_ns();
@@ -229,10 +322,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_co
     }
   }
   if constexpr (FT::rms1)
-    stage_rms_mma<BT, NR>(p, stats, red, xs, k0 >> 3, sc.KS >> 3, sc.xrs, tid, gpre);
+    stage_rms_mma<SBT, NR>(p, stats, red, xs, k0 >> 3, sc.KS >> 3, sc.xrs, tid, gpre);
   else
-    stage_copy_mma<BT>(p, xs, k0 >> 3, sc.KS >> 3, sc.xrs, tid);
+    stage_copy_mma<SBT>(p, xs, k0 >> 3, sc.KS >> 3, sc.xrs, tid);
   __syncthreads();
+  // 4-bit rows: per batch row (8, rows past the staged 4 zero) the sum of
+  // each 128-column group of the staged activations, and a zero row for the
+  // padding rows of the activation fragments
+  float* xsg = Q4 ? reinterpret_cast<float*>(smem + sc.off_xsum) : nullptr;
+  const int nxg = sc.KS >> 7;
+  if constexpr (Q4) {
+    for (int o = tid; o < 8 * nxg; o += kThreads) {
+      const int b = o / nxg, c = o - b * nxg;
+      float sum = 0.f;
+      if (b < SBT) {
+        const uint4* src = reinterpret_cast<const uint4*>(xs) + (size_t)b * sc.xrs + 16 * c;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const uint4 v = src[i];
+          sum += bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y);
+          sum += bf16lo(v.z) + bf16hi(v.z) + bf16lo(v.w) + bf16hi(v.w);
+        }
+      }
+      xsg[o] = sum;
+    }
+    if (tid < 4) reinterpret_cast<uint32_t*>(smem + sc.off_xzero)[tid] = 0u;
+    __syncthreads();
+  }
   if (stamp && tid == 0) stamp[2] = global_ns();
 
   const int xrow = sc.xrs * 16;  // bytes between activation rows
@@ -259,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_co
   int ti = 0, j = 0, slot = 0;
   uint32_t phase = 0;
   for (int q = 0; q < npw; ++q) {
-    const int rg = rgw + ti * kMmaWarps;
+    const int rg = rgw + ti * NWS;
     int seg, rgl;
     decode_rg(p, rg, seg, rgl);
     const int row0 = rgl * kMmaRows;
@@ -270,14 +386,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_co
       abort = true;
       if (lane == 0) raise_device_error(p.err, DERR_TIMEOUT);
     }
-    if (!abort)
-      mma_piece<BT, NMAT>(d, ring_a + (uint32_t)(slot * sc.piece_bytes),
-                          xs_a + (uint32_t)(j * sc.PC * 2), len, sc.prow, xrow, lane);
+    if (!abort) {
+      if constexpr (Q4)
+        mma_piece_q4<NMAT>(d, ring + (size_t)slot * sc.piece_bytes,
+                           xs_a + (uint32_t)(j * sc.PC * 2), smem_addr(smem + sc.off_xzero),
+                           xsg + j * (sc.PC >> 7), len, sc.prow, xrow, nxg, SBT, lane);
+      else
+        mma_piece<BT, NMAT>(d, ring_a + (uint32_t)(slot * sc.piece_bytes),
+                            xs_a + (uint32_t)(j * sc.PC * 2), len, sc.prow, xrow, lane);
+    }
     // ldmatrix has returned every lane's values (they fed the MMAs above):
     // refill the slot
     __syncwarp();
     if (lane == 0 && !abort && iq < npw) {
-      issue_piece_mma<NMAT>(p, rgw + iti * kMmaWarps, ij, islot, k0, ring, full, pol);
+      issue_piece_mma<NMAT, Q4>(p, rgw + iti * NWS, ij, islot, k0, ring, full, pol);
       ++iq;
       if (++ij == NP) { ij = 0; ++iti; }
       if (++islot == NSW) islot = 0;
@@ -426,5 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv_mma(const __grid_co
 }
 
 GemvKernel pick_kernel_mma(int BT, int nmat, int F);
+GemvKernel pick_kernel_q4mma(int nmat, int F);
 
 }  // namespace ws
