@@ -186,8 +186,16 @@ Q4_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("mma", [False, True])
-@pytest.mark.parametrize("M,K,B,nmat", Q4_SHAPES)
+# the tensor-core 4-bit kernel takes ops of at least two 16-row tasks per warp
+Q4_MMA_SHAPES = [
+    (151936, 1536, 1, 1),  # LM head
+    (40000, 640, 3, 1),    # ragged rows, a one-group tail
+    (40000, 1408, 2, 2),   # a pair, a three-group tail
+]
+
+
+@pytest.mark.parametrize("M,K,B,nmat,mma", [s + (False,) for s in Q4_SHAPES] +
+                         [s + (True,) for s in Q4_MMA_SHAPES])
 def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, mma):
     rb = wb.q4_row_bytes(K)
     _, sc = wb.debug_gemv_copies_q4(M, K, B, nmat, 0, mma)

@@ -85,6 +85,10 @@ MID = synth.QwenShape(hidden=512, kv_dim=128, inter=1408, vocab=4096, layers=2)
 
 @pytest.mark.parametrize("B,shape", [(1, SMALL), (2, SMALL), (4, SMALL), (1, MID), (3, MID)])
 def test_q4_chain_matches_oracle(B, shape):
+    _q4_chain_check(B, shape)
+
+
+def _q4_chain_check(B, shape):
     seed = 11 * B + shape.hidden
     blocks = [synth.qwen_block_weights(shape, seed, l) for l in range(shape.layers)]
     head = synth.qwen_head_weights(shape, seed)
@@ -121,3 +125,31 @@ def test_q4_chain_matches_oracle(B, shape):
     clear = (top2[:, 1] - top2[:, 0]) > 2 * 2e-3 * np.maximum(np.abs(top2[:, 1]), rms)
     ref_idx = oracle.argmax_rows(logits)
     assert np.array_equal(idx[clear], ref_idx[clear])
+
+
+@pytest.mark.parametrize("M,K,B", [(40000, 640, 1), (40000, 640, 3), (39000, 1408, 4)])
+def test_gemv_q4_tensor_core_kernel(M, K, B):
+    """Shapes with at least two 16-row tasks per warp take the tensor-core
+    4-bit kernel; every output against the oracle on a sample of rows (every
+    seventh, and the last 40: the ragged final task)."""
+    W = synth.normal_bf16((M, K), 0.02, M + K + B, "q4/Wbig")
+    Wq = torch.zeros((M, wb.q4_row_bytes(K)), dtype=torch.uint8, device="cuda")
+    wb.quantize_q4(dev_bf16(W), Wq)
+    rows = np.unique(np.concatenate([np.arange(0, M, 7), np.arange(M - 40, M)]))
+    codes, s, z = oq4.quantize(W[rows])
+    ref = oq4.pack(codes, s, z)
+    assert np.array_equal(Wq.cpu().numpy()[rows], ref)
+    x = synth.normal_bf16((B, K), 1.0, M + B, "q4/xbig")
+    y = torch.full((B, M), float("nan"), device="cuda")
+    wb.gemv_q4(Wq, dev_bf16(x), y, K)
+    torch.cuda.synchronize()
+    assert_fp32(y.cpu().numpy()[:, rows], oq4.gemv(ref, K, oracle.bf16_to_f64(x)),
+                what=f"{M}x{K} B={B}")
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_q4_chain_with_a_tensor_core_lm_head(B):
+    """A vocabulary of 40000 rows puts the LM head (RMSNorm, argmax) on the
+    tensor-core 4-bit kernel."""
+    shape = synth.QwenShape(hidden=256, kv_dim=64, inter=512, vocab=40000, layers=1)
+    _q4_chain_check(B, shape)

@@ -230,6 +230,11 @@ static bool plan_gemv_q4mma(GemvParams& p, int grid_target) {
   sc.BT = 8;
   sc.RT = kMmaTaskRows;
   const int RG = row_groups(p, kMmaTaskRows);
+  // only ops with at least two 16-row tasks per warp (the LM head): with
+  // fewer, most warps idle and a task's single warp streams its whole K
+  // (measured: the 1536 x 8960 Wd 37.6 us on this kernel, 5.6 on the
+  // CUDA-core one)
+  if (RG < 2 * grid_target * kWarps) return false;
   sc.RG = RG;
   sc.S = 1;
   sc.KS = K;
@@ -451,7 +456,12 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
     off += align_up(sc.BT * (sc.KS / 32) * 4, 128);
   }
   sc.off_ring = align_up(off, 128);
-  int ring_budget = tu.ring_bytes > 0 ? tu.ring_bytes : 96 * 1024;
+  // 4-bit rows: pieces are 3.76 times smaller for the same rows, so the ring
+  // takes the shared memory there is, less 4 KB for the residual rows
+  // (measured on the 4-bit chain: the LM head 87 -> 55 us, gate/up 11.5 ->
+  // 9.2 us)
+  int ring_budget =
+      tu.ring_bytes > 0 ? tu.ring_bytes : (q4 ? kSmemMax - sc.off_ring - 4096 : 96 * 1024);
   if (sc.off_ring + ring_budget > kSmemMax) ring_budget = kSmemMax - sc.off_ring;
   int NSW = ring_budget / (kWarps * sc.piece_bytes);
   if (NSW > kMaxStages) NSW = kMaxStages;

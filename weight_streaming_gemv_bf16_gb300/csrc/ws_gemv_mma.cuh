@@ -188,7 +188,9 @@ __device__ __forceinline__ uint32_t q4_mma_pair(uint32_t w, int j) {
 // staged activations over one piece, group by group.  Lane (g, t) builds the
 // A fragments of rows g and g + 8 from their code words (pair t of a word is
 // weights 2t and 2t + 1 of its eight, as 128 + q in bf16), one m16n8k16 MMA
-// per 16 columns into a fresh group accumulator (two chains), then
+// per 16 columns, each into its own accumulator (the eight MMAs of a group
+// are independent: the MMA's latency, not its rate, is what a chain would
+// pay), summed per group, then
 // d += s * D + (z - 136 s) * X with the group's (s, z) per row and X the
 // batch column's sum of the group's 128 activations: the sum of
 // (s (q - 8) + z) x.  Batch rows past the staged ones read a zero row.
@@ -202,18 +204,20 @@ __device__ __forceinline__ void mma_piece_q4(float (&d)[NMAT][1][4], const uint8
   const int br = lane & 7;
   const bool bz = br >= nb_rows;
   const uint32_t bbase = bz ? xzero : xa + (uint32_t)(br * xrow + (lane >> 3) * 16);
-#pragma unroll 1
+#pragma unroll 2
   for (int gg = 0; gg < ngr; ++gg) {
     const int u = gg >> 2, gi = gg & 3;
     const int gu = min(4, ngr - 4 * u);
     const int coff = u * kQ4SuperBytes + gi * 64;
     const int soff = u * kQ4SuperBytes + gu * 64 + gi * 4;
-    float dg[NMAT][2][4];
+    float dg[NMAT][8][4];
     uint32_t sz0[NMAT], sz1[NMAT];
 #pragma unroll
     for (int m = 0; m < NMAT; ++m) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dg[m][0][i] = dg[m][1][i] = 0.f;
+      for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dg[m][kk][i] = 0.f;
       sz0[m] = *reinterpret_cast<const uint32_t*>(st + (size_t)(m * kMmaRows + g) * prow + soff);
       sz1[m] = *reinterpret_cast<const uint32_t*>(st + (size_t)(m * kMmaRows + g + 8) * prow + soff);
     }
@@ -227,9 +231,9 @@ __device__ __forceinline__ void mma_piece_q4(float (&d)[NMAT][1][4], const uint8
             st + (size_t)(m * kMmaRows + g) * prow + coff + h * 16);
         const uint4 w1 = *reinterpret_cast<const uint4*>(
             st + (size_t)(m * kMmaRows + g + 8) * prow + coff + h * 16);
-        mma_bf16_16816(dg[m][0], q4_mma_pair(w0.x, t), q4_mma_pair(w1.x, t),
+        mma_bf16_16816(dg[m][2 * h], q4_mma_pair(w0.x, t), q4_mma_pair(w1.x, t),
                        q4_mma_pair(w0.y, t), q4_mma_pair(w1.y, t), b0, b1);
-        mma_bf16_16816(dg[m][1], q4_mma_pair(w0.z, t), q4_mma_pair(w1.z, t),
+        mma_bf16_16816(dg[m][2 * h + 1], q4_mma_pair(w0.z, t), q4_mma_pair(w1.z, t),
                        q4_mma_pair(w0.w, t), q4_mma_pair(w1.w, t), b2, b3);
       }
     }
@@ -238,10 +242,15 @@ __device__ __forceinline__ void mma_piece_q4(float (&d)[NMAT][1][4], const uint8
     for (int m = 0; m < NMAT; ++m) {
       const float s0 = bf16lo(sz0[m]), z0 = fmaf(-136.f, s0, bf16hi(sz0[m]));
       const float s1 = bf16lo(sz1[m]), z1 = fmaf(-136.f, s1, bf16hi(sz1[m]));
-      d[m][0][0] = fmaf(z0, x0, fmaf(s0, dg[m][0][0] + dg[m][1][0], d[m][0][0]));
-      d[m][0][1] = fmaf(z0, x1, fmaf(s0, dg[m][0][1] + dg[m][1][1], d[m][0][1]));
-      d[m][0][2] = fmaf(z1, x0, fmaf(s1, dg[m][0][2] + dg[m][1][2], d[m][0][2]));
-      d[m][0][3] = fmaf(z1, x1, fmaf(s1, dg[m][0][3] + dg[m][1][3], d[m][0][3]));
+      float D[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        D[i] = ((dg[m][0][i] + dg[m][1][i]) + (dg[m][2][i] + dg[m][3][i])) +
+               ((dg[m][4][i] + dg[m][5][i]) + (dg[m][6][i] + dg[m][7][i]));
+      d[m][0][0] = fmaf(z0, x0, fmaf(s0, D[0], d[m][0][0]));
+      d[m][0][1] = fmaf(z0, x1, fmaf(s0, D[1], d[m][0][1]));
+      d[m][0][2] = fmaf(z1, x0, fmaf(s1, D[2], d[m][0][2]));
+      d[m][0][3] = fmaf(z1, x1, fmaf(s1, D[3], d[m][0][3]));
     }
   }
 }
