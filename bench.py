@@ -58,6 +58,8 @@ def parse():
                          "a key-value cache at batch 1/4/16 and 1k-32k cached slots; q4: "
                          "4-bit group-128 weights, each GEMV shape and the decode step "
                          "beside bf16")
+    ap.add_argument("--attn-config", default=None,
+                    help="attention mode: one 'batch,slots' configuration instead of all nine")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
                     help="graph: one launch per op, PDL edges, one CUDA graph; persistent: "
                          "the whole step as one cooperative kernel")
@@ -890,8 +892,11 @@ def run_attention(args):
     hbm = peaks()[0]
     nh, nkv, d = 12, 2, 128
     rows = []
-    for B in (1, 4, 16):
-        for n in (1024, 4096, 32768):
+    configs = [(B, n) for B in (1, 4, 16) for n in (1024, 4096, 32768)]
+    if args.attn_config:
+        configs = [tuple(int(v) for v in args.attn_config.split(","))]
+    for B, n in configs:
+        if True:
             S = n
             cache_b = B * nkv * S * d * 2
             ncopy = max(2, -(-(256 << 20) // (2 * cache_b)))
