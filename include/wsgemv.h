@@ -262,8 +262,11 @@ enum { WS_WEIGHTS_BF16 = 0, WS_WEIGHTS_Q4 = 1 };
  * output is supplied in `attn` (bf16 [B][H]). */
 typedef struct {
   const void *gamma1, *Wq, *Wk, *Wv, *Wo, *gamma2, *Wg, *Wu, *Wd; /* bf16 */
-  const void *attn;      /* bf16 [B][H]                                  */
+  const void *attn;      /* bf16 [B][H]  (unused with opts.attention)    */
   float *q, *k, *v;      /* fp32 [B][H], [B][KV], [B][KV]; NULL: internal */
+  /* opts.attention: the block's key-value caches, bf16
+   * [B][KV / 128][s_max][128], updated at pos by every step */
+  void *k_cache, *v_cache;
 } ws_qwen_block;
 
 /* z = bf16(gelu(bf16(bf16(LayerNorm(x)) . W^T + bias))) ("Making small
@@ -330,6 +333,14 @@ typedef struct {
                            ahead across phase boundaries.  Prefetch plans do
                            not apply in this mode.  0: one launch per op with
                            programmatic dependent launch edges.              */
+  /* 1: each Qwen block runs decode attention (ws_decode_attention: the new
+   * key and value appended at pos[b], query heads of 128 over key-value
+   * heads of 128) on its QKV outputs, and Wo reads its bf16 output instead
+   * of `attn`.  pos: int32 [B] on the device, read when the step runs (the
+   * caller advances it between steps); s_max: slots of each cache. */
+  int attention;
+  int s_max;
+  const int32_t *pos;
 } ws_chain_opts;
 
 typedef struct ws_chain ws_chain;

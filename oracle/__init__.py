@@ -268,6 +268,33 @@ def qwen_block(h, blk: dict, attn, eps: float, threads: int = 1) -> dict:
     return {"q": q, "k": k, "v": v, "h_mid": h1, "s": s_bits, "h": h2}
 
 
+def qwen_block_attention(h, blk: dict, k_cache_bits, v_cache_bits, pos, n_kv_heads: int,
+                         eps: float, qkv=None, threads: int = 1) -> dict:
+    """One decoder block with decode attention over its key-value cache in
+    place of the stand-in ("One Token, Kernel by Kernel", Step 1: RMSNorm,
+    grouped-query attention, SwiGLU MLP; "The fix: Part 10's split-KV
+    kernel"): q, k, v from the first RMSNorm, the new key and value appended
+    at pos, attention with heads of 128, its output rounded once to bf16 as
+    Wo's input, then the residual and the MLP as in qwen_block.  qkv, when
+    given, is the (q, k, v) the attention uses instead of this block's own
+    (teacher forcing on another implementation's projections)."""
+    g1 = bf16_to_f64(blk["gamma1"])
+    g2 = bf16_to_f64(blk["gamma2"])
+    a = round_bf16(rmsnorm(h, g1, eps))
+    q = gemv(blk["Wq"], a, threads)
+    k = gemv(blk["Wk"], a, threads)
+    v = gemv(blk["Wv"], a, threads)
+    qa, ka, va = qkv if qkv is not None else (q, k, v)
+    att = decode_attention(qa, ka, va, k_cache_bits, v_cache_bits, pos, n_kv_heads, 128)
+    attn_bits = f64_to_bf16(att["out"])
+    h1 = round_f32(np.asarray(h, np.float64) + gemv(blk["Wo"], bf16_to_f64(attn_bits), threads))
+    m = round_bf16(rmsnorm(h1, g2, eps))
+    s_bits = f64_to_bf16(swiglu(gemv(blk["Wg"], m, threads), gemv(blk["Wu"], m, threads)))
+    h2 = round_f32(h1 + gemv(blk["Wd"], bf16_to_f64(s_bits), threads))
+    return {"q": q, "k": k, "v": v, "attn": attn_bits, "h_mid": h1, "s": s_bits, "h": h2,
+            "k_cache": att["k_cache"], "v_cache": att["v_cache"]}
+
+
 def qwen_chain(h0, blocks, attns, gamma_f, Wlm_bits, eps: float,
                threads: int = 1, keep_blocks: bool = False) -> dict:
     """The full decode weight chain: blocks in order, then the final RMSNorm,

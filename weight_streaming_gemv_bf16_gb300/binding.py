@@ -47,7 +47,7 @@ class PrefetchPlan(C.Structure):
 
 class QwenBlock(C.Structure):
     _fields_ = [(n, P) for n in ("gamma1", "Wq", "Wk", "Wv", "Wo", "gamma2", "Wg", "Wu", "Wd",
-                                 "attn", "q", "k", "v")]
+                                 "attn", "q", "k", "v", "k_cache", "v_cache")]
 
 
 class MlpBlock(C.Structure):
@@ -72,7 +72,7 @@ class ChainOpts(C.Structure):
                 ("y_out", P), ("h_trace", P), ("use_pdl", I32), ("prefetch", I32),
                 ("fixed_plan", PrefetchPlan), ("distance", I32), ("decoy", I32),
                 ("tune_pairs", I32), ("tune_min_gain", F32), ("weight_format", I32),
-                ("persistent", I32)]
+                ("persistent", I32), ("attention", I32), ("s_max", I32), ("pos", P)]
 
 
 class Tuning(C.Structure):

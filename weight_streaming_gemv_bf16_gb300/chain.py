@@ -66,11 +66,14 @@ def _opts(B, H, KV, I, V, eps, use_pdl, prefetch, fixed_plan, distance, decoy, t
 def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
                fixed_plan=None, distance=1, decoy=False, trace=False, keep_qkv=False,
                logits=False, tune_pairs=30, min_gain=0.01, persistent=False,
-               q4=False) -> QwenChain:
+               q4=False, caches=None, pos=None) -> QwenChain:
     """blocks: list of dicts of bf16 device tensors gamma1, Wq, Wk, Wv, Wo, gamma2,
     Wg, Wu, Wd; head: dict gamma_f, Wlm (or None); attn: bf16 [L, B, H];
     h_in: fp32 [B, H].  q4=True: the weight matrices are packed 4-bit rows
-    (uint8 [M, q4_row_bytes(K)], as binding.quantize_q4 writes them)."""
+    (uint8 [M, q4_row_bytes(K)], as binding.quantize_q4 writes them).
+    caches: per block (k_cache, v_cache) bf16 [B, KV/128, s_max, 128] and pos
+    int32 [B] on the device: each block runs decode attention on its q, k, v
+    (attn may then be None)."""
     B, H = h_in.shape
     L = len(blocks)
     KV = blocks[0]["Wk"].shape[0] if L else 0
@@ -88,12 +91,15 @@ def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
             k = torch.empty((B, KV), device=dev)
             v = torch.empty((B, KV), device=dev)
             qkv.append((q, k, v))
+        kc, vc = caches[l] if caches is not None else (None, None)
         d.u.qwen = wb.QwenBlock(*(w[n].data_ptr() for n in ("gamma1", "Wq", "Wk", "Wv", "Wo",
                                                              "gamma2", "Wg", "Wu", "Wd")),
-                                attn[l].data_ptr(),
+                                attn[l].data_ptr() if attn is not None else None,
                                 q.data_ptr() if q is not None else None,
                                 k.data_ptr() if k is not None else None,
-                                v.data_ptr() if v is not None else None)
+                                v.data_ptr() if v is not None else None,
+                                kc.data_ptr() if kc is not None else None,
+                                vc.data_ptr() if vc is not None else None)
         descs.append(d)
     idx = lg = None
     if head is not None:
@@ -109,6 +115,11 @@ def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
     o.h_out = h_out.data_ptr()
     o.h_trace = h_trace.data_ptr() if h_trace is not None else None
     o.weight_format = 1 if q4 else 0
+    if caches is not None:
+        o.attention = 1
+        o.s_max = caches[0][0].shape[2]
+        o.pos = pos.data_ptr()
+        keep += [caches, pos]
     keep += [h_out, h_trace, idx, lg, qkv]
     ch = wb.Chain(descs, o, keepalive=keep)
     return QwenChain(ch, h_in, h_out, attn, idx, lg, h_trace, qkv)

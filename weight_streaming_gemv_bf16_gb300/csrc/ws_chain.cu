@@ -46,6 +46,7 @@ struct ChainOp {
   int block;        // index in the block list
   int trace_block;  // Qwen block whose h is traced after this op, or -1
   std::vector<std::pair<const void*, size_t>> reads;  // weight ranges
+  int attn_call = -1;  // decode attention launched right after this op (QKV), or -1
   size_t bytes;     // algorithmic weight bytes
   std::string shape;
   size_t ws_off, ws_bytes;
@@ -106,6 +107,16 @@ struct ws_chain {
   cudaGraphExec_t host_exec = nullptr;
   const void* host_key[3] = {nullptr, nullptr, nullptr};
   std::vector<const void*> attn_dev;
+  // decode attention inside the chain: per Qwen block its q, k, v (the QKV
+  // op's fp32 outputs) and caches; the bf16 output feeds Wo
+  struct AttnCall {
+    const float *q, *k, *v;
+    void *k_cache, *v_cache;
+  };
+  std::vector<AttnCall> attn_calls;
+  void* attn_buf = nullptr;
+  void* attn_ws = nullptr;
+  size_t attn_ws_bytes = 0;
   int32_t* idx = nullptr;
   // persistent mode: all ops in one cooperative kernel per step
   bool persistent = false;
@@ -128,6 +139,8 @@ static void free_chain_buffers(ws_chain* c) {
   if (c->ws) cudaFree(c->ws);
   if (c->s_buf) cudaFree(c->s_buf);
   if (c->qkv_scratch) cudaFree(c->qkv_scratch);
+  if (c->attn_buf) cudaFree(c->attn_buf);
+  if (c->attn_ws) cudaFree(c->attn_ws);
   for (void* q : c->pp)
     if (q) cudaFree(q);
   c->exec = nullptr;
@@ -163,6 +176,14 @@ static ws_status build_ops(ws_chain* c) {
     bool need_qkv = false;
     for (const ws_block_desc& d : c->blocks)
       if (d.kind == WS_BLOCK_QWEN && (!d.u.qwen.q || !d.u.qwen.k || !d.u.qwen.v)) need_qkv = true;
+    if (o.attention) {
+      c->attn_ws_bytes =
+          ws_attention_workspace_bytes(B, H / 128, o.kv_dim / 128, 128, o.s_max);
+      if (cudaMalloc(&c->attn_buf, (size_t)B * H * 2) != cudaSuccess ||
+          cudaMalloc(&c->attn_ws, c->attn_ws_bytes) != cudaSuccess ||
+          cudaMemset(c->attn_ws, 0, c->attn_ws_bytes) != cudaSuccess)
+        return WS_ERR_NOMEM;
+    }
     if (need_qkv &&
         cudaMalloc((void**)&c->qkv_scratch, (size_t)B * (H + 2 * o.kv_dim) * 4) != cudaSuccess)
       return WS_ERR_NOMEM;
@@ -197,6 +218,10 @@ static ws_status build_ops(ws_chain* c) {
         base += Ms[s];
         op.reads.push_back({Ws[s], (size_t)Ms[s] * H * 2});
       }
+      if (o.attention) {
+        op.attn_call = (int)c->attn_calls.size();
+        c->attn_calls.push_back({qo, ko, vo, q.k_cache, q.v_cache});
+      }
       op.p.x = h_src;
       op.p.x_dtype = DT_F32;
       op.p.prologue = PRO_RMSNORM;
@@ -212,7 +237,7 @@ static ws_status build_ops(ws_chain* c) {
       wo.p.seg[0].W0 = static_cast<const uint16_t*>(q.Wo);
       wo.p.seg[0].out = o.h_out;
       wo.p.seg[0].M = H;
-      wo.p.x = q.attn;
+      wo.p.x = o.attention ? c->attn_buf : q.attn;
       wo.p.x_dtype = DT_BF16;
       wo.p.prologue = PRO_NONE;
       wo.p.epilogue = EPI_RESID;
@@ -259,7 +284,7 @@ static ws_status build_ops(ws_chain* c) {
         c->ops[k].block = bi;
         if (c->ops[k].kind != OP_WD) c->ops[k].trace_block = -1;
       }
-      c->attn_dev.push_back(q.attn);
+      if (!o.attention) c->attn_dev.push_back(q.attn);
       ++qwen_seen;
     } else if (d.kind == WS_BLOCK_MLP) {
       const ws_mlp_block& m = d.u.mlp;
@@ -447,6 +472,16 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
       return WS_ERR_CUDA;
     }
     prev_kernel = true;
+    if (ps.size() == c->ops.size() && c->ops[i].attn_call >= 0) {
+      // the block's decode attention on the QKV op's outputs (split-KV, the
+      // key-value append at pos, positions read on the device)
+      const ws_chain::AttnCall& a = c->attn_calls[c->ops[i].attn_call];
+      const ws_chain_opts& o = c->o;
+      const ws_status s = ws_decode_attention(
+          a.q, a.k, a.v, a.k_cache, a.v_cache, o.pos, nullptr, c->attn_buf, o.batch,
+          o.hidden / 128, o.kv_dim / 128, 128, o.s_max, c->attn_ws, c->attn_ws_bytes, stream);
+      if (s != WS_OK) return s;
+    }
     if (!trace.empty() && trace[i] >= 0) {
       const size_t bytes = trace_bytes(c);
       if (cudaMemcpyAsync(reinterpret_cast<char*>(c->o.h_trace) + (size_t)trace[i] * bytes,
@@ -650,7 +685,10 @@ ws_status ws_chain_create(const ws_block_desc* blocks, int n, const ws_chain_opt
       }
       ++nq;
       const ws_qwen_block& q = blocks[i].u.qwen;
-      const void* req[] = {q.gamma1, q.Wq, q.Wk, q.Wv, q.Wo, q.gamma2, q.Wg, q.Wu, q.Wd, q.attn};
+      const void* req[] = {q.gamma1, q.Wq,     q.Wk, q.Wv, q.Wo,
+                           q.gamma2, q.Wg,     q.Wu, q.Wd,
+                           o.attention ? q.k_cache : q.attn,
+                           o.attention ? q.v_cache : q.attn};
       for (const void* r : req)
         if (!r || !al16(r)) {
           set_error("block %d: null or unaligned pointer", i);
@@ -704,6 +742,14 @@ ws_status ws_chain_create(const ws_block_desc* blocks, int n, const ws_chain_opt
   }
   if (nh && (o.vocab <= 0 || (!nq && (!o.h_in || !al16(o.h_in))))) {
     set_error("head needs vocab > 0 and an input h");
+    return WS_ERR_ARG;
+  }
+  if (o.attention &&
+      (!nq || o.hidden % 128 || o.kv_dim % 128 || (o.hidden / 128) % (o.kv_dim / 128) ||
+       o.hidden / o.kv_dim > 8 || o.s_max < 64 || o.s_max % 64 || !o.pos || o.persistent)) {
+    set_error("attention in the chain: Qwen blocks, heads of 128 (hidden and kv_dim multiples "
+              "of 128, at most 8 query heads per key-value head), s_max a multiple of 64, pos, "
+              "one launch per op");
     return WS_ERR_ARG;
   }
   if (o.weight_format != WS_WEIGHTS_BF16 && o.weight_format != WS_WEIGHTS_Q4) {
