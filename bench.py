@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs", "attention", "q4"],
+    ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs", "attention", "q4",
+                                       "step-attention"],
                     default="chain",
                     help="chain: the decode step (the metric); kernel: gate/up alone (profiler "
                          "captures); sweep: the batch GEMV sweep, fp16 RMSNorm and the "
@@ -57,7 +58,8 @@ def parse():
                          "prefetch (one JSON line each); attention: decode attention over "
                          "a key-value cache at batch 1/4/16 and 1k-32k cached slots; q4: "
                          "4-bit group-128 weights, each GEMV shape and the decode step "
-                         "beside bf16")
+                         "beside bf16; step-attention: the decode step with decode "
+                         "attention over a key-value cache in every block")
     ap.add_argument("--attn-config", default=None,
                     help="attention mode: one 'batch,slots' configuration instead of all nine")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
@@ -874,6 +876,66 @@ def run_q4(args):
     return 0
 
 
+def run_step_attention(args):
+    """The Qwen2.5-1.5B decode step with decode attention in every block (the
+    configs' seeded stand-in replaced), one JSON line: per batch (1, 4) and
+    cached slots (1024, 4096, 32768 at batch 1) the time per step as graph
+    replays between CUDA events, beside the same step with the stand-in."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+    from weight_streaming_gemv_bf16_gb300 import synth
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda").manual_seed(args.seed)
+    sh = synth.QWEN2_5_1_5B
+    H, KV, I, V, L = sh.hidden, sh.kv_dim, sh.inter, sh.vocab, sh.layers
+
+    def rnd(*s, scale=0.02):
+        return (torch.randn(s, device="cuda", generator=gen) * scale).to(torch.bfloat16)
+    blocks = [{"gamma1": rnd(H, scale=0.1) + 1, "gamma2": rnd(H, scale=0.1) + 1,
+               "Wq": rnd(H, H), "Wk": rnd(KV, H), "Wv": rnd(KV, H), "Wo": rnd(H, H),
+               "Wg": rnd(I, H), "Wu": rnd(I, H), "Wd": rnd(H, I)} for _ in range(L)]
+    head = {"gamma_f": rnd(H, scale=0.1) + 1, "Wlm": rnd(V, H)}
+
+    def step_us(ch, n=100):
+        ch.chain.capture()
+        for _ in range(5):
+            ch.run(st)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(n):
+            ch.run(st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+    rows = []
+    for B, n in ((1, 1024), (1, 4096), (1, 32768), (4, 1024), (4, 4096)):
+        h0 = torch.randn((B, H), device="cuda", generator=gen)
+        attn = rnd(L, B, H, scale=1.0)
+        base = wc.qwen_chain(blocks, head, attn, h0, eps=sh.eps)
+        t_base = step_us(base)
+        del base
+        caches = [(rnd(B, KV // 128, n, 128, scale=1.0), rnd(B, KV // 128, n, 128, scale=1.0))
+                  for _ in range(L)]
+        pos = torch.full((B,), n - 1, dtype=torch.int32, device="cuda")
+        ch = wc.qwen_chain(blocks, head, None, h0, eps=sh.eps, caches=caches, pos=pos)
+        t_att = step_us(ch)
+        del ch, caches
+        torch.cuda.empty_cache()
+        cache_bytes = L * B * (KV // 128) * n * 128 * 2 * 2
+        rows.append({"batch": B, "cached_slots": n, "step_us": round(t_att, 1),
+                     "step_us_with_stand_in": round(t_base, 1),
+                     "attention_us_per_step": round(t_att - t_base, 1),
+                     "kv_cache_bytes_read": cache_bytes})
+    assert wb.device_error() == 0
+    print(json.dumps({"mode": "step-attention", "rows": rows}))
+    return 0
+
+
 def run_attention(args):
     """Decode attention with the key-value append, Qwen2.5-1.5B heads (12 query
     heads over 2 key-value heads of 128), one JSON line: per (batch, cached
@@ -961,6 +1023,8 @@ def main():
         return run_attention(args)
     if args.mode == "q4":
         return run_q4(args)
+    if args.mode == "step-attention":
+        return run_step_attention(args)
     return run_ours(args)
 
 
