@@ -213,14 +213,31 @@ __device__ __forceinline__ void merge_cta(const float* src, int n, int G, int t,
   }
 }
 
+// The new token's key and value (the whole warp, 4 dimensions a lane), rounded
+// to bf16, into row pos - 16 tile of a ring stage and into slot pos of the
+// cache.
+__device__ __forceinline__ void stage_new_row(const AttnParams& a, size_t row0, size_t kvn,
+                                              int tile, int pos, unsigned char* st, int lane) {
+  const int rp = pos - tile * kAttnTile;
+  const float4 kf = *reinterpret_cast<const float4*>(a.k_new + kvn + lane * 4);
+  const float4 vf = *reinterpret_cast<const float4*>(a.v_new + kvn + lane * 4);
+  const uint2 ku = make_uint2(bf16x2_bits(kf.x, kf.y), bf16x2_bits(kf.z, kf.w));
+  const uint2 vu = make_uint2(bf16x2_bits(vf.x, vf.y), bf16x2_bits(vf.z, vf.w));
+  *reinterpret_cast<uint2*>(st + rp * kAttnPitch + lane * 8) = ku;
+  *reinterpret_cast<uint2*>(st + (kAttnTile + rp) * kAttnPitch + lane * 8) = vu;
+  *reinterpret_cast<uint2*>(a.k_cache + (row0 + pos) * kAttnDim + lane * 4) = ku;
+  *reinterpret_cast<uint2*>(a.v_cache + (row0 + pos) * kAttnDim + lane * 4) = vu;
+}
+
 // Stage tile `tile` (slots 16 tile .. 16 tile + 15) of one (row, head) into a
 // warp's ring stage: lane l copies key row l (l < 16) or value row l - 16 of
-// the slots before pos; the slot pos comes from the new key and value (the
-// whole warp, 4 dimensions a lane, also written to the cache); later slots
-// are zero.
+// the slots before pos; later slots are zero; the slot pos comes from the new
+// key and value (stage_new_row), here unless with_new is false (the tiles
+// staged before the dependency wait: the new key and value come from the
+// previous kernel).
 __device__ __forceinline__ void stage_tile(const AttnParams& a, size_t row0, size_t kvn, int tile,
                                            int pos, unsigned char* st, uint64_t* bar, int lane,
-                                           uint64_t pol) {
+                                           uint64_t pol, bool with_new) {
   const int slot0 = tile * kAttnTile;
   const int ncopy = max(0, min(kAttnTile, pos - slot0));  // cached rows of this tile
   if (lane == 0) mbar_arrive_expect_tx(bar, 2u * ncopy * kAttnDim * 2);
@@ -237,17 +254,8 @@ __device__ __forceinline__ void stage_tile(const AttnParams& a, size_t row0, siz
 #pragma unroll
     for (int i = 0; i < kAttnDim * 2 / 16; ++i) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
-  if (pos >= slot0 && pos < slot0 + kAttnTile) {
-    const int rp = pos - slot0;
-    const float4 kf = *reinterpret_cast<const float4*>(a.k_new + kvn + lane * 4);
-    const float4 vf = *reinterpret_cast<const float4*>(a.v_new + kvn + lane * 4);
-    const uint2 ku = make_uint2(bf16x2_bits(kf.x, kf.y), bf16x2_bits(kf.z, kf.w));
-    const uint2 vu = make_uint2(bf16x2_bits(vf.x, vf.y), bf16x2_bits(vf.z, vf.w));
-    *reinterpret_cast<uint2*>(st + rp * kAttnPitch + lane * 8) = ku;
-    *reinterpret_cast<uint2*>(st + (kAttnTile + rp) * kAttnPitch + lane * 8) = vu;
-    *reinterpret_cast<uint2*>(a.k_cache + (row0 + pos) * kAttnDim + lane * 4) = ku;
-    *reinterpret_cast<uint2*>(a.v_cache + (row0 + pos) * kAttnDim + lane * 4) = vu;
-  }
+  if (with_new && pos >= slot0 && pos < slot0 + kAttnTile)
+    stage_new_row(a, row0, kvn, tile, pos, st, lane);
   __syncwarp();  // generic rows visible to the warp's ldmatrix
 }
 
@@ -269,29 +277,10 @@ __global__ void __launch_bounds__(kAttnThreads)
     k_decode_attention(const __grid_constant__ AttnParams a) {
   const int g = blockIdx.y, b = blockIdx.z, G = a.G;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  // (loaded before the position, which they do not depend on)
-  // the queries as the MMA's B operand: lane holds head lane / 4, dimensions
-  // 16 k + 2 (lane % 4) + {0, 1} and + 8, as hi and lo bf16 terms
-  uint32_t qh[8][2], ql[8][2];
-  {
-    // heads past G read head 0's row (all loads unconditional, in flight
-    // together) and are zeroed
-    const int h = lane >> 2, c = (lane & 3) * 2;
-    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + (h < G ? h : 0)) * kAttnDim;
-    float2 x0[8], x1[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      x0[k] = *reinterpret_cast<const float2*>(qr + k * 16 + c);
-      x1[k] = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
-    }
-    const float z = h < G ? 1.f : 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      split_bf16x2(x0[k].x * z, x0[k].y * z, qh[k][0], ql[k][0]);
-      split_bf16x2(x1[k].x * z, x1[k].y * z, qh[k][1], ql[k][1]);
-    }
-  }
-
+  // inside a chain (programmatic dependent launch) the next op may start its
+  // prologue now; the cached rows stream in before the wait on the previous
+  // op (the QKV product), which only q and the new key and value need
+  pdl_launch_dependents();
   const int pos = a.pos[b];
   if (pos < 0 || pos >= a.S) {  // no access outside the cache
     if (t == 0 && blockIdx.x == 0) atomicExch(a.err, kDerrBadPos);
@@ -333,7 +322,38 @@ __global__ void __launch_bounds__(kAttnThreads)
   for (int s = 0; s < kAttnStages; ++s)
     if (s < nt)
       stage_tile(a, row0, kvn, t0 + warp + s * kAttnWarps, pos, ring + s * kAttnStageBytes,
-                 &full[warp][s], lane, pol);
+                 &full[warp][s], lane, pol, false);
+  pdl_wait();
+#pragma unroll
+  for (int s = 0; s < kAttnStages; ++s) {
+    const int tile = t0 + warp + s * kAttnWarps;
+    if (s < nt && pos >= tile * kAttnTile && pos < (tile + 1) * kAttnTile) {
+      stage_new_row(a, row0, kvn, tile, pos, ring + s * kAttnStageBytes, lane);
+      __syncwarp();
+    }
+  }
+  // the queries as the MMA's B operand: lane holds head lane / 4, dimensions
+  // 16 k + 2 (lane % 4) + {0, 1} and + 8, as hi and lo bf16 terms
+  uint32_t qh[8][2], ql[8][2];
+  {
+    // heads past G read head 0's row (all loads unconditional, in flight
+    // together) and are zeroed
+    const int h = lane >> 2, c = (lane & 3) * 2;
+    const float* qr = a.q + ((size_t)b * a.nh + (size_t)g * G + (h < G ? h : 0)) * kAttnDim;
+    float2 x0[8], x1[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      x0[k] = *reinterpret_cast<const float2*>(qr + k * 16 + c);
+      x1[k] = *reinterpret_cast<const float2*>(qr + k * 16 + 8 + c);
+    }
+    const float z = h < G ? 1.f : 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      split_bf16x2(x0[k].x * z, x0[k].y * z, qh[k][0], ql[k][0]);
+      split_bf16x2(x1[k].x * z, x1[k].y * z, qh[k][1], ql[k][1]);
+    }
+  }
+
 
   // per lane: heads c, c + 1 of the accumulators (c = 2 (lane % 4)), dims
   // 16 mt + lane / 4 and + 8
@@ -418,7 +438,7 @@ __global__ void __launch_bounds__(kAttnThreads)
     __syncwarp();
     if (i + kAttnStages < nt)
       stage_tile(a, row0, kvn, tile + kAttnStages * kAttnWarps, pos, ring + s * kAttnStageBytes,
-                 &full[warp][s], lane, pol);
+                 &full[warp][s], lane, pol, true);
   }
   if (abort && lane == 0) {
     // no copy may land after the CTA exits: wait (bounded) for the stages
@@ -592,6 +612,12 @@ static int attention_splits(int B, int nkv, int s_max, cudaError_t* err) {
   return splits;
 }
 
+ws_status decode_attention(const float* q, const float* k_new, const float* v_new,
+                           void* k_cache, void* v_cache, const int32_t* pos, float* out_f32,
+                           void* out_bf16, int B, int n_heads, int n_kv_heads, int head_dim,
+                           int s_max, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream, bool pdl);
+
 }  // namespace ws
 
 using namespace ws;
@@ -611,6 +637,20 @@ ws_status ws_decode_attention(const float* q, const float* k_new, const float* v
                               void* out_bf16, int B, int n_heads, int n_kv_heads, int head_dim,
                               int s_max, void* workspace, size_t workspace_bytes,
                               ws_stream_t stream) {
+  return ws::decode_attention(q, k_new, v_new, k_cache, v_cache, pos, out_f32, out_bf16, B,
+                              n_heads, n_kv_heads, head_dim, s_max, workspace, workspace_bytes,
+                              (cudaStream_t)stream, false);
+}
+
+}  // extern "C"
+
+// The entry point's body; pdl: launched as a programmatic dependent of the
+// previous kernel on the stream (inside a chain).
+ws_status ws::decode_attention(const float* q, const float* k_new, const float* v_new,
+                               void* k_cache, void* v_cache, const int32_t* pos, float* out_f32,
+                               void* out_bf16, int B, int n_heads, int n_kv_heads, int head_dim,
+                               int s_max, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream, bool pdl) {
   if (!q || !k_new || !v_new || !k_cache || !v_cache || !pos || (!out_f32 && !out_bf16) ||
       !workspace) {
     set_error("null argument");
@@ -667,14 +707,21 @@ ws_status ws_decode_attention(const float* q, const float* k_new, const float* v
   a.timeout_ns = tuning().timeout_ns;
   // the tickets are zero on entry (a zero-filled workspace; the last arrival
   // at every ticket resets it, rows with a bad position take none)
-  const dim3 grid(splits, n_kv_heads, B);
-  k_decode_attention<<<grid, kAttnThreads, kAttnSmem, (cudaStream_t)stream>>>(a);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(splits, n_kv_heads, B);
+  cfg.blockDim = dim3(kAttnThreads);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, k_decode_attention, a);
   if (e != cudaSuccess) {
     set_error("launch failed: %s", cudaGetErrorString(e));
     return WS_ERR_CUDA;
   }
   return WS_OK;
 }
-
-}  // extern "C"

@@ -36,6 +36,16 @@
 
 using namespace ws;
 
+namespace ws {
+// decode attention on the stream (ws_attention.cu); pdl: as a programmatic
+// dependent of the previous kernel
+ws_status decode_attention(const float* q, const float* k_new, const float* v_new,
+                           void* k_cache, void* v_cache, const int32_t* pos, float* out_f32,
+                           void* out_bf16, int B, int n_heads, int n_kv_heads, int head_dim,
+                           int s_max, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream, bool pdl);
+}  // namespace ws
+
 namespace {
 
 enum OpKind { OP_QKV = 0, OP_WO = 1, OP_GATEUP = 2, OP_WD = 3, OP_HEAD = 4, OP_MLP = 5 };
@@ -477,9 +487,10 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
       // key-value append at pos, positions read on the device)
       const ws_chain::AttnCall& a = c->attn_calls[c->ops[i].attn_call];
       const ws_chain_opts& o = c->o;
-      const ws_status s = ws_decode_attention(
+      const ws_status s = ws::decode_attention(
           a.q, a.k, a.v, a.k_cache, a.v_cache, o.pos, nullptr, c->attn_buf, o.batch,
-          o.hidden / 128, o.kv_dim / 128, 128, o.s_max, c->attn_ws, c->attn_ws_bytes, stream);
+          o.hidden / 128, o.kv_dim / 128, 128, o.s_max, c->attn_ws, c->attn_ws_bytes, stream,
+          use_pdl);
       if (s != WS_OK) return s;
     }
     if (!trace.empty() && trace[i] >= 0) {
