@@ -894,14 +894,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)slot * sc.piece_bytes);
     // batch 1 in a chain form keeps the loop rolled: shorter code, and one
     // iteration per 16-byte chunk is far from the issue limit (measured: it
-    // is not at batch 4)
+    // is not at batch 4).  From batch 8 one iteration already holds 256-512
+    // independent fmas and its code overflows the instruction cache when
+    // unrolled (ncu at batch 16: "no instruction" the top stall)
     if constexpr (Q4) {
       dot_piece_q4<BT, NMAT, RT>(acc, reinterpret_cast<const uint8_t*>(st), q4_prefix(sc.PC),
                                  xs4 + j * ncp, xsum + j * (sc.PC >> 5), len, nchx, sc.KS >> 5,
                                  lane);
     } else {
-      dot_piece<BT, NMAT, RT, (F != F_ANY && BT == 1) ? 1 : 2>(acc, st, xs4 + j * ncp, len >> 3,
-                                                                ncp, nchx, lane);
+      dot_piece<BT, NMAT, RT, ((F != F_ANY && BT == 1) || BT >= 8) ? 1 : 2>(
+          acc, st, xs4 + j * ncp, len >> 3, ncp, nchx, lane);
     }
     // Every lane's shared-memory reads of this slot have returned (their
     // values fed the FMAs above, and issue is in order): refill the slot.
