@@ -60,6 +60,8 @@ def parse():
                          "4-bit group-128 weights, each GEMV shape and the decode step "
                          "beside bf16; step-attention: the decode step with decode "
                          "attention over a key-value cache in every block")
+    ap.add_argument("--q4-gemv", default=None,
+                    help="q4 mode: one 'M,K,B' GEMV only (no decode step)")
     ap.add_argument("--attn-config", default=None,
                     help="attention mode: one 'batch,slots' configuration instead of all nine")
     ap.add_argument("--chain-mode", choices=["graph", "persistent"], default="graph",
@@ -801,8 +803,13 @@ def run_q4(args):
     t.launch_pdl = 1
     wb.set_tuning(t)
     gemv = []
+    shapes = [(2048, 1536), (1536, 1536), (8960, 1536), (1536, 8960), (151936, 1536)]
+    batches = (1, 2, 4)
+    if args.q4_gemv:
+        M1, K1, B1 = (int(v) for v in args.q4_gemv.split(","))
+        shapes, batches = [(M1, K1)], (B1,)
     try:
-        for M, K in [(2048, 1536), (1536, 1536), (8960, 1536), (1536, 8960), (151936, 1536)]:
+        for M, K in shapes:
             rb = wb.q4_row_bytes(K)
             nbytes = M * rb
             ncopy = max(2, -(-(256 << 20) // nbytes))
@@ -813,7 +820,7 @@ def run_q4(args):
                 wb.quantize_q4(W, Wq)
                 Wqs.append(Wq)
             del W
-            for B in (1, 2, 4):
+            for B in batches:
                 x = torch.randn((B, K), device="cuda", generator=gen).to(torch.bfloat16)
                 y = torch.empty((B, M), device="cuda")
 
@@ -828,6 +835,9 @@ def run_q4(args):
             torch.cuda.empty_cache()
     finally:
         wb.set_tuning(base)
+    if args.q4_gemv:
+        print(json.dumps({"mode": "q4", "hbm_peak_gbs": hbm, "gemv": gemv}))
+        return 0
 
     sh, blocks, head, attn, h0 = make_host_inputs(4, args.seed)
     dblocks = [{k: to_dev(v, torch) for k, v in b.items()} for b in blocks]

@@ -224,3 +224,28 @@ def test_workspace_sizes(lib):
     assert wb.workspace_bytes(wb.OP_LMHEAD_ARGMAX, 151936, 1536, 1) > 0
     assert wb.workspace_bytes(wb.OP_ARGMAX_ROWS, 16, 151936, 1) > 0
     assert wb.workspace_bytes(wb.OP_GEMV, 1536, 8960, 16) > 0  # activations need a split
+
+
+def test_chain_create_rejects_bad_attention_and_weight_format(lib):
+    """Host-side checks of the chain options (nothing is allocated or
+    launched): attention needs heads of 128, s_max a multiple of 64 and
+    positions; 4-bit weights need batch <= 4 and no persistent mode."""
+    blk = wb.BlockDesc(kind=wb.BLOCK_QWEN)
+    blk.u.qwen = wb.QwenBlock(*([A] * 9), None, None, None, None, A, A)
+    blocks = (wb.BlockDesc * 1)(blk)
+    h = wb.P()
+
+    def create(**kw):
+        o = wb.ChainOpts(batch=1, hidden=768, kv_dim=256, inter=512, vocab=0, eps=1e-6,
+                         h_in=A, h_out=A + 4096)
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return lib.ws_chain_create(blocks, 1, wb.ctypes.byref(o), wb.ctypes.byref(h))
+    assert create(attention=1, s_max=256, pos=None) == -1          # no positions
+    assert create(attention=1, s_max=200, pos=A) == -1             # s_max not a multiple of 64
+    assert create(attention=1, s_max=256, pos=A, kv_dim=64) == -1  # key-value heads not 128
+    assert create(attention=1, s_max=256, pos=A, persistent=1) == -1
+    assert create(weight_format=2) == -1                           # unknown format
+    assert create(weight_format=1, batch=8) == -1                  # 4-bit: batch <= 4
+    assert create(weight_format=1, persistent=1) == -1
+    assert lib.ws_last_error()
