@@ -590,3 +590,37 @@ def test_q4_model_size_matches_the_pages():
     assert round(bf16 / 1e9, 2) == 3.09
     assert round(q4b / 1e9, 2) == 0.82
     assert round(bf16 / q4b, 2) == 3.76
+
+
+def test_qwen_block_attention_with_constant_values_reduces_to_wo_of_that_row():
+    """Every value row (cached and new) equal to one row c: attention returns
+    c whatever the scores, so the block equals h + bf16(c).Wo^T followed by
+    the MLP, as the stand-in block computes it with attn = c; the new key
+    lands at pos."""
+    rng = np.random.default_rng(31)
+    H, KV, I, B, S = 256, 128, 256, 2, 64
+    blk = {
+        "gamma1": oracle.f64_to_bf16(rng.uniform(0.5, 1.5, H)),
+        "gamma2": oracle.f64_to_bf16(rng.uniform(0.5, 1.5, H)),
+        "Wq": oracle.f64_to_bf16(rng.normal(0, 0.05, (H, H))),
+        "Wk": oracle.f64_to_bf16(rng.normal(0, 0.05, (KV, H))),
+        "Wv": np.zeros((KV, H), np.uint16),          # v = 0 for the new token
+        "Wo": oracle.f64_to_bf16(rng.normal(0, 0.05, (H, H))),
+        "Wg": oracle.f64_to_bf16(rng.normal(0, 0.05, (I, H))),
+        "Wu": oracle.f64_to_bf16(rng.normal(0, 0.05, (I, H))),
+        "Wd": oracle.f64_to_bf16(rng.normal(0, 0.05, (H, I))),
+    }
+    h = rng.normal(size=(B, H))
+    kc = oracle.f64_to_bf16(rng.normal(size=(B, 1, S, 128)))
+    vc = np.zeros((B, 1, S, 128), np.uint16)        # every cached value row is 0
+    pos = [10, 63]
+    out = oracle.qwen_block_attention(h, blk, kc, vc, pos, 1, 1e-6)
+    assert np.all(out["attn"] == 0)                 # attention of constant 0 rows
+    ref = oracle.qwen_block(h, blk, np.zeros((B, H)), 1e-6)
+    assert np.array_equal(out["h"], ref["h"])
+    a = oracle.round_bf16(oracle.rmsnorm(h, oracle.bf16_to_f64(blk["gamma1"]), 1e-6))
+    k_new = oracle.f64_to_bf16(oracle.gemv(blk["Wk"], a))
+    for b, p in enumerate(pos):
+        assert np.array_equal(out["k_cache"][b, 0, p], k_new[b])
+        assert np.array_equal(np.delete(out["k_cache"][b, 0], p, axis=0),
+                              np.delete(kc[b, 0], p, axis=0))
