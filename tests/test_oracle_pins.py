@@ -624,3 +624,28 @@ def test_qwen_block_attention_with_constant_values_reduces_to_wo_of_that_row():
         assert np.array_equal(out["k_cache"][b, 0, p], k_new[b])
         assert np.array_equal(np.delete(out["k_cache"][b, 0], p, axis=0),
                               np.delete(kc[b, 0], p, axis=0))
+
+
+def test_q4_block_with_all_codes_eight_is_the_bf16_block_of_the_zeros():
+    """Every code 8: each 4-bit weight equals its group's bf16 zero, so the
+    4-bit block equals the bf16 block whose matrices hold those zeros (the
+    steps and roundings of the two oracles must agree)."""
+    rng = np.random.default_rng(41)
+    H, KV, I, B = 256, 128, 384, 2
+    shapes = {"Wq": (H, H), "Wk": (KV, H), "Wv": (KV, H), "Wo": (H, H), "Wg": (I, H),
+              "Wu": (I, H), "Wd": (H, I)}
+    q4blk, bfblk = {"K": H, "KI": I}, {}
+    for n in ("gamma1", "gamma2"):
+        q4blk[n] = bfblk[n] = oracle.f64_to_bf16(rng.uniform(0.5, 1.5, H))
+    for n, (M, K) in shapes.items():
+        z = oracle.f64_to_bf16(rng.normal(0, 0.05, (M, K // 128)))
+        s = oracle.f64_to_bf16(rng.uniform(0.001, 0.01, (M, K // 128)))
+        q4blk[n] = oq4.pack(np.full((M, K), 8, np.uint8), s, z)
+        bfblk[n] = np.repeat(z, 128, axis=1)
+    h = rng.normal(size=(B, H))
+    attn = oracle.bf16_to_f64(oracle.f64_to_bf16(rng.normal(size=(B, H))))
+    a = oq4.qwen_block(h, q4blk, attn, 1e-6)
+    b = oracle.qwen_block(h, bfblk, attn, 1e-6)
+    for k in ("q", "k", "v", "h_mid", "h"):
+        assert np.allclose(a[k], b[k], rtol=1e-12, atol=1e-12), k
+    assert np.array_equal(a["s"], b["s"])
