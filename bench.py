@@ -159,6 +159,19 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- inputs
 
+def replicas_value(dt, steps, step_bytes, world, dist=None, device="cuda"):
+    """Whole-job throughput of N independent replicas: the timed region of
+    every rank reduced to the slowest (max over ranks), then all ranks' bytes
+    over it.  Returns (slowest seconds, seconds per step, GB/s)."""
+    if world > 1:
+        import torch
+        t = torch.tensor([dt], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    per_step = dt / max(steps, 1)
+    return dt, per_step, world * step_bytes / per_step / 1e9
+
+
 def make_host_inputs(B, seed):
     from weight_streaming_gemv_bf16_gb300 import synth
     sh = synth.QWEN2_5_1_5B
@@ -389,12 +402,7 @@ def run_ours(args):
     time.sleep(0.3)
     dt = timed(main, args.steps, args.warmup)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([dt], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
-    per_step = dt / max(args.steps, 1)
-    value = world * step_bytes / per_step / 1e9
+    dt, per_step, value = replicas_value(dt, args.steps, step_bytes, world, dist)
 
     # controls: no prefetch, and a decoy of the same traffic (when a plan was kept)
     variants = {}
