@@ -649,3 +649,78 @@ def test_q4_block_with_all_codes_eight_is_the_bf16_block_of_the_zeros():
     for k in ("q", "k", "v", "h_mid", "h"):
         assert np.allclose(a[k], b[k], rtol=1e-12, atol=1e-12), k
     assert np.array_equal(a["s"], b["s"])
+
+
+# ---- the LayerNorm -> Linear -> GELU block's backward ("It works in training too")
+
+from oracle import train as otr  # noqa: E402
+
+
+def _bf16_round(v):
+    return oracle.bf16_to_f64(oracle.f64_to_bf16(v))
+
+
+def test_gelu_grad_is_the_derivative_of_gelu():
+    t = np.linspace(-6, 6, 241)
+    h = 1e-5
+    fd = (oracle.gelu(t + h) - oracle.gelu(t - h)) / (2 * h)
+    assert np.max(np.abs(otr.gelu_grad(t) - fd)) < 1e-8
+    assert abs(otr.gelu_grad(np.array([0.0]))[0] - 0.5) < 1e-15
+
+
+def test_exact_block_backward_matches_finite_differences():
+    """L = sum(dz * z) of the exact block (no roundings): every gradient of
+    the exact backward against central differences of L."""
+    rng = np.random.default_rng(51)
+    B, w = 2, 8
+    x = rng.normal(size=(B, w))
+    gamma, beta, b = rng.uniform(0.5, 1.5, w), rng.normal(0, 0.1, w), rng.normal(0, 0.1, w)
+    W = rng.normal(0, 0.4, (w, w))
+    dz = rng.normal(size=(B, w))
+    g = otr.mlp_block_backward(x, gamma, beta, W, b, dz)
+
+    def loss(x_, gamma_, beta_, W_, b_):
+        return float((dz * otr.mlp_block_forward(x_, gamma_, beta_, W_, b_)["z"]).sum())
+    args = [x, gamma, beta, W, b]
+    names = ["dx", "dgamma", "dbeta", "dW", "db"]
+    h = 1e-6
+    for a, name in enumerate(names):
+        fd = np.zeros_like(args[a])
+        for idx in np.ndindex(args[a].shape):
+            p = [v.copy() for v in args]
+            m = [v.copy() for v in args]
+            p[a][idx] += h
+            m[a][idx] -= h
+            fd[idx] = (loss(*p) - loss(*m)) / (2 * h)
+        assert np.allclose(g[name], fd, rtol=1e-6, atol=1e-8), name
+
+
+def test_layernorm_gradient_sums_to_zero_per_row():
+    """LN(x + c) = LN(x): the exact input gradient has zero row sums."""
+    rng = np.random.default_rng(52)
+    x = rng.normal(size=(3, 16))
+    w = 16
+    g = otr.mlp_block_backward(x, rng.uniform(0.5, 1.5, w), rng.normal(0, 0.1, w),
+                               rng.normal(0, 0.3, (w, w)), rng.normal(0, 0.1, w),
+                               rng.normal(size=(3, w)))
+    assert np.max(np.abs(g["dx"].sum(axis=1))) < 1e-12
+
+
+def test_rounded_forward_is_the_bf16_block():
+    """The backward's saved forward with bf16 roundings is the forward block
+    of the C oracle bit for bit."""
+    rng = np.random.default_rng(53)
+    B, w = 4, 64
+    xb = oracle.f64_to_bf16(rng.normal(size=(B, w)))
+    blk = {"gamma": oracle.f64_to_bf16(rng.uniform(0.5, 1.5, w)),
+           "beta": oracle.f64_to_bf16(rng.normal(0, 0.1, w)),
+           "W": oracle.f64_to_bf16(rng.normal(0, 0.05, (w, w))),
+           "b": oracle.f64_to_bf16(rng.normal(0, 0.1, w))}
+    f = otr.mlp_block_forward(oracle.bf16_to_f64(xb), *(oracle.bf16_to_f64(blk[k])
+                              for k in ("gamma", "beta", "W", "b")), rounding=_bf16_round)
+    assert np.array_equal(oracle.f64_to_bf16(f["z"]), oracle.mlp_block(xb, blk))
+
+
+def test_backward_prefetch_order_fetches_the_previous_block():
+    assert otr.chain_prefetch_order(3, backward=False) == [(0, 1), (1, 2), (2, None)]
+    assert otr.chain_prefetch_order(3, backward=True) == [(2, 1), (1, 0), (0, None)]
