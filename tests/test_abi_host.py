@@ -249,3 +249,25 @@ def test_chain_create_rejects_bad_attention_and_weight_format(lib):
     assert create(weight_format=1, batch=8) == -1                  # 4-bit: batch <= 4
     assert create(weight_format=1, persistent=1) == -1
     assert lib.ws_last_error()
+
+
+def test_q4_plans_fit_every_k():
+    """Every K in 128..12288 (every tail length), batch 1-4, one matrix or a
+    pair: a 4-bit plan (CUDA-core kernel, or the tensor-core one where it
+    qualifies) fits shared memory, keeps two ring stages or more, cuts pieces
+    on super-groups, and CTA 0's copies stay inside the ring."""
+    for K in range(128, 12288 + 1, 128):
+        for B in (1, 2, 3, 4):
+            for nmat in (1, 2):
+                for mma, M in ((False, 3000), (True, 40000)):
+                    if B * K * 2 > 96 * 1024:
+                        continue  # activations of the full K must fit
+                    try:
+                        copies, sc = wb.debug_gemv_copies_q4(M, K, B, nmat, 0, mma)
+                    except wb.WsError:
+                        assert mma, (K, B, nmat)  # only the tensor-core plan may decline
+                        continue
+                    assert sc["smem_bytes"] <= 227 * 1024 and sc["NSW"] >= 2, (K, B, nmat, mma)
+                    assert sc["PC"] == K or sc["PC"] % 512 == 0, (K, sc["PC"])
+                    ring = 8 * sc["NSW"] * sc["piece_bytes"]
+                    assert all(dst + n <= ring for _, dst, n in copies), (K, B, nmat, mma)

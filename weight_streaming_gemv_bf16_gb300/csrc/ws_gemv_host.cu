@@ -468,9 +468,14 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   if (NSW < 2) {
     if (sc.off_ring + 2 * kWarps * sc.piece_bytes > kSmemMax) {
       // smaller pieces, so that two stages per warp fit beside the activations
-      const int pc_fit =
+      int pc_fit =
           q4 ? (kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * kQ4SuperBytes) * kQ4Super
              : ((kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * 2)) & ~7;
+      // each piece is rounded up to 128 bytes: shrink until that still fits
+      while (pc_fit >= pc_unit &&
+             sc.off_ring + 2 * kWarps * align_up(nmat * RT * piece_row_bytes(pc_fit), 128) >
+                 kSmemMax)
+        pc_fit -= pc_unit;
       if (pc_fit < pc_unit) {
         snprintf(why, why_len, "no two ring stages per warp fit beside %d bytes of activations",
                  sc.BT * sc.KS * 2);
@@ -485,6 +490,11 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   }
   sc.NSW = NSW;
   sc.smem_bytes = sc.off_ring + kWarps * NSW * sc.piece_bytes;
+  if (sc.smem_bytes > kSmemMax) {
+    snprintf(why, why_len, "no schedule fits shared memory (K=%d, B=%d, %d matrices)", K, p.B,
+             nmat);
+    return false;
+  }
   int Gs = grid_target / S;
   if (Gs < 1) Gs = 1;
   if (Gs > RG) Gs = RG;
