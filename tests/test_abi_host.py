@@ -271,3 +271,18 @@ def test_q4_plans_fit_every_k():
                     assert sc["PC"] == K or sc["PC"] % 512 == 0, (K, sc["PC"])
                     ring = 8 * sc["NSW"] * sc["piece_bytes"]
                     assert all(dst + n <= ring for _, dst, n in copies), (K, B, nmat, mma)
+
+
+def test_bf16_plans_fit_every_k():
+    """bf16 plans over K (every 8 up to 1024, every 64 up to 16384), batch
+    1-16, one matrix or a pair, with and without a K split: each that plans
+    fits shared memory and keeps two ring stages or more."""
+    for K in list(range(8, 1024, 8)) + list(range(1024, 16385, 64)):
+        for B in (1, 4, 8, 16):
+            for nmat in (1, 2):
+                for split in (False, True):
+                    try:
+                        sc = wb.gemv_plan(2000, K, B, nmat=nmat, allow_split=split)
+                    except wb.WsError:
+                        continue
+                    assert sc["smem_bytes"] <= 227 * 1024 and sc["NSW"] >= 2, (K, B, nmat, split)
