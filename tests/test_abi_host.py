@@ -94,6 +94,17 @@ def test_decode_attention_validation(lib, B, nh, nkv, d, S, kc, wsb, status):
     assert lib.ws_last_error()
 
 
+def test_decode_attention_alignment_checks(lib):
+    # q 8-byte aligned, k_new and v_new 16-byte aligned, checked before anything runs
+    args = dict(B=2, nh=12, nkv=2, d=128, S=256)
+    def call(q=A, kn=A, vn=A):
+        return lib.ws_decode_attention(q, kn, vn, A, A, A, A, None, args["B"], args["nh"],
+                                       args["nkv"], args["d"], args["S"], A, 1 << 20, None)
+    assert call(q=A + 4) == -2
+    assert call(kn=A + 8) == -2
+    assert call(vn=A + 8) == -2
+
+
 def test_decode_attention_workspace(lib):
     def expect(B, nh, nkv, S):
         # tickets per group of 16 splits, per (row, head); G x 130 floats per
