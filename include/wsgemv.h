@@ -91,6 +91,9 @@ ws_status ws_gemv_bf16(const void *W, const void *x, float *y, int M, int K, int
  *    WS_ERR_SHAPE and a message; use ws_gemv_bf16 with a workspace for those.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *    The address is kept for the life of the process: a device reset
+ *    (cudaDeviceReset) while the library is loaded is not supported, since
+ *    the array may come back at another address.
  *  - Each call clears the tickets on `stream` before its kernel.  All calls
  *    share the one array, which keeps the last call's contents: calls that
  *    overlap on the GPU (different streams, no ordering) race on it.
@@ -450,7 +453,24 @@ typedef struct {
                           launch runs on CUDA cores, the vector-product
                           design.  Sums are ordered differently; both stay
                           within the fp32 tolerance of the oracle.           */
+  int la_mask;         /* decode chains: ops that ask L2 (bulk prefetch) for
+                          the weights a later op of the same block fills its
+                          rings with first, CTA by CTA; WS_LA_* bits.  Only
+                          reads: outputs stay bit-identical.  Default 0.     */
+  int la_when;         /* 0: issued after the op's dependency wait (default),
+                          1: before it                                       */
+  int la_depth;        /* ring fills of the later op asked for (1..8)        */
 } ws_tuning;
+
+/* ws_tuning.la_mask bits: source op -> the later op whose first weights it
+ * asks L2 for (one target per source; the lower bit wins). */
+enum {
+  WS_LA_QKV_GATEUP = 1,  /* QKV -> gate/up of its block  */
+  WS_LA_WO_GATEUP = 2,   /* Wo -> gate/up                */
+  WS_LA_QKV_WD = 4,      /* QKV -> Wd                    */
+  WS_LA_WO_WD = 8,       /* Wo -> Wd                     */
+  WS_LA_GATEUP_WD = 16   /* gate/up -> Wd                */
+};
 
 void ws_get_tuning(ws_tuning *t);
 ws_status ws_set_tuning(const ws_tuning *t);

@@ -147,6 +147,33 @@ def test_graph_eager_and_pdl_are_bit_identical():
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("B,shape", [(1, SMALL), (4, SMALL), (16, SMALL), (2, SMALL_SPLIT),
+                                     (16, SMALL_SPLIT), (5, MID)])
+def test_untraced_pdl_graph_matches_traced_build(B, shape):
+    """The chain without trace copies (programmatic-dependent-launch edges at
+    every op boundary, as timed) against the traced build of the same weights
+    (whose blocks the oracle checks): final h, logits and argmax bit for bit,
+    replay after replay, and the argmax against the oracle end to end."""
+    blocks, head = _host_weights(shape, 27)
+    attn = np.stack([synth.qwen_attn(shape, B, 27, l) for l in range(shape.layers)])
+    h0 = synth.qwen_hidden(shape, B, 27)
+    db, dh, da, dx = [_dev(b) for b in blocks], _dev(head), dev_bf16(attn), dev_f32(h0)
+    traced = wc.qwen_chain(db, dh, da, dx, trace=True, logits=True)
+    traced.chain.capture()
+    traced.run()
+    timed = wc.qwen_chain(db, dh, da, dx, use_pdl=True, logits=True)
+    timed.chain.capture()
+    for _ in range(3):
+        timed.h_out.fill_(float("nan"))
+        timed.run()
+        torch.cuda.synchronize()
+        assert torch.equal(timed.h_out.cpu(), traced.h_out.cpu())
+        assert torch.equal(timed.logits.cpu(), traced.logits.cpu())
+        assert torch.equal(timed.idx.cpu(), traced.idx.cpu())
+    _oracle_end_to_end(timed.h_out.cpu().numpy(), timed.idx.cpu().numpy(),
+                       timed.logits.cpu().numpy(), blocks, head, attn, h0, 1e-6)
+
+
 def _set_tuning(**kw):
     base = wb.get_tuning()
     t = wb.Tuning()
@@ -226,8 +253,12 @@ def test_step_host_matches_device_run():
     h_host = torch.from_numpy(h0).pin_memory()
     attn_host = torch.from_numpy(attn.view(np.int16)).pin_memory()
     out = torch.full((B,), -1, dtype=torch.int32).pin_memory()
+    ch.h_out.fill_(float("nan"))
     ch.chain.step_host(h_host, attn_host, out)
     assert np.array_equal(out.numpy(), ref_idx)
+    # the host-staged step against the oracle: argmax where the margin allows,
+    # the final h it left on the device within the end-to-end drift bound
+    _oracle_end_to_end(ch.h_out.cpu().numpy(), out.numpy(), None, blocks, head, attn, h0, 1e-6)
     # new inputs through the host path change the answer the same way a device run does
     h2 = (h0[::-1].copy())
     ch.chain.step_host(torch.from_numpy(h2).pin_memory(), attn_host, out)
@@ -297,12 +328,29 @@ def test_mid_chain_tensor_cores_match_oracle(B):
     _check_chain(ch, blocks, head, attn, h0)
 
 
+@pytest.fixture(scope="module")
+def full_chain():
+    """The full-size chain's seeded inputs (Qwen2.5-1.5B shapes, batch 1, seed
+    0: the weights the benchmark times), on the host and on the device."""
+    sh = synth.QWEN2_5_1_5B
+    blocks, head = _host_weights(sh, 0)
+    attn = np.stack([synth.qwen_attn(sh, 1, 0, l) for l in range(sh.layers)])
+    h0 = synth.qwen_hidden(sh, 1, 0)
+    dev = ([_dev(b) for b in blocks], _dev(head), dev_bf16(attn), dev_f32(h0))
+    return sh, blocks, head, attn, h0, dev
+
+
+def _chain_on(full, **kw):
+    sh, blocks, head, attn, h0, (dblocks, dhead, dattn, dh0) = full
+    return wc.qwen_chain(dblocks, dhead, dattn, dh0, eps=sh.eps, **kw)
+
+
 @pytest.mark.parametrize("persistent", [False, True])
-def test_full_chain_28_blocks_matches_oracle(persistent):
+def test_full_chain_28_blocks_matches_oracle(full_chain, persistent):
     """The full 28-block chain + final RMSNorm + LM head 151936 x 1536 + argmax,
     batch 1, one CUDA graph: per-block teacher forcing and the end-to-end argmax."""
-    ch, blocks, head, attn, h0 = _make(synth.QWEN2_5_1_5B, 1, 0, trace=True, logits=True,
-                                       persistent=persistent)
+    sh, blocks, head, attn, h0, _ = full_chain
+    ch = _chain_on(full_chain, trace=True, logits=True, persistent=persistent)
     assert ch.chain.persistent == persistent
     ch.chain.capture()
     ch.run()
@@ -311,6 +359,95 @@ def test_full_chain_28_blocks_matches_oracle(persistent):
     assert wb.device_error() == 0
     eligible = _check_chain(ch, blocks, head, attn, h0)
     assert eligible == 1
+
+
+def _oracle_end_to_end(h_gpu, idx_gpu, logits_gpu, blocks, head, attn, h0, eps):
+    """The oracle's whole step from h0 against a GPU step's final h, argmax
+    and (when given) logits: the logits of the oracle's LM head on the GPU's
+    own final h within the fp32 bound, the argmax where the oracle's top-2
+    margin exceeds the tolerance, and the final h within the end-to-end drift
+    bound (bf16 rounding points compound over the blocks)."""
+    full = oracle.qwen_chain(h0, blocks, [bf16_bits_to_f64(a) for a in attn], head["gamma_f"],
+                             head["Wlm"], eps, threads=8)
+    ok = _margin_ok(full["logits"])
+    assert np.array_equal(idx_gpu[ok], full["idx"][ok])
+    drift = rel_err_rows(h_gpu, full["h"])
+    assert drift < 0.05, f"final h drift {drift:.3g}"
+    own = oracle.lmhead_logits(np.asarray(h_gpu, np.float64), oracle.bf16_to_f64(head["gamma_f"]),
+                               head["Wlm"], eps, threads=8)
+    ok_own = _margin_ok(own)
+    assert np.array_equal(idx_gpu[ok_own], oracle.argmax_rows(own)[ok_own])
+    if logits_gpu is not None:
+        e = assert_fp32(logits_gpu, own, what="logits of the timed graph")
+        print(f"timed graph: logits max rel err {e:.3g}, final-h drift {drift:.3g}")
+    return int(ok.sum())
+
+
+@pytest.mark.parametrize("prefetch", ["tuned", "off"])
+def test_timed_graph_matches_traced_build_and_oracle(full_chain, prefetch):
+    """The graph the benchmark times -- no trace copies, so every op boundary
+    (Wd -> next block's QKV and the last Wd -> LM head included) carries a
+    programmatic-dependent-launch edge, and prefetch plans tuned or none --
+    replayed several times.  Every replay's final h and argmax equal the
+    traced build's bit for bit (the traced build's blocks are checked against
+    the oracle one by one), and the step agrees with the oracle end to end.
+    The same graph with the logits written gives the logits for the fp32
+    check ("One Token, Kernel by Kernel", "The whole step")."""
+    sh, blocks, head, attn, h0, _ = full_chain
+    pf = 1 if prefetch == "tuned" else 0
+    timed = _chain_on(full_chain, use_pdl=True, prefetch=pf, tune_pairs=30, min_gain=0.01)
+    timed.chain.tune()
+    timed.chain.capture()
+    withlog = _chain_on(full_chain, use_pdl=True, prefetch=pf, logits=True, tune_pairs=30,
+                        min_gain=0.01)
+    withlog.chain.tune()
+    withlog.chain.capture()
+    traced = _chain_on(full_chain, trace=True, logits=True)
+    traced.chain.capture()
+    traced.run()
+    torch.cuda.synchronize()
+    ref_h, ref_idx = traced.h_out.cpu(), traced.idx.cpu()
+    assert torch.equal(ref_h, traced.h_trace[-1].cpu())
+    for rep in range(4):
+        timed.h_out.fill_(float("nan"))
+        timed.idx.fill_(-1)
+        timed.run()
+        withlog.run()
+        torch.cuda.synchronize()
+        assert torch.equal(timed.h_out.cpu(), ref_h), f"replay {rep}: final h differs"
+        assert torch.equal(timed.idx.cpu(), ref_idx), f"replay {rep}: argmax differs"
+        assert torch.equal(withlog.h_out.cpu(), ref_h)
+        assert torch.equal(withlog.logits.cpu(), traced.logits.cpu())
+    assert wb.device_error() == 0
+    eligible = _oracle_end_to_end(timed.h_out.cpu().numpy(), timed.idx.cpu().numpy(),
+                                  withlog.logits.cpu().numpy(), blocks, head, attn, h0, sh.eps)
+    assert eligible == 1
+
+
+def test_host_step_full_chain_matches_oracle(full_chain):
+    """ws_chain_step_host on the benchmark's chain: h and the 28 attention
+    inputs from pinned host buffers, the argmax back to a host buffer, all in
+    one graph launch.  The host result equals the oracle's argmax, and the
+    device-side final h it left behind agrees with the oracle end to end and
+    with the device-input run bit for bit."""
+    sh, blocks, head, attn, h0, _ = full_chain
+    ch = _chain_on(full_chain, use_pdl=True, prefetch=1, tune_pairs=30, min_gain=0.01)
+    ch.chain.tune()
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    dev_h, dev_idx = ch.h_out.cpu(), ch.idx.cpu()
+    h_host = torch.from_numpy(h0).pin_memory()
+    a_host = torch.from_numpy(np.ascontiguousarray(attn).view(np.int16)).pin_memory()
+    out = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    for _ in range(3):
+        ch.h_out.fill_(float("nan"))
+        out.fill_(-1)
+        ch.chain.step_host(h_host, a_host, out)
+        assert torch.equal(out, dev_idx)
+        assert torch.equal(ch.h_out.cpu(), dev_h)
+    assert wb.device_error() == 0
+    _oracle_end_to_end(ch.h_out.cpu().numpy(), out.numpy(), None, blocks, head, attn, h0, sh.eps)
 
 
 @pytest.mark.parametrize("B", [4, 16])

@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include <cstdint>
 #include <cstring>
 
@@ -586,23 +588,38 @@ static AttnLayout attention_workspace(int B, int nh, int nkv, int s_max) {
 
 // Splits per (row, head): one wave of resident CTAs over all rows and heads,
 // at most one split per four tiles.
+// The kernel attribute and the occupancy are set up once per device (the
+// attribute is per device), under a lock.
 static int attention_splits(int B, int nkv, int s_max, cudaError_t* err) {
-  static int ctas_per_sm = 0, nsm = 0;
-  if (!ctas_per_sm) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_decode_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kAttnSmem);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm, k_decode_attention,
-                                                        kAttnThreads, kAttnSmem);
-    if (e != cudaSuccess || ctas_per_sm < 1) {
-      *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-      ctas_per_sm = 0;
-      return 0;
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static int per_sm[kMaxDev] = {0}, sms[kMaxDev] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return 0;
+  }
+  int ctas_per_sm = 0, nsm = 0;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!per_sm[dev]) {
+      e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_decode_attention, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kAttnSmem);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas_per_sm, k_decode_attention,
+                                                          kAttnThreads, kAttnSmem);
+      if (e != cudaSuccess || ctas_per_sm < 1) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        return 0;
+      }
+      per_sm[dev] = ctas_per_sm;
+      sms[dev] = nsm;
     }
+    ctas_per_sm = per_sm[dev];
+    nsm = sms[dev];
   }
   const int maxs = s_max / (kAttnTile * kAttnWarps);
   const int fill = ctas_per_sm * nsm / (B * nkv);

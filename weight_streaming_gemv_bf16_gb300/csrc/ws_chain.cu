@@ -388,6 +388,38 @@ static ws_status build_ops(ws_chain* c) {
     op.plan = kNoPlan;
     op.gain_lo = op.gain_mean = 0.f;
   }
+  // L2 look-ahead (ws_tuning.la_mask): an op of a decoder block asks L2 for
+  // the weights a later op of the same block fills its rings with first
+  const int lam = tuning().la_mask;
+  if (lam && !c->persistent && o.weight_format == WS_WEIGHTS_BF16) {
+    const int n = (int)c->ops.size();
+    for (int i = 0; i < n; ++i) {
+      const int kind = c->ops[i].kind;
+      int t = -1;
+      if (kind == OP_QKV)
+        t = (lam & WS_LA_QKV_GATEUP) ? i + 2 : (lam & WS_LA_QKV_WD) ? i + 3 : -1;
+      else if (kind == OP_WO)
+        t = (lam & WS_LA_WO_GATEUP) ? i + 1 : (lam & WS_LA_WO_WD) ? i + 2 : -1;
+      else if (kind == OP_GATEUP)
+        t = (lam & WS_LA_GATEUP_WD) ? i + 1 : -1;
+      if (t < 0 || t >= n || c->ops[t].block != c->ops[i].block) continue;
+      const GemvParams& tp = c->ops[t].p;
+      if (tp.nseg != 1 || tp.sc.S != 1 || tp.sc.mma) continue;
+      GemvParams& p = c->ops[i].p;
+      const int d = tuning().la_depth;
+      const int pieces = d * tp.sc.NSW;  // pieces per warp asked for
+      p.la_W0 = tp.seg[0].W0;
+      p.la_W1 = tp.nmat == 2 ? tp.seg[0].W1 : nullptr;
+      p.la_K = tp.K;
+      p.la_M = tp.seg[0].M;
+      p.la_RT = tp.sc.RT;
+      p.la_RG = tp.sc.RG;
+      p.la_Gs = tp.sc.Gs;
+      p.la_groups = kWarps * ((pieces + tp.sc.NP - 1) / tp.sc.NP);
+      p.la_cols = pieces >= tp.sc.NP ? tp.K : pieces * tp.sc.PC;
+      p.la_when = tuning().la_when;
+    }
+  }
   c->ws_total = total;
   if (total) {
     if (cudaMalloc(&c->ws, total) != cudaSuccess) return WS_ERR_NOMEM;

@@ -124,6 +124,13 @@ struct alignas(16) GemvParams {
   unsigned long long timeout_ns;
   int evict_first;
   float* trace_out;  // persistent chain: copy seg[0].out ([B][M] fp32) here after the op
+  // L2 look-ahead inside a chain: CTA g asks L2 for the first la_groups row
+  // groups (la_RT rows each, la_cols columns from column 0) of the row range
+  // CTA g of a later op (la_RG row groups over la_Gs CTAs) streams first, in
+  // one or two matrices [la_M][la_K].  la_W0 null: none.
+  const uint16_t* la_W0;
+  const uint16_t* la_W1;
+  int la_K, la_M, la_RT, la_RG, la_Gs, la_groups, la_cols, la_when;
   // optional diagnostics of a launch inside a chain: globaltimer ns per CTA at
   // stamps[cta * stamp_stride + i], i = 0 entry, 1 dependency released,
   // 2 activations staged, 3 end
@@ -283,6 +290,9 @@ struct Tuning {
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
   int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
   int mma;           // 1: large chain-form ops at batch tiles 8 and 16 run on tensor cores (mma.sync)
+  int la_mask;       // chain ops that ask L2 for a later op's first weights (WS_LA_* bits)
+  int la_when;       // 0: after the op's dependency wait, 1: before it
+  int la_depth;      // ring fills of the later op to look ahead (>= 1)
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

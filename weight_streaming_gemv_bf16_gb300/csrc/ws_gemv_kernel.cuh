@@ -749,6 +749,26 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
   }
 }
 
+// L2 look-ahead: ask L2 (bulk prefetches, one per weight row) for the rows
+// that CTA blockIdx.x of a later op of the chain streams first, so that HBM
+// keeps streaming while this op waits on its inputs and computes.  Reads
+// nothing back and writes nothing.
+static __device__ __noinline__ void l2_lookahead(const GemvParams& p, int lane) {
+  const unsigned g = blockIdx.x;
+  if ((int)g >= p.la_Gs) return;
+  const int rg0 = (int)(g * (unsigned)p.la_RG / (unsigned)p.la_Gs);
+  const int rg1 = (int)((g + 1) * (unsigned)p.la_RG / (unsigned)p.la_Gs);
+  const int rows = min(p.la_groups, rg1 - rg0) * p.la_RT;
+  const int r0 = rg0 * p.la_RT;
+  const int n = (p.la_W1 ? 2 : 1) * rows;
+  const uint32_t bytes = (uint32_t)p.la_cols * 2u;
+  for (int i = lane; i < n; i += 32) {
+    const bool second = i >= rows;
+    const int r = r0 + (second ? i - rows : i);
+    if (r < p.la_M) bulk_prefetch_l2((second ? p.la_W1 : p.la_W0) + (size_t)r * p.la_K, bytes);
+  }
+}
+
 template <int BT, int NMAT, int RT, int F, bool Q4 = false>
 __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_constant__ GemvParams p) {
   using FT = FormTraits<F>;
@@ -801,8 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   uint4 bpre[FT::ln1 ? NR : 1];
   if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
   if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
+  if (p.la_W0 && p.la_when == 1 && warp == kWarps - 1) l2_lookahead(p, lane);
   pdl_launch_dependents();
   pdl_wait();
+  if (p.la_W0 && p.la_when == 0 && warp == kWarps - 1) l2_lookahead(p, lane);
   if (stamp && tid == 0) stamp[1] = global_ns();
 
   // the residual input of this CTA's rows, read while the activations stage

@@ -15,7 +15,9 @@
 // code may not use the array's name as a device pointer (on the host it names
 // a stand-in object); its device address is looked up once per device with
 // cudaGetSymbolAddress, on the first call made with that device current, and
-// passed to the kernel.
+// passed to the kernel.  The looked-up address is kept until the process
+// exits; a cudaDeviceReset while the library is loaded is not supported (the
+// module, and with it the array, may be reloaded at another address).
 #include <cuda_runtime.h>
 
 #include <cstdint>
