@@ -344,6 +344,19 @@ typedef struct {
   int attention;
   int s_max;
   const int32_t *pos;
+  /* MLP chains, training forward (one launch per block, not persistent;
+   * with h_trace set every block's output is written straight into its
+   * trace slot): what each module keeps for the backward, per block, any of
+   * them NULL to skip it.  mlp_ln: the Linear's input ln = bf16(LayerNorm(x)),
+   * bf16 [L][B][w]; mlp_pre: the GELU's input t = bf16(ln.W^T + bias), bf16
+   * [L][B][w]; mlp_gelu_grad: the GELU's derivative at t, Phi(t) + t phi(t),
+   * fp32 [L][B][w]; mlp_ln_stats: the LayerNorm's mean and rstd of every
+   * batch row of x, fp32 [L][B][2].  ws_mlp_backward_create reads mlp_ln,
+   * mlp_gelu_grad and mlp_ln_stats (mlp_pre is for checks). */
+  void *mlp_ln;
+  void *mlp_pre;
+  float *mlp_gelu_grad;
+  float *mlp_ln_stats;
 } ws_chain_opts;
 
 typedef struct ws_chain ws_chain;
@@ -401,6 +414,77 @@ ws_status ws_chain_op_bytes(const ws_chain *c, size_t *bytes, int n);
 void ws_chain_destroy(ws_chain *c);
 
 /* ------------------------------------------------------------------------
+ * Training: the backward pass of a chain of LayerNorm -> Linear(+bias) ->
+ * GELU blocks ("Making small PyTorch ops faster on a laptop GPU", "It works
+ * in training too": the gradient of block i reads W_i again, so while it runs
+ * the prefetch fetches W_(i-1), and the gradients are bit-identical with and
+ * without it).  Module by module in bf16, like the forward block: with t the
+ * GELU's input, ln the Linear's input, xh = (x - mean) rstd,
+ *   dlin = bf16(dz * gelu'(t)); dln = bf16(dlin . W); dW = bf16(dlin^T . ln);
+ *   db = bf16(sum_b dlin); g = dln * gamma;
+ *   dx = bf16(rstd (g - mean_k g - xh mean_k(g xh)));
+ *   dgamma = bf16(sum_b dln xh); dbeta = bf16(sum_b dln),
+ * and dx of block i is dz of block i - 1.  Sums in fp32 in a fixed order.
+ * One launch per block (plus one for block 0's LayerNorm), replayed as one
+ * CUDA graph with programmatic-dependent-launch edges; each launch streams
+ * its weight with 2-D TMA in 8-column slabs, one slab per CTA.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  void *dW, *db, *dgamma, *dbeta; /* bf16 [w][w], [w], [w], [w]: written */
+} ws_mlp_grads;
+
+typedef struct {
+  int batch;                /* B, 1..16                                      */
+  int width;                /* w, a multiple of 64, 64..1024                 */
+  /* the training forward's tensors (ws_chain_opts.mlp_* and h_trace):       */
+  const void *x_in;         /* bf16 [B][w]: block 0's input                   */
+  const void *acts;         /* bf16 [L][B][w]: every block's output          */
+  const void *ln;           /* bf16 [L][B][w]: every block's Linear input    */
+  const float *gelu_grad;   /* fp32 [L][B][w]: gelu' at every GELU input     */
+  const float *ln_stats;    /* fp32 [L][B][2]: LayerNorm mean and rstd       */
+  /* the gradient of the loss with respect to the last block's output, bf16
+   * [B][w]; NULL: the mean-square loss of the chain output z,
+   * mean(z^2) over B x w, whose gradient bf16(2 z / (B w)) is formed in fp32
+   * by the first launch */
+  const void *dz;
+  void *dx;                 /* bf16 [B][w]: gradient of the chain input      */
+  /* optional traces (NULL: not written): dx_trace bf16 [L+1][B][w], slot i
+   * the gradient of block i's input (slot 0 = dx), slot L the loss gradient;
+   * dlin_trace and dln_trace bf16 [L][B][w], block by block */
+  void *dx_trace, *dlin_trace, *dln_trace;
+  int use_pdl;              /* 1: programmatic dependent launch between launches */
+  int prefetch;             /* 0 off, 1 measured plan (ws_mlp_backward_tune), 2 fixed_plan */
+  ws_prefetch_plan fixed_plan;
+  int distance;             /* prefetch the weight of launch s + distance (>= 1)  */
+  int decoy;                /* 1: aim every prefetch at the wrong block (control) */
+  int tune_pairs;           /* paired replays per candidate plan (>= 8)           */
+  float tune_min_gain;      /* keep a plan only if its 95% CI lower bound exceeds */
+} ws_mlp_backward_opts;
+
+typedef struct ws_mlp_backward ws_mlp_backward;
+
+/* blocks[i] / grads[i]: block i's parameters and its gradients (all 16-byte
+ * aligned device pointers, owned by the caller, as are every tensor of
+ * opts); the handle owns two dln scratch rows (when dln_trace is NULL), its
+ * streams and its graph. */
+ws_status ws_mlp_backward_create(const ws_mlp_block *blocks, const ws_mlp_grads *grads, int n,
+                                 const ws_mlp_backward_opts *opts, ws_mlp_backward **out);
+/* prefetch == 1: time the whole backward graph with each candidate plan
+ * (every launch prefetching the weight of launch s + distance) against none
+ * in interleaved pairs, and keep the best plan only if the 95% confidence
+ * interval of its relative gain clears tune_min_gain ("Measuring instead of
+ * predicting").  Runs the backward (it only rewrites the same gradients). */
+ws_status ws_mlp_backward_tune(ws_mlp_backward *c, ws_stream_t stream);
+ws_status ws_mlp_backward_capture(ws_mlp_backward *c, ws_stream_t stream);
+/* One backward pass: one cudaGraphLaunch on `stream`. */
+ws_status ws_mlp_backward_run(ws_mlp_backward *c, ws_stream_t stream);
+/* The plan in use and its measured gain (95% CI lower bound, mean). */
+ws_status ws_mlp_backward_plan(const ws_mlp_backward *c, ws_prefetch_plan *plan, float *gain_lo,
+                               float *gain_mean);
+int ws_mlp_backward_num_launches(const ws_mlp_backward *c);
+void ws_mlp_backward_destroy(ws_mlp_backward *c);
+
+/* ------------------------------------------------------------------------
  * Sizing, errors, tuning knobs and measurement kernels.
  * ---------------------------------------------------------------------- */
 enum {
@@ -453,24 +537,11 @@ typedef struct {
                           launch runs on CUDA cores, the vector-product
                           design.  Sums are ordered differently; both stay
                           within the fp32 tolerance of the oracle.           */
-  int la_mask;         /* decode chains: ops that ask L2 (bulk prefetch) for
-                          the weights a later op of the same block fills its
-                          rings with first, CTA by CTA; WS_LA_* bits.  Only
-                          reads: outputs stay bit-identical.  Default 0.     */
-  int la_when;         /* 0: issued after the op's dependency wait (default),
-                          1: before it                                       */
-  int la_depth;        /* ring fills of the later op asked for (1..8)        */
+  int late_trigger;    /* chain ops: bit k set (k = 0 QKV, 1 Wo, 2 gate/up,
+                          3 Wd, 4 LM head, 5 LayerNorm block) lets the next
+                          launch start only once the op has staged its
+                          activations, instead of at its start.  Default 0. */
 } ws_tuning;
-
-/* ws_tuning.la_mask bits: source op -> the later op whose first weights it
- * asks L2 for (one target per source; the lower bit wins). */
-enum {
-  WS_LA_QKV_GATEUP = 1,  /* QKV -> gate/up of its block  */
-  WS_LA_WO_GATEUP = 2,   /* Wo -> gate/up                */
-  WS_LA_QKV_WD = 4,      /* QKV -> Wd                    */
-  WS_LA_WO_WD = 8,       /* Wo -> Wd                     */
-  WS_LA_GATEUP_WD = 16   /* gate/up -> Wd                */
-};
 
 void ws_get_tuning(ws_tuning *t);
 ws_status ws_set_tuning(const ws_tuning *t);

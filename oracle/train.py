@@ -62,18 +62,32 @@ def mlp_block_forward(x, gamma, beta, W, b, eps: float = 1e-5, rounding=None):
     return {"ln": ln, "lin": lin, "z": r(_gelu(lin))}
 
 
-def mlp_block_backward(x, gamma, beta, W, b, dz, eps: float = 1e-5, rounding=None) -> dict:
+def mlp_block_backward(x, gamma, beta, W, b, dz, eps: float = 1e-5, rounding=None,
+                       forced=None) -> dict:
     """Gradients of the block (see the module docstring) on double arrays:
     x [B][w], gamma, beta, b [w], W [w_out][w_in], dz [B][w_out].  With
     rounding=None every step is exact (the derivative of the exact block);
     with a rounding callable (bf16) each saved activation and each gradient
-    is rounded where the module-by-module reading puts it."""
+    is rounded where the module-by-module reading puts it.
+
+    forced: optional dict of module inputs taken as given instead of
+    computed -- "ln" (the Linear's input), "lin" (the GELU's input), "dlin"
+    (the Linear's output gradient), "dln" (the LayerNorm's output gradient).
+    Each module's outputs then follow from its actual inputs, so a rounded
+    intermediate that a GPU took to the other bf16 neighbour is checked
+    where it was formed, not in everything after it."""
     r = rounding if rounding is not None else (lambda v: v)
+    fz = forced or {}
     x = np.asarray(x, np.float64)
     f = mlp_block_forward(x, gamma, beta, W, b, eps, rounding)
-    ln, lin = f["ln"], f["lin"]
+    ln = np.asarray(fz["ln"], np.float64) if "ln" in fz else f["ln"]
+    lin = np.asarray(fz["lin"], np.float64) if "lin" in fz else f["lin"]
     dlin = r(np.asarray(dz, np.float64) * gelu_grad(lin))
+    if "dlin" in fz:
+        dlin = np.asarray(fz["dlin"], np.float64)
     dln = r(dlin @ W)
+    if "dln" in fz:
+        dln = np.asarray(fz["dln"], np.float64)
     dW = r(dlin.T @ ln)
     db = r(dlin.sum(axis=0))
     _, rstd, xh = _layernorm_parts(x, eps)
@@ -82,6 +96,34 @@ def mlp_block_backward(x, gamma, beta, W, b, dz, eps: float = 1e-5, rounding=Non
                    - xh * (g * xh).mean(axis=1, keepdims=True)))
     return {"dx": dx, "dW": dW, "db": db, "dgamma": r((dln * xh).sum(axis=0)),
             "dbeta": r(dln.sum(axis=0)), "dlin": dlin, "dln": dln, "z": f["z"]}
+
+
+def mean_square_loss_grad(z) -> np.ndarray:
+    """d/dz of mean(z^2) over all elements: 2 z / N."""
+    z = np.asarray(z, np.float64)
+    return 2.0 * z / z.size
+
+
+def mlp_chain_backward(x, blocks, eps: float = 1e-5, dz=None, rounding=None) -> dict:
+    """Forward then backward through a chain of blocks (dicts of double
+    arrays gamma, beta, W, b): block i's input gradient is block i-1's output
+    gradient.  dz: the loss gradient of the last output, or None for the
+    mean-square loss (rounded like every other gradient).  Returns per block
+    the gradients of mlp_block_backward and the chain input's dx."""
+    r = rounding if rounding is not None else (lambda v: v)
+    xs = [np.asarray(x, np.float64)]
+    for blk in blocks:
+        xs.append(mlp_block_forward(xs[-1], blk["gamma"], blk["beta"], blk["W"], blk["b"], eps,
+                                    rounding)["z"])
+    g = r(mean_square_loss_grad(xs[-1])) if dz is None else np.asarray(dz, np.float64)
+    loss_grad = g
+    grads = [None] * len(blocks)
+    for i in range(len(blocks) - 1, -1, -1):
+        blk = blocks[i]
+        grads[i] = mlp_block_backward(xs[i], blk["gamma"], blk["beta"], blk["W"], blk["b"], g,
+                                      eps, rounding)
+        g = grads[i]["dx"]
+    return {"grads": grads, "dx": g, "outputs": xs[1:], "loss_grad": loss_grad}
 
 
 def chain_prefetch_order(n_blocks: int, backward: bool) -> list:

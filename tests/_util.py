@@ -14,7 +14,8 @@ ULP_SEEN: dict = {}
 
 
 def note_ulps(what: str, max_ulp: int, frac_1ulp: float):
-    key = what.split(" block ")[0] if " block " in what else what
+    import re
+    key = re.sub(r"\s*block \d+\s*", " ", what).strip()
     old = ULP_SEEN.get(key)
     if old is None or max_ulp > old[0] or frac_1ulp < old[1]:
         ULP_SEEN[key] = (max(max_ulp, old[0] if old else 0), min(frac_1ulp, old[1] if old else 1.0))

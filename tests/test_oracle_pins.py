@@ -724,3 +724,68 @@ def test_rounded_forward_is_the_bf16_block():
 def test_backward_prefetch_order_fetches_the_previous_block():
     assert otr.chain_prefetch_order(3, backward=False) == [(0, 1), (1, 2), (2, None)]
     assert otr.chain_prefetch_order(3, backward=True) == [(2, 1), (1, 0), (0, None)]
+
+
+def test_chain_backward_matches_finite_differences_of_the_mean_square_loss():
+    """Two exact blocks chained, loss mean(z^2) of the last output: every
+    gradient of mlp_chain_backward against central differences of the loss
+    (a dropped link between blocks, a wrong loss gradient or a swapped
+    block order fails here)."""
+    rng = np.random.default_rng(54)
+    B, w, L = 2, 8, 2
+    x = rng.normal(size=(B, w))
+    blocks = [{"gamma": rng.uniform(0.5, 1.5, w), "beta": rng.normal(0, 0.1, w),
+               "W": rng.normal(0, 0.4, (w, w)), "b": rng.normal(0, 0.1, w)} for _ in range(L)]
+    res = otr.mlp_chain_backward(x, blocks)
+
+    def loss(x_, blocks_):
+        h = x_
+        for blk in blocks_:
+            h = otr.mlp_block_forward(h, blk["gamma"], blk["beta"], blk["W"], blk["b"])["z"]
+        return float(np.mean(h * h))
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd[idx] = (loss(xp, blocks) - loss(xm, blocks)) / (2 * h)
+    assert np.allclose(res["dx"], fd, rtol=1e-6, atol=1e-9)
+    for i, name, key in ((0, "W", "dW"), (1, "gamma", "dgamma"), (0, "b", "db"), (1, "beta", "dbeta")):
+        fd = np.zeros_like(blocks[i][name])
+        for idx in np.ndindex(fd.shape):
+            bp = [dict(b) for b in blocks]
+            bm = [dict(b) for b in blocks]
+            bp[i][name] = blocks[i][name].copy()
+            bm[i][name] = blocks[i][name].copy()
+            bp[i][name][idx] += h
+            bm[i][name][idx] -= h
+            fd[idx] = (loss(x, bp) - loss(x, bm)) / (2 * h)
+        assert np.allclose(res["grads"][i][key], fd, rtol=1e-6, atol=1e-9), (i, key)
+
+
+def test_mean_square_loss_grad_closed_form():
+    z = np.array([[1.0, -2.0], [0.5, 0.0]])
+    assert np.array_equal(otr.mean_square_loss_grad(z), np.array([[0.5, -1.0], [0.25, 0.0]]))
+
+
+def test_forced_module_inputs_equal_to_its_own_change_nothing():
+    """Teacher forcing plumbing: forcing each module input with the value the
+    oracle computes itself reproduces the unforced gradients bit for bit,
+    and forcing dlin changes exactly the gradients downstream of it."""
+    rng = np.random.default_rng(55)
+    B, w = 3, 16
+    x = oracle.bf16_to_f64(oracle.f64_to_bf16(rng.normal(size=(B, w))))
+    args = [_bf16_round(rng.uniform(0.5, 1.5, w)), _bf16_round(rng.normal(0, 0.1, w)),
+            _bf16_round(rng.normal(0, 0.2, (w, w))), _bf16_round(rng.normal(0, 0.1, w))]
+    dz = _bf16_round(rng.normal(size=(B, w)))
+    g = otr.mlp_block_backward(x, *args, dz, rounding=_bf16_round)
+    f = otr.mlp_block_forward(x, *args, rounding=_bf16_round)
+    g2 = otr.mlp_block_backward(x, *args, dz, rounding=_bf16_round,
+                                forced={"ln": f["ln"], "lin": f["lin"], "dlin": g["dlin"],
+                                        "dln": g["dln"]})
+    for k in ("dx", "dW", "db", "dgamma", "dbeta", "dlin", "dln"):
+        assert np.array_equal(g[k], g2[k]), k
+    g3 = otr.mlp_block_backward(x, *args, dz, rounding=_bf16_round,
+                                forced={"dlin": np.zeros((B, w))})
+    assert not np.any(g3["dW"]) and not np.any(g3["db"]) and not np.any(g3["dx"])

@@ -72,15 +72,27 @@ class ChainOpts(C.Structure):
                 ("y_out", P), ("h_trace", P), ("use_pdl", I32), ("prefetch", I32),
                 ("fixed_plan", PrefetchPlan), ("distance", I32), ("decoy", I32),
                 ("tune_pairs", I32), ("tune_min_gain", F32), ("weight_format", I32),
-                ("persistent", I32), ("attention", I32), ("s_max", I32), ("pos", P)]
+                ("persistent", I32), ("attention", I32), ("s_max", I32), ("pos", P),
+                ("mlp_ln", P), ("mlp_pre", P), ("mlp_gelu_grad", P), ("mlp_ln_stats", P)]
+
+
+class MlpGrads(C.Structure):
+    _fields_ = [("dW", P), ("db", P), ("dgamma", P), ("dbeta", P)]
+
+
+class MlpBackwardOpts(C.Structure):
+    _fields_ = [("batch", I32), ("width", I32), ("x_in", P), ("acts", P), ("ln", P),
+                ("gelu_grad", P), ("ln_stats", P), ("dz", P), ("dx", P), ("dx_trace", P),
+                ("dlin_trace", P), ("dln_trace", P), ("use_pdl", I32), ("prefetch", I32),
+                ("fixed_plan", PrefetchPlan), ("distance", I32), ("decoy", I32),
+                ("tune_pairs", I32), ("tune_min_gain", F32)]
 
 
 class Tuning(C.Structure):
     _fields_ = [("ring_bytes", I32), ("grid_cap", I32), ("force_ksplit", I32),
                 ("force_rt", I32), ("evict_first", I32), ("piece_bytes", I32),
                 ("timeout_ns", C.c_ulonglong), ("l2_ahead", I32),
-                ("forms", I32), ("launch_pdl", I32), ("mma", I32), ("la_mask", I32),
-                ("la_when", I32), ("la_depth", I32)]
+                ("forms", I32), ("launch_pdl", I32), ("mma", I32), ("late_trigger", I32)]
 
 
 class GemvSchedule(C.Structure):
@@ -111,6 +123,11 @@ _SIGS = {
     "ws_chain_step_host": [P, P, P, P, P],
     "ws_chain_plans": [P, P, P, P, I32],
     "ws_chain_op_bytes": [P, P, I32],
+    "ws_mlp_backward_create": [P, P, I32, P, P],
+    "ws_mlp_backward_tune": [P, P],
+    "ws_mlp_backward_capture": [P, P],
+    "ws_mlp_backward_run": [P, P],
+    "ws_mlp_backward_plan": [P, P, P, P],
     "ws_set_tuning": [P],
     "ws_gemv_plan": [I32, I32, I32, I32, I32, I32, I32, P],
     "ws_read_probe": [P, SZ, I32, P, P],
@@ -128,6 +145,8 @@ _OTHER = {
     "ws_chain_grid": ([P], I32),
     "ws_chain_debug_stamps": ([P, P, SZ], I32),
     "ws_chain_destroy": ([P], None),
+    "ws_mlp_backward_num_launches": ([P], I32),
+    "ws_mlp_backward_destroy": ([P], None),
     "ws_get_tuning": ([P], None),
     "ws_debug_gemv_copies": ([I32, I32, I32, I32, I32, I32, P, C.c_long], C.c_long),
     "ws_debug_gemv_copies_q4": ([I32, I32, I32, I32, I32, I32, P, C.c_long, P], C.c_long),
@@ -447,6 +466,49 @@ class Chain:
     def close(self):
         if self.handle:
             load().ws_chain_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MlpBackward:
+    """The backward pass of a LayerNorm -> Linear -> GELU chain:
+    ws_mlp_backward_create / tune / capture / run / destroy.  Keeps the
+    Python objects whose device memory it points at alive."""
+
+    def __init__(self, blocks, grads, opts: MlpBackwardOpts, keepalive=()):
+        n = len(blocks)
+        barr = (MlpBlock * n)(*blocks)
+        garr = (MlpGrads * n)(*grads)
+        h = P()
+        _check(load().ws_mlp_backward_create(barr, garr, n, C.byref(opts), C.byref(h)))
+        self.handle = h
+        self.opts = opts
+        self._keep = list(keepalive)
+        self.n_launches = int(load().ws_mlp_backward_num_launches(h))
+
+    def tune(self, stream=None):
+        _check(load().ws_mlp_backward_tune(self.handle, _stream(stream)))
+
+    def capture(self, stream=None):
+        _check(load().ws_mlp_backward_capture(self.handle, _stream(stream)))
+
+    def run(self, stream=None):
+        _check(load().ws_mlp_backward_run(self.handle, _stream(stream)))
+
+    def plan(self):
+        pl = PrefetchPlan()
+        lo, mean = F32(), F32()
+        _check(load().ws_mlp_backward_plan(self.handle, C.byref(pl), C.byref(lo), C.byref(mean)))
+        return (pl.mode, pl.blocks, pl.threads, pl.stride_bytes), lo.value, mean.value
+
+    def close(self):
+        if self.handle:
+            load().ws_mlp_backward_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

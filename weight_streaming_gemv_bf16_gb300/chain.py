@@ -42,6 +42,10 @@ class MlpChain:
     x_in: torch.Tensor
     y_out: torch.Tensor
     trace: torch.Tensor | None = None
+    gelu_grad: torch.Tensor | None = None
+    ln_stats: torch.Tensor | None = None
+    ln: torch.Tensor | None = None
+    pre: torch.Tensor | None = None
 
     def run(self, stream=None):
         self.chain.run(stream)
@@ -127,12 +131,23 @@ def qwen_chain(blocks, head, attn, h_in, *, eps=1e-6, use_pdl=True, prefetch=0,
 
 def mlp_chain(blocks, x_in, *, eps=1e-5, use_pdl=True, prefetch=0, fixed_plan=None,
               distance=1, decoy=False, tune_pairs=30, min_gain=0.01,
-              persistent=False, trace=False) -> MlpChain:
+              persistent=False, trace=False, training=False) -> MlpChain:
     """blocks: list of dicts of bf16 device tensors gamma, beta, W, b; x_in bf16 [B, w].
-    trace=True keeps every block's output in `trace` (bf16 [L, B, w])."""
+    trace=True keeps every block's output in `trace` (bf16 [L, B, w]).
+    training=True (implies trace) also keeps what each module keeps for the
+    backward: the Linear's input (`ln`, bf16 [L, B, w]), the GELU's input
+    (`pre`, bf16 [L, B, w]) and derivative there (`gelu_grad`, fp32
+    [L, B, w]), and the LayerNorm mean and rstd of every block's input
+    (`ln_stats`, fp32 [L, B, 2])."""
     B, w = x_in.shape
+    L = len(blocks)
+    trace = trace or training
     y_out = torch.empty_like(x_in)
-    tr = torch.empty((len(blocks), B, w), dtype=torch.bfloat16, device=x_in.device) if trace else None
+    tr = torch.empty((L, B, w), dtype=torch.bfloat16, device=x_in.device) if trace else None
+    gg = torch.empty((L, B, w), dtype=torch.float32, device=x_in.device) if training else None
+    st = torch.empty((L, B, 2), dtype=torch.float32, device=x_in.device) if training else None
+    ln = torch.empty((L, B, w), dtype=torch.bfloat16, device=x_in.device) if training else None
+    pre = torch.empty((L, B, w), dtype=torch.bfloat16, device=x_in.device) if training else None
     descs = []
     for blk in blocks:
         d = wb.BlockDesc(kind=wb.BLOCK_MLP)
@@ -144,5 +159,74 @@ def mlp_chain(blocks, x_in, *, eps=1e-5, use_pdl=True, prefetch=0, fixed_plan=No
     o.x_in = x_in.data_ptr()
     o.y_out = y_out.data_ptr()
     o.h_trace = tr.data_ptr() if tr is not None else None
-    ch = wb.Chain(descs, o, keepalive=[blocks, x_in, y_out, tr])
-    return MlpChain(ch, x_in, y_out, tr)
+    o.mlp_gelu_grad = gg.data_ptr() if gg is not None else None
+    o.mlp_ln_stats = st.data_ptr() if st is not None else None
+    o.mlp_ln = ln.data_ptr() if ln is not None else None
+    o.mlp_pre = pre.data_ptr() if pre is not None else None
+    ch = wb.Chain(descs, o, keepalive=[blocks, x_in, y_out, tr, gg, st, ln, pre])
+    return MlpChain(ch, x_in, y_out, tr, gg, st, ln, pre)
+
+
+@dataclass
+class MlpBackwardRun:
+    bwd: wb.MlpBackward
+    grads: list
+    dx: torch.Tensor
+    dx_trace: torch.Tensor | None = None
+    dlin_trace: torch.Tensor | None = None
+    dln_trace: torch.Tensor | None = None
+
+    def run(self, stream=None):
+        self.bwd.run(stream)
+
+
+def mlp_backward(blocks, fwd: MlpChain, *, dz=None, use_pdl=True, prefetch=0, fixed_plan=None,
+                 distance=1, decoy=False, tune_pairs=30, min_gain=0.01,
+                 traces=False) -> MlpBackwardRun:
+    """The backward pass of the chain `fwd` (built with training=True) over
+    the same blocks ("Making small PyTorch ops faster on a laptop GPU", "It
+    works in training too").  dz: bf16 [B, w] gradient of the loss with
+    respect to the chain output, or None for the mean-square loss of the
+    output.  Returns the gradient tensors (per block dW, db, dgamma, dbeta
+    in `grads`; dx of the chain input); traces=True also keeps every block's
+    input gradient (dx_trace [L+1, B, w], slot L the loss gradient), dlin
+    and dln (bf16 [L, B, w])."""
+    if fwd.gelu_grad is None:
+        raise ValueError("the forward chain was not built with training=True")
+    B, w = fwd.x_in.shape
+    L = len(blocks)
+    dev = fwd.x_in.device
+    grads = [{"dW": torch.empty((w, w), dtype=torch.bfloat16, device=dev),
+              "db": torch.empty((w,), dtype=torch.bfloat16, device=dev),
+              "dgamma": torch.empty((w,), dtype=torch.bfloat16, device=dev),
+              "dbeta": torch.empty((w,), dtype=torch.bfloat16, device=dev)} for _ in range(L)]
+    dx = torch.empty((B, w), dtype=torch.bfloat16, device=dev)
+    dxt = torch.empty((L + 1, B, w), dtype=torch.bfloat16, device=dev) if traces else None
+    dlt = torch.empty((L, B, w), dtype=torch.bfloat16, device=dev) if traces else None
+    dnt = torch.empty((L, B, w), dtype=torch.bfloat16, device=dev) if traces else None
+    o = wb.MlpBackwardOpts()
+    o.batch, o.width = B, w
+    o.x_in = fwd.x_in.data_ptr()
+    o.acts = fwd.trace.data_ptr()
+    o.ln = fwd.ln.data_ptr()
+    o.gelu_grad = fwd.gelu_grad.data_ptr()
+    o.ln_stats = fwd.ln_stats.data_ptr()
+    o.dz = dz.data_ptr() if dz is not None else None
+    o.dx = dx.data_ptr()
+    o.dx_trace = dxt.data_ptr() if dxt is not None else None
+    o.dlin_trace = dlt.data_ptr() if dlt is not None else None
+    o.dln_trace = dnt.data_ptr() if dnt is not None else None
+    o.use_pdl = 1 if use_pdl else 0
+    o.prefetch = prefetch
+    if fixed_plan is not None:
+        o.fixed_plan = fixed_plan
+    o.distance = distance
+    o.decoy = 1 if decoy else 0
+    o.tune_pairs = tune_pairs
+    o.tune_min_gain = min_gain
+    bl = [wb.MlpBlock(b["gamma"].data_ptr(), b["beta"].data_ptr(), b["W"].data_ptr(),
+                      b["b"].data_ptr()) for b in blocks]
+    gr = [wb.MlpGrads(g["dW"].data_ptr(), g["db"].data_ptr(), g["dgamma"].data_ptr(),
+                      g["dbeta"].data_ptr()) for g in grads]
+    bwd = wb.MlpBackward(bl, gr, o, keepalive=[blocks, fwd, grads, dx, dxt, dlt, dnt, dz])
+    return MlpBackwardRun(bwd, grads, dx, dxt, dlt, dnt)

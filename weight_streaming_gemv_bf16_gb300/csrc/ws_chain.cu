@@ -198,7 +198,7 @@ static ws_status build_ops(ws_chain* c) {
         cudaMalloc((void**)&c->qkv_scratch, (size_t)B * (H + 2 * o.kv_dim) * 4) != cudaSuccess)
       return WS_ERR_NOMEM;
   }
-  if (c->n_mlp > 1) {
+  if (c->n_mlp > 1 && !o.h_trace) {
     for (int i = 0; i < 2; ++i)
       if (cudaMalloc(&c->pp[i], (size_t)B * H * 2) != cudaSuccess) return WS_ERR_NOMEM;
   }
@@ -299,8 +299,16 @@ static ws_status build_ops(ws_chain* c) {
     } else if (d.kind == WS_BLOCK_MLP) {
       const ws_mlp_block& m = d.u.mlp;
       const int w = H;
-      const void* xin = mlp_seen == 0 ? o.x_in : c->pp[(mlp_seen - 1) % 2];
-      void* yout = mlp_seen == c->n_mlp - 1 ? o.y_out : c->pp[mlp_seen % 2];
+      // with a trace every block but the last writes its output straight
+      // into its trace slot (no copy, so every op boundary keeps its
+      // programmatic edge) and the next block reads it there
+      const size_t tb = trace_bytes(c);
+      auto slot = [&](int i) -> void* {
+        return o.h_trace ? static_cast<void*>(reinterpret_cast<char*>(o.h_trace) + (size_t)i * tb)
+                         : c->pp[i % 2];
+      };
+      const void* xin = mlp_seen == 0 ? o.x_in : slot(mlp_seen - 1);
+      void* yout = mlp_seen == c->n_mlp - 1 ? o.y_out : slot(mlp_seen);
       ChainOp op{};
       init_gemv_params(op.p, w, B);
       op.p.nseg = 1;
@@ -318,7 +326,13 @@ static ws_status build_ops(ws_chain* c) {
       op.reads.push_back({m.W, (size_t)w * w * 2});
       op.kind = OP_MLP;
       op.block = bi;
-      op.trace_block = mlp_seen;
+      // only the last block's output is copied into the trace
+      op.trace_block = (o.h_trace && mlp_seen == c->n_mlp - 1) ? mlp_seen : -1;
+      const size_t bw = (size_t)mlp_seen * B * w;
+      if (o.mlp_ln) op.p.ln_out = static_cast<uint16_t*>(o.mlp_ln) + bw;
+      if (o.mlp_pre) op.p.pre_out = static_cast<uint16_t*>(o.mlp_pre) + bw;
+      if (o.mlp_gelu_grad) op.p.gelu_grad = o.mlp_gelu_grad + bw;
+      if (o.mlp_ln_stats) op.p.ln_stats = o.mlp_ln_stats + (size_t)mlp_seen * B * 2;
       c->ops.push_back(op);
       ++mlp_seen;
     } else {
@@ -356,7 +370,7 @@ static ws_status build_ops(ws_chain* c) {
 
   // persistent mode when asked for and every op fits its stage layout
   c->persistent = false;
-  if (o.persistent && B <= 4) {
+  if (o.persistent && B <= 4 && !o.mlp_gelu_grad && !o.mlp_ln_stats && !o.mlp_ln && !o.mlp_pre) {
     int kmax = 8;
     for (ChainOp& op : c->ops) kmax = op.p.K > kmax ? op.p.K : kmax;
     const int ring = persistent_ring_bytes(B, kmax);
@@ -388,38 +402,7 @@ static ws_status build_ops(ws_chain* c) {
     op.plan = kNoPlan;
     op.gain_lo = op.gain_mean = 0.f;
   }
-  // L2 look-ahead (ws_tuning.la_mask): an op of a decoder block asks L2 for
-  // the weights a later op of the same block fills its rings with first
-  const int lam = tuning().la_mask;
-  if (lam && !c->persistent && o.weight_format == WS_WEIGHTS_BF16) {
-    const int n = (int)c->ops.size();
-    for (int i = 0; i < n; ++i) {
-      const int kind = c->ops[i].kind;
-      int t = -1;
-      if (kind == OP_QKV)
-        t = (lam & WS_LA_QKV_GATEUP) ? i + 2 : (lam & WS_LA_QKV_WD) ? i + 3 : -1;
-      else if (kind == OP_WO)
-        t = (lam & WS_LA_WO_GATEUP) ? i + 1 : (lam & WS_LA_WO_WD) ? i + 2 : -1;
-      else if (kind == OP_GATEUP)
-        t = (lam & WS_LA_GATEUP_WD) ? i + 1 : -1;
-      if (t < 0 || t >= n || c->ops[t].block != c->ops[i].block) continue;
-      const GemvParams& tp = c->ops[t].p;
-      if (tp.nseg != 1 || tp.sc.S != 1 || tp.sc.mma) continue;
-      GemvParams& p = c->ops[i].p;
-      const int d = tuning().la_depth;
-      const int pieces = d * tp.sc.NSW;  // pieces per warp asked for
-      p.la_W0 = tp.seg[0].W0;
-      p.la_W1 = tp.nmat == 2 ? tp.seg[0].W1 : nullptr;
-      p.la_K = tp.K;
-      p.la_M = tp.seg[0].M;
-      p.la_RT = tp.sc.RT;
-      p.la_RG = tp.sc.RG;
-      p.la_Gs = tp.sc.Gs;
-      p.la_groups = kWarps * ((pieces + tp.sc.NP - 1) / tp.sc.NP);
-      p.la_cols = pieces >= tp.sc.NP ? tp.K : pieces * tp.sc.PC;
-      p.la_when = tuning().la_when;
-    }
-  }
+  for (ChainOp& op : c->ops) op.p.trigger_late = (tuning().late_trigger >> op.kind) & 1;
   c->ws_total = total;
   if (total) {
     if (cudaMalloc(&c->ws, total) != cudaSuccess) return WS_ERR_NOMEM;

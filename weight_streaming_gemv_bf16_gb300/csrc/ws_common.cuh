@@ -124,13 +124,16 @@ struct alignas(16) GemvParams {
   unsigned long long timeout_ns;
   int evict_first;
   float* trace_out;  // persistent chain: copy seg[0].out ([B][M] fp32) here after the op
-  // L2 look-ahead inside a chain: CTA g asks L2 for the first la_groups row
-  // groups (la_RT rows each, la_cols columns from column 0) of the row range
-  // CTA g of a later op (la_RG row groups over la_Gs CTAs) streams first, in
-  // one or two matrices [la_M][la_K].  la_W0 null: none.
-  const uint16_t* la_W0;
-  const uint16_t* la_W1;
-  int la_K, la_M, la_RT, la_RG, la_Gs, la_groups, la_cols, la_when;
+  int trigger_late;  // 1: let the next launch start only after the activations are staged
+  // training forward of the LayerNorm -> Linear -> GELU block, each kept for
+  // the backward when not null: the GELU's input t = bf16(ln.W^T + bias),
+  // bf16 [B][M]; the GELU's derivative at t, fp32 [B][M]; the Linear's input
+  // ln = bf16(LayerNorm(x)), bf16 [B][K]; the LayerNorm's mean and rstd per
+  // batch row, fp32 [B][2]
+  uint16_t* pre_out;
+  float* gelu_grad;
+  uint16_t* ln_out;
+  float* ln_stats;
   // optional diagnostics of a launch inside a chain: globaltimer ns per CTA at
   // stamps[cta * stamp_stride + i], i = 0 entry, 1 dependency released,
   // 2 activations staged, 3 end
@@ -290,9 +293,7 @@ struct Tuning {
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
   int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
   int mma;           // 1: large chain-form ops at batch tiles 8 and 16 run on tensor cores (mma.sync)
-  int la_mask;       // chain ops that ask L2 for a later op's first weights (WS_LA_* bits)
-  int la_when;       // 0: after the op's dependency wait, 1: before it
-  int la_depth;      // ring fills of the later op to look ahead (>= 1)
+  int late_trigger;  // chain op kinds (bit per kind) whose dependents start after staging
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

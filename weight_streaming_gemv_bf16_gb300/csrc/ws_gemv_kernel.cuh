@@ -84,8 +84,13 @@ __device__ __forceinline__ void apply_epilogue(const GemvParams& p, int seg, int
     }
     case EPI_BIAS_GELU: {
       const float t = bf16_round(v0 + __uint_as_float((uint32_t)p.bias[m] << 16));
-      const float z = 0.5f * t * (1.0f + erff(t * 0.70710678118654752f));
+      const float e = erff(t * 0.70710678118654752f);
+      const float z = 0.5f * t * (1.0f + e);
       static_cast<__nv_bfloat16*>(S.out)[o] = __float2bfloat16_rn(z);
+      if (p.pre_out) reinterpret_cast<__nv_bfloat16*>(p.pre_out)[o] = __float2bfloat16_rn(t);
+      // d/dt of t Phi(t): Phi(t) + t phi(t), phi the standard normal density
+      if (p.gelu_grad)
+        p.gelu_grad[o] = 0.5f * (1.0f + e) + t * 0.39894228040143268f * expf(-0.5f * t * t);
       break;
     }
     case EPI_SWIGLU: {
@@ -749,26 +754,6 @@ __device__ __forceinline__ void issue_piece(const GemvParams& p, int rg, int j, 
   }
 }
 
-// L2 look-ahead: ask L2 (bulk prefetches, one per weight row) for the rows
-// that CTA blockIdx.x of a later op of the chain streams first, so that HBM
-// keeps streaming while this op waits on its inputs and computes.  Reads
-// nothing back and writes nothing.
-static __device__ __noinline__ void l2_lookahead(const GemvParams& p, int lane) {
-  const unsigned g = blockIdx.x;
-  if ((int)g >= p.la_Gs) return;
-  const int rg0 = (int)(g * (unsigned)p.la_RG / (unsigned)p.la_Gs);
-  const int rg1 = (int)((g + 1) * (unsigned)p.la_RG / (unsigned)p.la_Gs);
-  const int rows = min(p.la_groups, rg1 - rg0) * p.la_RT;
-  const int r0 = rg0 * p.la_RT;
-  const int n = (p.la_W1 ? 2 : 1) * rows;
-  const uint32_t bytes = (uint32_t)p.la_cols * 2u;
-  for (int i = lane; i < n; i += 32) {
-    const bool second = i >= rows;
-    const int r = r0 + (second ? i - rows : i);
-    if (r < p.la_M) bulk_prefetch_l2((second ? p.la_W1 : p.la_W0) + (size_t)r * p.la_K, bytes);
-  }
-}
-
 template <int BT, int NMAT, int RT, int F, bool Q4 = false>
 __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_constant__ GemvParams p) {
   using FT = FormTraits<F>;
@@ -821,10 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   uint4 bpre[FT::ln1 ? NR : 1];
   if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
   if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
-  if (p.la_W0 && p.la_when == 1 && warp == kWarps - 1) l2_lookahead(p, lane);
-  pdl_launch_dependents();
+  if (!p.trigger_late) pdl_launch_dependents();
   pdl_wait();
-  if (p.la_W0 && p.la_when == 0 && warp == kWarps - 1) l2_lookahead(p, lane);
   if (stamp && tid == 0) stamp[1] = global_ns();
 
   // the residual input of this CTA's rows, read while the activations stage
@@ -860,7 +843,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     stage_x<BT>(p, stats, xs, k0 >> 3, sc.KS >> 3, tid);
   }
   __syncthreads();
+  if (p.trigger_late) pdl_launch_dependents();
   if (stamp && tid == 0) stamp[2] = global_ns();
+  if constexpr (FT::ln1 || F == F_ANY) {
+    // training forward: the LayerNorm statistics of every batch row, and the
+    // normalised rows (the first CTA of each K split writes its columns)
+    if (p.prologue == PRO_LAYERNORM) {
+      if (p.ln_stats && blockIdx.x == 0 && tid < p.B) {
+        p.ln_stats[2 * tid] = stats[2 * tid];
+        p.ln_stats[2 * tid + 1] = stats[2 * tid + 1];
+      }
+      if (p.ln_out && (int)blockIdx.x == ks * sc.Gs) {
+        const int nch = sc.KS >> 3;
+        for (int o = tid; o < p.B * nch; o += kThreads) {
+          const int b = o / nch, c = o - b * nch;
+          reinterpret_cast<uint4*>(p.ln_out + (size_t)b * p.K + k0)[c] =
+              reinterpret_cast<const uint4*>(xs)[o];
+        }
+      }
+    }
+  }
 
   const int nchx = sc.KS >> 3;  // chunks of x in shared memory
   const int ncp = sc.PC >> 3;   // chunk stride of one row of a piece
