@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--mode", choices=["chain", "kernel", "sweep", "configs", "attention", "q4",
-                                       "step-attention", "prefetch"],
+                                       "step-attention", "prefetch", "train", "crossover"],
                     default="chain",
                     help="chain: the decode step (the metric); kernel: gate/up alone (profiler "
                          "captures); sweep: the batch GEMV sweep, fp16 RMSNorm and the "
@@ -60,7 +60,11 @@ def parse():
                          "4-bit group-128 weights, each GEMV shape and the decode step "
                          "beside bf16; step-attention: the decode step with decode "
                          "attention over a key-value cache in every block; prefetch: gate/up "
-                         "after the L2 prefetch of its own weights, of none and of a decoy")
+                         "after the L2 prefetch of its own weights, of none and of a decoy; "
+                         "train: forward + backward of the 72-block LayerNorm chain at batch "
+                         "4 and 16 with the backward's W_(i-1) prefetch off, tuned, decoy; "
+                         "crossover: the decode step at batch 1..128 on CUDA cores and tensor "
+                         "cores, against its HBM and FMA floors")
     ap.add_argument("--q4-gemv", default=None,
                     help="q4 mode: one 'M,K,B' GEMV only (no decode step)")
     ap.add_argument("--attn-config", default=None,
@@ -652,6 +656,164 @@ def run_prefetch_probe(args):
     return 0
 
 
+def run_train(args):
+    """Small-batch training of the 72-block LayerNorm(768) -> Linear(768, 768)
+    -> GELU chain ("Making small PyTorch ops faster on a laptop GPU", "It works
+    in training too"): one step = the training forward (one CUDA graph) and
+    the backward with the mean-square loss of the output (one CUDA graph),
+    at batch 4 and 16, with the backward's L2 prefetch of W_(i-1) off, tuned
+    (measured plan, kept only if its 95% CI clears +1%) and as a decoy aimed
+    at the wrong block.  Gradients are checked bit-identical across the
+    variants.  Prints one JSON line per batch size."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+    from weight_streaming_gemv_bf16_gb300 import synth
+    sh = synth.MlpShape()
+    w, L = sh.width, sh.blocks
+    st = torch.cuda.current_stream()
+    for B in ([args.batch] if args.batch != 1 else [4, 16]):
+        blocks = [{k: to_dev(v, torch) for k, v in synth.mlp_block_weights(sh, args.seed, i).items()}
+                  for i in range(L)]
+        x = to_dev(synth.mlp_input(sh, B, args.seed), torch)
+        fwd = wc.mlp_chain(blocks, x, eps=sh.eps, training=True)
+        fwd.chain.capture()
+        fwd.run()
+        runs = {"none": wc.mlp_backward(blocks, fwd),
+                "tuned": wc.mlp_backward(blocks, fwd, prefetch=1, tune_pairs=30),
+                "decoy": wc.mlp_backward(blocks, fwd, prefetch=2, decoy=True,
+                                         fixed_plan=wb.PrefetchPlan(16, 256, 16384, 3))}
+        t0 = time.perf_counter()
+        runs["tuned"].bwd.tune()
+        t_tune = time.perf_counter() - t0
+        (mode, nb, nt, stride), lo, mean = runs["tuned"].bwd.plan()
+        for r in runs.values():
+            r.bwd.capture()
+
+        def timed(fn, n):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(n):
+                fn()
+            b.record(st)
+            b.synchronize()
+            return a.elapsed_time(b) / n * 1e3
+
+        n = max(20, min(args.steps, 400))
+        res = {"fwd_us": [], "none": [], "tuned": [], "decoy": []}
+        ref = None
+        for rnd in range(5):  # interleaved rounds
+            res["fwd_us"].append(timed(lambda: fwd.run(st), n))
+            for k, r in runs.items():
+                res[k].append(timed(lambda r=r: (fwd.run(st), r.run(st)), n))
+                g = [r.dx.cpu()] + [t.cpu() for gg in r.grads for t in gg.values()]
+                if ref is None:
+                    ref = g
+                assert all(torch.equal(a_, b_) for a_, b_ in zip(g, ref)), f"{k}: gradients differ"
+        med = {k: float(np.median(v)) for k, v in res.items()}
+        wbytes = L * (w * w + 3 * w) * 2
+        step_bytes = 2 * wbytes + L * w * w * 2  # W read forward and backward, dW written
+        print(json.dumps({
+            "mode": "train", "workload": f"72 x [LayerNorm({w}) -> Linear({w},{w}) -> GELU], "
+                                         "mean-square loss, bf16",
+            "batch": B, "steps_per_round": n, "rounds": 5,
+            "forward_us": round(med["fwd_us"], 2),
+            "step_us": {k: round(med[k], 2) for k in ("none", "tuned", "decoy")},
+            "backward_us": {k: round(med[k] - med["fwd_us"], 2) for k in ("none", "tuned", "decoy")},
+            "prefetch_gain_tuned": round(1 - med["tuned"] / med["none"], 4),
+            "prefetch_gain_decoy": round(1 - med["decoy"] / med["none"], 4),
+            "tuned_plan": {"mode": mode, "blocks": nb, "threads": nt, "stride": stride,
+                           "gain_lower_95": round(lo, 4), "gain_mean": round(mean, 4),
+                           "tune_seconds": round(t_tune, 2)},
+            "bytes_per_step": step_bytes,
+            "gbs_none": round(step_bytes / (med["none"] * 1e-6) / 1e9, 1),
+            "launches_per_step": L + (L + 1),
+            "gradients_bit_identical": True}), flush=True)
+    return 0
+
+
+def run_crossover(args):
+    """Batching: when does the decode step stop being memory-bound ("One
+    Token, Kernel by Kernel", "Batching: when does decode stop being
+    memory-bound?").  The full Qwen2.5-1.5B-shaped chain (seeded N(0, 0.02)
+    weights drawn on the device) at B = 1 .. 128, on CUDA cores (the default
+    kernels) and with the optional warp-level tensor-core kernel; batches
+    above 16 run every op once per 16-row tile.  Per batch: us per step, the
+    weight bytes read once per step over that time (GB/s), the FLOP rate
+    (2 x weights x B per step), and the step's floors: HBM (weights once at
+    the measured copy peak) and, for CUDA cores, the FP32 FMA issue rate."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    from weight_streaming_gemv_bf16_gb300 import chain as wc
+    from weight_streaming_gemv_bf16_gb300 import synth
+    sh = synth.QWEN2_5_1_5B
+    H, KV, I, V, L = sh.hidden, sh.kv_dim, sh.inter, sh.vocab, sh.layers
+    g = torch.Generator(device="cuda")
+    g.manual_seed(args.seed)
+
+    def rw(*shape):
+        return (torch.randn(shape, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+
+    def gam():
+        return (torch.rand(H, device="cuda", generator=g) + 0.5).to(torch.bfloat16)
+    blocks = [dict(gamma1=gam(), Wq=rw(H, H), Wk=rw(KV, H), Wv=rw(KV, H), Wo=rw(H, H),
+                   gamma2=gam(), Wg=rw(I, H), Wu=rw(I, H), Wd=rw(H, I)) for _ in range(L)]
+    head = dict(gamma_f=gam(), Wlm=rw(V, H))
+    wbytes = sh.chain_weight_bytes()
+    weights = wbytes / 2
+    hbm, _ = peaks()
+    fma_rate = 36.3e12  # measured mixed bf16 FMA rate of this part (see the design notes)
+    st = torch.cuda.current_stream()
+    base = wb.get_tuning()
+    rows = []
+    for B in [1, 2, 4, 8, 16, 32, 64, 128]:
+        attn = (torch.randn((L, B, H), device="cuda", generator=g)).to(torch.bfloat16)
+        h0 = torch.randn((B, H), device="cuda", generator=g)
+        for mma in (0, 1):
+            t = wb.Tuning()
+            for f, _ in wb.Tuning._fields_:
+                setattr(t, f, getattr(base, f))
+            t.mma = mma
+            wb.set_tuning(t)
+            try:
+                ch = wc.qwen_chain(blocks, head, attn, h0, eps=sh.eps)
+                ch.chain.capture()
+            finally:
+                wb.set_tuning(base)
+            n = max(5, min(args.steps, int(0.5e6 / (650 * max(1, B / 4)))))
+            times = []
+            for _ in range(3):
+                for _ in range(3):
+                    ch.run(st)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                for _ in range(n):
+                    ch.run(st)
+                b.record(st)
+                b.synchronize()
+                times.append(a.elapsed_time(b) / n * 1e3)
+            us = float(np.median(times))
+            row = {"B": B, "kernel": "tensor-core (mma.sync)" if mma else "CUDA cores",
+                   "us_per_step": round(us, 1), "weight_gbs": round(wbytes / (us * 1e-6) / 1e9, 1),
+                   "tflops": round(2 * weights * B / (us * 1e-6) / 1e12, 2),
+                   "hbm_floor_us": round(wbytes / (hbm * 1e9) * 1e6, 1),
+                   "launches_per_step": ch.chain.n_ops}
+            if not mma:
+                row["fma_floor_us"] = round(weights * B / fma_rate * 1e6, 1)
+            rows.append(row)
+            print(json.dumps(dict(mode="crossover", **row)), flush=True)
+            ch.chain.close()
+    return 0
+
+
 def run_sweep(args):
     """The standalone workloads of the batch sweep and of the LayerNorm block
     chain, one JSON line: each GEMV shape of the decode step at batch 1..16
@@ -1170,6 +1332,10 @@ def main():
         return run_step_attention(args)
     if args.mode == "prefetch":
         return run_prefetch_probe(args)
+    if args.mode == "train":
+        return run_train(args)
+    if args.mode == "crossover":
+        return run_crossover(args)
     return run_ours(args)
 
 

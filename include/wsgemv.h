@@ -297,7 +297,9 @@ typedef struct {
 } ws_block_desc;
 
 typedef struct {
-  int batch;        /* B, 1..16                                             */
+  int batch;        /* B, 1..128; above 16 every op runs once per 16-row
+                       batch tile, tiles of an op back to back (bf16 weights,
+                       no attention, no training saves)                     */
   int hidden;       /* H (Qwen) or width (MLP)                              */
   int kv_dim;       /* K/V projection rows (Qwen)                           */
   int inter;        /* MLP rows I (Qwen)                                    */
@@ -537,10 +539,6 @@ typedef struct {
                           launch runs on CUDA cores, the vector-product
                           design.  Sums are ordered differently; both stay
                           within the fp32 tolerance of the oracle.           */
-  int late_trigger;    /* chain ops: bit k set (k = 0 QKV, 1 Wo, 2 gate/up,
-                          3 Wd, 4 LM head, 5 LayerNorm block) lets the next
-                          launch start only once the op has staged its
-                          activations, instead of at its start.  Default 0. */
 } ws_tuning;
 
 void ws_get_tuning(ws_tuning *t);

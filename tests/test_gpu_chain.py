@@ -277,6 +277,34 @@ def test_step_host_matches_device_run():
     assert np.array_equal(out.numpy(), ch.idx.cpu().numpy())
 
 
+@pytest.mark.parametrize("mma", [0, 1])
+@pytest.mark.parametrize("B,shape", [(32, SMALL), (128, SMALL), (40, MID), (128, MID)])
+def test_large_batch_chain_in_tiles_matches_oracle(B, shape, mma):
+    """Batches past the kernels' 16-row tile ("One Token, Kernel by Kernel",
+    "Batching: when does decode stop being memory-bound?"): every op runs
+    once per 16-row tile (40 = two full tiles and one of 8); per-block
+    teacher-forced parity, the end-to-end argmax, and the graph without trace
+    copies equal to the traced one bit for bit."""
+    base = _set_tuning(mma=mma)
+    try:
+        ch, blocks, head, attn, h0 = _make(shape, B, 28, trace=True, keep_qkv=True, logits=True)
+        ch.chain.capture()
+        ch.run()
+        ch.run()
+        plain = wc.qwen_chain([_dev(b) for b in blocks], _dev(head), dev_bf16(attn), dev_f32(h0),
+                              logits=True)
+        plain.chain.capture()
+        plain.run()
+        torch.cuda.synchronize()
+    finally:
+        wb.set_tuning(base)
+    assert wb.device_error() == 0
+    assert torch.equal(plain.h_out.cpu(), ch.h_out.cpu())
+    assert torch.equal(plain.idx.cpu(), ch.idx.cpu())
+    assert torch.equal(plain.logits.cpu(), ch.logits.cpu())
+    _check_chain(ch, blocks, head, attn, h0)
+
+
 @pytest.mark.parametrize("persistent", [False, True])
 def test_one_full_size_block_matches_oracle(persistent):
     """One Qwen2.5-1.5B-shaped block at batch 1 (hidden 1536, KV 256, MLP 8960)."""

@@ -55,6 +55,7 @@ struct ChainOp {
   int kind;
   int block;        // index in the block list
   int trace_block;  // Qwen block whose h is traced after this op, or -1
+  const void* trace_src = nullptr;  // the whole batch's output that the trace copies
   std::vector<std::pair<const void*, size_t>> reads;  // weight ranges
   int attn_call = -1;  // decode attention launched right after this op (QKV), or -1
   size_t bytes;     // algorithmic weight bytes
@@ -175,6 +176,21 @@ static size_t trace_bytes(const ws_chain* c) {
   return (size_t)c->o.batch * c->o.hidden * (c->n_mlp ? 2 : 4);
 }
 
+// Point a launch planned for the whole batch at batch rows b0 .. b0 + p.B - 1
+// of its activations and outputs (all row-major [B][...]).
+static void tile_rows(GemvParams& p, int b0) {
+  const size_t xb = p.x_dtype == DT_F32 ? 4 : 2;
+  p.x = static_cast<const char*>(p.x) + (size_t)b0 * p.K * xb;
+  const bool f32_out =
+      p.epilogue == EPI_F32 || p.epilogue == EPI_RESID || p.epilogue == EPI_ARGMAX;
+  for (int s = 0; s < p.nseg; ++s)
+    if (p.seg[s].out)
+      p.seg[s].out = static_cast<char*>(p.seg[s].out) + (size_t)b0 * p.seg[s].M * (f32_out ? 4 : 2);
+  if (p.res_in) p.res_in += (size_t)b0 * p.seg[0].M;
+  if (p.argmax_idx) p.argmax_idx += b0;
+  if (p.logits) p.logits += (size_t)b0 * p.seg[0].M;
+}
+
 static ws_status build_ops(ws_chain* c) {
   const ws_chain_opts& o = c->o;
   const int B = o.batch;
@@ -289,6 +305,7 @@ static ws_status build_ops(ws_chain* c) {
       wd.reads.push_back({q.Wd, (size_t)H * o.inter * 2});
       wd.kind = OP_WD;
       wd.trace_block = qwen_seen;
+      wd.trace_src = o.h_out;
       c->ops.push_back(wd);
       for (size_t k = c->ops.size() - 4; k < c->ops.size(); ++k) {
         c->ops[k].block = bi;
@@ -328,6 +345,7 @@ static ws_status build_ops(ws_chain* c) {
       op.block = bi;
       // only the last block's output is copied into the trace
       op.trace_block = (o.h_trace && mlp_seen == c->n_mlp - 1) ? mlp_seen : -1;
+      op.trace_src = yout;
       const size_t bw = (size_t)mlp_seen * B * w;
       if (o.mlp_ln) op.p.ln_out = static_cast<uint16_t*>(o.mlp_ln) + bw;
       if (o.mlp_pre) op.p.pre_out = static_cast<uint16_t*>(o.mlp_pre) + bw;
@@ -368,6 +386,29 @@ static ws_status build_ops(ws_chain* c) {
     }
   }
 
+  // batches above the kernels' batch tile: every op runs once per tile of
+  // kMaxBatch rows, tiles of one op back to back (rows are independent, so
+  // each launch sees its tile's rows of every activation and output); all
+  // but the last tile stream the weights with the normal L2 policy, so the
+  // next tile finds what still fits in L2
+  if (B > kMaxBatch) {
+    const int nt = (B + kMaxBatch - 1) / kMaxBatch;
+    std::vector<ChainOp> tiled;
+    for (const ChainOp& op : c->ops)
+      for (int t = 0; t < nt; ++t) {
+        ChainOp s = op;
+        const int b0 = t * kMaxBatch;
+        s.p.B = std::min(kMaxBatch, B - b0);
+        tile_rows(s.p, b0);
+        if (t != nt - 1) {
+          s.trace_block = -1;
+          s.p.evict_first = 0;
+        }
+        tiled.push_back(s);
+      }
+    c->ops.swap(tiled);
+  }
+
   // persistent mode when asked for and every op fits its stage layout
   c->persistent = false;
   if (o.persistent && B <= 4 && !o.mlp_gelu_grad && !o.mlp_ln_stats && !o.mlp_ln && !o.mlp_pre) {
@@ -402,7 +443,6 @@ static ws_status build_ops(ws_chain* c) {
     op.plan = kNoPlan;
     op.gain_lo = op.gain_mean = 0.f;
   }
-  for (ChainOp& op : c->ops) op.p.trigger_late = (tuning().late_trigger >> op.kind) & 1;
   c->ws_total = total;
   if (total) {
     if (cudaMalloc(&c->ws, total) != cudaSuccess) return WS_ERR_NOMEM;
@@ -509,9 +549,11 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
       if (s != WS_OK) return s;
     }
     if (!trace.empty() && trace[i] >= 0) {
+      // the whole batch's output (a tiled op's own pointer starts at its tile)
       const size_t bytes = trace_bytes(c);
       if (cudaMemcpyAsync(reinterpret_cast<char*>(c->o.h_trace) + (size_t)trace[i] * bytes,
-                          ps[i].seg[0].out, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+                          c->ops[i].trace_src, bytes, cudaMemcpyDeviceToDevice,
+                          stream) != cudaSuccess)
         return WS_ERR_CUDA;
       prev_kernel = false;
     }
@@ -693,8 +735,15 @@ ws_status ws_chain_create(const ws_block_desc* blocks, int n, const ws_chain_opt
   }
   *out = nullptr;
   const ws_chain_opts& o = *opts;
-  if (o.batch < 1 || o.batch > kMaxBatch || o.hidden <= 0 || o.hidden % 8 != 0) {
+  if (o.batch < 1 || o.batch > kMaxChainBatch || o.hidden <= 0 || o.hidden % 8 != 0) {
     set_error("bad batch %d or hidden %d", o.batch, o.hidden);
+    return WS_ERR_SHAPE;
+  }
+  if (o.batch > kMaxBatch &&
+      (o.attention || o.weight_format != WS_WEIGHTS_BF16 || o.mlp_ln || o.mlp_pre ||
+       o.mlp_gelu_grad || o.mlp_ln_stats)) {
+    set_error("batch %d > %d runs in batch tiles: bf16 weights, no attention, no training "
+              "saves", o.batch, kMaxBatch);
     return WS_ERR_SHAPE;
   }
   if (o.distance < 1 && o.prefetch) {
@@ -1074,7 +1123,7 @@ ws_status ws_chain_run_eager(ws_chain* c, ws_stream_t stream) {
       const size_t bytes = trace_bytes(c);
       if (cudaMemcpyAsync(reinterpret_cast<char*>(c->o.h_trace) +
                               (size_t)c->ops[i].trace_block * bytes,
-                          c->ops[i].p.seg[0].out, bytes, cudaMemcpyDeviceToDevice,
+                          c->ops[i].trace_src, bytes, cudaMemcpyDeviceToDevice,
                           (cudaStream_t)stream) != cudaSuccess)
         return WS_ERR_CUDA;
     }

@@ -32,6 +32,7 @@ constexpr int kMaxStages = 8;  // ring stages per warp
 // only stage): fewer rows in flight per CTA, so that each row's copy is longer
 constexpr int kMmaWarps = 4;
 constexpr int kMaxBatch = 16;
+constexpr int kMaxChainBatch = 128;  // chains: larger batches run in tiles of kMaxBatch rows
 
 enum Prologue { PRO_NONE = 0, PRO_RMSNORM = 1, PRO_LAYERNORM = 2 };
 enum Epilogue {
@@ -124,7 +125,6 @@ struct alignas(16) GemvParams {
   unsigned long long timeout_ns;
   int evict_first;
   float* trace_out;  // persistent chain: copy seg[0].out ([B][M] fp32) here after the op
-  int trigger_late;  // 1: let the next launch start only after the activations are staged
   // training forward of the LayerNorm -> Linear -> GELU block, each kept for
   // the backward when not null: the GELU's input t = bf16(ln.W^T + bias),
   // bf16 [B][M]; the GELU's derivative at t, fp32 [B][M]; the Linear's input
@@ -293,7 +293,6 @@ struct Tuning {
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
   int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
   int mma;           // 1: large chain-form ops at batch tiles 8 and 16 run on tensor cores (mma.sync)
-  int late_trigger;  // chain op kinds (bit per kind) whose dependents start after staging
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

@@ -34,7 +34,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 0, 0};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 0};
   return t;
 }
 
@@ -1013,7 +1013,6 @@ void ws_get_tuning(ws_tuning* t) {
   t->forms = tu.forms;
   t->launch_pdl = tu.launch_pdl;
   t->mma = tu.mma;
-  t->late_trigger = tu.late_trigger;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
@@ -1022,8 +1021,7 @@ ws_status ws_set_tuning(const ws_tuning* t) {
       t->piece_bytes < 0 ||
       t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
       t->l2_ahead > 64 || t->forms < 0 || t->forms > 1 || t->launch_pdl < 0 ||
-      t->launch_pdl > 1 || t->mma < 0 || t->mma > 1 || t->late_trigger < 0 ||
-      t->late_trigger > 63) {
+      t->launch_pdl > 1 || t->mma < 0 || t->mma > 1) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -1039,7 +1037,6 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.forms = t->forms;
   tu.launch_pdl = t->launch_pdl;
   tu.mma = t->mma;
-  tu.late_trigger = t->late_trigger;
   return WS_OK;
 }
 

@@ -806,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   uint4 bpre[FT::ln1 ? NR : 1];
   if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
   if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
-  if (!p.trigger_late) pdl_launch_dependents();
+  pdl_launch_dependents();
   pdl_wait();
   if (stamp && tid == 0) stamp[1] = global_ns();
 
@@ -843,7 +843,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     stage_x<BT>(p, stats, xs, k0 >> 3, sc.KS >> 3, tid);
   }
   __syncthreads();
-  if (p.trigger_late) pdl_launch_dependents();
   if (stamp && tid == 0) stamp[2] = global_ns();
   if constexpr (FT::ln1 || F == F_ANY) {
     // training forward: the LayerNorm statistics of every batch row, and the
