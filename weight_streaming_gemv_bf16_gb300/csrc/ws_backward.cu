@@ -74,11 +74,8 @@ struct alignas(64) BwdParams {
   float loss_scale;
   uint16_t* dz_out;         // the first launch: dz written back (this CTA's columns), or null
   const float* f_gelu;      // gelu'(t) of block j [B][w] fp32 (forward)
-  const uint16_t* f_ln;     // ln of block j [B][w] bf16 (forward)
-  uint16_t* f_dlin;         // dlin of block j [B][w] (this CTA's columns), or null
+  uint16_t* f_dlin;         // dlin of block j [B][w] (this CTA's columns)
   uint16_t* f_dln;          // dln of block j [B][w] (this CTA's columns)
-  uint16_t* f_dW;           // [w][w]
-  uint16_t* f_db;           // [w]
   int* err;
   unsigned long long timeout_ns;
   // shared-memory layout (bytes)
@@ -139,7 +136,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_mlp_backward(const __grid_co
   float* misc = reinterpret_cast<float*>(smem + p.off_misc);
   float* tot = misc;             // [2 BT] tail sums
   float* st = misc + 2 * BT;     // [2 BT] tail mean, rstd
-  float* lns = misc + 4 * BT;    // [BT][8] ln of the slab
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.B, w = p.w, nch = w >> 3;
   const int k0 = blockIdx.x * kSlab;
@@ -280,7 +276,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_mlp_backward(const __grid_co
         float4* d4 = reinterpret_cast<float4*>(dl + (size_t)b * p.dl_stride + 8 * c);
         d4[0] = make_float4(v[0], v[1], v[2], v[3]);
         d4[1] = make_float4(v[4], v[5], v[6], v[7]);
-        if (p.f_dlin && c == (k0 >> 3))
+        if (c == (k0 >> 3))
           reinterpret_cast<uint4*>(p.f_dlin)[o] =
               make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]),
                          pack2_bf16(v[4], v[5]), pack2_bf16(v[6], v[7]));
@@ -302,11 +298,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_mlp_backward(const __grid_co
     reinterpret_cast<__nv_bfloat16*>(p.t_dbeta)[k] = __float2bfloat16_rn(dbt);
   }
   if (!p.has_front) return;
-  // ln of the slab (the forward's, bf16) for dW
-  if (tid < B * kSlab) {
-    const int b = tid / kSlab, e = tid - b * kSlab;
-    lns[b * kSlab + e] = __uint_as_float((uint32_t)__ldg(p.f_ln + (size_t)b * w + k0 + e) << 16);
-  }
   __syncthreads();
 
   // ---- dln[:, slab] = dlin . W[:, slab] ----
@@ -352,15 +343,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_mlp_backward(const __grid_co
     }
   }
 
-  // ---- dW[:, slab] = dlin^T . ln[:, slab]; db for rows k0 .. k0+7 ----
-  for (int m = tid; m < w; m += kBwdThreads) {
+}
+
+// dW and db of every block, after the chain: dW_j[m][k] = bf16(sum_b
+// dlin_j[b][m] ln_j[b][k]), db_j[m] = bf16(sum_b dlin_j[b][m]).  Nothing
+// downstream of a block's backward reads them, so they are kept off the
+// chain of launches (each of which waits for all of the previous one's
+// stores) and written here in one pass at the HBM rate.  CTA (j, t) takes
+// rows m0 = t*kDwRows .. m0+kDwRows-1 of block j; a thread forms whole
+// 16-byte row chunks.  The sums run over b in order, as in the forward of
+// the reading.
+constexpr int kDwRows = 32;
+
+struct DwParams {
+  const uint16_t* dlin;  // [L][B][w] bf16
+  const uint16_t* ln;    // [L][B][w] bf16
+  uint16_t* const* dW;   // [L] pointers to [w][w] bf16
+  uint16_t* const* db;   // [L] pointers to [w] bf16
+  int B, w, tiles;       // tiles = w / kDwRows per block
+};
+
+__global__ void __launch_bounds__(kBwdThreads) k_mlp_dw(const __grid_constant__ DwParams p) {
+  extern __shared__ __align__(16) float dws[];
+  const int B = p.B, w = p.w;
+  const int j = blockIdx.x / p.tiles, m0 = (blockIdx.x - j * p.tiles) * kDwRows;
+  float* lnf = dws;                   // [B][w]
+  float* dlf = dws + (size_t)B * w;   // [B][kDwRows]
+  pdl_launch_dependents();
+  pdl_wait();
+  const size_t bw = (size_t)B * w;
+  const uint16_t* lnj = p.ln + (size_t)j * bw;
+  const uint16_t* dlj = p.dlin + (size_t)j * bw;
+  for (int i = threadIdx.x; i < B * w / 8; i += kBwdThreads) {
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(lnj) + i);
+    float4* d = reinterpret_cast<float4*>(lnf + 8 * i);
+    d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+    d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+  }
+  for (int i = threadIdx.x; i < B * kDwRows; i += kBwdThreads) {
+    const int b = i / kDwRows, r = i - b * kDwRows;
+    dlf[i] = __uint_as_float((uint32_t)__ldcg(dlj + (size_t)b * w + m0 + r) << 16);
+  }
+  __syncthreads();
+  const int nch = w / kSlab;
+  uint16_t* dW = p.dW[j];
+  for (int i = threadIdx.x; i < kDwRows * nch; i += kBwdThreads) {
+    const int r = i / nch, c = i - r * nch;
     float a[kSlab];
 #pragma unroll
     for (int e = 0; e < kSlab; ++e) a[e] = 0.f;
     for (int b = 0; b < B; ++b) {
-      const float d = dl[(size_t)b * p.dl_stride + m];
-      const float4 l0 = *reinterpret_cast<const float4*>(lns + b * kSlab);
-      const float4 l1 = *reinterpret_cast<const float4*>(lns + b * kSlab + 4);
+      const float d = dlf[b * kDwRows + r];
+      const float4 l0 = *reinterpret_cast<const float4*>(lnf + (size_t)b * w + kSlab * c);
+      const float4 l1 = *reinterpret_cast<const float4*>(lnf + (size_t)b * w + kSlab * c + 4);
       a[0] = fmaf(d, l0.x, a[0]);
       a[1] = fmaf(d, l0.y, a[1]);
       a[2] = fmaf(d, l0.z, a[2]);
@@ -370,15 +405,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_mlp_backward(const __grid_co
       a[6] = fmaf(d, l1.z, a[6]);
       a[7] = fmaf(d, l1.w, a[7]);
     }
-    reinterpret_cast<uint4*>(p.f_dW + (size_t)m * w + k0)[0] =
+    reinterpret_cast<uint4*>(dW + (size_t)(m0 + r) * w)[c] =
         make_uint4(pack2_bf16(a[0], a[1]), pack2_bf16(a[2], a[3]), pack2_bf16(a[4], a[5]),
                    pack2_bf16(a[6], a[7]));
   }
-  if (tid < kSlab) {
-    const int m = k0 + tid;
+  if (threadIdx.x < kDwRows) {
     float t = 0.f;
-    for (int b = 0; b < B; ++b) t += dl[(size_t)b * p.dl_stride + m];
-    reinterpret_cast<__nv_bfloat16*>(p.f_db)[m] = __float2bfloat16_rn(t);
+    for (int b = 0; b < B; ++b) t += dlf[b * kDwRows + threadIdx.x];
+    reinterpret_cast<__nv_bfloat16*>(p.db[j])[m0 + threadIdx.x] = __float2bfloat16_rn(t);
   }
 }
 
@@ -491,6 +525,10 @@ struct ws_mlp_backward {
   std::vector<BwdParams> launches;
   std::vector<std::pair<const void*, size_t>> reads;  // weight each launch reads (or empty)
   void* dln[2] = {nullptr, nullptr};
+  void* dlin_buf = nullptr;       // every block's dlin when no trace is given
+  uint16_t** d_tabs = nullptr;    // device tables: dW pointers, then db pointers
+  DwParams dw;
+  int dw_smem = 0;
   cudaStream_t cap = nullptr, side = nullptr;
   std::vector<cudaEvent_t> fork;
   cudaEvent_t join = nullptr;
@@ -508,6 +546,8 @@ static void bwd_free(ws_mlp_backward* c) {
   if (c->side) cudaStreamDestroy(c->side);
   for (void* d : c->dln)
     if (d) cudaFree(d);
+  if (c->dlin_buf) cudaFree(c->dlin_buf);
+  if (c->d_tabs) cudaFree(c->d_tabs);
   delete c;
 }
 
@@ -536,6 +576,24 @@ static ws_status bwd_enqueue(ws_mlp_backward* c, const ws_prefetch_plan& pl, boo
     const cudaError_t e = bwd_launch(c->launches[s], c->BT, st, c->o.use_pdl && s > 0);
     if (e != cudaSuccess) {
       set_error("backward launch %d failed: %s", s, cudaGetErrorString(e));
+      return WS_ERR_CUDA;
+    }
+  }
+  // dW and db of every block, once every dlin is written
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(c->L * c->dw.tiles);
+    cfg.blockDim = dim3(kBwdThreads);
+    cfg.dynamicSmemBytes = c->dw_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = c->o.use_pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_mlp_dw, c->dw);
+    if (e != cudaSuccess) {
+      set_error("dW launch failed: %s", cudaGetErrorString(e));
       return WS_ERR_CUDA;
     }
   }
@@ -637,6 +695,47 @@ ws_status ws_mlp_backward_create(const ws_mlp_block* blocks, const ws_mlp_grads*
     return o.dln_trace ? static_cast<uint16_t*>(o.dln_trace) + (size_t)j * bw
                        : static_cast<uint16_t*>(c->dln[j % 2]);
   };
+  // every block's dlin (the trace, or the handle's own rows) for the dW pass
+  void* dlin_base = o.dlin_trace;
+  if (!dlin_base) {
+    if (cudaMalloc(&c->dlin_buf, (size_t)n * bw * 2) != cudaSuccess) {
+      bwd_free(c);
+      return WS_ERR_NOMEM;
+    }
+    dlin_base = c->dlin_buf;
+  }
+  {
+    std::vector<uint16_t*> tw(n), tb(n);
+    for (int i = 0; i < n; ++i) {
+      tw[i] = static_cast<uint16_t*>(grads[i].dW);
+      tb[i] = static_cast<uint16_t*>(grads[i].db);
+    }
+    if (cudaMalloc((void**)&c->d_tabs, sizeof(uint16_t*) * 2 * n) != cudaSuccess) {
+      bwd_free(c);
+      return WS_ERR_NOMEM;
+    }
+    if (cudaMemcpy(c->d_tabs, tw.data(), sizeof(uint16_t*) * n, cudaMemcpyHostToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(c->d_tabs + n, tb.data(), sizeof(uint16_t*) * n, cudaMemcpyHostToDevice) !=
+            cudaSuccess) {
+      bwd_free(c);
+      return WS_ERR_CUDA;
+    }
+    c->dw.dlin = static_cast<const uint16_t*>(dlin_base);
+    c->dw.ln = static_cast<const uint16_t*>(o.ln);
+    c->dw.dW = c->d_tabs;
+    c->dw.db = c->d_tabs + n;
+    c->dw.B = B;
+    c->dw.w = w;
+    c->dw.tiles = w / kDwRows;
+    c->dw_smem = (int)(((size_t)B * w + (size_t)B * kDwRows) * 4);
+    if (cudaFuncSetAttribute(k_mlp_dw, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             c->dw_smem) != cudaSuccess) {
+      set_error("could not configure the dW kernel");
+      bwd_free(c);
+      return WS_ERR_CUDA;
+    }
+  }
   const int R = w < 256 ? w : 256, nbox = (w + R - 1) / R;
   for (int s = 0; s <= n; ++s) {
     BwdParams p;
@@ -668,11 +767,8 @@ ws_status ws_mlp_backward_create(const ws_mlp_block* blocks, const ws_mlp_grads*
         p.dz_out = bfw(o.dx_trace, (size_t)n * bw);
       }
       p.f_gelu = o.gelu_grad + (size_t)j * bw;
-      p.f_ln = bf(o.ln, (size_t)j * bw);
-      p.f_dlin = bfw(o.dlin_trace, (size_t)j * bw);
+      p.f_dlin = static_cast<uint16_t*>(dlin_base) + (size_t)j * bw;
       p.f_dln = dln_of(j);
-      p.f_dW = static_cast<uint16_t*>(grads[j].dW);
-      p.f_db = static_cast<uint16_t*>(grads[j].db);
       const cuuint64_t dims[2] = {(cuuint64_t)w, (cuuint64_t)w};
       const cuuint64_t strides[1] = {(cuuint64_t)w * 2};
       const cuuint32_t box[2] = {(cuuint32_t)kSlab, (cuuint32_t)R};
@@ -828,7 +924,7 @@ ws_status ws_mlp_backward_plan(const ws_mlp_backward* c, ws_prefetch_plan* plan,
 }
 
 int ws_mlp_backward_num_launches(const ws_mlp_backward* c) {
-  return c ? (int)c->launches.size() : 0;
+  return c ? (int)c->launches.size() + 1 : 0;
 }
 
 void ws_mlp_backward_destroy(ws_mlp_backward* c) { bwd_free(c); }
