@@ -681,14 +681,17 @@ def run_train(args):
         fwd = wc.mlp_chain(blocks, x, eps=sh.eps, training=True)
         fwd.chain.capture()
         fwd.run()
-        runs = {"none": wc.mlp_backward(blocks, fwd),
-                "tuned": wc.mlp_backward(blocks, fwd, prefetch=1, tune_pairs=30),
-                "decoy": wc.mlp_backward(blocks, fwd, prefetch=2, decoy=True,
-                                         fixed_plan=wb.PrefetchPlan(16, 256, 16384, 3))}
+        runs = {"none": wc.mlp_backward(blocks, fwd)}
+        if args.prefetch != "off":  # --prefetch off: the no-prefetch backward alone
+            runs["tuned"] = wc.mlp_backward(blocks, fwd, prefetch=1, tune_pairs=30)
+            runs["decoy"] = wc.mlp_backward(blocks, fwd, prefetch=2, decoy=True,
+                                            fixed_plan=wb.PrefetchPlan(16, 256, 16384, 3))
         t0 = time.perf_counter()
-        runs["tuned"].bwd.tune()
+        if "tuned" in runs:
+            runs["tuned"].bwd.tune()
         t_tune = time.perf_counter() - t0
-        (mode, nb, nt, stride), lo, mean = runs["tuned"].bwd.plan()
+        (mode, nb, nt, stride), lo, mean = (runs["tuned"].bwd.plan() if "tuned" in runs
+                                            else ((0, 0, 0, 0), float("nan"), float("nan")))
         for r in runs.values():
             r.bwd.capture()
 
@@ -705,7 +708,7 @@ def run_train(args):
             return a.elapsed_time(b) / n * 1e3
 
         n = max(20, min(args.steps, 400))
-        res = {"fwd_us": [], "none": [], "tuned": [], "decoy": []}
+        res = {"fwd_us": [], **{k: [] for k in runs}}
         ref = None
         for rnd in range(5):  # interleaved rounds
             res["fwd_us"].append(timed(lambda: fwd.run(st), n))
@@ -723,16 +726,18 @@ def run_train(args):
                                          "mean-square loss, bf16",
             "batch": B, "steps_per_round": n, "rounds": 5,
             "forward_us": round(med["fwd_us"], 2),
-            "step_us": {k: round(med[k], 2) for k in ("none", "tuned", "decoy")},
-            "backward_us": {k: round(med[k] - med["fwd_us"], 2) for k in ("none", "tuned", "decoy")},
-            "prefetch_gain_tuned": round(1 - med["tuned"] / med["none"], 4),
-            "prefetch_gain_decoy": round(1 - med["decoy"] / med["none"], 4),
+            "step_us": {k: round(med[k], 2) for k in runs},
+            "backward_us": {k: round(med[k] - med["fwd_us"], 2) for k in runs},
+            "prefetch_gain_tuned": (round(1 - med["tuned"] / med["none"], 4) if "tuned" in med
+                                    else None),
+            "prefetch_gain_decoy": (round(1 - med["decoy"] / med["none"], 4) if "decoy" in med
+                                    else None),
             "tuned_plan": {"mode": mode, "blocks": nb, "threads": nt, "stride": stride,
                            "gain_lower_95": round(lo, 4), "gain_mean": round(mean, 4),
                            "tune_seconds": round(t_tune, 2)},
             "bytes_per_step": step_bytes,
             "gbs_none": round(step_bytes / (med["none"] * 1e-6) / 1e9, 1),
-            "launches_per_step": L + (L + 1),
+            "launches_per_step": L + (L + 2),
             "gradients_bit_identical": True}), flush=True)
     return 0
 
