@@ -314,9 +314,10 @@ typedef struct {
    * [B][w]. */
   const void *x_in;
   void *y_out;
-  /* Optional per-block trace (for per-block checks; one copy per block):
-   * Qwen chains get h after every block, fp32 [L][B][H]; MLP chains get
-   * every block's output, bf16 [L][B][w]. */
+  /* Optional per-block trace (for per-block checks): Qwen chains get h
+   * after every block, fp32 [L][B][H] (a copy after each block); MLP chains
+   * get every block's output, bf16 [L][B][w] (written in place by the block,
+   * the last one copied from y_out). */
   float *h_trace;
   int use_pdl;          /* 1: programmatic dependent launch between ops      */
   int prefetch;         /* 0 off, 1 tuned plans, 2 fixed_plan for every op   */
@@ -429,7 +430,9 @@ void ws_chain_destroy(ws_chain *c);
  * and dx of block i is dz of block i - 1.  Sums in fp32 in a fixed order.
  * One launch per block (plus one for block 0's LayerNorm), replayed as one
  * CUDA graph with programmatic-dependent-launch edges; each launch streams
- * its weight with 2-D TMA in 8-column slabs, one slab per CTA.
+ * its weight with 2-D TMA in 8-column slabs, one slab per CTA.  dW and db of
+ * every block, which nothing in the chain reads, are formed by one more
+ * launch after it.
  * ---------------------------------------------------------------------- */
 typedef struct {
   void *dW, *db, *dgamma, *dbeta; /* bf16 [w][w], [w], [w], [w]: written */
@@ -483,6 +486,8 @@ ws_status ws_mlp_backward_run(ws_mlp_backward *c, ws_stream_t stream);
 /* The plan in use and its measured gain (95% CI lower bound, mean). */
 ws_status ws_mlp_backward_plan(const ws_mlp_backward *c, ws_prefetch_plan *plan, float *gain_lo,
                                float *gain_mean);
+/* Kernel launches per backward pass: one per block, one for block 0's
+ * LayerNorm, one for the dW and db of every block. */
 int ws_mlp_backward_num_launches(const ws_mlp_backward *c);
 void ws_mlp_backward_destroy(ws_mlp_backward *c);
 

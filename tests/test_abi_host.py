@@ -297,3 +297,57 @@ def test_bf16_plans_fit_every_k():
                     except wb.WsError:
                         continue
                     assert sc["smem_bytes"] <= 227 * 1024 and sc["NSW"] >= 2, (K, B, nmat, split)
+
+
+def test_chain_create_rejects_what_batch_tiles_do_not_cover(lib):
+    """Batches above 16 run in 16-row tiles: up to 128 rows, bf16 weights,
+    no attention, no training saves (checked before anything is allocated)."""
+    blk = wb.BlockDesc(kind=wb.BLOCK_QWEN)
+    blk.u.qwen = wb.QwenBlock(*([A] * 9), None, None, None, None, A, A)
+    blocks = (wb.BlockDesc * 1)(blk)
+    h = wb.P()
+
+    def create(**kw):
+        o = wb.ChainOpts(batch=32, hidden=768, kv_dim=256, inter=512, vocab=0, eps=1e-6,
+                         h_in=A, h_out=A + 4096)
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return lib.ws_chain_create(blocks, 1, wb.ctypes.byref(o), wb.ctypes.byref(h))
+    assert create(batch=129) == -3
+    assert create(weight_format=1) == -3
+    assert create(attention=1, s_max=256, pos=A) == -3
+    mlp = wb.BlockDesc(kind=wb.BLOCK_MLP)
+    mlp.u.mlp = wb.MlpBlock(A, A, A, A)
+    o = wb.ChainOpts(batch=17, hidden=768, eps=1e-5, x_in=A, y_out=A + 4096, mlp_gelu_grad=A)
+    assert lib.ws_chain_create((wb.BlockDesc * 1)(mlp), 1, wb.ctypes.byref(o),
+                               wb.ctypes.byref(h)) == -3
+    assert b"batch tiles" in lib.ws_last_error()
+
+
+def test_mlp_backward_create_validates_before_allocating(lib):
+    """The backward's shape, alignment and option checks (no GPU needed: they
+    come before any device call)."""
+    blocks = (wb.MlpBlock * 2)(wb.MlpBlock(A, A, A, A), wb.MlpBlock(A, A, A, A))
+    grads = (wb.MlpGrads * 2)(wb.MlpGrads(A, A, A, A), wb.MlpGrads(A, A, A, A))
+    h = wb.P()
+
+    def create(n=2, **kw):
+        o = wb.MlpBackwardOpts(batch=4, width=768, x_in=A, acts=A, ln=A, gelu_grad=A,
+                               ln_stats=A, dx=A, distance=1)
+        for k, v in kw.items():
+            setattr(o, k, v)
+        return lib.ws_mlp_backward_create(blocks, grads, n, wb.ctypes.byref(o), wb.ctypes.byref(h))
+    assert create(batch=0) == -3
+    assert create(batch=17) == -3
+    assert create(width=96) == -3        # not a multiple of 64
+    assert create(width=2048) == -3      # wider than 1024
+    assert create(distance=0) == -1
+    assert create(dx=None) == -2
+    assert create(acts=A + 8) == -2      # not 16-byte aligned
+    assert create(dln_trace=A + 2) == -2
+    assert create(n=0) == -1
+    bad = (wb.MlpGrads * 2)(wb.MlpGrads(A, A, A, A), wb.MlpGrads(A, None, A, A))
+    o = wb.MlpBackwardOpts(batch=4, width=768, x_in=A, acts=A, ln=A, gelu_grad=A, ln_stats=A,
+                           dx=A, distance=1)
+    assert lib.ws_mlp_backward_create(blocks, bad, 2, wb.ctypes.byref(o), wb.ctypes.byref(h)) == -2
+    assert lib.ws_last_error()
