@@ -93,7 +93,7 @@ struct Sched {
   // memory (both odd multiples of 16 bytes: ldmatrix rows in distinct banks)
   int mma, prow, xrs;
   int form;      // its chain form (F_ANY for none)
-  int off_xsum;  // 4-bit weights: sums of 32 staged activations, [BT][KS / 32] fp32
+  int off_xsum;  // 4-bit weights: sums of 16 staged activations, [BT][KS / 16] fp32
                  // (tensor-core kernel: of 128, [8][KS / 128])
   int off_xzero;  // 4-bit weights, tensor-core kernel: a 16-byte zero row
 };

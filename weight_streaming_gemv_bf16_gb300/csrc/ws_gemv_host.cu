@@ -453,7 +453,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   off = sc.off_xs + align_up(sc.BT * sc.KS * 2, 128);
   if (q4) {
     sc.off_xsum = off;
-    off += align_up(sc.BT * (sc.KS / 32) * 4, 128);
+    off += align_up(sc.BT * (sc.KS / 16) * 4, 128);
   }
   sc.off_ring = align_up(off, 128);
   // 4-bit rows: pieces are 3.76 times smaller for the same rows, so the ring

@@ -622,34 +622,35 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t w, int j) {
 
 // Dot products of one ring piece of 4-bit rows against the staged
 // activations.  The piece holds NMAT x RT rows pst bytes apart, each len
-// columns of whole super-groups.  Lane l takes 32-column chunks l, l + 32,
-// ...: a 16-byte code chunk (four words, 32 weights) and its group's (s, z)
-// per row, four activation chunks and their sum X per batch row.  With
-// t = sum (128 + q) x (mixed fma: bf16 operands, exact products, fp32 sums),
-// s t + (z - 136 s) X = sum (s (q - 8) + z) x.
+// columns of whole super-groups.  Lane l takes 16-column chunks l, l + 32,
+// ...: two code words (16 weights) and their group's (s, z) per row, two
+// activation chunks and their sum X per batch row.  (16-column chunks keep
+// every lane of a warp busy on a 1536-column row: 96 chunks, three a lane.)
+// With t = sum (128 + q) x (mixed fma: bf16 operands, exact products, fp32
+// sums), s t + (z - 136 s) X = sum (s (q - 8) + z) x.
 template <int BT, int NMAT, int RT>
 __device__ __forceinline__ void dot_piece_q4(float (&acc)[2][4][BT], const uint8_t* st, int pst,
                                              const uint4* xs, const float* xsum, int len,
-                                             int nchx, int nx32, int lane) {
-  const int nc = len >> 5, ngr = len >> 7;
+                                             int nchx, int nx16, int lane) {
+  const int nc = len >> 4, ngr = len >> 7;
 #pragma unroll 1
   for (int c = lane; c < nc; c += 32) {
-    const int u = c >> 4, w = c & 15;
+    const int u = c >> 5, w = c & 31;    // super-group, 16-column chunk within it
     const int gu = min(4, ngr - 4 * u);  // groups of super-group u
-    const int off = u * kQ4SuperBytes + w * 16;
-    const int soff = u * kQ4SuperBytes + gu * 64 + (w >> 2) * 4;
-    uint32_t qp[NMAT][RT][16];
+    const int off = u * kQ4SuperBytes + w * 8;
+    const int soff = u * kQ4SuperBytes + gu * 64 + (w >> 3) * 4;
+    uint32_t qp[NMAT][RT][8];
     float sc[NMAT][RT], zc[NMAT][RT];
 #pragma unroll
     for (int m = 0; m < NMAT; ++m)
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
         const uint8_t* row = st + (size_t)(m * RT + r) * pst;
-        const uint4 q = *reinterpret_cast<const uint4*>(row + off);
+        const uint2 q = *reinterpret_cast<const uint2*>(row + off);
         const uint32_t sz = *reinterpret_cast<const uint32_t*>(row + soff);
-        const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+        const uint32_t qw[2] = {q.x, q.y};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) qp[m][r][4 * i + jj] = q4_pair(qw[i], jj);
         sc[m][r] = bf16lo(sz);
@@ -657,18 +658,17 @@ __device__ __forceinline__ void dot_piece_q4(float (&acc)[2][4][BT], const uint8
       }
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
-      const uint4* xb = xs + (size_t)b * nchx + 4 * c;
-      const uint4 x0 = xb[0], x1 = xb[1], x2 = xb[2], x3 = xb[3];
-      const uint32_t xw[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
-                               x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
-      const float X = xsum[b * nx32 + c];
+      const uint4* xb = xs + (size_t)b * nchx + 2 * c;
+      const uint4 x0 = xb[0], x1 = xb[1];
+      const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float X = xsum[b * nx16 + c];
 #pragma unroll
       for (int m = 0; m < NMAT; ++m)
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
           float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
+          for (int e = 0; e < 8; e += 2) {
             t0 = fma_bf16x2(qp[m][r][e], xw[e], t0);
             t1 = fma_bf16x2(qp[m][r][e + 1], xw[e + 1], t1);
           }
@@ -868,15 +868,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
   float* xsum = Q4 ? reinterpret_cast<float*>(smem + sc.off_xsum) : nullptr;
   if constexpr (Q4) {
-    // per batch row the sum of every 32 staged (rounded) activations, in
+    // per batch row the sum of every 16 staged (rounded) activations, in
     // column order
-    const int n32 = sc.KS >> 5;
-    for (int o = tid; o < BT * n32; o += kThreads) {
-      const int b = o / n32, c = o - b * n32;
-      const uint4* src = xs4 + (size_t)b * nchx + 4 * c;
+    const int n16 = sc.KS >> 4;
+    for (int o = tid; o < BT * n16; o += kThreads) {
+      const int b = o / n16, c = o - b * n16;
+      const uint4* src = xs4 + (size_t)b * nchx + 2 * c;
       float sum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         const uint4 v = src[i];
         sum += bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y);
         sum += bf16lo(v.z) + bf16hi(v.z) + bf16lo(v.w) + bf16hi(v.w);
@@ -922,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
     // unrolled (ncu at batch 16: "no instruction" the top stall)
     if constexpr (Q4) {
       dot_piece_q4<BT, NMAT, RT>(acc, reinterpret_cast<const uint8_t*>(st), q4_prefix(sc.PC),
-                                 xs4 + j * ncp, xsum + j * (sc.PC >> 5), len, nchx, sc.KS >> 5,
+                                 xs4 + j * ncp, xsum + j * (sc.PC >> 4), len, nchx, sc.KS >> 4,
                                  lane);
     } else {
       dot_piece<BT, NMAT, RT, ((F != F_ANY && BT == 1) || BT >= 8) ? 1 : 2>(
