@@ -508,6 +508,34 @@ def test_mlp_chain_72_blocks(B):
         assert torch.equal(pch.y_out.cpu(), ch.y_out.cpu())
 
 
+@pytest.mark.parametrize("B", [4, 16])
+def test_mlp_step_host_matches_device_run(B):
+    """The LayerNorm chain's host step: x from a pinned host buffer, the
+    output back to one, one graph launch (the word copies chained to the
+    first and last op), equal bit for bit to the device-input run."""
+    sh = synth.MlpShape(blocks=12)
+    blocks = [synth.mlp_block_weights(sh, 4, i) for i in range(sh.blocks)]
+    x = synth.mlp_input(sh, B, 4)
+    ch = wc.mlp_chain([_dev(b) for b in blocks], dev_bf16(x))
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    ref = ch.y_out.cpu().clone()
+    x_host = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+    out = torch.zeros((B, sh.width), dtype=torch.int16).pin_memory()
+    for _ in range(3):
+        out.fill_(0)
+        ch.chain.step_host(x_host, None, out)
+        assert torch.equal(out.view(torch.bfloat16), ref)
+    x2 = synth.mlp_input(sh, B, 5)
+    x_host.copy_(torch.from_numpy(np.ascontiguousarray(x2).view(np.int16)))
+    ch.chain.step_host(x_host, None, out)
+    ch.x_in.copy_(dev_bf16(x2))
+    ch.run()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.bfloat16), ch.y_out.cpu())
+
+
 @pytest.mark.parametrize("persistent,B", [(False, 4), (True, 4), (True, 1), (False, 16)])
 def test_mlp_chain_72_blocks_trace(persistent, B):
     """Every block of the 72-block chain, teacher-forced on the chain's own

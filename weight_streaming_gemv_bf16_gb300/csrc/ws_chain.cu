@@ -516,9 +516,12 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
                              const std::vector<std::vector<std::pair<const void*, size_t>>>& reads,
                              const std::vector<ws_prefetch_plan>& plans, int distance,
                              bool decoy, cudaStream_t stream, const std::vector<int>& trace,
-                             bool use_pdl) {
+                             bool use_pdl, bool after_kernel = false,
+                             bool* ends_kernel = nullptr) {
   const int n = (int)ps.size();
-  bool forked = false, prev_kernel = false;
+  // after_kernel: the node before the first op is a kernel (the copy of a
+  // host step's inputs), so the first op may start as its dependent
+  bool forked = false, prev_kernel = after_kernel;
   for (int i = 0; i < n; ++i) {
     const int j = i + distance;
     if (j < n && plans[j].mode != WS_PREFETCH_NONE) {
@@ -562,13 +565,14 @@ static ws_status enqueue_ops(ws_chain* c, const std::vector<GemvParams>& ps,
     if (cudaEventRecord(c->join_ev, c->side) != cudaSuccess) return WS_ERR_CUDA;
     if (cudaStreamWaitEvent(stream, c->join_ev, 0) != cudaSuccess) return WS_ERR_CUDA;
   }
+  if (ends_kernel) *ends_kernel = prev_kernel && !forked;
   return WS_OK;
 }
 
 namespace ws {
 // word copies between device-accessible buffers (ws_misc.cu)
 cudaError_t launch_copy_words(void* d0, const void* s0, size_t b0, void* d1, const void* s1,
-                              size_t b1, cudaStream_t stream);
+                              size_t b1, cudaStream_t stream, bool pdl);
 }  // namespace ws
 
 // Host buffers of one ws_chain_step_host graph, and their device aliases
@@ -595,8 +599,9 @@ static void* mapped_alias(const void* p) {
   return ((uintptr_t)a.devicePointer & 3u) ? nullptr : a.devicePointer;
 }
 
-static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st);
-static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st);
+static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st,
+                                 bool* by_kernel);
+static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st, bool pdl);
 
 // Capture the ops (with prefetches and trace copies) into *out; with io, the
 // copies of ws_chain_step_host's inputs come first and its result copy last.
@@ -611,12 +616,17 @@ static ws_status capture_graph(ws_chain* c, const std::vector<GemvParams>& ps,
     set_error("cudaStreamBeginCapture failed");
     return WS_ERR_CUDA;
   }
-  ws_status s = io ? enqueue_host_in(c, *io, stream) : WS_OK;
+  // with a host step's word copies, the first op starts as a programmatic
+  // dependent of the input copy, and the output copy of the last op
+  bool in_kernel = false, out_pdl = false;
+  ws_status s = io ? enqueue_host_in(c, *io, stream, &in_kernel) : WS_OK;
   if (s == WS_OK)
     s = c->persistent ? (launch_persistent(c->persist, stream) == cudaSuccess ? WS_OK : WS_ERR_CUDA)
                       : enqueue_ops(c, ps, reads, plans, c->o.distance, decoy, stream, trace,
-                                    c->o.use_pdl != 0);
-  if (s == WS_OK && io) s = enqueue_host_out(c, *io, stream);
+                                    c->o.use_pdl != 0, in_kernel && c->o.use_pdl != 0,
+                                    &out_pdl);
+  if (s == WS_OK && io)
+    s = enqueue_host_out(c, *io, stream, out_pdl && !c->persistent && c->o.use_pdl != 0);
   const cudaError_t e = cudaStreamEndCapture(stream, &g);
   if (s != WS_OK || e != cudaSuccess) {
     if (g) cudaGraphDestroy(g);
@@ -655,14 +665,18 @@ static std::vector<std::vector<std::pair<const void*, size_t>>> chain_reads(cons
 // The copies of one step's inputs from host buffers to the chain's device
 // inputs (Qwen: fp32 h and, if given, the bf16 attention stand-ins of every
 // block; MLP: bf16 x), and of its result back.
-static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st) {
+static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st,
+                                 bool* by_kernel) {
   const int B = c->o.batch, H = c->o.hidden;
+  *by_kernel = false;
   if (c->n_mlp) {
-    if (io.in_d)  // one word-copy launch reading the mapped host buffer
+    if (io.in_d) {  // one word-copy launch reading the mapped host buffer
+      *by_kernel = true;
       return launch_copy_words(const_cast<void*>(c->o.x_in), io.in_d, (size_t)B * H * 2, nullptr,
-                               nullptr, 0, st) == cudaSuccess
+                               nullptr, 0, st, false) == cudaSuccess
                  ? WS_OK
                  : WS_ERR_CUDA;
+    }
     return cudaMemcpyAsync(const_cast<void*>(c->o.x_in), io.in, (size_t)B * H * 2,
                            cudaMemcpyHostToDevice, st) == cudaSuccess
                ? WS_OK
@@ -677,10 +691,12 @@ static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st)
   const bool with_attn = io.attn && !c->attn_dev.empty();
   if (io.in_d && (!with_attn || (io.attn_d && contiguous))) {
     // h and every block's attention input in one word-copy launch
+    *by_kernel = true;
     return launch_copy_words(const_cast<float*>(c->o.h_in), io.in_d, (size_t)B * H * 4,
                              with_attn ? const_cast<void*>(c->attn_dev[0]) : nullptr,
                              with_attn ? io.attn_d : nullptr,
-                             with_attn ? blk * c->attn_dev.size() : 0, st) == cudaSuccess
+                             with_attn ? blk * c->attn_dev.size() : 0, st,
+                             false) == cudaSuccess
                ? WS_OK
                : WS_ERR_CUDA;
   }
@@ -702,7 +718,7 @@ static ws_status enqueue_host_in(ws_chain* c, const HostIO& io, cudaStream_t st)
   return WS_OK;
 }
 
-static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st) {
+static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st, bool pdl) {
   const int B = c->o.batch, H = c->o.hidden;
   const void* src;
   size_t bytes;
@@ -717,7 +733,7 @@ static ws_status enqueue_host_out(ws_chain* c, const HostIO& io, cudaStream_t st
     bytes = (size_t)B * H * 4;
   }
   if (io.out_d)  // written through the mapped host buffer by one word-copy launch
-    return launch_copy_words(io.out_d, src, bytes, nullptr, nullptr, 0, st) == cudaSuccess
+    return launch_copy_words(io.out_d, src, bytes, nullptr, nullptr, 0, st, pdl) == cudaSuccess
                ? WS_OK
                : WS_ERR_CUDA;
   return cudaMemcpyAsync(io.out, src, bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess
@@ -1176,9 +1192,10 @@ ws_status ws_chain_step_host(ws_chain* c, const void* in_host, const void* attn_
       return WS_ERR_CUDA;
     }
   } else {
-    ws_status s = enqueue_host_in(c, io, st);
+    bool by_kernel = false;
+    ws_status s = enqueue_host_in(c, io, st, &by_kernel);
     if (s == WS_OK) s = ws_chain_run(c, stream);
-    if (s == WS_OK) s = enqueue_host_out(c, io, st);
+    if (s == WS_OK) s = enqueue_host_out(c, io, st, false);
     if (s != WS_OK) return s;
   }
   const cudaError_t e = cudaStreamSynchronize(st);

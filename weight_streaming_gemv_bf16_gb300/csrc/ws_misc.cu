@@ -245,8 +245,13 @@ __global__ void k_test_bounded_wait(unsigned long long timeout_ns, int* err) {
 // bytes a multiple of 4, 4-byte aligned.  SMs move the few kilobytes of a
 // decode step's inputs with one launch instead of a copy-engine transfer
 // per buffer.
+// Launched as a programmatic dependent of the kernel before it, it waits
+// for that kernel's results before copying; the kernel after it may start
+// (and stream its weights) at once, and waits for the copy before it reads.
 __global__ void __launch_bounds__(256) k_copy_words(uint32_t* d0, const uint32_t* s0, long long n0,
                                                     uint32_t* d1, const uint32_t* s1, long long n1) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = t; i < n0; i += stride) d0[i] = s0[i];
@@ -254,17 +259,24 @@ __global__ void __launch_bounds__(256) k_copy_words(uint32_t* d0, const uint32_t
 }
 
 cudaError_t launch_copy_words(void* d0, const void* s0, size_t b0, void* d1, const void* s1,
-                              size_t b1, cudaStream_t stream) {
+                              size_t b1, cudaStream_t stream, bool pdl) {
   const long long n0 = (long long)(b0 / 4), n1 = (long long)(b1 / 4);
   const long long n = n0 > n1 ? n0 : n1;
   int blocks = (int)((n + 255) / 256);
   if (blocks < 1) blocks = 1;
   if (blocks > 148) blocks = 148;
-  k_copy_words<<<blocks, 256, 0, stream>>>(static_cast<uint32_t*>(d0),
-                                           static_cast<const uint32_t*>(s0), n0,
-                                           static_cast<uint32_t*>(d1),
-                                           static_cast<const uint32_t*>(s1), n1);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_copy_words, static_cast<uint32_t*>(d0),
+                            static_cast<const uint32_t*>(s0), n0, static_cast<uint32_t*>(d1),
+                            static_cast<const uint32_t*>(s1), n1);
 }
 
 size_t argmax_rows_workspace(int rows, int cols) {
