@@ -50,7 +50,7 @@
 
 namespace ws {
 
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 512;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kSlab = 8;         // columns per CTA (16 bytes of bf16: one TMA box row)
 constexpr int kBwdMaxWidth = 1024;
