@@ -54,6 +54,12 @@ constexpr int kBwdThreads = 512;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kSlab = 8;         // columns per CTA (16 bytes of bf16: one TMA box row)
 constexpr int kBwdMaxWidth = 1024;
+constexpr int kBwdWidthUnit = 64;  // widths are multiples of this
+// The transposed product gives each warp w / kBwdWarps rows of dlin, read
+// four rows at a time as aligned float4: every allowed width must give each
+// warp a multiple of four rows.
+static_assert(kBwdWidthUnit % (4 * kBwdWarps) == 0,
+              "each warp's rows of the transposed product must be a multiple of four");
 
 struct alignas(64) BwdParams {
   CUtensorMap tmW;  // the block's W [w rows][w columns] bf16, box {8, R}
@@ -642,8 +648,9 @@ ws_status ws_mlp_backward_create(const ws_mlp_block* blocks, const ws_mlp_grads*
   *out = nullptr;
   const ws_mlp_backward_opts& o = *opts;
   const int B = o.batch, w = o.width;
-  if (B < 1 || B > kMaxBatch || w < 64 || w > kBwdMaxWidth || w % 64 != 0) {
-    set_error("bad shape B=%d w=%d (need 1<=B<=16, 64<=w<=%d, w%%64==0)", B, w, kBwdMaxWidth);
+  if (B < 1 || B > kMaxBatch || w < kBwdWidthUnit || w > kBwdMaxWidth || w % kBwdWidthUnit != 0) {
+    set_error("bad shape B=%d w=%d (need 1<=B<=16, %d<=w<=%d, w a multiple of %d)", B, w,
+              kBwdWidthUnit, kBwdMaxWidth, kBwdWidthUnit);
     return WS_ERR_SHAPE;
   }
   if (o.distance < 1) {
