@@ -395,7 +395,8 @@ int ws_chain_num_ops(const ws_chain *c);
 /* 1 if the chain runs as one persistent kernel per step, else 0. */
 int ws_chain_is_persistent(const ws_chain *c);
 /* Diagnostics.  ws_chain_grid: the CTA dimension of the stamp buffer (the
- * persistent kernel's grid, else the SM count, the largest grid of any op).
+ * persistent kernel's grid, else the largest grid of any op: an op may run
+ * more than one CTA per SM).
  * ws_chain_debug_stamps: a device buffer (uint64 [grid][ops][44], or NULL to
  * stop) where every later-captured step records globaltimer ns per CTA and
  * op.  Persistent chains: at the op's start (after its grid barrier), after
@@ -544,6 +545,17 @@ typedef struct {
                           launch runs on CUDA cores, the vector-product
                           design.  Sums are ordered differently; both stay
                           within the fp32 tolerance of the oracle.           */
+  int ctas_per_sm;     /* CUDA-core launches: CTAs each SM holds at once, 1..3;
+                          the grid is that many per SM and every CTA's shared
+                          memory (rings included) is sized so that they fit.
+                          0 (default): the planner's choice -- two for 4-bit
+                          rows at batch 1, else one.  A plan whose kernel's
+                          registers or shared memory would not let that many
+                          CTAs share an SM falls back to one.                */
+  int q4_mma;          /* 4-bit ops of a chain form with at least two 16-row
+                          tasks per warp (the LM head) run on the tensor-core
+                          kernel: 1 (default) at batch 2..4, 2 at every
+                          batch 1..4, 0 never (the CUDA-core kernel).       */
 } ws_tuning;
 
 void ws_get_tuning(ws_tuning *t);

@@ -1,6 +1,8 @@
 """Shared helpers for the tests: device transfer of bit patterns and the
 comparison metrics (fp32: |g - r| / max(|r|, rms(r)) <= 2e-3 per row; bf16 and
 fp16: at most 1 unit in the last place)."""
+import contextlib
+
 import numpy as np
 import torch
 
@@ -19,6 +21,23 @@ def note_ulps(what: str, max_ulp: int, frac_1ulp: float):
     old = ULP_SEEN.get(key)
     if old is None or max_ulp > old[0] or frac_1ulp < old[1]:
         ULP_SEEN[key] = (max(max_ulp, old[0] if old else 0), min(frac_1ulp, old[1] if old else 1.0))
+
+
+@contextlib.contextmanager
+def tuning(**fields):
+    """The library's tuning with the given fields changed, restored after."""
+    from weight_streaming_gemv_bf16_gb300 import binding as wb
+    base = wb.get_tuning()
+    t = wb.Tuning()
+    for f, _ in wb.Tuning._fields_:
+        setattr(t, f, getattr(base, f))
+    for k, v in fields.items():
+        setattr(t, k, v)
+    wb.set_tuning(t)
+    try:
+        yield
+    finally:
+        wb.set_tuning(base)
 
 
 def dev_bf16(bits, device="cuda"):

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 from weight_streaming_gemv_bf16_gb300 import binding as wb
+from _util import tuning
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -208,6 +209,11 @@ Q4_MMA_SHAPES = [
 @pytest.mark.parametrize("M,K,B,nmat,mma", [s + (False,) for s in Q4_SHAPES] +
                          [s + (True,) for s in Q4_MMA_SHAPES])
 def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, mma):
+    with tuning(q4_mma=2):  # the tensor-core plan at batch 1 too
+        _q4_copies_check(M, K, B, nmat, mma)
+
+
+def _q4_copies_check(M, K, B, nmat, mma):
     rb = wb.q4_row_bytes(K)
     _, sc = wb.debug_gemv_copies_q4(M, K, B, nmat, 0, mma)
     assert sc["smem_bytes"] <= 227 * 1024 and 2 <= sc["NSW"] <= 8
@@ -227,6 +233,23 @@ def test_q4_bulk_copies_in_bounds_aligned_and_covering(lib, M, K, B, nmat, mma):
             assert warp < 8 and slot < sc["NSW"] and off + n <= sc["piece_bytes"]
             covered[src // 16:(src + n) // 16] += 1
     assert covered.min() == 1 and covered.max() == 1
+
+
+@pytest.mark.parametrize("M,K,nmat", [(2048, 1536, 1), (1536, 1536, 1), (8960, 1536, 2),
+                                      (1536, 8960, 1), (151936, 1536, 1)])
+def test_q4_batch1_plans_hold_two_ctas_per_sm(lib, M, K, nmat):
+    """4-bit rows at batch 1 (the decode chain's shapes) plan two CTAs per SM:
+    twice the grid of batch 4 and shared memory that leaves room for a
+    second CTA (228 KB an SM, 1 KB of it kept per CTA); bf16 rows keep one."""
+    _, b1 = wb.debug_gemv_copies_q4(M, K, 1, nmat, 0, 0)
+    _, b4 = wb.debug_gemv_copies_q4(M, K, 4, nmat, 0, 0)
+    assert b1["grid"] == 2 * b4["grid"]
+    assert 2 * (b1["smem_bytes"] + 1024) <= 228 * 1024 and b1["NSW"] >= 2
+    with tuning(ctas_per_sm=1):
+        _, one = wb.debug_gemv_copies_q4(M, K, 1, nmat, 0, 0)
+    assert one["grid"] == b4["grid"]
+    bf = wb.gemv_plan(M, K, 1, nmat=nmat, allow_split=False)
+    assert bf["grid"] <= b4["grid"]
 
 
 def test_workspace_sizes(lib):

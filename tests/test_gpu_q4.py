@@ -12,7 +12,7 @@ from oracle import q4 as oq4
 from weight_streaming_gemv_bf16_gb300 import binding as wb
 from weight_streaming_gemv_bf16_gb300 import chain as wc
 from weight_streaming_gemv_bf16_gb300 import synth
-from _util import assert_fp32, dev_bf16, dev_f32, host_bits
+from _util import assert_fp32, dev_bf16, dev_f32, host_bits, tuning
 
 pytestmark = pytest.mark.gpu
 
@@ -141,8 +141,9 @@ def test_gemv_q4_tensor_core_kernel(M, K, B):
     assert np.array_equal(Wq.cpu().numpy()[rows], ref)
     x = synth.normal_bf16((B, K), 1.0, M + B, "q4/xbig")
     y = torch.full((B, M), float("nan"), device="cuda")
-    wb.gemv_q4(Wq, dev_bf16(x), y, K)
-    torch.cuda.synchronize()
+    with tuning(q4_mma=2):  # batch 1 too
+        wb.gemv_q4(Wq, dev_bf16(x), y, K)
+        torch.cuda.synchronize()
     assert_fp32(y.cpu().numpy()[:, rows], oq4.gemv(ref, K, oracle.bf16_to_f64(x)),
                 what=f"{M}x{K} B={B}")
 
@@ -150,6 +151,18 @@ def test_gemv_q4_tensor_core_kernel(M, K, B):
 @pytest.mark.parametrize("B", [1, 4])
 def test_q4_chain_with_a_tensor_core_lm_head(B):
     """A vocabulary of 40000 rows puts the LM head (RMSNorm, argmax) on the
-    tensor-core 4-bit kernel."""
+    tensor-core 4-bit kernel (at batch 1 only when asked for)."""
     shape = synth.QwenShape(hidden=256, kv_dim=64, inter=512, vocab=40000, layers=1)
-    _q4_chain_check(B, shape)
+    with tuning(q4_mma=2):
+        _q4_chain_check(B, shape)
+
+
+@pytest.mark.parametrize("cps", [1, 2, 3])
+@pytest.mark.parametrize("B", [1, 4])
+def test_q4_chain_at_every_residency(B, cps):
+    """The CUDA-core 4-bit plans for one, two and three CTAs per SM (rings
+    and grids sized for each; a vocabulary of 40000 on CUDA cores too) all
+    match the oracle."""
+    shape = synth.QwenShape(hidden=256, kv_dim=64, inter=1408, vocab=40000, layers=2)
+    with tuning(ctas_per_sm=cps, q4_mma=0):
+        _q4_chain_check(B, shape)

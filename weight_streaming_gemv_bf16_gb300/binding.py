@@ -92,7 +92,8 @@ class Tuning(C.Structure):
     _fields_ = [("ring_bytes", I32), ("grid_cap", I32), ("force_ksplit", I32),
                 ("force_rt", I32), ("evict_first", I32), ("piece_bytes", I32),
                 ("timeout_ns", C.c_ulonglong), ("l2_ahead", I32),
-                ("forms", I32), ("launch_pdl", I32), ("mma", I32)]
+                ("forms", I32), ("launch_pdl", I32), ("mma", I32), ("ctas_per_sm", I32),
+                ("q4_mma", I32)]
 
 
 class GemvSchedule(C.Structure):

@@ -1229,7 +1229,11 @@ ws_status ws_chain_debug_stamps(ws_chain* c, unsigned long long* stamps, size_t 
 
 int ws_chain_grid(const ws_chain* c) {
   if (!c) return 0;
-  return c->persistent ? c->persist.grid : device_sm_count();
+  if (c->persistent) return c->persist.grid;
+  // every CTA of every op writes its own row: the largest grid of any op
+  int g = 0;
+  for (const ChainOp& op : c->ops) g = op.p.sc.grid > g ? op.p.sc.grid : g;
+  return g;
 }
 
 ws_status ws_chain_plans(const ws_chain* c, ws_prefetch_plan* plans, float* gain_lo,

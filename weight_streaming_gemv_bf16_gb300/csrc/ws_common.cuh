@@ -293,6 +293,8 @@ struct Tuning {
   int forms;         // 1: launches of a known form run that form's kernel (0: the general one)
   int launch_pdl;    // 1: standalone GEMV launches carry the programmatic-dependent-launch attribute
   int mma;           // 1: large chain-form ops at batch tiles 8 and 16 run on tensor cores (mma.sync)
+  int ctas_per_sm;   // CUDA-core launches: CTAs resident per SM (0: the planner's choice)
+  int q4_mma;        // 4-bit ops with two 16-row tasks per warp or more on tensor cores: 1 at B 2..4, 2 always
 };
 
 // Host-side helpers implemented in ws_gemv.cu / ws_misc.cu.

@@ -34,7 +34,7 @@ void set_error(const char* fmt, ...) {
 }
 
 Tuning& tuning() {
-  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 0};
+  static Tuning t = {96 * 1024, 0, 0, 0, 1, 12288, 2000000000ull, 0, 1, 0, 0, 0, 1};
   return t;
 }
 
@@ -77,6 +77,25 @@ static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 static constexpr int kXsMax = 96 * 1024;  // activations in shared memory without a K split
 static constexpr int kSmemMax = 227 * 1024;
+static constexpr int kSmemReserved = 1024;  // shared memory the runtime keeps per resident CTA
+
+// Shared memory of one SM of the current device (228 KB on GB300).
+static int smem_per_sm() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 228 * 1024;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        n <= 0)
+      n = 228 * 1024;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static int resident_ctas(const GemvParams& p);
 
 static int row_groups(GemvParams& p, int RT) {
   int RG = 0;
@@ -308,16 +327,16 @@ static bool plan_gemv_q4mma(GemvParams& p, int grid_target) {
   return true;
 }
 
-// Choose the schedule.  force_S > 0 fixes the K split; force_S == 0 lets the
-// heuristic split skinny shapes; force_S < 0 forbids splitting.
-bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
+// Schedule of the CUDA-core kernel with `cps` CTAs resident per SM: the grid
+// targets cps CTAs per SM and the shared memory of each (activations, rings,
+// residual rows) stays within the SM's share for that many.
+static bool plan_gemv_cc(GemvParams& p, int force_S, int cps, char* why, size_t why_len) {
   const Tuning& tu = tuning();
   const int nsm = device_sm_count();
-  const int grid_target = tu.grid_cap > 0 ? tu.grid_cap : nsm;
+  const int grid_target = tu.grid_cap > 0 ? tu.grid_cap : nsm * cps;
   const int warps_total = grid_target * kWarps;
   const bool q4 = p.wfmt == WF_Q4;
-  if (!q4 && tu.mma && tu.forms && plan_gemv_mma(p, force_S, grid_target)) return true;
-  if (q4 && tu.forms && plan_gemv_q4mma(p, grid_target)) return true;
+  const int smem_cap = cps > 1 ? smem_per_sm() / cps - kSmemReserved : kSmemMax;
   Sched sc;
   memset(&sc, 0, sizeof sc);
   sc.BT = batch_template(p.B);
@@ -461,20 +480,20 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   // (measured on the 4-bit chain: the LM head 87 -> 55 us, gate/up 11.5 ->
   // 9.2 us)
   int ring_budget =
-      tu.ring_bytes > 0 ? tu.ring_bytes : (q4 ? kSmemMax - sc.off_ring - 4096 : 96 * 1024);
-  if (sc.off_ring + ring_budget > kSmemMax) ring_budget = kSmemMax - sc.off_ring;
+      tu.ring_bytes > 0 ? tu.ring_bytes : (q4 ? smem_cap - sc.off_ring - 4096 : 96 * 1024);
+  if (sc.off_ring + ring_budget > smem_cap) ring_budget = smem_cap - sc.off_ring;
   int NSW = ring_budget / (kWarps * sc.piece_bytes);
   if (NSW > kMaxStages) NSW = kMaxStages;
   if (NSW < 2) {
-    if (sc.off_ring + 2 * kWarps * sc.piece_bytes > kSmemMax) {
+    if (sc.off_ring + 2 * kWarps * sc.piece_bytes > smem_cap) {
       // smaller pieces, so that two stages per warp fit beside the activations
       int pc_fit =
-          q4 ? (kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * kQ4SuperBytes) * kQ4Super
-             : ((kSmemMax - sc.off_ring) / (2 * kWarps) / (nmat * RT * 2)) & ~7;
+          q4 ? (smem_cap - sc.off_ring) / (2 * kWarps) / (nmat * RT * kQ4SuperBytes) * kQ4Super
+             : ((smem_cap - sc.off_ring) / (2 * kWarps) / (nmat * RT * 2)) & ~7;
       // each piece is rounded up to 128 bytes: shrink until that still fits
       while (pc_fit >= pc_unit &&
              sc.off_ring + 2 * kWarps * align_up(nmat * RT * piece_row_bytes(pc_fit), 128) >
-                 kSmemMax)
+                 smem_cap)
         pc_fit -= pc_unit;
       if (pc_fit < pc_unit) {
         snprintf(why, why_len, "no two ring stages per warp fit beside %d bytes of activations",
@@ -490,7 +509,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   }
   sc.NSW = NSW;
   sc.smem_bytes = sc.off_ring + kWarps * NSW * sc.piece_bytes;
-  if (sc.smem_bytes > kSmemMax) {
+  if (sc.smem_bytes > smem_cap) {
     snprintf(why, why_len, "no schedule fits shared memory (K=%d, B=%d, %d matrices)", K, p.B,
              nmat);
     return false;
@@ -511,7 +530,7 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   if (p.epilogue == EPI_RESID && p.nseg == 1) {
     const int rows = (RG + Gs - 1) / Gs * RT;
     const int off_res = align_up(sc.smem_bytes, 16);
-    if (off_res + rows * sc.BT * 4 <= kSmemMax) {
+    if (off_res + rows * sc.BT * 4 <= smem_cap) {
       sc.off_res = off_res;
       sc.res_rows = rows;
       sc.smem_bytes = off_res + rows * sc.BT * 4;
@@ -521,6 +540,35 @@ bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
   p.M_total = 0;
   for (int s = 0; s < p.nseg; ++s) p.M_total += p.seg[s].M;
   return true;
+}
+
+// Choose the schedule.  force_S > 0 fixes the K split; force_S == 0 lets the
+// heuristic split skinny shapes; force_S < 0 forbids splitting.  The tensor-
+// core kernels first where they apply (4-bit rows: at batch 2-4); else the
+// CUDA-core one, with two CTAs per SM for 4-bit rows at batch 1 when its
+// registers and shared memory allow, else one.  Measured on the 4-bit decode
+// chain at batch 1: one CTA's eight warps leave the SM waiting on copies
+// (gate/up 10.3 -> 7.1 us a launch, the LM head on CUDA cores 40.5 us against
+// 52.5 on tensor cores; the step 682 -> 567 us); three CTAs lose again (619
+// us), and so do two at batch 4 (1074 -> 1147 us) and for bf16 rows (637 ->
+// 691 us at batch 1).
+bool plan_gemv(GemvParams& p, int force_S, char* why, size_t why_len) {
+  const Tuning& tu = tuning();
+  const int nsm = device_sm_count();
+  const int grid_target = tu.grid_cap > 0 ? tu.grid_cap : nsm;
+  const bool q4 = p.wfmt == WF_Q4;
+  if (!q4 && tu.mma && tu.forms && plan_gemv_mma(p, force_S, grid_target)) return true;
+  const bool q4_mma = tu.q4_mma == 2 || (tu.q4_mma == 1 && p.B > 1);
+  if (q4 && q4_mma && tu.forms && plan_gemv_q4mma(p, grid_target)) return true;
+  const int cps = tu.ctas_per_sm > 0 ? tu.ctas_per_sm : (q4 && batch_template(p.B) == 1 ? 2 : 1);
+  for (int c = cps; c > 1; --c) {
+    GemvParams t = p;
+    if (plan_gemv_cc(t, force_S, c, why, why_len) && resident_ctas(t) >= c) {
+      p = t;
+      return true;
+    }
+  }
+  return plan_gemv_cc(p, force_S, 1, why, why_len);
 }
 
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
@@ -609,6 +657,20 @@ static bool ensure_smem_attr(GemvKernel k) {
     return false;
   done.insert(key);
   return true;
+}
+
+// CTAs of a planned launch that one SM holds at once, by the kernel's
+// registers and the plan's shared memory (the occupancy calculator); with no
+// device to ask, by shared memory alone.
+static int resident_ctas(const GemvParams& p) {
+  GemvKernel k = pick_kernel(p);
+  if (!k) return 0;
+  int n = 0;
+  if (ensure_smem_attr(k) && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                 &n, k, kThreads, p.sc.smem_bytes) == cudaSuccess)
+    return n;
+  cudaGetLastError();
+  return smem_per_sm() / (p.sc.smem_bytes + kSmemReserved);
 }
 
 bool prepare_gemv(const GemvParams& p) {
@@ -1013,6 +1075,8 @@ void ws_get_tuning(ws_tuning* t) {
   t->forms = tu.forms;
   t->launch_pdl = tu.launch_pdl;
   t->mma = tu.mma;
+  t->ctas_per_sm = tu.ctas_per_sm;
+  t->q4_mma = tu.q4_mma;
 }
 
 ws_status ws_set_tuning(const ws_tuning* t) {
@@ -1021,7 +1085,8 @@ ws_status ws_set_tuning(const ws_tuning* t) {
       t->piece_bytes < 0 ||
       t->piece_bytes > 64 * 1024 || t->timeout_ns == 0 || t->l2_ahead < 0 ||
       t->l2_ahead > 64 || t->forms < 0 || t->forms > 1 || t->launch_pdl < 0 ||
-      t->launch_pdl > 1 || t->mma < 0 || t->mma > 1) {
+      t->launch_pdl > 1 || t->mma < 0 || t->mma > 1 || t->ctas_per_sm < 0 ||
+      t->ctas_per_sm > 3 || t->q4_mma < 0 || t->q4_mma > 2) {
     set_error("bad tuning values");
     return WS_ERR_ARG;
   }
@@ -1037,6 +1102,8 @@ ws_status ws_set_tuning(const ws_tuning* t) {
   tu.forms = t->forms;
   tu.launch_pdl = t->launch_pdl;
   tu.mma = t->mma;
+  tu.ctas_per_sm = t->ctas_per_sm;
+  tu.q4_mma = t->q4_mma;
   return WS_OK;
 }
 
