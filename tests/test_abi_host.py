@@ -79,6 +79,15 @@ def test_other_entry_points_validate(lib):
     assert lib.ws_set_tuning(wb.ctypes.byref(t)) == -1
 
 
+@pytest.mark.parametrize("field,value", [("ctas_per_sm", 4), ("ctas_per_sm", -1), ("q4_mma", 3),
+                                         ("q4_mma", -1)])
+def test_tuning_rejects_out_of_range_residency_fields(lib, field, value):
+    t = wb.get_tuning()
+    setattr(t, field, value)
+    assert lib.ws_set_tuning(wb.ctypes.byref(t)) == -1
+    assert wb.get_tuning().ctas_per_sm == 0 and wb.get_tuning().q4_mma == 1  # unchanged
+
+
 @pytest.mark.parametrize("B,nh,nkv,d,S,kc,wsb,status", [
     (2, 12, 2, 64, 256, A, 1 << 20, -3),     # head_dim != 128
     (2, 12, 1, 128, 256, A, 1 << 20, -3),    # 12 query heads per key-value head (> 8)

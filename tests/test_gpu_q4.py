@@ -166,3 +166,43 @@ def test_q4_chain_at_every_residency(B, cps):
     shape = synth.QwenShape(hidden=256, kv_dim=64, inter=1408, vocab=40000, layers=2)
     with tuning(ctas_per_sm=cps, q4_mma=0):
         _q4_chain_check(B, shape)
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_q4_full_size_block_and_vocabulary(B):
+    """One Qwen2.5-1.5B-sized block and the full 151936-row LM head on 4-bit
+    weights, as the decode step runs them (batch 1: the CUDA-core kernel at
+    two CTAs per SM, 304 CTAs, the head included; batch 4: one CTA per SM and
+    the tensor-core head).  The block against the oracle; the head's packed
+    rows and logits on sampled rows (every 97th and the last 40) against the
+    oracle on the GPU's final h; the fused argmax over all rows equal to the
+    first maximum of the GPU's own logits."""
+    shape = synth.QwenShape(layers=1)
+    seed = 101 + B
+    blk = synth.qwen_block_weights(shape, seed, 0)
+    head = synth.qwen_head_weights(shape, seed)
+    attn = synth.qwen_attn(shape, B, seed, 0)[None]
+    h0 = synth.qwen_hidden(shape, B, seed)
+    d = {n: dev_bf16(blk[n]) for n in ("gamma1", "gamma2")}
+    r = {n: blk[n] for n in ("gamma1", "gamma2")}
+    for n in ("Wq", "Wk", "Wv", "Wo", "Wg", "Wu", "Wd"):
+        d[n], r[n] = _quantize_both(blk[n])
+    r["K"], r["KI"] = shape.hidden, shape.inter
+    V, H = shape.vocab, shape.hidden
+    Wlm = torch.zeros((V, wb.q4_row_bytes(H)), dtype=torch.uint8, device="cuda")
+    wb.quantize_q4(dev_bf16(head["Wlm"]), Wlm)
+    rows = np.unique(np.concatenate([np.arange(0, V, 97), np.arange(V - 40, V)]))
+    ref_rows = oq4.pack(*oq4.quantize(head["Wlm"][rows]))
+    assert np.array_equal(Wlm.cpu().numpy()[rows], ref_rows)
+    ch = wc.qwen_chain([d], {"gamma_f": dev_bf16(head["gamma_f"]), "Wlm": Wlm}, dev_bf16(attn),
+                       dev_f32(h0), eps=shape.eps, trace=True, logits=True, q4=True)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    trace = ch.h_trace.cpu().numpy().astype(np.float64)
+    ref = oq4.qwen_block(h0.astype(np.float64), r, oracle.bf16_to_f64(attn[0]), shape.eps)
+    assert_fp32(trace[0], ref["h"], what="full-size 4-bit block")
+    logits = ch.logits.cpu().numpy()
+    ref_logits = oq4.lmhead_logits(trace[0], head["gamma_f"], ref_rows, H, shape.eps)
+    assert_fp32(logits[:, rows], ref_logits, what="4-bit LM head, sampled rows")
+    assert np.array_equal(ch.idx.cpu().numpy(), np.argmax(logits, axis=1))
