@@ -268,9 +268,16 @@ __device__ __forceinline__ void gamma_preload(const GemvParams& p, int tid, uint
                       : make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int BT, int NR>  // NR chunks per thread
+// NG = NR: gamma was read per chunk before the dependency wait (g[i]);
+// NG = 1 (batch tiles 8 and 16): gamma is read after the reduction instead,
+// so that a thread's up to twelve activation chunks are all in flight at once
+// rather than competing with twelve more chunks of gamma for registers
+// (measured, the LayerNorm twin below: 7.2 us of staging at batch 16).
+template <int BT, int NR, int NG>  // NR chunks per thread
 __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* red, uint16_t* xs,
-                                    int tid, const uint4 (&g)[NR]) {
+                                    int tid, const uint4 (&g)[NG]) {
+  static_assert(NG == NR || NG == 1, "gamma per chunk, or read late");
+  constexpr bool late = NG != NR;
   const int nch = p.K >> 3, n = p.B * nch;
   float* tot = red + kWarps * BT;
   float v[NR][8];
@@ -279,21 +286,27 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
   chunk_coords<NR, BT>(tid, kThreads, nch, rb, rc);
 #pragma unroll
   for (int b = 0; b < BT; ++b) s[b] = 0.f;
+  // every load first (fp32, rows K apart: o = b * nch + c), then the sums
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
     const int o = tid + i * kThreads;
     if (o < n) {
-      const int b = rb[i];
       const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x)) + 2 * o;
-      const float4 lo4 = __ldcg(src), hi4 = __ldcg(src + 1);  // fp32, rows K apart: o = b*nch + c
+      const float4 lo4 = __ldcg(src), hi4 = __ldcg(src + 1);
       v[i][0] = lo4.x; v[i][1] = lo4.y; v[i][2] = lo4.z; v[i][3] = lo4.w;
       v[i][4] = hi4.x; v[i][5] = hi4.y; v[i][6] = hi4.z; v[i][7] = hi4.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int o = tid + i * kThreads;
+    if (o < n) {
       float t = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) t = fmaf(v[i][e], v[i][e], t);
 #pragma unroll
       for (int bb = 0; bb < BT; ++bb)
-        if (bb == b) s[bb] += t;
+        if (bb == rb[i]) s[bb] += t;
     }
   }
   block_sum<BT>(s, red, tot, p.B, tid);
@@ -305,8 +318,9 @@ __device__ void stage_rms_one_round(const GemvParams& p, float* stats, float* re
     const int o = tid + i * kThreads;
     if (o < n) {
       const float r = stats[2 * rb[i]];
-      const float gf[8] = {bf16lo(g[i].x), bf16hi(g[i].x), bf16lo(g[i].y), bf16hi(g[i].y),
-                           bf16lo(g[i].z), bf16hi(g[i].z), bf16lo(g[i].w), bf16hi(g[i].w)};
+      const uint4 gi = late ? __ldg(reinterpret_cast<const uint4*>(p.gamma) + rc[i]) : g[late ? 0 : i];
+      const float gf[8] = {bf16lo(gi.x), bf16hi(gi.x), bf16lo(gi.y), bf16hi(gi.y),
+                           bf16lo(gi.z), bf16hi(gi.z), bf16lo(gi.w), bf16hi(gi.w)};
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -335,13 +349,21 @@ __device__ __forceinline__ void beta_preload(const GemvParams& p, int tid, uint4
 // round of memory latency), then (x - mean) * rstd * gamma + beta rounded once
 // to bf16 for this split's columns [c0, c0 + nch).  The arithmetic of
 // prologue_stats + stage_x, with the sums grouped by thread.
-template <int BT, int NR>
+// With NG = 1 (batch tiles 8 and 16) gamma and beta are read after the
+// reductions, and the activations stay in registers as their bf16 words (four
+// registers a chunk, widened at each use): a thread's chunks are all loaded
+// before any is used.  With gamma and beta held per chunk and the widened
+// values kept, the staging took 7.2 us at batch 16 against 2.3 at batch 4
+// (768 columns: six chunks a thread at batch 16, two at batch 4).
+template <int BT, int NR, int NG>
 __device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red, uint16_t* xs,
-                                   int c0, int nch, int tid, const uint4 (&g)[NR],
-                                   const uint4 (&bt)[NR]) {
+                                   int c0, int nch, int tid, const uint4 (&g)[NG],
+                                   const uint4 (&bt)[NG]) {
+  static_assert(NG == NR || NG == 1, "gamma and beta per chunk, or read late");
+  constexpr bool late = NG != NR;
   const int kch = p.K >> 3, n = p.B * kch;
   float* tot = red + kWarps * BT;
-  float v[NR][8];
+  uint4 u[NR];
   float s[BT];
   int rb[NR], rc[NR];
   chunk_coords<NR, BT>(tid, kThreads, kch, rb, rc);
@@ -351,13 +373,17 @@ __device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
     const int o = tid + i * kThreads;
+    u[i] = o < n ? __ldcg(src + o) : make_uint4(0u, 0u, 0u, 0u);  // rows K apart: o = b * kch + c
+  }
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int o = tid + i * kThreads;
     if (o < n) {
-      const uint4 u = __ldcg(src + o);  // rows K apart: o = b * kch + c
-      v[i][0] = bf16lo(u.x); v[i][1] = bf16hi(u.x); v[i][2] = bf16lo(u.y); v[i][3] = bf16hi(u.y);
-      v[i][4] = bf16lo(u.z); v[i][5] = bf16hi(u.z); v[i][6] = bf16lo(u.w); v[i][7] = bf16hi(u.w);
+      const float v[8] = {bf16lo(u[i].x), bf16hi(u[i].x), bf16lo(u[i].y), bf16hi(u[i].y),
+                          bf16lo(u[i].z), bf16hi(u[i].z), bf16lo(u[i].w), bf16hi(u[i].w)};
       float t = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) t += v[i][e];
+      for (int e = 0; e < 8; ++e) t += v[e];
 #pragma unroll
       for (int bb = 0; bb < BT; ++bb)
         if (bb == rb[i]) s[bb] += t;
@@ -373,9 +399,11 @@ __device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red
     const int o = tid + i * kThreads;
     if (o < n) {
       const float mean = stats[2 * rb[i]];
+      const float v[8] = {bf16lo(u[i].x), bf16hi(u[i].x), bf16lo(u[i].y), bf16hi(u[i].y),
+                          bf16lo(u[i].z), bf16hi(u[i].z), bf16lo(u[i].w), bf16hi(u[i].w)};
       float t = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) t = fmaf(v[i][e] - mean, v[i][e] - mean, t);
+      for (int e = 0; e < 8; ++e) t = fmaf(v[e] - mean, v[e] - mean, t);
 #pragma unroll
       for (int bb = 0; bb < BT; ++bb)
         if (bb == rb[i]) s[bb] += t;
@@ -391,20 +419,160 @@ __device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red
     const int c = rc[i] - c0;
     if (o < n && c >= 0 && c < nch) {
       const float mean = stats[2 * rb[i]], rstd = stats[2 * rb[i] + 1];
-      const float gf[8] = {bf16lo(g[i].x), bf16hi(g[i].x), bf16lo(g[i].y), bf16hi(g[i].y),
-                           bf16lo(g[i].z), bf16hi(g[i].z), bf16lo(g[i].w), bf16hi(g[i].w)};
-      const float bf[8] = {bf16lo(bt[i].x), bf16hi(bt[i].x), bf16lo(bt[i].y), bf16hi(bt[i].y),
-                           bf16lo(bt[i].z), bf16hi(bt[i].z), bf16lo(bt[i].w), bf16hi(bt[i].w)};
+      const uint4 gi = late ? __ldg(reinterpret_cast<const uint4*>(p.gamma) + rc[i]) : g[late ? 0 : i];
+      const uint4 bi = late ? __ldg(reinterpret_cast<const uint4*>(p.beta) + rc[i]) : bt[late ? 0 : i];
+      const float gf[8] = {bf16lo(gi.x), bf16hi(gi.x), bf16lo(gi.y), bf16hi(gi.y),
+                           bf16lo(gi.z), bf16hi(gi.z), bf16lo(gi.w), bf16hi(gi.w)};
+      const float bf[8] = {bf16lo(bi.x), bf16hi(bi.x), bf16lo(bi.y), bf16hi(bi.y),
+                           bf16lo(bi.z), bf16hi(bi.z), bf16lo(bi.w), bf16hi(bi.w)};
+      const float v[8] = {bf16lo(u[i].x), bf16hi(u[i].x), bf16lo(u[i].y), bf16hi(u[i].y),
+                          bf16lo(u[i].z), bf16hi(u[i].z), bf16lo(u[i].w), bf16hi(u[i].w)};
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        w[e] = pack_bf16x2((v[i][2 * e] - mean) * rstd * gf[2 * e] + bf[2 * e],
-                           (v[i][2 * e + 1] - mean) * rstd * gf[2 * e + 1] + bf[2 * e + 1]);
+        w[e] = pack_bf16x2((v[2 * e] - mean) * rstd * gf[2 * e] + bf[2 * e],
+                           (v[2 * e + 1] - mean) * rstd * gf[2 * e + 1] + bf[2 * e + 1]);
       xs4[rb[i] * nch + c] = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
   // batch rows the kernel computes past B read zeros
   for (int o = p.B * nch + tid; o < BT * nch; o += kThreads) xs4[o] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Staging for batch tiles 8 and 16 when a row has at most 32 * MC 8-column
+// chunks (K <= 256 * MC): warp w normalises batch rows w + 8 j (j < BT / 8) by
+// itself, lane l taking the row's chunks l, l + 32, ..., so the statistics
+// need warp shuffles only -- no CTA barrier -- and the code stays short.  A
+// launch starts with cold instruction caches, and the CTA-wide version (each
+// chunk's sum selected into one of BT partials, BT-wide block reductions)
+// spent 6.5 us of a batch-16 LayerNorm block staging 16 x 768 values, most
+// of it in code that ran once.  Every load is issued before any is used; gc
+// (and bc) are gamma (and beta) at the lane's chunk columns, read before the
+// dependency wait.  LayerNorm: mean, then the variance about it (two warp
+// reductions), (x - mean) * rstd * gamma + beta; RMSNorm: x * rsqrt(mean x^2
+// + eps) * gamma; rounded once to bf16 into columns [c0, c0 + nch) of xs.
+template <int BT, int MC, bool LN>
+__device__ void stage_rows(const GemvParams& p, float* stats, uint16_t* xs, int c0, int nch,
+                           int warp, int lane, const uint4 (&gc)[MC], const uint4 (&bc)[MC]) {
+  static_assert(BT % kWarps == 0, "whole rows per warp");
+  constexpr int RPW = BT / kWarps;
+  const int kch = p.K >> 3;
+  uint4* xs4 = reinterpret_cast<uint4*>(xs);
+  // LayerNorm keeps the bf16 words (widened at each use), RMSNorm the fp32
+  // values it loaded
+  uint4 u[LN ? RPW : 1][LN ? MC : 1];
+  float4 f[LN ? 1 : RPW][LN ? 1 : 2 * MC];
+#pragma unroll
+  for (int j = 0; j < RPW; ++j) {
+    const int b = warp + kWarps * j;
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+      const int c = lane + 32 * m;
+      const bool ok = b < p.B && c < kch;
+      if constexpr (LN) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x));
+        u[j][m] = ok ? __ldcg(src + (size_t)b * kch + c) : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x)) +
+                            2 * ((size_t)b * kch + c);
+        f[j][2 * m] = ok ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f[j][2 * m + 1] = ok ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < RPW; ++j) {
+    const int b = warp + kWarps * j;
+    if (b >= p.B) {  // batch rows the kernel computes past B read zeros
+      for (int c = lane; c < nch; c += 32) xs4[b * nch + c] = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
+    auto vals = [&](int m, float (&v)[8]) {
+      if constexpr (LN) {
+        const uint4 w = u[j][m];
+        v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
+        v[4] = bf16lo(w.z); v[5] = bf16hi(w.z); v[6] = bf16lo(w.w); v[7] = bf16hi(w.w);
+      } else {
+        const float4 a = f[j][2 * m], c = f[j][2 * m + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+      }
+    };
+    float mean = 0.f, scale;
+    if constexpr (LN) {
+      float t = 0.f;
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        float v[8];
+        vals(m, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t += v[e];
+      }
+      mean = warp_sum(t) / (float)p.K;
+      float q = 0.f;
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        if (lane + 32 * m < kch) {
+          float v[8];
+          vals(m, v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
+        }
+      }
+      scale = rsqrtf(warp_sum(q) / (float)p.K + p.eps);
+    } else {
+      float q = 0.f;
+#pragma unroll
+      for (int m = 0; m < MC; ++m) {
+        float v[8];
+        vals(m, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) q = fmaf(v[e], v[e], q);
+      }
+      scale = rsqrtf(warp_sum(q) / (float)p.K + p.eps);
+    }
+    if (lane == 0) {
+      stats[2 * b] = LN ? mean : scale;
+      stats[2 * b + 1] = scale;
+    }
+#pragma unroll
+    for (int m = 0; m < MC; ++m) {
+      const int c = lane + 32 * m, cc = c - c0;
+      if (c < kch && cc >= 0 && cc < nch) {
+        float v[8];
+        vals(m, v);
+        const uint4 g = gc[m];
+        const float gf[8] = {bf16lo(g.x), bf16hi(g.x), bf16lo(g.y), bf16hi(g.y),
+                             bf16lo(g.z), bf16hi(g.z), bf16lo(g.w), bf16hi(g.w)};
+        float bf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if constexpr (LN) {
+          const uint4 h = bc[m];
+          bf[0] = bf16lo(h.x); bf[1] = bf16hi(h.x); bf[2] = bf16lo(h.y); bf[3] = bf16hi(h.y);
+          bf[4] = bf16lo(h.z); bf[5] = bf16hi(h.z); bf[6] = bf16lo(h.w); bf[7] = bf16hi(h.w);
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if constexpr (LN)
+            w[e] = pack_bf16x2((v[2 * e] - mean) * scale * gf[2 * e] + bf[2 * e],
+                               (v[2 * e + 1] - mean) * scale * gf[2 * e + 1] + bf[2 * e + 1]);
+          else
+            w[e] = pack_bf16x2(v[2 * e] * scale * gf[2 * e], v[2 * e + 1] * scale * gf[2 * e + 1]);
+        }
+        xs4[b * nch + cc] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+// gamma (or beta) at a lane's chunk columns lane, lane + 32, ... (zeros past K).
+template <int MC>
+__device__ __forceinline__ void cols_preload(const uint16_t* g, int kch, int lane, uint4 (&out)[MC]) {
+#pragma unroll
+  for (int m = 0; m < MC; ++m) {
+    const int c = lane + 32 * m;
+    out[m] = c < kch ? *reinterpret_cast<const uint4*>(g + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // Staging without a prologue, bf16 activations: a copy into shared memory,
@@ -805,10 +973,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // gamma does not depend on the previous op either
   const bool one_round = FT::rms1 || (!FT::copy_bf16 && !FT::ln1 && one_round_rms(p));
   constexpr int NR = (FT::rms1 || FT::ln1) ? form_round_chunks(BT) : kOneRound;
-  uint4 gpre[NR];
-  uint4 bpre[FT::ln1 ? NR : 1];
-  if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
-  if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
+  // From batch tile 8 the normalising prologues stage whole rows per warp
+  // (stage_rows) when a row has at most 32 * MC chunks, with gamma and beta
+  // read per lane column here; otherwise the CTA-wide staging, which then
+  // reads gamma and beta after its reductions.
+  constexpr int NG = BT >= 8 ? 1 : NR;
+  constexpr int MC = BT >= 16 ? 6 : 8;
+  constexpr int NC = BT >= 8 ? MC : 1;
+  const bool by_rows = BT >= 8 && (FT::rms1 || FT::ln1 || one_round) && (p.K >> 3) <= 32 * MC;
+  uint4 gpre[NG];
+  uint4 bpre[FT::ln1 ? NG : 1];
+  uint4 gcol[NC], bcol[NC];
+  if constexpr (NG == NR) {
+    if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
+    if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
+  } else {
+    if (by_rows) {
+      cols_preload<NC>(p.gamma, p.K >> 3, lane, gcol);
+      if constexpr (FT::ln1) cols_preload<NC>(p.beta, p.K >> 3, lane, bcol);
+    }
+  }
   pdl_launch_dependents();
   pdl_wait();
   if (stamp && tid == 0) stamp[1] = global_ns();
@@ -831,7 +1015,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // then normalise and store) rather than the one-round fused path: the
   // fused code is 24 KB, and a launch of a chain starts with cold
   // instruction caches (measured: 817 vs 897 us per Qwen chain step).
-  if constexpr (FT::rms1) {
+  if (BT >= 8 && by_rows) {
+    if constexpr (BT >= 8) {
+      if constexpr (FT::ln1)
+        stage_rows<BT, NC, true>(p, stats, xs, k0 >> 3, sc.KS >> 3, warp, lane, gcol, bcol);
+      else
+        stage_rows<BT, NC, false>(p, stats, xs, 0, p.K >> 3, warp, lane, gcol, bcol);
+    }
+  } else if constexpr (FT::rms1) {
     stage_rms_one_round<BT, NR>(p, stats, red, xs, tid, gpre);
   } else if constexpr (FT::ln1) {
     stage_ln_one_round<BT, NR>(p, stats, red, xs, k0 >> 3, sc.KS >> 3, tid, gpre, bpre);
