@@ -454,8 +454,9 @@ __device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red
 template <int BT, int MC, bool LN>
 __device__ void stage_rows(const GemvParams& p, float* stats, uint16_t* xs, int c0, int nch,
                            int warp, int lane, const uint4 (&gc)[MC], const uint4 (&bc)[MC]) {
-  static_assert(BT % kWarps == 0, "whole rows per warp");
-  constexpr int RPW = BT / kWarps;
+  static_assert(BT % kWarps == 0 || BT < kWarps, "whole rows per warp");
+  constexpr int RPW = BT >= kWarps ? BT / kWarps : 1;  // below 8 rows: warps < BT, a row each
+  if (BT < kWarps && warp >= BT) return;
   const int kch = p.K >> 3;
   uint4* xs4 = reinterpret_cast<uint4*>(xs);
   // LayerNorm keeps the bf16 words (widened at each use), RMSNorm the fp32
@@ -979,19 +980,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // reads gamma and beta after its reductions.
   constexpr int NG = BT >= 8 ? 1 : NR;
   constexpr int MC = BT >= 16 ? 6 : 8;
-  constexpr int NC = BT >= 8 ? MC : 1;
-  const bool by_rows = BT >= 8 && (FT::rms1 || FT::ln1 || one_round) && (p.K >> 3) <= 32 * MC;
+  constexpr int NC = MC;
+  // Below batch tile 8 only BT warps stage, a row each.  Measured on the
+  // decode step: for the QKV form at batch tile 4 that pays (QKV 6.2 -> 4.4
+  // us a launch, the step 975.5 -> 946.8 us); at batch tile 2 the step lost
+  // (760.1 -> 778.5 us: gate/up, next but one, 10.2 -> 12.1 us, with less of
+  // Wo's time left for its ring fill); for gate/up itself, whose few staging
+  // warps' loads queue behind its own 192 KB ring fill, and at batch 1 it
+  // lost too (the step 636 -> 698 us with every RMSNorm form staged by rows).
+  constexpr bool kRowsSmall = BT == 4 && F == F_RMS_F32 && !Q4;
+  const bool by_rows = (BT >= kWarps || kRowsSmall) && (FT::rms1 || FT::ln1 || one_round) &&
+                       (p.K >> 3) <= 32 * MC;
   uint4 gpre[NG];
   uint4 bpre[FT::ln1 ? NG : 1];
   uint4 gcol[NC], bcol[NC];
-  if constexpr (NG == NR) {
+  if (by_rows) {
+    if constexpr (BT >= kWarps || kRowsSmall) {
+      if (BT >= kWarps || warp < BT) {
+        cols_preload<NC>(p.gamma, p.K >> 3, lane, gcol);
+        if constexpr (FT::ln1) cols_preload<NC>(p.beta, p.K >> 3, lane, bcol);
+      }
+    }
+  } else if constexpr (NG == NR) {
     if (one_round || FT::ln1) gamma_preload<NR, BT>(p, tid, gpre);
     if constexpr (FT::ln1) beta_preload<NR, BT>(p, tid, bpre);
-  } else {
-    if (by_rows) {
-      cols_preload<NC>(p.gamma, p.K >> 3, lane, gcol);
-      if constexpr (FT::ln1) cols_preload<NC>(p.beta, p.K >> 3, lane, bcol);
-    }
   }
   pdl_launch_dependents();
   pdl_wait();
@@ -1015,8 +1027,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // then normalise and store) rather than the one-round fused path: the
   // fused code is 24 KB, and a launch of a chain starts with cold
   // instruction caches (measured: 817 vs 897 us per Qwen chain step).
-  if (BT >= 8 && by_rows) {
-    if constexpr (BT >= 8) {
+  if (by_rows) {
+    if constexpr (BT >= kWarps || kRowsSmall) {
       if constexpr (FT::ln1)
         stage_rows<BT, NC, true>(p, stats, xs, k0 >> 3, sc.KS >> 3, warp, lane, gcol, bcol);
       else
