@@ -206,3 +206,44 @@ def test_q4_full_size_block_and_vocabulary(B):
     ref_logits = oq4.lmhead_logits(trace[0], head["gamma_f"], ref_rows, H, shape.eps)
     assert_fp32(logits[:, rows], ref_logits, what="4-bit LM head, sampled rows")
     assert np.array_equal(ch.idx.cpu().numpy(), np.argmax(logits, axis=1))
+
+
+def test_stamp_rows_cover_two_ctas_per_sm():
+    """Per-CTA diagnostics of a chain whose ops run more CTAs than SMs (4-bit
+    rows at batch 1: two CTAs per SM): the stamp buffer's CTA dimension is the
+    widest op's grid, every CTA of every op writes its own row and no row
+    past an op's grid, and a buffer one row short is refused."""
+    shape = synth.QwenShape(hidden=512, kv_dim=128, inter=1408, vocab=40000, layers=2)
+    blocks = [synth.qwen_block_weights(shape, 3, l) for l in range(shape.layers)]
+    head = synth.qwen_head_weights(shape, 3)
+    mats = ("Wq", "Wk", "Wv", "Wo", "Wg", "Wu", "Wd")
+    dblocks = []
+    for blk in blocks:
+        d = {n: dev_bf16(blk[n]) for n in ("gamma1", "gamma2")}
+        for n in mats:
+            d[n], _ = _quantize_both(blk[n])
+        dblocks.append(d)
+    Wlm, _ = _quantize_both(head["Wlm"])
+    attn = np.stack([synth.qwen_attn(shape, 1, 3, l) for l in range(shape.layers)])
+    h0 = synth.qwen_hidden(shape, 1, 3)
+    ch = wc.qwen_chain(dblocks, {"gamma_f": dev_bf16(head["gamma_f"]), "Wlm": Wlm},
+                       dev_bf16(attn), dev_f32(h0), eps=shape.eps, q4=True)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    g, nops = ch.chain.grid(), ch.chain.n_ops
+    assert g == 2 * nsm  # the widest op: two CTAs per SM
+    short = torch.zeros((g - 1, nops, 44), dtype=torch.int64, device="cuda")
+    with pytest.raises(wb.WsError):
+        ch.chain.debug_stamps(short)
+    buf = torch.zeros((g, nops, 44), dtype=torch.int64, device="cuda")
+    ch.chain.debug_stamps(buf)
+    ch.chain.capture()
+    ch.run()
+    torch.cuda.synchronize()
+    written = (buf[:, :, 0] > 0).cpu().numpy()  # [cta, op]
+    per_op = written.sum(axis=0)
+    # every op's CTAs are a prefix of the rows: rows past its grid untouched
+    for f in range(nops):
+        n = int(per_op[f])
+        assert n > 0 and written[:n, f].all() and not written[n:, f].any(), (f, n)
+    assert per_op.max() == g
+    ch.chain.debug_stamps(None)
