@@ -19,7 +19,7 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libwsgemv.so")
 SOURCES = ["ws_gemv_host.cu", "ws_gemv_k12.cu", "ws_gemv_k4.cu", "ws_gemv_k816.cu", "ws_gemv_k16.cu",
            "ws_gemv_forms_b1.cu", "ws_gemv_forms_b24.cu", "ws_gemv_forms_b8.cu",
-           "ws_gemv_forms_b16.cu", "ws_gemv_mma.cu", "ws_gemv_q4.cu", "ws_gemv_q4_forms.cu", "ws_gemv_q4mma.cu", "ws_attention.cu", "ws_misc.cu",
+           "ws_gemv_forms_b16.cu", "ws_gemv_mma.cu", "ws_gemv_q4.cu", "ws_gemv_q4_forms.cu", "ws_gemv_q4_forms_b24.cu", "ws_gemv_q4mma.cu", "ws_attention.cu", "ws_misc.cu",
            "ws_chain.cu",
            "ws_noalloc.cu", "ws_persist.cu", "ws_backward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

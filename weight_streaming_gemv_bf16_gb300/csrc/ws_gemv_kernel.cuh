@@ -988,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   // Wo's time left for its ring fill); for gate/up itself, whose few staging
   // warps' loads queue behind its own 192 KB ring fill, and at batch 1 it
   // lost too (the step 636 -> 698 us with every RMSNorm form staged by rows).
-  constexpr bool kRowsSmall = BT == 4 && F == F_RMS_F32 && !Q4;
+  constexpr bool kRowsSmall = BT == 4 && F == F_RMS_F32;
   const bool by_rows = (BT >= kWarps || kRowsSmall) && (FT::rms1 || FT::ln1 || one_round) &&
                        (p.K >> 3) <= 32 * MC;
   uint4 gpre[NG];

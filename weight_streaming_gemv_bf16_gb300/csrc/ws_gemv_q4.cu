@@ -10,12 +10,13 @@
 namespace ws {
 
 GemvKernel pick_form_q4_b1(int BT, int nmat, int RT, int F);
+GemvKernel pick_form_q4_b24(int BT, int nmat, int RT, int F);
 
 #define WS_Q4(bt, nm, rt) \
   if (BT == bt && nmat == nm && RT == rt) return (GemvKernel)k_stream_gemv<bt, nm, rt, F_ANY, true>;
 
 GemvKernel pick_kernel_q4(int BT, int nmat, int RT, int F) {
-  if (F != F_ANY) return BT == 1 ? pick_form_q4_b1(BT, nmat, RT, F) : nullptr;
+  if (F != F_ANY) return BT == 1 ? pick_form_q4_b1(BT, nmat, RT, F) : pick_form_q4_b24(BT, nmat, RT, F);
   WS_Q4(1, 1, 1) WS_Q4(1, 1, 2) WS_Q4(1, 1, 4) WS_Q4(1, 2, 1) WS_Q4(1, 2, 2)
   WS_Q4(2, 1, 1) WS_Q4(2, 1, 2) WS_Q4(2, 1, 4) WS_Q4(2, 2, 1) WS_Q4(2, 2, 2)
   WS_Q4(4, 1, 1) WS_Q4(4, 1, 2) WS_Q4(4, 1, 4) WS_Q4(4, 2, 1) WS_Q4(4, 2, 2)
