@@ -9,7 +9,7 @@ import oracle
 from weight_streaming_gemv_bf16_gb300 import binding as wb
 from weight_streaming_gemv_bf16_gb300 import synth
 from _util import (assert_bf16_close, assert_fp32, assert_mlp_block_close, assert_ulp, dev_bf16,
-                   dev_f32, dev_fp16, host_bits)
+                   dev_f32, dev_fp16, host_bits, tuning)
 
 pytestmark = pytest.mark.gpu
 
@@ -198,6 +198,45 @@ def test_ln_gemv_gelu(B):
     wb.ln_gemv_gelu(dev_bf16(x), dev_bf16(blk["gamma"]), dev_bf16(blk["beta"]), dev_bf16(blk["W"]),
                     dev_bf16(blk["b"]), z, 1e-5, workspace=_ws(wb.OP_GEMV, sh.width, sh.width, B))
     assert_mlp_block_close(host_bits(z), x, blk, 1e-5, what=f"ln_gemv_gelu B={B}")
+
+
+@pytest.mark.parametrize("B,K", [(16, 1536), (16, 1544), (13, 1536), (9, 2048), (8, 2048),
+                                 (8, 2056), (5, 3072), (4, 1536), (3, 1536)])
+def test_rmsnorm_staging_by_rows_and_cta_wide(B, K):
+    """The RMSNorm-fused GEMV on fp32 activations on both sides of the widths
+    the row-wise staging takes (from batch tile 8 at most 6 chunks of 8
+    columns a lane at tile 16 and 8 at tile 8; the fp32-output form at tile
+    4), ragged batches inside the tile included; one-round CTA-wide staging
+    past them (9 x 2048, 5 x 3072) and the two-pass general kernel past
+    that (16 x 1544, 8 x 2056): all against the oracle."""
+    M = 700
+    W = synth.normal_bf16((M, K), 0.02, K + B, "rs/W")
+    g = synth.uniform_bf16((K,), 0.5, 1.5, K + B, "rs/g")
+    xh = synth.normal_f32((B, K), 1.0, K + B, "rs/x") * 3
+    y = torch.empty((B, M), device="cuda")
+    wb.rmsnorm_gemv(dev_f32(xh), dev_bf16(g), dev_bf16(W), y, 1e-6,
+                    workspace=_ws(wb.OP_GEMV, M, K, B))
+    ref = oracle.rmsnorm_gemv(xh.astype(np.float64), oracle.bf16_to_f64(g), W, 1e-6)
+    assert_fp32(y.cpu().numpy(), ref, what=f"rmsnorm_gemv B={B} K={K}")
+
+
+@pytest.mark.parametrize("B,K,split", [(16, 768, 0), (13, 768, 0), (5, 768, 0), (16, 1536, 0),
+                                       (16, 1536, 2), (9, 2048, 0), (8, 2048, 0)])
+def test_layernorm_staging_by_rows_and_cta_wide(B, K, split):
+    """The LayerNorm + GEMV + bias + GELU block by rows (768 and 1536 wide at
+    batch tile 16, ragged batches, 2048 at tile 8), by rows with a forced K
+    split (each CTA staging its half of the columns), and CTA-wide past the
+    row limit (9 x 2048), against the oracle."""
+    sh = synth.MlpShape(width=K)
+    blk = synth.mlp_block_weights(sh, 12, 0)
+    x = synth.mlp_input(sh, B, 12)
+    z = torch.empty((B, K), dtype=torch.bfloat16, device="cuda")
+    with tuning(force_ksplit=split):
+        wb.ln_gemv_gelu(dev_bf16(x), dev_bf16(blk["gamma"]), dev_bf16(blk["beta"]),
+                        dev_bf16(blk["W"]), dev_bf16(blk["b"]), z, 1e-5,
+                        workspace=_ws(wb.OP_GEMV, K, K, B))
+        torch.cuda.synchronize()
+    assert_mlp_block_close(host_bits(z), x, blk, 1e-5, what=f"ln_gemv_gelu B={B} K={K} S={split}")
 
 
 def _margin_ok(logits):
