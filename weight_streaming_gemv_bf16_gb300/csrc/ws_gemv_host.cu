@@ -76,6 +76,13 @@ static int batch_template(int B) {
 static int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 static constexpr int kXsMax = 96 * 1024;  // activations in shared memory without a K split
+// The same for the CUDA-core kernel: Wd (1536 x 8960) keeps an unsplit K at
+// batch 8 and two splits at batch 16 (a ring of 2 x 5 KB a warp beside
+// 140 KB of activations) instead of two and four: every split costs each task
+// a fence and a ticket round trip, and the last split's epilogue a tail
+// (measured on the decode step: batch 8 1431 -> 1279 us, Wd 19.6 -> 15.0 us;
+// batch 16 2349 -> 2286 us, Wd's CTA end spread 10.2 -> 2.8 us).
+static constexpr int kXsMaxCC = 144 * 1024;
 static constexpr int kSmemMax = 227 * 1024;
 static constexpr int kSmemReserved = 1024;  // shared memory the runtime keeps per resident CTA
 
@@ -394,7 +401,7 @@ static bool plan_gemv_cc(GemvParams& p, int force_S, int cps, char* why, size_t 
   sc.RG = RG;
 
   auto valid_split = [&](int S) { return S >= 1 && K % (8 * S) == 0; };
-  auto xs_fits = [&](int S) { return (long)sc.BT * (K / S) * 2 <= kXsMax; };
+  auto xs_fits = [&](int S) { return (long)sc.BT * (K / S) * 2 <= kXsMaxCC; };
   int S = 1;
   if (q4) {
     // 4-bit rows are not split along K (a split would have to start on a
