@@ -981,14 +981,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream_gemv(const __grid_consta
   constexpr int NG = BT >= 8 ? 1 : NR;
   constexpr int MC = BT >= 16 ? 6 : 8;
   constexpr int NC = MC;
-  // Below batch tile 8 only BT warps stage, a row each.  Measured on the
-  // decode step: for the QKV form at batch tile 4 that pays (QKV 6.2 -> 4.4
-  // us a launch, the step 975.5 -> 946.8 us); at batch tile 2 the step lost
-  // (760.1 -> 778.5 us: gate/up, next but one, 10.2 -> 12.1 us, with less of
-  // Wo's time left for its ring fill); for gate/up itself, whose few staging
-  // warps' loads queue behind its own 192 KB ring fill, and at batch 1 it
-  // lost too (the step 636 -> 698 us with every RMSNorm form staged by rows).
-  constexpr bool kRowsSmall = BT == 4 && F == F_RMS_F32;
+  // Below batch tile 8 only BT warps stage, a row each.  Measured: at batch
+  // tile 4 that pays for the QKV form (QKV 6.2 -> 4.4 us a launch, the decode
+  // step 975.5 -> 946.8 us) and the LayerNorm form (the 72-block chain 256.3
+  // -> 223.3 us); at batch tile 2 the decode step lost (760.1 -> 778.5 us:
+  // gate/up, next but one, 10.2 -> 12.1 us, with less of Wo's time left for
+  // its ring fill) and so did the LayerNorm chain (209 -> 213 us); gate/up
+  // itself loses, its few staging warps' loads queued behind its own 192 KB
+  // ring fill; at batch 1 everything lost (the decode step 636 -> 698 us, the
+  // LayerNorm chain 182 -> 227 us).
+  constexpr bool kRowsSmall = BT == 4 && (F == F_RMS_F32 || F == F_LN_GELU);
   const bool by_rows = (BT >= kWarps || kRowsSmall) && (FT::rms1 || FT::ln1 || one_round) &&
                        (p.K >> 3) <= 32 * MC;
   uint4 gpre[NG];
