@@ -221,12 +221,14 @@ def test_rmsnorm_staging_by_rows_and_cta_wide(B, K):
 
 
 @pytest.mark.parametrize("B,K,split", [(16, 768, 0), (13, 768, 0), (5, 768, 0), (16, 1536, 0),
-                                       (16, 1536, 2), (9, 2048, 0), (8, 2048, 0)])
+                                       (16, 1536, 2), (9, 2048, 0), (8, 2048, 0), (4, 768, 0),
+                                       (3, 768, 0), (4, 2048, 0), (2, 768, 0), (1, 768, 0)])
 def test_layernorm_staging_by_rows_and_cta_wide(B, K, split):
     """The LayerNorm + GEMV + bias + GELU block by rows (768 and 1536 wide at
-    batch tile 16, ragged batches, 2048 at tile 8), by rows with a forced K
-    split (each CTA staging its half of the columns), and CTA-wide past the
-    row limit (9 x 2048), against the oracle."""
+    batch tile 16, ragged batches, 2048 at tile 8, 768 and 2048 at tile 4 with
+    warps 0-3 staging a row each), by rows with a forced K split (each CTA
+    staging its half of the columns), and CTA-wide past the row limit
+    (9 x 2048) and below tile 4 (batch 2 and 1), against the oracle."""
     sh = synth.MlpShape(width=K)
     blk = synth.mlp_block_weights(sh, 12, 0)
     x = synth.mlp_input(sh, B, 12)
