@@ -439,10 +439,12 @@ __device__ void stage_ln_one_round(const GemvParams& p, float* stats, float* red
   for (int o = p.B * nch + tid; o < BT * nch; o += kThreads) xs4[o] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Staging for batch tiles 8 and 16 when a row has at most 32 * MC 8-column
-// chunks (K <= 256 * MC): warp w normalises batch rows w + 8 j (j < BT / 8) by
-// itself, lane l taking the row's chunks l, l + 32, ..., so the statistics
-// need warp shuffles only -- no CTA barrier -- and the code stays short.  A
+// Staging by rows when a row has at most 32 * MC 8-column chunks (K <= 256 *
+// MC), at batch tiles 8 and 16 and, for the forms that gain from it, 4 (the
+// kernel decides): warp w normalises batch rows w + 8 j (j < BT / 8; below
+// eight rows warps w < BT, row w) by itself, lane l taking the row's chunks
+// l, l + 32, ..., so the statistics need warp shuffles only -- no CTA
+// barrier -- and the code stays short.  A
 // launch starts with cold instruction caches, and the CTA-wide version (each
 // chunk's sum selected into one of BT partials, BT-wide block reductions)
 // spent 6.5 us of a batch-16 LayerNorm block staging 16 x 768 values, most
